@@ -1,0 +1,279 @@
+/*
+ * gla_oracle.c -- fp64 CPU oracle of causal gated linear attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code with
+ * the CUDA path and is deliberately plain: one token at a time, in float64,
+ * in the order the pages write the method.
+ *
+ * Sources (page title, section):
+ *  [GLA]  "Gated Linear Attention" (garden note), "GLA / Recurrent Form":
+ *         S_t = Diag(alpha_t) S_{t-1} + (outer product of k_t and v_t),
+ *         with alpha_t in (0,1)^{d_k}; the flowchart multiplies q_t with the
+ *         *updated* state S_t to give o_t.
+ *  [LA]   "linear-attention" blog, "Linear attention" and "Gated linear
+ *         attention": o_n depends on (S_{n-1}, q_n, k_n, v_n); the state
+ *         update is S_n = S_{n-1} + k_n^T v_n (row-vector convention, so the
+ *         state is d_k x d_v), gated by alpha_n.
+ *  [RNN]  "Transformers are RNNs" notes, kernel derivation: normalised form
+ *         V'_i = sum_j sim(Q_i,K_j) V_j / sum_j sim(Q_i,K_j) with
+ *         sim = phi(Q_i)^T phi(K_j), made causal (j <= i).
+ *  [CHK]  "Gated Linear Attention", "Summary" / "Chunk-Wise Block-Parallel":
+ *         the chunk-wise form that interpolates between the parallel and the
+ *         recurrent form (used only by oracle_gla_fwd_chunked).
+ *
+ * Readings taken where the pages are silent or garbled:
+ *  - state S is d_k x d_v, the update is k_t v_t^T, the decay scales the d_k
+ *    rows, and o_t = S_t^T q_t (inclusive: S_t already holds token t);
+ *  - phi(x) = elu(x) + 1 (x + 1 for x > 0, e^x otherwise) when requested;
+ *  - the normaliser z_t is carried like one extra all-ones value column of
+ *    the state, so it decays with the same Diag(alpha_t) when a gate is
+ *    present; no epsilon is added (phi > 0 keeps the denominator positive).
+ *
+ * Planted mistakes: compiling with -DORACLE_PLANT=n (n >= 1) builds a
+ * deliberately wrong variant that the pinning tests must reject.  The normal
+ * build has ORACLE_PLANT = 0 and none of those branches.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifndef ORACLE_PLANT
+#define ORACLE_PLANT 0
+#endif
+
+#define ORACLE_FEATURE_ELU1 1
+#define ORACLE_NORMALIZE 2
+
+static double phi_elu1(double x) { return x > 0.0 ? x + 1.0 : exp(x); }
+
+static void set_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* One token of the recurrence for one (batch, head) pair.
+ *   S  [dk][dv] in/out, z [dk] in/out (normalised mode only)
+ *   q, k [dk], v [dv], la [dk] (log alpha; NULL means alpha == 1)
+ *   o  [dv] out
+ */
+static void recur_token(double *S, double *z, const double *q, const double *k,
+                        const double *v, const double *la, double *o,
+                        long dk, long dv, int flags, double *qf, double *kf) {
+    const int elu1 = flags & ORACLE_FEATURE_ELU1;
+    const int norm = flags & ORACLE_NORMALIZE;
+    for (long i = 0; i < dk; i++) {
+        qf[i] = elu1 ? phi_elu1(q[i]) : q[i];
+        kf[i] = elu1 ? phi_elu1(k[i]) : k[i];
+    }
+    /* S_t = Diag(alpha_t) S_{t-1} + k_t v_t^T   [GLA Recurrent Form] */
+    for (long i = 0; i < dk; i++) {
+        double a = la ? exp(la[i]) : 1.0;
+#if ORACLE_PLANT == 1
+        /* planted: decay applied after the write (write decays at its own step) */
+        for (long j = 0; j < dv; j++) S[i * dv + j] = a * (S[i * dv + j] + kf[i] * v[j]);
+        if (norm) z[i] = a * (z[i] + kf[i]);
+        continue;
+#endif
+        for (long j = 0; j < dv; j++) S[i * dv + j] = a * S[i * dv + j] + kf[i] * v[j];
+        if (norm) z[i] = a * z[i] + kf[i];
+    }
+    /* o_t = S_t^T q_t  (q multiplies the updated state)   [GLA flowchart] */
+    for (long j = 0; j < dv; j++) {
+        double acc = 0.0;
+#if ORACLE_PLANT == 2
+        /* planted: transposed contraction (only meaningful when dk == dv) */
+        for (long i = 0; i < dk; i++) acc += qf[i] * S[j * dv + i];
+#else
+        for (long i = 0; i < dk; i++) acc += qf[i] * S[i * dv + j];
+#endif
+        o[j] = acc;
+    }
+    if (norm) {
+        double den = 0.0;
+        for (long i = 0; i < dk; i++) den += qf[i] * z[i];
+#if ORACLE_PLANT == 3
+        den = 1.0; /* planted: normaliser dropped */
+#endif
+        for (long j = 0; j < dv; j++) o[j] /= den;
+    }
+}
+
+#if ORACLE_PLANT == 4
+/* planted: output taken from S_{t-1} (exclusive) instead of S_t */
+#define PLANT_EXCLUSIVE 1
+#endif
+
+/*
+ * Prefill: every (b, h) runs the recurrence over t = 0 .. L-1.
+ * Layouts (row-major): q, k, log_alpha [B][H][L][dk]; v, out [B][H][L][dv];
+ * init_state, final_state [B][H][dk][dv]; init_z, final_z [B][H][dk].
+ * log_alpha, init_state, init_z, final_state, final_z may be NULL.
+ */
+int oracle_gla_fwd(const double *q, const double *k, const double *v,
+                   const double *log_alpha, const double *init_state,
+                   const double *init_z, double *out, double *final_state,
+                   double *final_z, long B, long H, long L, long dk, long dv,
+                   int flags, int nthreads) {
+    if (B < 0 || H < 0 || L < 0 || dk <= 0 || dv <= 0) return 1;
+    set_threads(nthreads);
+    long BH = B * H;
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long bh = 0; bh < BH; bh++) {
+        double *S = (double *)calloc((size_t)(dk * dv), sizeof(double));
+        double *z = (double *)calloc((size_t)dk, sizeof(double));
+        double *qf = (double *)malloc((size_t)dk * sizeof(double));
+        double *kf = (double *)malloc((size_t)dk * sizeof(double));
+        double *prev = (double *)malloc((size_t)(dk * dv) * sizeof(double));
+        if (!S || !z || !qf || !kf || !prev) {
+#pragma omp atomic write
+            err = 2;
+            free(S); free(z); free(qf); free(kf); free(prev);
+            continue;
+        }
+        if (init_state) memcpy(S, init_state + bh * dk * dv, (size_t)(dk * dv) * sizeof(double));
+        if (init_z) memcpy(z, init_z + bh * dk, (size_t)dk * sizeof(double));
+        for (long t = 0; t < L; t++) {
+            const double *qt = q + (bh * L + t) * dk;
+            const double *kt = k + (bh * L + t) * dk;
+            const double *vt = v + (bh * L + t) * dv;
+            const double *lat = log_alpha ? log_alpha + (bh * L + t) * dk : NULL;
+            double *ot = out + (bh * L + t) * dv;
+#ifdef PLANT_EXCLUSIVE
+            memcpy(prev, S, (size_t)(dk * dv) * sizeof(double));
+            recur_token(S, z, qt, kt, vt, lat, ot, dk, dv, flags, qf, kf);
+            for (long j = 0; j < dv; j++) {
+                double acc = 0.0;
+                for (long i = 0; i < dk; i++) acc += qf[i] * prev[i * dv + j];
+                ot[j] = acc;
+            }
+#else
+            recur_token(S, z, qt, kt, vt, lat, ot, dk, dv, flags, qf, kf);
+#endif
+        }
+        if (final_state) memcpy(final_state + bh * dk * dv, S, (size_t)(dk * dv) * sizeof(double));
+        if (final_z) memcpy(final_z + bh * dk, z, (size_t)dk * sizeof(double));
+        free(S); free(z); free(qf); free(kf); free(prev);
+    }
+    return err;
+}
+
+/*
+ * Decode: one token per (sequence, head); the state is updated in place.
+ * q, k, log_alpha [NS][H][dk]; v, out [NS][H][dv]; state [NS][H][dk][dv].
+ */
+int oracle_gla_decode_step(const double *q, const double *k, const double *v,
+                           const double *log_alpha, double *state, double *out,
+                           long NS, long H, long dk, long dv, int nthreads) {
+    if (NS < 0 || H < 0 || dk <= 0 || dv <= 0) return 1;
+    set_threads(nthreads);
+    long n = NS * H;
+    int err = 0;
+#pragma omp parallel for schedule(static)
+    for (long s = 0; s < n; s++) {
+        double *qf = (double *)malloc((size_t)dk * sizeof(double));
+        double *kf = (double *)malloc((size_t)dk * sizeof(double));
+        if (!qf || !kf) {
+#pragma omp atomic write
+            err = 2;
+            free(qf); free(kf);
+            continue;
+        }
+        recur_token(state + s * dk * dv, NULL, q + s * dk, k + s * dk, v + s * dv,
+                    log_alpha ? log_alpha + s * dk : NULL, out + s * dv, dk, dv, 0, qf, kf);
+        free(qf); free(kf);
+    }
+    return err;
+}
+
+/*
+ * Chunk-wise restatement [CHK], in fp64, for chunk size C >= 1.  It is the
+ * same function of the inputs as oracle_gla_fwd (an exact refactoring of the
+ * recurrence); tests compare the two.  With b_t the inclusive cumulative sum
+ * of log alpha from the chunk start and b_C its value at the chunk's last
+ * token, unrolling the gated recurrence over one chunk gives
+ *   o_t = (q_t * e^{b_t})^T S_prev
+ *         + sum_{i in chunk, i <= t} [(q_t * e^{b_t}) . (k_i * e^{-b_i})] v_i
+ *   S   = Diag(e^{b_C}) S_prev + sum_{i in chunk} (k_i * e^{b_C - b_i}) v_i^T
+ * (no feature map or normaliser here).
+ */
+int oracle_gla_fwd_chunked(const double *q, const double *k, const double *v,
+                           const double *log_alpha, const double *init_state,
+                           double *out, double *final_state, long B, long H,
+                           long L, long dk, long dv, long C, int nthreads) {
+    if (B < 0 || H < 0 || L < 0 || dk <= 0 || dv <= 0 || C <= 0) return 1;
+    set_threads(nthreads);
+    long BH = B * H;
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long bh = 0; bh < BH; bh++) {
+        double *S = (double *)calloc((size_t)(dk * dv), sizeof(double));
+        double *b = (double *)malloc((size_t)(C * dk) * sizeof(double));
+        if (!S || !b) {
+#pragma omp atomic write
+            err = 2;
+            free(S); free(b);
+            continue;
+        }
+        if (init_state) memcpy(S, init_state + bh * dk * dv, (size_t)(dk * dv) * sizeof(double));
+        for (long c0 = 0; c0 < L; c0 += C) {
+            long n = (L - c0) < C ? (L - c0) : C;
+            for (long d = 0; d < dk; d++) {
+                double run = 0.0;
+                for (long t = 0; t < n; t++) {
+                    if (log_alpha) run += log_alpha[(bh * L + c0 + t) * dk + d];
+                    b[t * dk + d] = run;
+                }
+            }
+            const double *bC = b + (n - 1) * dk;
+            for (long t = 0; t < n; t++) {
+                const double *qt = q + (bh * L + c0 + t) * dk;
+                double *ot = out + (bh * L + c0 + t) * dv;
+                for (long j = 0; j < dv; j++) {
+                    double acc = 0.0;
+                    for (long d = 0; d < dk; d++) acc += qt[d] * exp(b[t * dk + d]) * S[d * dv + j];
+                    ot[j] = acc;
+                }
+                for (long i = 0; i <= t; i++) {
+                    const double *ki = k + (bh * L + c0 + i) * dk;
+                    const double *vi = v + (bh * L + c0 + i) * dv;
+                    double a = 0.0;
+                    for (long d = 0; d < dk; d++)
+                        a += (qt[d] * exp(b[t * dk + d])) * (ki[d] * exp(-b[i * dk + d]));
+                    for (long j = 0; j < dv; j++) ot[j] += a * vi[j];
+                }
+            }
+            for (long d = 0; d < dk; d++) {
+                double g = exp(bC[d]);
+                for (long j = 0; j < dv; j++) S[d * dv + j] *= g;
+            }
+            for (long i = 0; i < n; i++) {
+                const double *ki = k + (bh * L + c0 + i) * dk;
+                const double *vi = v + (bh * L + c0 + i) * dv;
+                for (long d = 0; d < dk; d++) {
+                    double kh = ki[d] * exp(bC[d] - b[i * dk + d]);
+                    for (long j = 0; j < dv; j++) S[d * dv + j] += kh * vi[j];
+                }
+            }
+        }
+        if (final_state) memcpy(final_state + bh * dk * dv, S, (size_t)(dk * dv) * sizeof(double));
+        free(S); free(b);
+    }
+    return err;
+}

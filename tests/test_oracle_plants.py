@@ -1,0 +1,63 @@
+"""Planted mistakes: each deliberately wrong oracle variant must fail a pin.
+
+The variants are compiled from the oracle source with -DORACLE_PLANT=n into a
+temporary directory (CPU only).  This shows the pins in test_oracle_pins.py
+are sharp enough to catch a dropped term, a wrong index or an off-by-one in
+the decay range.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from test_oracle_pins import _close, _golden, _inputs, _phi, quadratic_masked
+
+
+@pytest.fixture(scope="module")
+def plant_dir(tmp_path_factory):
+    d = str(tmp_path_factory.mktemp("plants"))
+    for n in (1, 2, 3, 4):
+        oracle.build(plant=n, build_dir=d)
+    return d
+
+
+def _fwd(plant, d, *a, **kw):
+    return oracle.gla_fwd(*a, plant=plant, build_dir=d, **kw)
+
+
+def test_plant1_decay_after_write_is_caught(plant_dir):
+    q, k, v, la = _inputs(2, 64, 6, 4)
+    out, _, _ = _fwd(1, plant_dir, q, k, v, la)
+    assert not _close(out, quadratic_masked(q, k, v, la))
+    g = _golden("scalar_halving.json")
+    o, _, _ = _fwd(1, plant_dir, np.array(g["q"], float)[None], np.array(g["k"], float)[None],
+                   np.array(g["v"], float)[None], np.log(np.array(g["alpha"], float))[None])
+    assert not _close(o[0], g["expect_out"], 1e-13)
+
+
+def test_plant2_transposed_contraction_is_caught(plant_dir):
+    g = _golden("per_channel_2x2.json")
+    o, _, _ = _fwd(2, plant_dir, np.array(g["q"], float)[None], np.array(g["k"], float)[None],
+                   np.array(g["v"], float)[None], np.log(np.array(g["alpha"], float))[None])
+    assert not _close(o[0], g["expect_out"], 1e-13)
+    q, k, v, _ = _inputs(4, 29, 6, 6, gate=False)
+    out, _, _ = _fwd(2, plant_dir, q, k, v)
+    S = np.cumsum(np.einsum("bld,blj->bldj", k, v), axis=1)
+    assert not _close(out, np.einsum("bld,bldj->blj", q, S))
+
+
+def test_plant3_dropped_normaliser_is_caught(plant_dir):
+    q, k, v, _ = _inputs(5, 50, 4, 3, gate=False)
+    out, _, _ = _fwd(3, plant_dir, q, k, v, feature_elu1=True, normalize=True)
+    pq, pk = _phi(q), _phi(k)
+    sim = np.tril(pq[0] @ pk[0].T)
+    assert not _close(out[0], (sim @ v[0]) / sim.sum(axis=1, keepdims=True))
+
+
+def test_plant4_exclusive_output_is_caught(plant_dir):
+    q, k, v, _ = _inputs(1, 37, 5, 3, gate=False)
+    out, _, _ = _fwd(4, plant_dir, q, k, v)
+    S = np.cumsum(np.einsum("bld,blj->bldj", k, v), axis=1)
+    assert not _close(out, np.einsum("bld,bldj->blj", q, S))
