@@ -1,0 +1,444 @@
+"""Benchmark of the GB300 causal gated-linear-attention path.
+
+Headline (value): long-context GLA prefill, B=1 H=32 L=65536 dk=128 dv=256,
+chunk 64, bf16 q/k/v, fp32 log alpha, fp32 initial state ~N(0, 0.1), returns
+the final state -- tokens/s for the whole job (all ranks).  One step is one
+gla_fwd call over the whole batch (the fused cumsum-gate / intra-chunk /
+inter-chunk / output kernel).  The same run also measures the decode step
+(256 sequences x H32, d128, fp32 state) as achieved state HBM GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gla|reference]
+
+Under torchrun every rank runs an independent replica on its own seeded
+inputs (no collective on the data path): "scaling": "weak".  Inputs are
+larger than L2 (4.3 GB per prefill step, 537 MB of decode state), so no L2
+flush is needed between timed iterations.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = ("GLA prefill tokens/s & % bf16 tensor peak; decode-step state HBM GB/s (1×GB300)")
+PREFILL = synth.CONFIGS[3]
+DEC = synth.DECODE
+C = 64
+
+
+def prefill_flops(w) -> float:
+    per_head = 2.0 * w.L * C * (w.dk + w.dv) + 4.0 * w.L * w.dk * w.dv
+    return per_head * w.B * w.H
+
+
+def prefill_bytes(w) -> float:
+    """Algorithmic bytes: q, k, v, log alpha read once, out written once, init/final state."""
+    BH, L = w.B * w.H, w.L
+    per_tok = 2 * w.dk + 2 * w.dk + 2 * w.dv + 4 * w.dk + 2 * w.dv
+    states = (2 if w.init_std > 0 else 1) * w.dk * w.dv * 4
+    return float(BH * (L * per_tok + states))
+
+
+def decode_bytes(NS, H, dk, dv) -> float:
+    """Per step: fp32 state read + write, bf16 q/k/v, fp32 log alpha, fp32 out."""
+    return float(NS * H * (2 * dk * dv * 4 + 2 * dk * 2 + dv * 2 + dk * 4 + dv * 4))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("gla_tc.cu", "gla_ptx.cuh", "gla_decode.cu"):
+        with open(os.path.join(ROOT, "causal_gated_linear_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------- oracle leg
+
+def oracle_sample(seconds_target: float = 10.0):
+    """Time the fp64 oracle on a bounded sample of the prefill workload.
+
+    Sample: `nh` heads x `Ls` tokens of the long-context shape (dk 128, dv 256),
+    one OpenMP thread per head.  Returns (tokens/s of the full workload's
+    token definition, cores, sample description, seconds).
+    """
+    import oracle
+    cores = max(1, oracle.max_threads())
+    nh = min(PREFILL.H, max(1, cores))
+    Ls = 256
+    # grow the sample until it takes a noticeable fraction of the target
+    while True:
+        w = synth.with_shape(PREFILL, B=1, H=nh, L=Ls)
+        x = synth.make_prefill(w, heads=list(range(nh)))
+        args = [synth.as_f64(x[n]) for n in ("q", "k", "v", "log_alpha", "init_state")]
+        t0 = time.perf_counter()
+        oracle.gla_fwd(*args, nthreads=cores)
+        dt = time.perf_counter() - t0
+        if dt >= seconds_target / 4 or Ls >= PREFILL.L:
+            break
+        Ls = min(PREFILL.L, Ls * max(2, int(math.ceil(seconds_target / 4 / max(dt, 1e-3)))))
+    token_heads_per_s = nh * Ls / dt
+    tps = token_heads_per_s / (PREFILL.B * PREFILL.H)   # tokens/s of the B*H workload
+    desc = f"{nh} heads x {Ls} tokens of the B1 H32 L65536 dk128 dv256 workload, fp64, {cores} threads"
+    return tps, cores, desc, dt
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    times = []
+    cores, desc = None, None
+    for i in range(args.warmup + args.steps):
+        tps, cores, desc, dt = oracle_sample(seconds_target=args.ref_seconds)
+        if i >= args.warmup:
+            times.append(tps)
+    v = statistics.median(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": PREFILL.name, "B": PREFILL.B, "H": PREFILL.H, "L": PREFILL.L,
+                   "dk": PREFILL.dk, "dv": PREFILL.dv, "chunk": C},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------- GPU legs
+
+def to_dev(x, device):
+    import torch
+    if x is None:
+        return None
+    if x.dtype == np.uint16:
+        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(x).to(device)
+
+
+def bench_prefill(args, device, rank, world):
+    import torch
+
+    import causal_gated_linear_gb300 as gla
+    w = synth.with_shape(PREFILL, seed=PREFILL.seed + 1000 * rank)
+    x = synth.make_prefill(w)
+    BH = w.B * w.H
+    q, k, v = (to_dev(x[n], device) for n in ("q", "k", "v"))
+    la, s0 = to_dev(x["log_alpha"], device), to_dev(x["init_state"], device)
+    out = torch.empty((w.B, w.H, w.L, w.dv), dtype=torch.bfloat16, device=device)
+    fs = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        st = gla.gla_fwd(q, k, v, la, s0, out, fs, w.B, w.H, w.L, w.dk, w.dv, C, stream=stream)
+        if st != 0:
+            raise RuntimeError(gla.gla_status_string(st))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    gla.check(gla.gla_device_error(stream))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    per = []
+    with ClockSampler(device.index) as clk:
+        barrier(world)
+        torch.cuda.synchronize(device)
+        t_wall = time.perf_counter()
+        ev0.record(stream)
+        evs = []
+        for _ in range(args.steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step()
+            b.record(stream)
+            evs.append((a, b))
+        ev1.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(world)
+        wall = time.perf_counter() - t_wall
+    gla.check(gla.gla_device_error(stream))
+    total_ms = ev0.elapsed_time(ev1)
+    per = [a.elapsed_time(b) for a, b in evs]
+    total_ms = max_over_ranks(total_ms, world, device)
+    res = dict(total_ms=total_ms, per_launch_ms=statistics.mean(per), wall_s=wall, clocks=clk.summary())
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    if args.e2e:
+        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        hla, hs0 = la.cpu().pin_memory(), s0.cpu().pin_memory()
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hfs = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hla, hs0))
+        d2h = hout.numel() * hout.element_size() + hfs.numel() * hfs.element_size()
+        dq, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dla, ds0 = torch.empty_like(la), torch.empty_like(s0)
+
+        def e2e_step():
+            for d, h in ((dq, hq), (dk_, hk), (dv_, hv), (dla, hla), (ds0, hs0)):
+                d.copy_(h, non_blocking=True)
+            st = gla.gla_fwd(dq, dk_, dv_, dla, ds0, out, fs, w.B, w.H, w.L, w.dk, w.dv, C, stream=stream)
+            if st != 0:
+                raise RuntimeError(gla.gla_status_string(st))
+            hout.copy_(out, non_blocking=True)
+            hfs.copy_(fs, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(device)
+        ne = max(1, min(args.steps, 3))
+        barrier(world)
+        torch.cuda.synchronize(device)
+        ev0.record(stream)
+        for _ in range(ne):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize(device)
+        e_ms = max_over_ranks(ev0.elapsed_time(ev1), world, device)
+        res["e2e"] = dict(ms_per_step=e_ms / ne, h2d=h2d, d2h=d2h)
+        del hq, hk, hv, hla, hs0, hout, hfs, dq, dk_, dv_, dla, ds0
+    del q, k, v, la, s0, out, fs
+    torch.cuda.empty_cache()
+    return w, BH, res
+
+
+def bench_decode(args, device, rank):
+    import torch
+
+    import causal_gated_linear_gb300 as gla
+    NS, H, dk, dv = DEC["NS"], DEC["H"], DEC["dk"], DEC["dv"]
+    seed = DEC["seed"] + 1000 * rank
+    st = to_dev(synth.decode_state(NS, H, dk, dv, DEC["state_std"], seed), device)
+    pool = []
+    for s in range(args.decode_pool):
+        t = synth.decode_token(NS, H, dk, dv, s, seed, DEC["gate_mean"], DEC["gate_std"])
+        pool.append(tuple(to_dev(t[n], device) for n in ("q", "k", "v", "log_alpha")))
+    out = torch.empty((NS, H, dv), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(i):
+        q, k, v, la = pool[i % len(pool)]
+        r = gla.gla_decode_step(q, k, v, la, st, out, NS, H, dk, dv, stream=stream)
+        if r != 0:
+            raise RuntimeError(gla.gla_status_string(r))
+
+    for i in range(8):
+        step(i)
+    torch.cuda.synchronize(device)
+    n = args.decode_steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(n):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(device)
+    gla.check(gla.gla_device_error(stream))
+    ms = ev0.elapsed_time(ev1) / n
+    return dict(ms_per_step=ms, steps=n, NS=NS, H=H, dk=dk, dv=dv)
+
+
+def run_gla(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    import causal_gated_linear_gb300 as gla
+    gla.load()
+    peaks = load_peaks()
+
+    w, BH, pre = bench_prefill(args, device, rank, world)
+    dec = bench_decode(args, device, rank) if args.decode_steps > 0 else None
+
+    ms = pre["total_ms"] / args.steps
+    tokens = w.B * w.L
+    value = tokens * world * args.steps / (pre["total_ms"] / 1e3)
+    flops = prefill_flops(w)
+    abytes = prefill_bytes(w)
+    lt = pre["per_launch_ms"] / 1e3
+    ach_gbs = abytes / lt / 1e9
+    tflops = flops / lt / 1e12
+    traffic = recorded_traffic("gla_prefill_tc_kernel")
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "dk": w.dk, "dv": w.dv, "chunk": C,
+                   "inputs": "bf16 q/k/v, fp32 log alpha, fp32 init state, out bf16 + final state",
+                   "l2": "inputs (4.3 GB/step) larger than L2: no flush", "parallelism": f"replicas x{world}"},
+        "tflops": tflops,
+        "tensor_frac": tflops / peaks["bf16_tflops"],
+        "roofline": {"bound": "hbm", "achieved": ach_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": "gla_prefill_tc_kernel", "alg_bytes_per_launch": abytes,
+                     "peak_source": peaks["source"]},
+        "gpu_launches": args.steps,
+        "clocks": pre["clocks"],
+    }
+    if dec is not None:
+        dbytes = decode_bytes(dec["NS"], dec["H"], dec["dk"], dec["dv"])
+        gbs = dbytes / (dec["ms_per_step"] / 1e3) / 1e9
+        line["decode"] = {"workload": DEC["name"], "ms_per_step": dec["ms_per_step"], "steps": dec["steps"],
+                          "state_hbm_gbs": gbs, "unit": "GB/s",
+                          "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                       "frac": gbs / peaks["hbm_gbs"],
+                                       "traffic": recorded_traffic("gla_decode_kernel"),
+                                       "kernel": "gla_decode_kernel", "alg_bytes_per_launch": dbytes},
+                          "tokens_per_s": dec["NS"] * dec["H"] / (dec["ms_per_step"] / 1e3) / dec["H"],
+                          "token_pool": f"{args.decode_pool} distinct token sets reused cyclically"}
+    if "e2e" in pre:
+        e = pre["e2e"]
+        line["e2e"] = {"value": tokens * world / (e["ms_per_step"] / 1e3), "unit": "tokens/s",
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
+                       "ms_per_step": e["ms_per_step"]}
+    if rank == 0 and world == 1 and args.cpu_baseline:
+        tps, cores, desc, dt = oracle_sample(args.ref_seconds)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gla", choices=["gla", "reference"])
+    ap.add_argument("--decode-steps", type=int, default=256)
+    ap.add_argument("--decode-pool", type=int, default=8)
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--ref-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # timing rule: at least 3 warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gla(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

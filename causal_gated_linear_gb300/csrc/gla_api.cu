@@ -1,0 +1,221 @@
+// gla_api.cu -- the C ABI declared in include/gla.h: host-side validation,
+// dispatch to the kernels, and the device error word.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include "gla_internal.h"
+
+namespace gla {
+
+// Set (bitwise OR) by kernels whose bounded pipeline waits ran out.
+__device__ unsigned g_err_word;
+
+EncodeTiledFn encode_tiled_fn() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(fn);
+}
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+bool sync_check_enabled() {
+    const char* e = std::getenv("GLA_SYNC_CHECK");
+    return e && e[0] == '1';
+}
+
+unsigned* err_word_ptr() {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return nullptr;
+    return static_cast<unsigned*>(p);
+}
+
+int read_and_clear_error(cudaStream_t s) {
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GLA_ERR_CUDA;
+    unsigned w = 0;
+    if (cudaMemcpyFromSymbol(&w, g_err_word, sizeof(w)) != cudaSuccess) return GLA_ERR_CUDA;
+    if (w) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(zero)) != cudaSuccess) return GLA_ERR_CUDA;
+        return GLA_ERR_TIMEOUT;
+    }
+    return GLA_OK;
+}
+
+int finish(cudaError_t e, cudaStream_t s) {
+    if (e != cudaSuccess) return GLA_ERR_CUDA;
+    if (sync_check_enabled()) {
+        if (cudaGetLastError() != cudaSuccess) return GLA_ERR_CUDA;
+        return read_and_clear_error(s);
+    }
+    return GLA_OK;
+}
+
+int validate_prefill(const gla_fwd_args* a) {
+    if (!a) return GLA_ERR_INVALID;
+    if (a->B < 1 || a->H < 1 || a->L < 0 || a->dk < 1 || a->dv < 1) return GLA_ERR_INVALID;
+    if (a->in_dtype != GLA_DTYPE_BF16 && a->in_dtype != GLA_DTYPE_F32) return GLA_ERR_INVALID;
+    if (a->out_dtype != GLA_DTYPE_BF16 && a->out_dtype != GLA_DTYPE_F32) return GLA_ERR_INVALID;
+    if (a->flags & ~7u) return GLA_ERR_INVALID;
+    if (a->L > 0 && (!a->q || !a->k || !a->v || !a->out)) return GLA_ERR_INVALID;
+    if (a->chunk != 64) return GLA_ERR_UNSUPPORTED;
+    if (a->dk > 256) return GLA_ERR_UNSUPPORTED;
+    const void* ptrs[] = {a->q, a->k, a->v, a->log_alpha, a->init_state, a->init_z, a->out, a->final_state,
+                          a->final_z};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return GLA_ERR_MISALIGNED;
+    const size_t BH = (size_t)a->B * a->H, L = (size_t)a->L;
+    const size_t es = a->in_dtype == GLA_DTYPE_F32 ? 4 : 2, eo = a->out_dtype == GLA_DTYPE_F32 ? 4 : 2;
+    const size_t nq = BH * L * a->dk * es, nv = BH * L * a->dv * es, no = BH * L * a->dv * eo;
+    const size_t nla = BH * L * a->dk * 4, ns = BH * a->dk * a->dv * 4, nz = BH * a->dk * 4;
+    if (overlaps(a->out, no, a->q, nq) || overlaps(a->out, no, a->k, nq) || overlaps(a->out, no, a->v, nv) ||
+        overlaps(a->out, no, a->log_alpha, nla) || overlaps(a->out, no, a->init_state, ns) ||
+        overlaps(a->out, no, a->final_state, ns))
+        return GLA_ERR_INVALID;
+    // final_state may alias init_state exactly, but not partially
+    if (a->final_state && a->init_state && a->final_state != a->init_state &&
+        overlaps(a->final_state, ns, a->init_state, ns))
+        return GLA_ERR_INVALID;
+    if (a->final_z && a->init_z && a->final_z != a->init_z && overlaps(a->final_z, nz, a->init_z, nz))
+        return GLA_ERR_INVALID;
+    return GLA_OK;
+}
+
+}  // namespace
+}  // namespace gla
+
+using namespace gla;
+
+extern "C" {
+
+int gla_fwd_ex(const gla_fwd_args* a, void* stream) {
+    int st = validate_prefill(a);
+    if (st != GLA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    PrefillArgs pa;
+    pa.q = a->q;
+    pa.k = a->k;
+    pa.v = a->v;
+    pa.log_alpha = a->log_alpha;
+    pa.init_state = a->init_state;
+    pa.init_z = a->init_z;
+    pa.out = a->out;
+    pa.final_state = a->final_state;
+    pa.final_z = a->final_z;
+    pa.B = a->B;
+    pa.H = a->H;
+    pa.L = a->L;
+    pa.dk = a->dk;
+    pa.dv = a->dv;
+    pa.in_dtype = a->in_dtype;
+    pa.out_dtype = a->out_dtype;
+    pa.flags = a->flags;
+    const size_t BH = (size_t)a->B * a->H;
+    if (a->L == 0) {
+        // no tokens: the final state is the initial one
+        cudaError_t e = cudaSuccess;
+        const size_t ns = BH * a->dk * a->dv * sizeof(float), nz = BH * a->dk * sizeof(float);
+        if (a->final_state && a->final_state != a->init_state)
+            e = a->init_state ? cudaMemcpyAsync(a->final_state, a->init_state, ns, cudaMemcpyDeviceToDevice, s)
+                              : cudaMemsetAsync(a->final_state, 0, ns, s);
+        if (e == cudaSuccess && a->final_z && (a->flags & GLA_FLAG_NORMALIZE) && a->final_z != a->init_z)
+            e = a->init_z ? cudaMemcpyAsync(a->final_z, a->init_z, nz, cudaMemcpyDeviceToDevice, s)
+                          : cudaMemsetAsync(a->final_z, 0, nz, s);
+        return finish(e, s);
+    }
+    pa.err_word = err_word_ptr();
+    if (!pa.err_word) return GLA_ERR_CUDA;
+    cudaError_t e;
+    if (prefill_tc_supported(pa)) {
+        e = launch_prefill_tc(pa, s);
+    } else {
+        if (BH > 65535) return GLA_ERR_UNSUPPORTED;
+        e = launch_prefill_simt(pa, s);
+    }
+    return finish(e, s);
+}
+
+int gla_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* init_state, void* out,
+            float* final_state, int B, int H, int L, int dk, int dv, int chunk, void* stream) {
+    gla_fwd_args a;
+    std::memset(&a, 0, sizeof(a));
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.log_alpha = log_alpha;
+    a.init_state = init_state;
+    a.out = out;
+    a.final_state = final_state;
+    a.B = B;
+    a.H = H;
+    a.L = L;
+    a.dk = dk;
+    a.dv = dv;
+    a.chunk = chunk;
+    a.in_dtype = GLA_DTYPE_BF16;
+    a.out_dtype = GLA_DTYPE_BF16;
+    a.flags = 0;
+    return gla_fwd_ex(&a, stream);
+}
+
+int gla_decode_step(const void* q, const void* k, const void* v, const float* log_alpha, float* state, float* out,
+                    int B, int H, int dk, int dv, void* stream) {
+    if (B < 1 || H < 1 || dk < 1 || dv < 1) return GLA_ERR_INVALID;
+    if (!q || !k || !v || !state || !out) return GLA_ERR_INVALID;
+    if (dv % 4 != 0 || dv > 512 || dk > 512) return GLA_ERR_UNSUPPORTED;
+    if ((size_t)B * H > 0x7fffffffu) return GLA_ERR_UNSUPPORTED;
+    const void* ptrs[] = {q, k, v, log_alpha, state, out};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return GLA_ERR_MISALIGNED;
+    const size_t BH = (size_t)B * H;
+    const size_t no = BH * dv * 4;
+    if (overlaps(out, no, state, BH * dk * dv * 4) || overlaps(out, no, q, BH * dk * 2) ||
+        overlaps(out, no, k, BH * dk * 2) || overlaps(out, no, v, BH * dv * 2) ||
+        overlaps(out, no, log_alpha, BH * dk * 4))
+        return GLA_ERR_INVALID;
+    DecodeArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.log_alpha = log_alpha;
+    a.state = state;
+    a.out = out;
+    a.B = B;
+    a.H = H;
+    a.dk = dk;
+    a.dv = dv;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish(launch_decode(a, s), s);
+}
+
+int gla_device_error(void* stream) { return read_and_clear_error(static_cast<cudaStream_t>(stream)); }
+
+const char* gla_status_string(int status) {
+    switch (status) {
+        case GLA_OK: return "GLA_OK";
+        case GLA_ERR_INVALID: return "GLA_ERR_INVALID";
+        case GLA_ERR_UNSUPPORTED: return "GLA_ERR_UNSUPPORTED";
+        case GLA_ERR_MISALIGNED: return "GLA_ERR_MISALIGNED";
+        case GLA_ERR_CUDA: return "GLA_ERR_CUDA";
+        case GLA_ERR_TIMEOUT: return "GLA_ERR_TIMEOUT";
+        default: return "GLA_ERR_UNKNOWN";
+    }
+}
+
+const char* gla_version(void) { return "gla-gb300 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// gla_internal.h -- launcher interfaces shared by the C-ABI layer and the
+// kernel translation units (host side only; no torch types).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda.h>
+
+#include "../../include/gla.h"
+
+namespace gla {
+
+struct PrefillArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* log_alpha;
+    const float* init_state;
+    const float* init_z;
+    void* out;
+    float* final_state;
+    float* final_z;
+    int B, H, L, dk, dv;
+    int in_dtype, out_dtype;
+    unsigned flags;
+    unsigned* err_word;  // device address of the error word
+};
+
+struct DecodeArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* log_alpha;
+    float* state;
+    float* out;
+    int B, H, dk, dv;
+};
+
+// fp32 SIMT chunk kernel (any dtype; dk <= 256, dv >= 1).
+cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t s);
+
+// Whether the tensor-core prefill kernel supports this shape/flag combination.
+bool prefill_tc_supported(const PrefillArgs& a);
+
+// tcgen05 chunk kernel (bf16 in; dk in {64,128}; dv multiple of 64).
+// Returns cudaSuccess, or an error from encoding the tensor maps / launching.
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
+
+// Memory-bound decode step.
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+// Driver entry point for cuTensorMapEncodeTiled (resolved through the runtime).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
+}  // namespace gla

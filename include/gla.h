@@ -1,0 +1,140 @@
+/*
+ * gla.h -- C ABI of the GB300 (sm_103a) causal gated-linear-attention library.
+ *
+ * The operation (sources are the pages' titles and sections):
+ *
+ *   "Gated Linear Attention" (garden note), GLA Recurrent Form, eq. block:
+ *       S_t = Diag(alpha_t) S_{t-1} + k_t v_t^T,   alpha_t in (0,1)^{d_k},
+ *   and its flowchart: o_t is q_t applied to the updated state, o_t = S_t^T q_t.
+ *   "linear-attention" blog, Linear attention: the fixed-size state replaces
+ *   the KV cache, o_n = o_n(S_{n-1}, q_n, k_n, v_n); with alpha == 1 the state
+ *   is a running sum of k_i v_i^T (section Prefill: "just a cumulative sum").
+ *   "Gated Linear Attention", Summary / Chunk-Wise Block-Parallel: prefill
+ *   evaluates the same function chunk by chunk, O(L C d + L d^2).
+ *   "Transformers are RNNs" notes, kernel derivation: optional feature map
+ *   phi and normalised form o_t = phi(q_t)^T S_t / phi(q_t)^T z_t.
+ *
+ * Conventions of this library:
+ *   - S is d_k x d_v (rows = key channels, decayed by alpha; columns = value
+ *     channels), stored fp32 row-major per (batch, head).
+ *   - Inputs are head-major: q, k, log_alpha [B][H][L][d_k]; v, out
+ *     [B][H][L][d_v]; states [B][H][d_k][d_v].  All contiguous.
+ *   - log_alpha is the natural log of the gate (fp32, <= 0); the library never
+ *     applies a sigmoid or a temperature: the caller passes log alpha.
+ *   - phi(x) = elu(x) + 1 when GLA_FLAG_FEATURE_ELU1 is set; the normaliser
+ *     z (GLA_FLAG_NORMALIZE) is carried like one extra all-ones value column
+ *     of the state, so it is decayed by alpha exactly like S.
+ *
+ * Ownership and threading: every pointer is caller-owned DEVICE memory
+ * (16-byte aligned).  The library allocates no memory and holds no state
+ * between calls except one device-side error word (see gla_device_error);
+ * calls are asynchronous on the caller's stream.
+ *
+ * Errors: argument validation happens on the host before any launch and
+ * returns a non-zero gla_status without touching the GPU.  Launch failures
+ * return GLA_ERR_CUDA.  Device-side pipeline waits are bounded; a wait that
+ * runs out sets the device error word (GLA_ERR_TIMEOUT) and the kernel
+ * returns early, leaving the outputs undefined.  With the environment
+ * variable GLA_SYNC_CHECK=1 every call synchronises its stream and reports
+ * both kinds of error directly.
+ */
+#ifndef GLA_H
+#define GLA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GLA_OK = 0,
+    GLA_ERR_INVALID = 1,      /* NULL where required, negative size, out/in alias */
+    GLA_ERR_UNSUPPORTED = 2,  /* shape/dtype/chunk combination not implemented */
+    GLA_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned */
+    GLA_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, attribute, ...) */
+    GLA_ERR_TIMEOUT = 5       /* a bounded device-side wait ran out */
+} gla_status;
+
+enum { GLA_DTYPE_BF16 = 0, GLA_DTYPE_F32 = 1 };
+
+enum {
+    GLA_FLAG_FEATURE_ELU1 = 1u,  /* apply phi(x) = elu(x) + 1 to q and k */
+    GLA_FLAG_NORMALIZE = 2u,     /* o_t = phi(q_t)^T S_t / phi(q_t)^T z_t */
+    GLA_FLAG_FORCE_SIMT = 4u     /* use the fp32 SIMT chunk kernel even for bf16 */
+};
+
+/*
+ * gla_fwd -- chunk-wise prefill ("Gated Linear Attention", Chunk-Wise
+ * Block-Parallel; recurrence from GLA Recurrent Form).
+ *
+ *   q, k        bf16 [B][H][L][dk]
+ *   v           bf16 [B][H][L][dv]
+ *   log_alpha   fp32 [B][H][L][dk], or NULL for alpha == 1 (plain linear attention)
+ *   init_state  fp32 [B][H][dk][dv], or NULL for S_{-1} = 0
+ *   out         bf16 [B][H][L][dv]  (o_t = S_t^T q_t, inclusive of token t)
+ *   final_state fp32 [B][H][dk][dv], or NULL; may alias init_state
+ *   chunk       chunk length C; must be 64
+ *   stream      cudaStream_t (NULL = legacy default stream)
+ * Supported: dk in {64, 128}, dv a multiple of 64 (tensor-core kernel); any
+ * other dk, dv in [1, 256] runs on the SIMT kernel.  L >= 0, B, H >= 1.
+ * out must not alias any input.
+ */
+int gla_fwd(const void* q, const void* k, const void* v, const float* log_alpha,
+            const float* init_state, void* out, float* final_state,
+            int B, int H, int L, int dk, int dv, int chunk, void* stream);
+
+/* Extended prefill arguments (same layouts as gla_fwd). */
+typedef struct {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* log_alpha;     /* NULL: alpha == 1 */
+    const float* init_state;    /* NULL: zero */
+    const float* init_z;        /* [B][H][dk], NORMALIZE only; NULL: zero */
+    void* out;
+    float* final_state;         /* NULL: not written */
+    float* final_z;             /* [B][H][dk], NORMALIZE only; NULL: not written */
+    int B, H, L, dk, dv, chunk;
+    int in_dtype;               /* GLA_DTYPE_BF16 or GLA_DTYPE_F32 (q, k, v) */
+    int out_dtype;              /* GLA_DTYPE_BF16 or GLA_DTYPE_F32 */
+    unsigned flags;             /* GLA_FLAG_* */
+} gla_fwd_args;
+
+/*
+ * gla_fwd_ex -- gla_fwd with input/output dtypes, feature map, normaliser and
+ * the normaliser state.  fp32 inputs run on the SIMT kernel in exact fp32
+ * arithmetic (no TF32).  Same validation and error behaviour as gla_fwd.
+ */
+int gla_fwd_ex(const gla_fwd_args* a, void* stream);
+
+/*
+ * gla_decode_step -- one recurrent step per (sequence, head) ("linear-attention"
+ * blog, Linear attention: o_n from S_{n-1}, q_n, k_n, v_n; gate from GLA
+ * Recurrent Form).
+ *
+ *   q, k       bf16 [B][H][dk]     (one token per sequence)
+ *   v          bf16 [B][H][dv]
+ *   log_alpha  fp32 [B][H][dk], or NULL for alpha == 1
+ *   state      fp32 [B][H][dk][dv], updated IN PLACE: S <- Diag(alpha) S + k v^T
+ *   out        fp32 [B][H][dv]: o = S_new^T q
+ * Supported: dv a multiple of 4, dv <= 512, dk in [1, 512].  out must not alias.
+ */
+int gla_decode_step(const void* q, const void* k, const void* v, const float* log_alpha,
+                    float* state, float* out, int B, int H, int dk, int dv, void* stream);
+
+/*
+ * gla_device_error -- synchronise `stream`, read and clear the device error
+ * word that bounded waits set.  Returns GLA_OK, GLA_ERR_TIMEOUT or GLA_ERR_CUDA.
+ */
+int gla_device_error(void* stream);
+
+/* Human-readable name of a gla_status value (static string). */
+const char* gla_status_string(int status);
+
+/* Library version string (static). */
+const char* gla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GLA_H */

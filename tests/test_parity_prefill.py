@@ -1,0 +1,219 @@
+"""GPU parity of the prefill path (gla_fwd / gla_fwd_ex) against the fp64 oracle.
+
+Bar: bf16 inputs -> relative L2 <= 1e-2 and max-abs <= 5e-2 on the outputs and
+the final state; fp32 inputs -> relative L2 <= 1e-5.
+"""
+import numpy as np
+import pytest
+
+import causal_gated_linear_gb300 as gla
+import synth
+from gpu_util import (F32_REL, assert_bf16_close, max_abs, oracle_prefill, rel_l2, run_prefill,
+                      to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    gla.load()
+
+
+def _cfg(base, **kw):
+    return synth.with_shape(synth.CONFIGS[base], **kw)
+
+
+# ------------------------------------------------------------------ fp32 SIMT path
+
+def test_config0_fp32_full():
+    w = synth.CONFIGS[0]
+    x = synth.make_prefill(w)
+    o, s, _ = run_prefill(w, x)
+    ro, rs, _ = oracle_prefill(w, x)
+    assert rel_l2(o, ro) <= F32_REL, rel_l2(o, ro)
+    assert rel_l2(s, rs) <= F32_REL, rel_l2(s, rs)
+
+
+@pytest.mark.parametrize("L,dk,dv", [(1, 32, 32), (63, 16, 48), (130, 64, 40), (65, 200, 24)])
+def test_simt_fp32_shapes(L, dk, dv):
+    w = _cfg(0, B=2, H=2, L=L, dk=dk, dv=dv, seed=11 + L)
+    x = synth.make_prefill(w)
+    o, s, _ = run_prefill(w, x)
+    ro, rs, _ = oracle_prefill(w, x)
+    assert rel_l2(o, ro) <= F32_REL and rel_l2(s, rs) <= F32_REL, (rel_l2(o, ro), rel_l2(s, rs))
+
+
+@pytest.mark.parametrize("L,dk,dv", [(100, 32, 32), (257, 128, 96)])
+def test_simt_bf16_forced(L, dk, dv):
+    w = _cfg(2, B=1, H=3, L=L, dk=dk, dv=dv, init_std=0.1, seed=5 + L)
+    x = synth.make_prefill(w)
+    o, s, _ = run_prefill(w, x, force_simt=True)
+    ro, rs, _ = oracle_prefill(w, x)
+    assert_bf16_close(o, ro, "out")
+    assert_bf16_close(s, rs, "state")
+
+
+# ------------------------------------------------------------------ tcgen05 path
+
+TC_SHAPES = [
+    # (B, H, L, dk, dv, gate, init)
+    (1, 1, 64, 128, 128, True, False),
+    (1, 2, 200, 128, 128, True, True),
+    (2, 1, 65, 64, 64, True, True),
+    (1, 2, 63, 128, 256, True, True),
+    (1, 1, 1, 64, 128, True, False),
+    (2, 2, 130, 64, 192, False, True),
+    (1, 3, 513, 128, 128, False, False),
+]
+
+
+@pytest.mark.parametrize("B,H,L,dk,dv,gate,init", TC_SHAPES)
+def test_tc_shapes(B, H, L, dk, dv, gate, init):
+    w = _cfg(2, B=B, H=H, L=L, dk=dk, dv=dv, gate=gate, init_std=0.1 if init else 0.0,
+             seed=100 + L + dk + dv)
+    x = synth.make_prefill(w)
+    o, s, _ = run_prefill(w, x)
+    ro, rs, _ = oracle_prefill(w, x)
+    assert_bf16_close(o, ro, "out")
+    assert_bf16_close(s, rs, "state")
+
+
+def test_tc_fp32_output():
+    w = _cfg(2, B=1, H=2, L=300, init_std=0.1, seed=77)
+    x = synth.make_prefill(w)
+    o, s, _ = run_prefill(w, x, out_f32=True)
+    ro, rs, _ = oracle_prefill(w, x)
+    assert_bf16_close(o, ro, "out")
+    assert_bf16_close(s, rs, "state")
+
+
+def test_tc_strong_decay_and_long_chunks():
+    """log alpha = logsigmoid(N(3,1)) without temperature: |b_C| reaches ~9 per chunk."""
+    w = _cfg(2, B=1, H=2, L=256, dk=64, dv=64, gate_mean=3.0, gate_std=1.0, gate_temp=1.0, seed=9)
+    x = synth.make_prefill(w)
+    o, s, _ = run_prefill(w, x)
+    ro, rs, _ = oracle_prefill(w, x)
+    assert_bf16_close(o, ro, "out")
+    assert_bf16_close(s, rs, "state")
+
+
+def test_config1_normalised_full():
+    w = synth.CONFIGS[1]
+    x = synth.make_prefill(w)
+    o, s, z = run_prefill(w, x, final_z=True)
+    ro, rs, rz = oracle_prefill(w, x)
+    assert_bf16_close(o, ro, "out")
+    assert rel_l2(s, rs) <= 1e-2 and rel_l2(z, rz) <= 1e-2
+
+
+def test_config1_normalised_tail_and_resume():
+    w = _cfg(1, B=1, H=2, L=150, seed=31)
+    x = synth.make_prefill(w)
+    o, s, z = run_prefill(w, x, final_z=True)
+    ro, rs, rz = oracle_prefill(w, x)
+    assert_bf16_close(o, ro, "out")
+    assert rel_l2(z, rz) <= 1e-2, rel_l2(z, rz)
+    # resume from (S, z) on a second segment
+    w2 = _cfg(1, B=1, H=2, L=70, seed=32)
+    x2 = synth.make_prefill(w2)
+    x2["init_state"] = s.astype(np.float32)
+    o2, _, _ = run_prefill(w2, x2, init_z=z.astype(np.float32))
+    ro2, _, _ = oracle_prefill(w2, x2, init_z=z)
+    assert_bf16_close(o2, ro2, "resumed out")
+
+
+def test_config2_full_sampled():
+    w = synth.CONFIGS[2]
+    x = synth.make_prefill(w)
+    o, s, _ = run_prefill(w, x)
+    heads = [0, 37, 64, 127]
+    xs = synth.make_prefill(w, heads=heads)
+    ro, rs, _ = oracle_prefill(w, xs)
+    o = o.reshape(w.B * w.H, w.L, w.dv)[heads]
+    s = s.reshape(w.B * w.H, w.dk, w.dv)[heads]
+    assert_bf16_close(o, ro, "out")
+    assert_bf16_close(s, rs, "state")
+
+
+def test_config3_full_sampled():
+    import torch
+    w = synth.CONFIGS[3]
+    x = synth.make_prefill(w)
+    q, k, v = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"])
+    la, s0 = to_dev(x["log_alpha"]), to_dev(x["init_state"])
+    del x
+    out = torch.empty((1, 32, w.L, w.dv), dtype=torch.bfloat16, device="cuda:0")
+    fs = torch.empty((1, 32, w.dk, w.dv), dtype=torch.float32, device="cuda:0")
+    gla.check(gla.gla_fwd(q, k, v, la, s0, out, fs, 1, 32, w.L, w.dk, w.dv, 64))
+    torch.cuda.synchronize()
+    gla.check(gla.gla_device_error())
+    heads = [0, 17, 31]
+    xs = synth.make_prefill(w, heads=heads)
+    ro, rs, _ = oracle_prefill(w, xs)
+    o = out[0, heads].float().cpu().numpy()
+    s = fs[0, heads].cpu().numpy()
+    assert_bf16_close(o, ro, "out")
+    assert_bf16_close(s, rs, "state")
+
+
+# ------------------------------------------------------------------ properties
+
+def test_split_resume_on_gpu():
+    w = _cfg(2, B=1, H=2, L=300, init_std=0.1, seed=41)
+    x = synth.make_prefill(w)
+    o, s, _ = run_prefill(w, x)
+    for L1 in (128, 77):
+        w1 = _cfg(2, B=1, H=2, L=L1)
+        x1 = {kk: (vv[:, :, :L1] if kk in ("q", "k", "v", "log_alpha") else vv) for kk, vv in x.items()}
+        o1, s1, _ = run_prefill(w1, x1)
+        w2 = _cfg(2, B=1, H=2, L=300 - L1)
+        x2 = {kk: (vv[:, :, L1:] if kk in ("q", "k", "v", "log_alpha") else vv) for kk, vv in x.items()}
+        x2["init_state"] = s1.astype(np.float32)
+        o2, s2, _ = run_prefill(w2, x2)
+        assert_bf16_close(np.concatenate([o1, o2], axis=2), o, "split out")
+        assert_bf16_close(s2, s, "split state")
+
+
+def test_deterministic_bitwise():
+    w = _cfg(2, B=2, H=2, L=333, init_std=0.1, seed=51)
+    x = synth.make_prefill(w)
+    a = run_prefill(w, x)
+    b = run_prefill(w, x)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_final_state_may_alias_initial_state():
+    import torch
+    w = _cfg(2, B=1, H=2, L=100, init_std=0.1, seed=61)
+    x = synth.make_prefill(w)
+    ro, rs, _ = oracle_prefill(w, x)
+    q, k, v, la = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"]), to_dev(x["log_alpha"])
+    st = to_dev(x["init_state"])
+    out = torch.empty((1, 2, 100, 128), dtype=torch.bfloat16, device="cuda:0")
+    gla.check(gla.gla_fwd(q, k, v, la, st, out, st, 1, 2, 100, 128, 128, 64))
+    torch.cuda.synchronize()
+    assert_bf16_close(st.cpu().numpy(), rs, "in-place state")
+    assert_bf16_close(out.float().cpu().numpy(), ro, "out")
+
+
+def test_empty_sequence_copies_state():
+    import torch
+    s0 = torch.randn(2, 3, 64, 64, device="cuda:0")
+    fs = torch.full_like(s0, float("nan"))
+    gla.check(gla.gla_fwd(None, None, None, None, s0, None, fs, 2, 3, 0, 64, 64, 64))
+    torch.cuda.synchronize()
+    assert torch.equal(fs, s0)
+    gla.check(gla.gla_fwd(None, None, None, None, None, None, fs, 2, 3, 0, 64, 64, 64))
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(fs).item() == 0
+
+
+def test_no_gate_matches_cumsum_closed_form():
+    """alpha == 1 on the GPU: the final state equals K^T V in fp64 (closed form)."""
+    w = _cfg(2, B=1, H=2, L=192, gate=False, seed=71)
+    x = synth.make_prefill(w)
+    _, s, _ = run_prefill(w, x)
+    k = synth.as_f64(x["k"]).reshape(2, 192, 128)
+    v = synth.as_f64(x["v"]).reshape(2, 192, 128)
+    ref = np.einsum("bld,blj->bdj", k, v)
+    assert_bf16_close(s.reshape(2, 128, 128), ref, "K^T V")
