@@ -153,7 +153,8 @@ def dist_env():
     return rank, world, local
 
 
-def max_over_ranks(x: float, world: int, device) -> float:
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Slowest rank's value (timing is max over ranks); `device` may be CPU under gloo."""
     if world == 1:
         return x
     import torch
@@ -161,6 +162,11 @@ def max_over_ranks(x: float, world: int, device) -> float:
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: units processed by all ranks / slowest rank's time."""
+    return units_per_rank * world * steps / (max_ms / 1e3)
 
 
 def barrier(world):
@@ -370,7 +376,7 @@ def run_gla(args):
 
     ms = pre["total_ms"] / args.steps
     tokens = w.B * w.L
-    value = tokens * world * args.steps / (pre["total_ms"] / 1e3)
+    value = job_throughput(tokens, args.steps, world, pre["total_ms"])
     flops = prefill_flops(w)
     abytes = prefill_bytes(w)
     lt = pre["per_launch_ms"] / 1e3
