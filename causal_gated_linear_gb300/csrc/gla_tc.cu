@@ -13,44 +13,72 @@
 //   S    = S' + Kh^T V
 // which is exactly the recurrence, since (Qh_t . Kh_i) carries e^{b_t - b_i}.
 //
-// One CTA owns one (batch*head, 128-column slice of d_v) for the whole
-// sequence.  The state is kept TRANSPOSED in tensor memory, S^T (lane = value
-// column j, column = key channel d, fp32), so that every state/output
-// product has M = 128 value columns:
-//   MMA_A   A[t][i]  = Qh Kh^T            M=128 (rows 64..127 unused), N=64, K=dk
-//   MMA_dS  S^T     += V^T Kh             M=128, N=dk, K=64      (V, Kh MN-major)
-//   MMA_Oi  O^T      = S'^T_bf16 Qh^T     M=128, N=64, K=dk      (A from TMEM)
-//   MMA_Oa  O^T     += V^T P^T            M=128, N=64, K=64      (P = tril(A), bf16)
-// Warp roles (16 warps): 0-3 gate (cumsum + factors, in place on the q/k
-// tiles), 4-7 state (decay S^T, write the bf16 copy), 8-11 output (O^T ->
-// global), 12-13 P (mask A -> bf16 P in shared memory), 14 TMA producer,
-// 15 MMA issuer and TMEM owner.  Every pipeline wait is bounded.
+// One CTA owns one (batch*head, DVT-column slice of d_v) for the whole
+// sequence (DVT = 64 or 128, chosen by the host so that enough CTAs exist to
+// cover the GPU).  The state is kept TRANSPOSED in tensor memory, S^T (lane =
+// value column j, column = key channel d, fp32), so that every state/output
+// product has M = DVT:
+//   MMA_A   A[t][i] = Qh Kh^T          M=128 (rows 64..127 unused), N=64, K=dk
+//   MMA_dS  dS^T    = V^T Kh           M=DVT, N=dk, K=64  (V, Kh MN-major; own buffer)
+//   MMA_Oi  O^T     = S'^T_bf16 Qh^T   M=DVT, N=64, K=dk  (A operand from TMEM)
+//   MMA_Oa  O^T    += V^T P^T          M=DVT, N=64, K=64  (P = tril(A) in bf16)
+// The state warps apply S' = Diag(e^{b_C}) S, write the bf16 copy of S' and
+// S = S' + dS in fp32, entirely in TMEM; no state ever leaves the chip
+// between chunks.  With M = 64 the accumulator rows live in TMEM lanes
+// 16q + r -> lane 32q + r (r < 16) of each 32-lane quarter q.
+//
+// Warp roles (24 warps): 0-7 gate (cumsum with a cross-warp segment
+// exchange, factors written in place over the TMA-landed q/k tiles), 8-15
+// state, 16-19 output (TMEM -> shared staging -> TMA bulk store), 20-21 P
+// (mask A -> bf16 P), 22 TMA producer, 23 MMA issuer and TMEM owner.  Every
+// pipeline wait is bounded (gla_ptx.cuh).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <climits>
+#include <cstdlib>
+#include <cstring>
 
 #include "gla_internal.h"
 #include "gla_ptx.cuh"
 
+// Optional per-role timestamps of CTA 0 (compiled in only with -DGLA_TRACE).
+#ifdef GLA_TRACE
+__device__ unsigned long long* g_gla_trace;
+#define GLA_TRACE_POINT(ev, c)                                                           \
+    do {                                                                                 \
+        if (blockIdx.x == 0 && g_gla_trace && (c) < 512) g_gla_trace[(ev) * 512 + (c)] = \
+            gla::globaltimer();                                                          \
+    } while (0)
+#else
+#define GLA_TRACE_POINT(ev, c) \
+    do {                       \
+    } while (0)
+#endif
+
 namespace gla {
 namespace {
 
-constexpr int C = 64;      // chunk length (tokens)
-constexpr int DVT = 128;   // value columns per CTA (MMA M)
-constexpr int NS = 3;      // q/k stages (hold Qh/Kh until the chunk's MMAs finish)
-constexpr int NL = 2;      // log-alpha stages
-constexpr int NV = 2;      // v stages
-constexpr int kThreads = 512;
-
-constexpr int W_STATE0 = 4, W_OUT0 = 8, W_P0 = 12, W_TMA = 14, W_MMA = 15;
+constexpr int C = 64;  // chunk length (tokens)
+constexpr int NS = 3;  // q/k stages (hold Qh/Kh until the chunk's MMAs finish)
+constexpr int NL = 2;  // log-alpha stages
+constexpr int kWarps = 24;
+constexpr int kThreads = kWarps * 32;
+constexpr int W_STATE0 = 8, W_OUT0 = 16, W_P0 = 20, W_TMA = 22, W_MMA = 23;
+constexpr int kGateThreads = 256;
 
 // tensor-memory column map (512 columns allocated)
 constexpr uint32_t TM_S = 0;     // S^T fp32, dk columns
-constexpr uint32_t TM_SB = 128;  // 2 x bf16 copies of S'^T, dk/2 columns each
-constexpr uint32_t TM_O = 256;   // 2 x O^T fp32, 64 columns each
-constexpr uint32_t TM_A = 384;   // 2 x A fp32, 64 columns each
+constexpr uint32_t TM_DS = 128;  // dS^T fp32, dk columns
+constexpr uint32_t TM_SB = 256;  // 2 x bf16 copies of S'^T, dk/2 columns each
+constexpr uint32_t TM_O = 384;   // O^T fp32, 64 columns
+constexpr uint32_t TM_A = 448;   // A fp32, 64 columns
 constexpr uint32_t TM_COLS = 512;
+
+template <int DVT>
+struct VRing {
+    static constexpr int N = DVT == 64 ? 3 : 2;
+};
 
 enum {
     B_QK_FULL = 0,
@@ -59,42 +87,50 @@ enum {
     B_LA_FULL = B_QK_EMPTY + NS,
     B_LA_EMPTY = B_LA_FULL + NL,
     B_V_FULL = B_LA_EMPTY + NL,
-    B_V_EMPTY = B_V_FULL + NV,
-    B_A_FULL = B_V_EMPTY + NV,
-    B_A_EMPTY = B_A_FULL + 2,
-    B_P_FULL = B_A_EMPTY + 2,
-    B_P_EMPTY = B_P_FULL + 2,
-    B_S_READY = B_P_EMPTY + 2,
-    B_S_FULL = B_S_READY + 1,
-    B_O_FULL = B_S_FULL + 1,
-    B_O_EMPTY = B_O_FULL + 2,
-    B_DRAIN = B_O_EMPTY + 2,
-    B_COUNT = B_DRAIN + 1
+    B_V_EMPTY = B_V_FULL + 3,
+    B_A_FULL = B_V_EMPTY + 3,
+    B_A_EMPTY,
+    B_P_FULL,
+    B_P_EMPTY,
+    B_DS_FULL,
+    B_DS_EMPTY,
+    B_S_READY,
+    B_SB_EMPTY,  // 2
+    B_O_FULL = B_SB_EMPTY + 2,
+    B_O_EMPTY,
+    B_DRAIN,
+    B_COUNT
 };
 
-template <int DK>
+template <int DK, int DVT>
 struct Layout {
-    static constexpr int QB = DK * C * 2;          // one bf16 [64][DK] tile (DK/64 swizzle atoms)
+    static constexpr int NV = VRing<DVT>::N;
+    static constexpr int QB = DK * C * 2;        // one bf16 [64][DK] tile (DK/64 swizzle atoms)
     static constexpr int STAGE_QK = 2 * QB;
-    static constexpr int LAB = DK * C * 4;         // fp32 [64][DK]
-    static constexpr int VB = DVT * C * 2;         // bf16 [64][128] as two 64-column atoms
-    static constexpr int PB = C * C * 2;           // bf16 [64][64]
-    static constexpr int SEG = 128 / (DK / 2);     // token segments in the gate mapping
+    static constexpr int LAB = DK * C * 4;       // fp32 [64][DK]
+    static constexpr int VB = DVT * C * 2;       // bf16 [64][DVT] as DVT/64 atoms of 64 columns
+    static constexpr int PB = C * C * 2;         // bf16 [64][64]
+    static constexpr int OSB = C * DVT * 2;      // output staging, DVT/64 blocks of [64][64] bf16
+    static constexpr int QUADS = DK / 4;
+    static constexpr int SEG = kGateThreads / QUADS;  // token segments in the gate mapping
+    static constexpr int TPS = C / SEG;               // tokens per segment
     static constexpr int off_qk = 0;
     static constexpr int off_la = off_qk + NS * STAGE_QK;
     static constexpr int off_v = off_la + NL * LAB;
     static constexpr int off_p = off_v + NV * VB;
-    static constexpr int off_gamma = off_p + 2 * PB;
+    static constexpr int off_ost = off_p + PB;
+    static constexpr int off_gamma = off_ost + OSB;
     static constexpr int off_segtot = off_gamma + NS * DK * 4;
     static constexpr int off_den = off_segtot + 2 * SEG * DK * 4;
-    static constexpr int off_bar = off_den + 2 * C * 4;
+    static constexpr int off_bar = off_den + C * 4;
     static constexpr int off_misc = off_bar + B_COUNT * 8;
     static constexpr int total = off_misc + 16;
-    static constexpr int alloc = total + 1024;
+    static constexpr int alloc = total + 1008;  // round-up to 1024 from a >= 16-byte aligned base
+    static_assert(alloc <= 232448, "shared memory budget");
 };
 
 struct TcParams {
-    CUtensorMap tm_q, tm_k, tm_la, tm_v;
+    CUtensorMap tm_q, tm_k, tm_la, tm_v, tm_out;
     const float* init_state;
     const float* init_z;
     void* out;
@@ -106,9 +142,18 @@ struct TcParams {
     int out_f32;
 };
 
-template <int DK, bool GATE>
+// TMEM lane <-> value column within the CTA's DVT slice.  M = 128: lane j is
+// column j.  M = 64: column 16q + r sits in lane 32q + r (r < 16).
+template <int DVT>
+__device__ __forceinline__ int lane_to_col(int warp_quarter, int lane) {
+    if (DVT == 128) return warp_quarter * 32 + lane;
+    return lane < 16 ? warp_quarter * 16 + lane : -1;
+}
+
+template <int DK, int DVT, bool GATE>
 __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __grid_constant__ TcParams p) {
-    using Ly = Layout<DK>;
+    using Ly = Layout<DK, DVT>;
+    constexpr int NV = Ly::NV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -128,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
     const int L = p.L, dv = p.dv, N = p.nchunks;
     const bool norm = p.flags & GLA_FLAG_NORMALIZE;
     const bool elu = p.flags & GLA_FLAG_FEATURE_ELU1;
-    // value lanes holding real columns; with the normaliser (dv == 64) lane 64 holds z
+    // value columns holding real data; with the normaliser (dv == 64, DVT == 128) column 64 holds z
     const int jvalid = min(DVT, dv - j0);
     const int nvb = jvalid / 64;  // TMA-loaded 64-column blocks of V
 
@@ -136,27 +181,28 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; i++) {
             mbar_init(bar(B_QK_FULL + i), 1);
-            mbar_init(bar(B_QK_GATED + i), 4);
+            mbar_init(bar(B_QK_GATED + i), 8);
             mbar_init(bar(B_QK_EMPTY + i), 1);
         }
         for (int i = 0; i < NL; i++) {
             mbar_init(bar(B_LA_FULL + i), 1);
-            mbar_init(bar(B_LA_EMPTY + i), 4);
+            mbar_init(bar(B_LA_EMPTY + i), 8);
         }
-        for (int i = 0; i < NV; i++) {
+        for (int i = 0; i < 3; i++) {
             mbar_init(bar(B_V_FULL + i), 1);
             mbar_init(bar(B_V_EMPTY + i), 1);
         }
-        for (int i = 0; i < 2; i++) {
-            mbar_init(bar(B_A_FULL + i), 1);
-            mbar_init(bar(B_A_EMPTY + i), 2);
-            mbar_init(bar(B_P_FULL + i), 2);
-            mbar_init(bar(B_P_EMPTY + i), 1);
-            mbar_init(bar(B_O_FULL + i), 1);
-            mbar_init(bar(B_O_EMPTY + i), 4);
-        }
-        mbar_init(bar(B_S_READY), 4);
-        mbar_init(bar(B_S_FULL), 1);
+        mbar_init(bar(B_A_FULL), 1);
+        mbar_init(bar(B_A_EMPTY), 2);
+        mbar_init(bar(B_P_FULL), 2);
+        mbar_init(bar(B_P_EMPTY), 1);
+        mbar_init(bar(B_DS_FULL), 1);
+        mbar_init(bar(B_DS_EMPTY), 8);
+        mbar_init(bar(B_S_READY), 8);
+        mbar_init(bar(B_SB_EMPTY), 1);
+        mbar_init(bar(B_SB_EMPTY + 1), 1);
+        mbar_init(bar(B_O_FULL), 1);
+        mbar_init(bar(B_O_EMPTY), 4);
         mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0;
         mbar_fence_init();
@@ -165,8 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
         tmem_alloc(smem_u32(tmem_slot), TM_COLS);
         tmem_relinquish();
     }
-    // V columns the TMA never writes: zero, plus the all-ones normaliser column
-    if (nvb < 2) {
+    // V columns the TMA never writes (dv == 64 on a 128-column tile): zero,
+    // plus the all-ones normaliser column
+    if (DVT == 128 && nvb < 2) {
         for (int idx = threadIdx.x; idx < NV * C * 64; idx += kThreads) {
             const int st = idx / (C * 64), rem = idx % (C * 64);
             const int row = rem / 64, col = rem % 64;
@@ -183,263 +230,320 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
     const uint32_t tmem = *tmem_slot;
     const uint32_t lane_field = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
-    // track outstanding TMA loads for the teardown (producer lane only)
-    int last_issued = -1;
+    int last_issued = -1;  // producer: last chunk whose loads were issued
 
-    if (warp < 4) {
+    if (warp < W_STATE0) {
         // ============================================================ gate
-        constexpr int PAIRS = DK / 2;
-        constexpr int SEG = Ly::SEG;
-        constexpr int TPS = C / SEG;
+        constexpr int QUADS = Ly::QUADS, SEG = Ly::SEG, TPS = Ly::TPS;
+        constexpr int G = TPS < 4 ? TPS : 4;  // tokens per factor group
         const int gt = threadIdx.x;
-        const int pr = gt % PAIRS, h = gt / PAIRS;
-        const int ch = 2 * pr;
+        const int quad = gt % QUADS, seg = gt / QUADS;
+        const int ch = 4 * quad;
         const int atom = ch >> 6, col = ch & 63;
         for (int c = 0; c < N; c++) {
             const int s = c % NS, l = c % NL;
             bool ok = true;
             if (GATE) ok = mbar_wait(bar(B_LA_FULL + l), (c / NL) & 1, abort_flag, p.err);
             if (ok) ok = mbar_wait(bar(B_QK_FULL + s), (c / NS) & 1, abort_flag, p.err);
-            if (!GATE && !__all_sync(0xffffffffu, ok)) break;
-            uint8_t* qt = sm + Ly::off_qk + s * Ly::STAGE_QK + atom * 8192;
-            uint8_t* kt = qt + Ly::QB;
-            const int nval = min(C, L - c * C);
-            float b0[TPS], b1[TPS];
-            float off0 = 0.f, off1 = 0.f, tot0 = 0.f, tot1 = 0.f;
+            float b[TPS][4];
+            float off[4] = {0.f, 0.f, 0.f, 0.f}, tot[4] = {0.f, 0.f, 0.f, 0.f};
             if (GATE) {
-                const float* la = reinterpret_cast<const float*>(sm + Ly::off_la + l * Ly::LAB);
-                float r0 = 0.f, r1 = 0.f;
                 float* st = segtot + (c & 1) * SEG * DK;
                 if (ok) {
+                    const float* la = reinterpret_cast<const float*>(sm + Ly::off_la + l * Ly::LAB);
+                    float4 x[TPS];
+#pragma unroll
+                    for (int i = 0; i < TPS; i++)
+                        x[i] = *reinterpret_cast<const float4*>(la + (seg * TPS + i) * DK + ch);
+                    float r[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int i = 0; i < TPS; i++) {
-                        const float2 x = *reinterpret_cast<const float2*>(la + (h * TPS + i) * DK + ch);
-                        r0 += x.x;
-                        r1 += x.y;
-                        b0[i] = r0;
-                        b1[i] = r1;
+                        r[0] += x[i].x;
+                        r[1] += x[i].y;
+                        r[2] += x[i].z;
+                        r[3] += x[i].w;
+#pragma unroll
+                        for (int e = 0; e < 4; e++) b[i][e] = r[e];
                     }
-                    st[h * DK + ch] = r0;
-                    st[h * DK + ch + 1] = r1;
+                    *reinterpret_cast<float4*>(st + seg * DK + ch) = make_float4(r[0], r[1], r[2], r[3]);
                 }
-                // exchange of segment totals doubles as the gate role's agreement to go on
-                if (!bar_red_and(1, 128, ok)) break;
+                // the segment-total exchange doubles as the gate role's agreement to go on
+                if (!bar_red_and(1, kGateThreads, ok)) break;
 #pragma unroll
                 for (int g = 0; g < SEG; g++) {
-                    const float u0 = st[g * DK + ch], u1 = st[g * DK + ch + 1];
-                    if (g < h) {
-                        off0 += u0;
-                        off1 += u1;
+                    const float4 u = *reinterpret_cast<const float4*>(st + g * DK + ch);
+                    if (g < seg) {
+                        off[0] += u.x;
+                        off[1] += u.y;
+                        off[2] += u.z;
+                        off[3] += u.w;
                     }
-                    tot0 += u0;
-                    tot1 += u1;
+                    tot[0] += u.x;
+                    tot[1] += u.y;
+                    tot[2] += u.z;
+                    tot[3] += u.w;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_LA_EMPTY + l));
-                if (h == 0) {
-                    gamma[s * DK + ch] = __expf(tot0);
-                    gamma[s * DK + ch + 1] = __expf(tot1);
-                }
-            }
-            if (GATE || elu || nval < C) {
+                if (seg == 0)
+                    *reinterpret_cast<float4*>(gamma + s * DK + ch) =
+                        make_float4(__expf(tot[0]), __expf(tot[1]), __expf(tot[2]), __expf(tot[3]));
 #pragma unroll
-                for (int i = 0; i < TPS; i++) {
-                    const int t = h * TPS + i;
-                    const uint32_t o = sw128_offset(t, col);
-                    uint32_t* qp = reinterpret_cast<uint32_t*>(qt + o);
-                    uint32_t* kp = reinterpret_cast<uint32_t*>(kt + o);
-                    float2 qv = unpack_bf16x2(*qp), kv = unpack_bf16x2(*kp);
-                    if (elu) {
-                        qv.x = elu1(qv.x);
-                        qv.y = elu1(qv.y);
-                        kv.x = elu1(kv.x);
-                        kv.y = elu1(kv.y);
+                for (int e = 0; e < 4; e++) off[e] -= tot[e];  // d = b_t + off - tot = b_t - b_C
+            } else {
+                if (!bar_red_and(1, kGateThreads, ok)) break;
+            }
+            if (threadIdx.x == 0) GLA_TRACE_POINT(2, c);
+            const int nval = min(C, L - c * C);
+            if (GATE || elu || nval < C) {
+                uint8_t* qt = sm + Ly::off_qk + s * Ly::STAGE_QK + atom * 8192;
+                uint8_t* kt = qt + Ly::QB;
+#pragma unroll
+                for (int i0 = 0; i0 < TPS; i0 += G) {
+                    uint2 qr[G], kr[G];
+#pragma unroll
+                    for (int u = 0; u < G; u++) {
+                        const uint32_t o = sw128_offset(seg * TPS + i0 + u, col);
+                        qr[u] = *reinterpret_cast<const uint2*>(qt + o);
+                        kr[u] = *reinterpret_cast<const uint2*>(kt + o);
                     }
-                    if (GATE) {
-                        const float d0 = (b0[i] + off0) - tot0;  // b_t - b_C >= 0
-                        const float d1 = (b1[i] + off1) - tot1;
-                        qv.x *= __expf(d0);
-                        qv.y *= __expf(d1);
-                        kv.x *= __expf(-d0);
-                        kv.y *= __expf(-d1);
+#pragma unroll
+                    for (int u = 0; u < G; u++) {
+                        const int t = seg * TPS + i0 + u;
+                        const float2 q01 = unpack_bf16x2(qr[u].x), q23 = unpack_bf16x2(qr[u].y);
+                        const float2 k01 = unpack_bf16x2(kr[u].x), k23 = unpack_bf16x2(kr[u].y);
+                        float qv[4] = {q01.x, q01.y, q23.x, q23.y};
+                        float kv[4] = {k01.x, k01.y, k23.x, k23.y};
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            if (elu) {
+                                qv[e] = elu1(qv[e]);
+                                kv[e] = elu1(kv[e]);
+                            }
+                            if (GATE) {
+                                const float d = b[i0 + u][e] + off[e];  // b_t - b_C >= 0
+                                qv[e] *= __expf(d);
+                                kv[e] *= __expf(-d);
+                            }
+                            if (t >= nval) {  // padding tokens must not write the state (elu(0)+1 != 0)
+                                qv[e] = 0.f;
+                                kv[e] = 0.f;
+                            }
+                        }
+                        qr[u] = make_uint2(pack_bf16x2(qv[0], qv[1]), pack_bf16x2(qv[2], qv[3]));
+                        kr[u] = make_uint2(pack_bf16x2(kv[0], kv[1]), pack_bf16x2(kv[2], kv[3]));
                     }
-                    if (t >= nval) {  // padding tokens must not write the state (elu(0)+1 != 0)
-                        qv = make_float2(0.f, 0.f);
-                        kv = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int u = 0; u < G; u++) {
+                        const uint32_t o = sw128_offset(seg * TPS + i0 + u, col);
+                        *reinterpret_cast<uint2*>(qt + o) = qr[u];
+                        *reinterpret_cast<uint2*>(kt + o) = kr[u];
                     }
-                    *qp = pack_bf16x2(qv.x, qv.y);
-                    *kp = pack_bf16x2(kv.x, kv.y);
                 }
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_QK_GATED + s));
+            if (threadIdx.x == 0) GLA_TRACE_POINT(3, c);
         }
     } else if (warp < W_OUT0) {
         // ============================================================ state
-        const int j = threadIdx.x - W_STATE0 * 32;
+        constexpr int COLS = DK / 2;  // key channels per warp (two warps per lane quarter)
+        const int half = (warp - W_STATE0) >> 2;
+        const int cbase = half * COLS;
+        const int jl = lane_to_col<DVT>(warp & 3, lane);  // column in the slice, -1 if unused lane
+        const int j = j0 + jl;
         const uint32_t tS = tmem + lane_field + TM_S;
-        const float* s0 = p.init_state ? p.init_state + (long)bh * DK * dv + j0 + j : nullptr;
-        for (int g = 0; g < DK / 32; g++) {
-            uint32_t r[32];
+        const uint32_t tD = tmem + lane_field + TM_DS;
+        {
+            const float* s0 =
+                (p.init_state && jl >= 0 && jl < jvalid) ? p.init_state + (long)bh * DK * dv + j : nullptr;
+            const bool zl = norm && jl == 64;
+            for (int g = 0; g < COLS / 16; g++) {
+                uint32_t r[16];
 #pragma unroll
-            for (int i = 0; i < 32; i++) {
-                float x = 0.f;
-                const int d = g * 32 + i;
-                if (j < jvalid) {
-                    if (s0) x = s0[(long)d * dv];
-                } else if (norm && j == 64 && p.init_z) {
-                    x = p.init_z[(long)bh * DK + d];
+                for (int i = 0; i < 16; i++) {
+                    const int d = cbase + g * 16 + i;
+                    float x = 0.f;
+                    if (s0)
+                        x = s0[(long)d * dv];
+                    else if (zl && p.init_z)
+                        x = p.init_z[(long)bh * DK + d];
+                    r[i] = __float_as_uint(x);
                 }
-                r[i] = __float_as_uint(x);
+                tmem_st16(tS + cbase + g * 16, r);
             }
-            tmem_st32(tS + g * 32, r);
+            tmem_wait_st();
         }
-        tmem_wait_st();
         bool ok = true;
-        for (int c = 0; c < N && ok; c++) {
+        for (int c = 0; c < N; c++) {
             const int s = c % NS;
-            if (GATE && !mbar_wait_warp(bar(B_QK_GATED + s), (c / NS) & 1, abort_flag, p.err)) { ok = false; break; }
-            if (c > 0 && !mbar_wait_warp(bar(B_S_FULL), (c - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+            ok = mbar_wait_warp(bar(B_DS_FULL), c & 1, abort_flag, p.err);
+            if (ok && GATE) ok = mbar_wait_warp(bar(B_QK_GATED + s), (c / NS) & 1, abort_flag, p.err);
+            if (ok) ok = mbar_wait_warp(bar(B_SB_EMPTY + (c & 1)), ((c >> 1) & 1) ^ 1, abort_flag, p.err);
+            if (!ok) break;
             tc_fence_after();
+            if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(4, c);
             const uint32_t tSB = tmem + lane_field + TM_SB + (c & 1) * (DK / 2);
-            for (int g = 0; g < DK / 32; g++) {
-                uint32_t r[32];
-                tmem_ld32(tS + g * 32, r);
+#pragma unroll 1
+            for (int g = 0; g < COLS / 16; g++) {
+                const int c0 = cbase + g * 16;
+                uint32_t rs[16], rd[16];
+                tmem_ld16(tS + c0, rs);
+                tmem_ld16(tD + c0, rd);
                 tmem_wait_ld();
-                if (GATE) {
-                    const float* gm = gamma + s * DK + g * 32;
+                uint32_t pk[8];
 #pragma unroll
-                    for (int i = 0; i < 32; i++) r[i] = __float_as_uint(__uint_as_float(r[i]) * gm[i]);
-                    tmem_st32(tS + g * 32, r);
+                for (int i = 0; i < 16; i += 2) {
+                    float s0v = __uint_as_float(rs[i]), s1v = __uint_as_float(rs[i + 1]);
+                    if (GATE) {
+                        s0v *= gamma[s * DK + c0 + i];
+                        s1v *= gamma[s * DK + c0 + i + 1];
+                    }
+                    pk[i / 2] = pack_bf16x2(s0v, s1v);
+                    rs[i] = __float_as_uint(s0v + __uint_as_float(rd[i]));
+                    rs[i + 1] = __float_as_uint(s1v + __uint_as_float(rd[i + 1]));
                 }
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; i++)
-                    pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                tmem_st16(tSB + g * 16, pk);
+                tmem_st16(tS + c0, rs);
+                tmem_st8(tSB + c0 / 2, pk);
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_S_READY));
+            if (lane == 0) {
+                mbar_arrive(bar(B_DS_EMPTY));
+                mbar_arrive(bar(B_S_READY));
+            }
+            if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(5, c);
         }
-        if (ok && N > 0) ok = mbar_wait_warp(bar(B_S_FULL), (N - 1) & 1, abort_flag, p.err);
         if (ok) {
             tc_fence_after();
-            float* fs = p.final_state ? p.final_state + (long)bh * DK * dv + j0 + j : nullptr;
-            for (int g = 0; g < DK / 32; g++) {
-                uint32_t r[32];
-                tmem_ld32(tS + g * 32, r);
+            float* fs = (p.final_state && jl >= 0 && jl < jvalid) ? p.final_state + (long)bh * DK * dv + j : nullptr;
+            const bool zl = norm && jl == 64 && p.final_z;
+            for (int g = 0; g < COLS / 16; g++) {
+                uint32_t r[16];
+                tmem_ld16(tS + cbase + g * 16, r);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; i++) {
-                    const int d = g * 32 + i;
-                    if (j < jvalid) {
-                        if (fs) fs[(long)d * dv] = __uint_as_float(r[i]);
-                    } else if (norm && j == 64 && p.final_z) {
+                for (int i = 0; i < 16; i++) {
+                    const int d = cbase + g * 16 + i;
+                    if (fs)
+                        fs[(long)d * dv] = __uint_as_float(r[i]);
+                    else if (zl)
                         p.final_z[(long)bh * DK + d] = __uint_as_float(r[i]);
-                    }
                 }
             }
         }
     } else if (warp < W_P0) {
         // ============================================================ output
-        const int j = threadIdx.x - W_OUT0 * 32;
+        const int jl = lane_to_col<DVT>(warp & 3, lane);
+        const bool store_col = jl >= 0 && jl < jvalid && !(norm && jl >= 64);
+        const bool leader = warp == W_OUT0 && lane == 0;
+        uint8_t* ost = sm + Ly::off_ost;
         for (int c = 0; c < N; c++) {
-            const int ob = c & 1;
-            bool ok = mbar_wait_warp(bar(B_O_FULL + ob), (c >> 1) & 1, abort_flag, p.err);
+            bool ok = mbar_wait_warp(bar(B_O_FULL), c & 1, abort_flag, p.err);
             uint32_t r0[32], r1[32];
-            float* dn = den + ob * C;
             if (ok) {
                 tc_fence_after();
-                const uint32_t tO = tmem + lane_field + TM_O + ob * 64;
+                const uint32_t tO = tmem + lane_field + TM_O;
                 tmem_ld32(tO, r0);
                 tmem_ld32(tO + 32, r1);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_O_EMPTY + ob));
-                if (norm && j == 64) {
+                if (lane == 0) mbar_arrive(bar(B_O_EMPTY));
+                if (norm && jl == 64) {
 #pragma unroll
                     for (int t = 0; t < 32; t++) {
-                        dn[t] = __uint_as_float(r0[t]);
-                        dn[t + 32] = __uint_as_float(r1[t]);
+                        den[t] = __uint_as_float(r0[t]);
+                        den[t + 32] = __uint_as_float(r1[t]);
                     }
                 }
             }
-            if (norm) ok = bar_red_and(2, 128, ok);
+            // staging may be rewritten once the previous bulk store has read it
+            if (leader && !p.out_f32) bulk_wait_group_read0();
+            ok = bar_red_and(2, 128, ok);
             if (!ok) break;
+            if (warp == W_OUT0 && lane == 0) GLA_TRACE_POINT(12, c);
             const int nval = min(C, L - c * C);
-            if (j < jvalid && j < dv - j0) {
-                const long base = ((long)bh * L + (long)c * C) * dv + j0 + j;
-                if (p.out_f32) {
-                    float* o = static_cast<float*>(p.out) + base;
+            if (!p.out_f32) {
+                if (store_col) {
+                    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(ost + (jl >> 6) * 8192) + (jl & 63);
 #pragma unroll
                     for (int t = 0; t < 32; t++) {
-                        float x = __uint_as_float(r0[t]);
-                        if (norm) x = x / dn[t];
-                        if (t < nval) o[(long)t * dv] = x;
-                    }
-#pragma unroll
-                    for (int t = 0; t < 32; t++) {
-                        float x = __uint_as_float(r1[t]);
-                        if (norm) x = x / dn[t + 32];
-                        if (t + 32 < nval) o[(long)(t + 32) * dv] = x;
-                    }
-                } else {
-                    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + base;
-#pragma unroll
-                    for (int t = 0; t < 32; t++) {
-                        float x = __uint_as_float(r0[t]);
-                        if (norm) x = x / dn[t];
-                        if (t < nval) o[(long)t * dv] = __float2bfloat16_rn(x);
-                    }
-#pragma unroll
-                    for (int t = 0; t < 32; t++) {
-                        float x = __uint_as_float(r1[t]);
-                        if (norm) x = x / dn[t + 32];
-                        if (t + 32 < nval) o[(long)(t + 32) * dv] = __float2bfloat16_rn(x);
+                        float x0 = __uint_as_float(r0[t]), x1 = __uint_as_float(r1[t]);
+                        if (norm) {
+                            x0 = x0 / den[t];
+                            x1 = x1 / den[t + 32];
+                        }
+                        o[t * 64] = __float2bfloat16_rn(x0);
+                        o[(t + 32) * 64] = __float2bfloat16_rn(x1);
                     }
                 }
+                fence_proxy_async_smem();
+                named_bar_sync(3, 128);
+                if (leader) {
+                    const int nblk = norm ? 1 : jvalid / 64;
+                    for (int blk = 0; blk < nblk; blk++)
+                        tma_store_3d(&p.tm_out, smem_u32(ost) + blk * 8192, j0 + blk * 64, c * C, bh);
+                    bulk_commit_group();
+                }
+            } else if (store_col) {
+                float* o = static_cast<float*>(p.out) + ((long)bh * L + (long)c * C) * dv + j0 + jl;
+#pragma unroll
+                for (int t = 0; t < 32; t++) {
+                    float x0 = __uint_as_float(r0[t]), x1 = __uint_as_float(r1[t]);
+                    if (norm) {
+                        x0 = x0 / den[t];
+                        x1 = x1 / den[t + 32];
+                    }
+                    if (t < nval) o[(long)t * dv] = x0;
+                    if (t + 32 < nval) o[(long)(t + 32) * dv] = x1;
+                }
             }
+            if (norm) named_bar_sync(3, 128);  // den is rewritten next chunk
+            if (warp == W_OUT0 && lane == 0) GLA_TRACE_POINT(13, c);
         }
+        if (leader && !p.out_f32) bulk_wait_group0();
     } else if (warp < W_TMA) {
         // ============================================================ P = tril(A) -> bf16
         const int t = threadIdx.x - W_P0 * 32;  // token row 0..63 (TMEM lanes 0..63)
+        uint8_t* P = sm + Ly::off_p;
         for (int c = 0; c < N; c++) {
-            const int ob = c & 1;
-            if (!mbar_wait_warp(bar(B_A_FULL + ob), (c >> 1) & 1, abort_flag, p.err)) break;
-            if (!mbar_wait_warp(bar(B_P_EMPTY + ob), ((c >> 1) & 1) ^ 1, abort_flag, p.err)) break;
+            if (!mbar_wait_warp(bar(B_A_FULL), c & 1, abort_flag, p.err)) break;
+            if (!mbar_wait_warp(bar(B_P_EMPTY), (c & 1) ^ 1, abort_flag, p.err)) break;
             tc_fence_after();
-            uint32_t r[2][32];
-            const uint32_t tA = tmem + lane_field + TM_A + ob * 64;
-            tmem_ld32(tA, r[0]);
-            tmem_ld32(tA + 32, r[1]);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_A_EMPTY + ob));
-            uint8_t* P = sm + Ly::off_p + ob * Ly::PB;
+            if (t == 0) GLA_TRACE_POINT(10, c);
 #pragma unroll
-            for (int k8 = 0; k8 < 8; k8++) {
-                float x[8];
-#pragma unroll
-                for (int e = 0; e < 8; e++) {
-                    const int i = k8 * 8 + e;
-                    const float a = __uint_as_float(r[i >> 5][i & 31]);
-                    x[e] = (i <= t) ? a : 0.f;
+            for (int h = 0; h < 2; h++) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_field + TM_A + h * 32, r);
+                tmem_wait_ld();
+                if (h == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_A_EMPTY));
                 }
-                uint4 w;
-                w.x = pack_bf16x2(x[0], x[1]);
-                w.y = pack_bf16x2(x[2], x[3]);
-                w.z = pack_bf16x2(x[4], x[5]);
-                w.w = pack_bf16x2(x[6], x[7]);
-                *reinterpret_cast<uint4*>(P + sw128_offset(t, k8 * 8)) = w;
+#pragma unroll
+                for (int k8 = 0; k8 < 4; k8++) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; e++) {
+                        const int i = h * 32 + k8 * 8 + e;
+                        x[e] = (i <= t) ? __uint_as_float(r[k8 * 8 + e]) : 0.f;
+                    }
+                    uint4 w;
+                    w.x = pack_bf16x2(x[0], x[1]);
+                    w.y = pack_bf16x2(x[2], x[3]);
+                    w.z = pack_bf16x2(x[4], x[5]);
+                    w.w = pack_bf16x2(x[6], x[7]);
+                    *reinterpret_cast<uint4*>(P + sw128_offset(t, h * 32 + k8 * 8)) = w;
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_P_FULL + ob));
+            if (lane == 0) mbar_arrive(bar(B_P_FULL));
+            if (t == 0) GLA_TRACE_POINT(11, c);
         }
     } else if (warp == W_TMA) {
         // ============================================================ TMA producer
@@ -448,8 +552,10 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             tma_prefetch_desc(&p.tm_k);
             tma_prefetch_desc(&p.tm_v);
             if (GATE) tma_prefetch_desc(&p.tm_la);
+            if (!p.out_f32) tma_prefetch_desc(&p.tm_out);
             for (int c = 0; c < N; c++) {
                 const int row = c * C;
+                GLA_TRACE_POINT(0, c);
                 if (GATE) {
                     const int l = c % NL;
                     if (!mbar_wait(bar(B_LA_EMPTY + l), ((c / NL) & 1) ^ 1, abort_flag, p.err)) break;
@@ -471,65 +577,81 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                     tma_load_3d(sbase + Ly::off_v + v * Ly::VB + blk * 8192, &p.tm_v, bar(B_V_FULL + v),
                                 j0 + blk * 64, row, bh);
                 last_issued = c;
+                GLA_TRACE_POINT(1, c);
             }
         }
     } else {
         // ============================================================ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idA = make_idesc_bf16(128, 64, 0, 0);
-            constexpr uint32_t idS = make_idesc_bf16(128, DK, 1, 1);
-            constexpr uint32_t idOi = make_idesc_bf16(128, 64, 0, 0);
-            constexpr uint32_t idOa = make_idesc_bf16(128, 64, 1, 0);
-            for (int c = 0; c < N; c++) {
-                const int s = c % NS, v = c % NV, ob = c & 1;
-                const uint32_t Qs = sbase + Ly::off_qk + s * Ly::STAGE_QK;
-                const uint32_t Ks = Qs + Ly::QB;
-                const uint32_t Vs = sbase + Ly::off_v + v * Ly::VB;
-                const uint32_t Ps = sbase + Ly::off_p + ob * Ly::PB;
-                if (!mbar_wait(bar(B_QK_GATED + s), (c / NS) & 1, abort_flag, p.err)) break;
-                if (!mbar_wait(bar(B_A_EMPTY + ob), ((c >> 1) & 1) ^ 1, abort_flag, p.err)) break;
+            constexpr uint32_t idS = make_idesc_bf16(DVT, DK, 1, 1);
+            constexpr uint32_t idOi = make_idesc_bf16(DVT, 64, 0, 0);
+            constexpr uint32_t idOa = make_idesc_bf16(DVT, 64, 1, 0);
+            const uint32_t Ps = sbase + Ly::off_p;
+            auto qs_of = [&](int c) { return sbase + Ly::off_qk + (c % NS) * Ly::STAGE_QK; };
+            auto vs_of = [&](int c) { return sbase + Ly::off_v + (c % NV) * Ly::VB; };
+            // dS(c) = V_c^T Kh_c into its own TMEM buffer
+            auto issue_ds = [&](int c) -> bool {
+                if (!mbar_wait(bar(B_QK_GATED + c % NS), (c / NS) & 1, abort_flag, p.err)) return false;
+                if (!mbar_wait(bar(B_V_FULL + c % NV), (c / NV) & 1, abort_flag, p.err)) return false;
+                if (!mbar_wait(bar(B_DS_EMPTY), (c & 1) ^ 1, abort_flag, p.err)) return false;
                 tc_fence_after();
-                // A = Qh Kh^T (rows 64..127 of the M=128 tile read past the Q tile and are ignored)
+                const uint32_t Ks = qs_of(c) + Ly::QB, Vs = vs_of(c);
+#pragma unroll
+                for (int kk = 0; kk < C / 16; kk++)
+                    mma_ss(tmem + TM_DS, make_sdesc(Vs + kk * 2048, 8192, 1024),
+                           make_sdesc(Ks + kk * 2048, 8192, 1024), idS, kk > 0);
+                mma_commit(bar(B_DS_FULL));
+                return true;
+            };
+            // A(c) = Qh_c Kh_c^T (rows 64..127 of the M=128 tile read past the Q tile and are ignored)
+            auto issue_a = [&](int c) -> bool {
+                if (!mbar_wait(bar(B_A_EMPTY), (c & 1) ^ 1, abort_flag, p.err)) return false;
+                tc_fence_after();
+                const uint32_t Qs = qs_of(c), Ks = Qs + Ly::QB;
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; kk++) {
                     const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-                    mma_ss(tmem + TM_A + ob * 64, make_sdesc(Qs + off, 16, 1024), make_sdesc(Ks + off, 16, 1024),
-                           idA, kk > 0);
+                    mma_ss(tmem + TM_A, make_sdesc(Qs + off, 16, 1024), make_sdesc(Ks + off, 16, 1024), idA, kk > 0);
                 }
-                mma_commit(bar(B_A_FULL + ob));
-                if (!mbar_wait(bar(B_V_FULL + v), (c / NV) & 1, abort_flag, p.err)) break;
+                mma_commit(bar(B_A_FULL));
+                return true;
+            };
+            bool ok = N == 0 || (issue_ds(0) && issue_a(0));
+            for (int c = 0; ok && c < N; c++) {
+                if (c + 1 < N && !issue_ds(c + 1)) break;
                 if (!mbar_wait(bar(B_S_READY), c & 1, abort_flag, p.err)) break;
+                if (!mbar_wait(bar(B_O_EMPTY), (c & 1) ^ 1, abort_flag, p.err)) break;
                 tc_fence_after();
-                // S^T += V^T Kh
-#pragma unroll
-                for (int kk = 0; kk < C / 16; kk++)
-                    mma_ss(tmem + TM_S, make_sdesc(Vs + kk * 2048, 8192, 1024), make_sdesc(Ks + kk * 2048, 8192, 1024),
-                           idS, 1);
-                mma_commit(bar(B_S_FULL));
-                if (!mbar_wait(bar(B_O_EMPTY + ob), ((c >> 1) & 1) ^ 1, abort_flag, p.err)) break;
-                tc_fence_after();
+                GLA_TRACE_POINT(7, c);
+                const uint32_t Qs = qs_of(c), Vs = vs_of(c);
                 // O^T = S'^T Qh^T  (A operand: bf16 copy of the decayed state in TMEM)
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; kk++) {
                     const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-                    mma_ts(tmem + TM_O + ob * 64, tmem + TM_SB + ob * (DK / 2) + kk * 8,
-                           make_sdesc(Qs + off, 16, 1024), idOi, kk > 0);
+                    mma_ts(tmem + TM_O, tmem + TM_SB + (c & 1) * (DK / 2) + kk * 8, make_sdesc(Qs + off, 16, 1024),
+                           idOi, kk > 0);
                 }
-                if (!mbar_wait(bar(B_P_FULL + ob), (c >> 1) & 1, abort_flag, p.err)) break;
+                mma_commit(bar(B_SB_EMPTY + (c & 1)));
+                GLA_TRACE_POINT(8, c);
+                if (c + 1 < N && !issue_a(c + 1)) break;
+                if (!mbar_wait(bar(B_P_FULL), c & 1, abort_flag, p.err)) break;
                 tc_fence_after();
+                GLA_TRACE_POINT(9, c);
                 // O^T += V^T P^T
 #pragma unroll
                 for (int kk = 0; kk < C / 16; kk++)
-                    mma_ss(tmem + TM_O + ob * 64, make_sdesc(Vs + kk * 2048, 8192, 1024),
-                           make_sdesc(Ps + kk * 32, 16, 1024), idOa, 1);
-                mma_commit(bar(B_O_FULL + ob));
-                mma_commit(bar(B_P_EMPTY + ob));
-                mma_commit(bar(B_V_EMPTY + v));
-                mma_commit(bar(B_QK_EMPTY + s));
+                    mma_ss(tmem + TM_O, make_sdesc(Vs + kk * 2048, 8192, 1024), make_sdesc(Ps + kk * 32, 16, 1024),
+                           idOa, 1);
+                mma_commit(bar(B_O_FULL));
+                mma_commit(bar(B_P_EMPTY));
+                mma_commit(bar(B_V_EMPTY + c % NV));
+                mma_commit(bar(B_QK_EMPTY + c % NS));
+                GLA_TRACE_POINT(6, c);
             }
             // drain: every issued tcgen05 op has finished before TMEM is released
             mma_commit(bar(B_DRAIN));
-            volatile int no_abort = 0;  // the drain wait is not cut short by an earlier abort
+            volatile int no_abort = 0;
             mbar_wait(bar(B_DRAIN), 0, &no_abort, p.err);
         }
     }
@@ -565,20 +687,24 @@ CUresult encode_3d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <int DK, bool GATE>
+template <int DK, int DVT, bool GATE>
 cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
     TcParams p;
     memset(&p, 0, sizeof(p));
     const int BH = a.B * a.H;
-    if (encode_3d(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, DK, a.L, BH, 64, C,
-                  CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
-        encode_3d(&p.tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, DK, a.L, BH, 64, C,
-                  CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+    if (encode_3d(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, DK, a.L, BH, 64, C, CU_TENSOR_MAP_SWIZZLE_128B) !=
+            CUDA_SUCCESS ||
+        encode_3d(&p.tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, DK, a.L, BH, 64, C, CU_TENSOR_MAP_SWIZZLE_128B) !=
+            CUDA_SUCCESS ||
         encode_3d(&p.tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, a.dv, a.L, BH, 64, C,
                   CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     if (GATE && encode_3d(&p.tm_la, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.log_alpha, DK, a.L, BH, DK, C,
                           CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    p.out_f32 = a.out_dtype == GLA_DTYPE_F32;
+    if (!p.out_f32 && encode_3d(&p.tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out, a.dv, a.L, BH, 64, C,
+                                CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     p.init_state = a.init_state;
     p.init_z = a.init_z;
@@ -591,14 +717,35 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
     p.nchunks = (a.L + C - 1) / C;
     p.ntile = (a.dv + DVT - 1) / DVT;
     p.flags = a.flags;
-    p.out_f32 = a.out_dtype == GLA_DTYPE_F32;
-    auto kern = gla_prefill_tc_kernel<DK, GATE>;
-    const int smem = Layout<DK>::alloc;
+    auto kern = gla_prefill_tc_kernel<DK, DVT, GATE>;
+    const int smem = Layout<DK, DVT>::alloc;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const long grid = (long)BH * p.ntile;
     kern<<<dim3((unsigned)grid), kThreads, smem, s>>>(p);
     return cudaGetLastError();
+}
+
+// Value-tile width: 128 columns unless that leaves too few CTAs to cover the
+// GPU's SMs, in which case 64 (twice the CTAs, M = 64 MMAs).
+// GLA_TC_DVT=64|128 in the environment forces the width (used by the tests to
+// cover both kernel variants on small shapes).
+int choose_dvt(const PrefillArgs& a) {
+    if (a.flags & GLA_FLAG_NORMALIZE) return 128;  // the normaliser column needs a spare lane
+    if (const char* e = getenv("GLA_TC_DVT")) {
+        if (e[0] == '6') return 64;
+        if (e[0] == '1') return 128;
+    }
+    int sms = 148;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long ctas128 = (long)a.B * a.H * ((a.dv + 127) / 128);
+    return ctas128 * 4 < (long)sms * 3 ? 64 : 128;
+}
+
+template <int DK, int DVT>
+cudaError_t launch_g(const PrefillArgs& a, cudaStream_t s) {
+    return a.log_alpha ? launch_t<DK, DVT, true>(a, s) : launch_t<DK, DVT, false>(a, s);
 }
 
 }  // namespace
@@ -610,15 +757,15 @@ bool prefill_tc_supported(const PrefillArgs& a) {
     if (a.dv < 64 || a.dv % 64 != 0) return false;
     if ((a.flags & GLA_FLAG_NORMALIZE) && a.dv != 64) return false;
     if (a.L < 1) return false;
-    const long grid = (long)a.B * a.H * ((a.dv + DVT - 1) / DVT);
+    const long grid = (long)a.B * a.H * (a.dv / 64);
     if (grid > INT_MAX) return false;
     return true;
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
-    const bool gate = a.log_alpha != nullptr;
-    if (a.dk == 64) return gate ? launch_t<64, true>(a, s) : launch_t<64, false>(a, s);
-    return gate ? launch_t<128, true>(a, s) : launch_t<128, false>(a, s);
+    const int dvt = choose_dvt(a);
+    if (a.dk == 64) return dvt == 64 ? launch_g<64, 64>(a, s) : launch_g<64, 128>(a, s);
+    return dvt == 64 ? launch_g<128, 64>(a, s) : launch_g<128, 128>(a, s);
 }
 
 }  // namespace gla

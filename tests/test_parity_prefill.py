@@ -78,6 +78,24 @@ def test_tc_shapes(B, H, L, dk, dv, gate, init):
     assert_bf16_close(s, rs, "state")
 
 
+@pytest.mark.parametrize("dvt", ["64", "128"])
+@pytest.mark.parametrize("B,H,L,dk,dv,gate,init", [
+    (1, 2, 200, 128, 128, True, True),
+    (1, 1, 130, 64, 256, True, True),
+    (2, 1, 65, 128, 64, False, False),
+])
+def test_tc_both_tile_widths(monkeypatch, dvt, B, H, L, dk, dv, gate, init):
+    """The 64- and 128-column value tiles (M = 64 / M = 128 MMAs) give the same parity."""
+    monkeypatch.setenv("GLA_TC_DVT", dvt)
+    w = _cfg(2, B=B, H=H, L=L, dk=dk, dv=dv, gate=gate, init_std=0.1 if init else 0.0,
+             seed=200 + L + dk + dv)
+    x = synth.make_prefill(w)
+    o, s, _ = run_prefill(w, x)
+    ro, rs, _ = oracle_prefill(w, x)
+    assert_bf16_close(o, ro, "out")
+    assert_bf16_close(s, rs, "state")
+
+
 def test_tc_fp32_output():
     w = _cfg(2, B=1, H=2, L=300, init_std=0.1, seed=77)
     x = synth.make_prefill(w)
