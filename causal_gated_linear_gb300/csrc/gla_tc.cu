@@ -245,27 +245,25 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             bool ok = true;
             if (GATE) ok = mbar_wait(bar(B_LA_FULL + l), (c / NL) & 1, abort_flag, p.err);
             if (ok) ok = mbar_wait(bar(B_QK_FULL + s), (c / NS) & 1, abort_flag, p.err);
-            float b[TPS][4];
+            // Phase 1: per-segment cumulative sums of log alpha, exchanged across the
+            // gate warps to give each thread the prefix before its segment (off) and
+            // the chunk total b_C (tot).  Phase 2 re-reads log alpha from shared
+            // memory and re-accumulates, so no per-token sums are held in registers.
             float off[4] = {0.f, 0.f, 0.f, 0.f}, tot[4] = {0.f, 0.f, 0.f, 0.f};
+            const float* la = reinterpret_cast<const float*>(sm + Ly::off_la + l * Ly::LAB) + ch;
             if (GATE) {
                 float* st = segtot + (c & 1) * SEG * DK;
                 if (ok) {
-                    const float* la = reinterpret_cast<const float*>(sm + Ly::off_la + l * Ly::LAB);
-                    float4 x[TPS];
-#pragma unroll
-                    for (int i = 0; i < TPS; i++)
-                        x[i] = *reinterpret_cast<const float4*>(la + (seg * TPS + i) * DK + ch);
-                    float r[4] = {0.f, 0.f, 0.f, 0.f};
+                    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                     for (int i = 0; i < TPS; i++) {
-                        r[0] += x[i].x;
-                        r[1] += x[i].y;
-                        r[2] += x[i].z;
-                        r[3] += x[i].w;
-#pragma unroll
-                        for (int e = 0; e < 4; e++) b[i][e] = r[e];
+                        const float4 x = *reinterpret_cast<const float4*>(la + (seg * TPS + i) * DK);
+                        r.x += x.x;
+                        r.y += x.y;
+                        r.z += x.z;
+                        r.w += x.w;
                     }
-                    *reinterpret_cast<float4*>(st + seg * DK + ch) = make_float4(r[0], r[1], r[2], r[3]);
+                    *reinterpret_cast<float4*>(st + seg * DK + ch) = r;
                 }
                 // the segment-total exchange doubles as the gate role's agreement to go on
                 if (!bar_red_and(1, kGateThreads, ok)) break;
@@ -283,13 +281,11 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                     tot[2] += u.z;
                     tot[3] += u.w;
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_LA_EMPTY + l));
                 if (seg == 0)
                     *reinterpret_cast<float4*>(gamma + s * DK + ch) =
                         make_float4(__expf(tot[0]), __expf(tot[1]), __expf(tot[2]), __expf(tot[3]));
 #pragma unroll
-                for (int e = 0; e < 4; e++) off[e] -= tot[e];  // d = b_t + off - tot = b_t - b_C
+                for (int e = 0; e < 4; e++) off[e] -= tot[e];  // running value is now b_t - b_C
             } else {
                 if (!bar_red_and(1, kGateThreads, ok)) break;
             }
@@ -298,14 +294,18 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             if (GATE || elu || nval < C) {
                 uint8_t* qt = sm + Ly::off_qk + s * Ly::STAGE_QK + atom * 8192;
                 uint8_t* kt = qt + Ly::QB;
+                float run[4] = {off[0], off[1], off[2], off[3]};
 #pragma unroll
                 for (int i0 = 0; i0 < TPS; i0 += G) {
                     uint2 qr[G], kr[G];
+                    float4 lx[G];
 #pragma unroll
                     for (int u = 0; u < G; u++) {
-                        const uint32_t o = sw128_offset(seg * TPS + i0 + u, col);
+                        const int t = seg * TPS + i0 + u;
+                        const uint32_t o = sw128_offset(t, col);
                         qr[u] = *reinterpret_cast<const uint2*>(qt + o);
                         kr[u] = *reinterpret_cast<const uint2*>(kt + o);
+                        if (GATE) lx[u] = *reinterpret_cast<const float4*>(la + t * DK);
                     }
 #pragma unroll
                     for (int u = 0; u < G; u++) {
@@ -314,6 +314,12 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                         const float2 k01 = unpack_bf16x2(kr[u].x), k23 = unpack_bf16x2(kr[u].y);
                         float qv[4] = {q01.x, q01.y, q23.x, q23.y};
                         float kv[4] = {k01.x, k01.y, k23.x, k23.y};
+                        if (GATE) {
+                            run[0] += lx[u].x;
+                            run[1] += lx[u].y;
+                            run[2] += lx[u].z;
+                            run[3] += lx[u].w;
+                        }
 #pragma unroll
                         for (int e = 0; e < 4; e++) {
                             if (elu) {
@@ -321,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                                 kv[e] = elu1(kv[e]);
                             }
                             if (GATE) {
-                                const float d = b[i0 + u][e] + off[e];  // b_t - b_C >= 0
+                                const float d = run[e];  // b_t - b_C >= 0
                                 qv[e] *= __expf(d);
                                 kv[e] *= __expf(-d);
                             }
@@ -340,6 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                         *reinterpret_cast<uint2*>(kt + o) = kr[u];
                     }
                 }
+            }
+            if (GATE) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_LA_EMPTY + l));
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -442,44 +452,51 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
         uint8_t* ost = sm + Ly::off_ost;
         for (int c = 0; c < N; c++) {
             bool ok = mbar_wait_warp(bar(B_O_FULL), c & 1, abort_flag, p.err);
-            uint32_t r0[32], r1[32];
-            if (ok) {
-                tc_fence_after();
-                const uint32_t tO = tmem + lane_field + TM_O;
-                tmem_ld32(tO, r0);
-                tmem_ld32(tO + 32, r1);
-                tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_O_EMPTY));
-                if (norm && jl == 64) {
-#pragma unroll
-                    for (int t = 0; t < 32; t++) {
-                        den[t] = __uint_as_float(r0[t]);
-                        den[t + 32] = __uint_as_float(r1[t]);
-                    }
-                }
-            }
             // staging may be rewritten once the previous bulk store has read it
             if (leader && !p.out_f32) bulk_wait_group_read0();
             ok = bar_red_and(2, 128, ok);
             if (!ok) break;
+            tc_fence_after();
             if (warp == W_OUT0 && lane == 0) GLA_TRACE_POINT(12, c);
             const int nval = min(C, L - c * C);
-            if (!p.out_f32) {
-                if (store_col) {
-                    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(ost + (jl >> 6) * 8192) + (jl & 63);
+#pragma unroll 1
+            for (int h = 0; h < 2; h++) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_field + TM_O + h * 32, r);
+                tmem_wait_ld();
+                if (h == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_O_EMPTY));
+                }
+                if (norm) {
+                    if (jl == 64) {
+#pragma unroll
+                        for (int t = 0; t < 32; t++) den[h * 32 + t] = __uint_as_float(r[t]);
+                    }
+                    named_bar_sync(3, 128);
+                }
+                if (!store_col) continue;
+                if (!p.out_f32) {
+                    __nv_bfloat16* o =
+                        reinterpret_cast<__nv_bfloat16*>(ost + (jl >> 6) * 8192) + (jl & 63) + h * 32 * 64;
 #pragma unroll
                     for (int t = 0; t < 32; t++) {
-                        float x0 = __uint_as_float(r0[t]), x1 = __uint_as_float(r1[t]);
-                        if (norm) {
-                            x0 = x0 / den[t];
-                            x1 = x1 / den[t + 32];
-                        }
-                        o[t * 64] = __float2bfloat16_rn(x0);
-                        o[(t + 32) * 64] = __float2bfloat16_rn(x1);
+                        float x = __uint_as_float(r[t]);
+                        if (norm) x = x / den[h * 32 + t];
+                        o[t * 64] = __float2bfloat16_rn(x);
+                    }
+                } else {
+                    float* o = static_cast<float*>(p.out) + ((long)bh * L + (long)c * C + h * 32) * dv + j0 + jl;
+#pragma unroll
+                    for (int t = 0; t < 32; t++) {
+                        float x = __uint_as_float(r[t]);
+                        if (norm) x = x / den[h * 32 + t];
+                        if (h * 32 + t < nval) o[(long)t * dv] = x;
                     }
                 }
+            }
+            if (!p.out_f32) {
                 fence_proxy_async_smem();
                 named_bar_sync(3, 128);
                 if (leader) {
@@ -488,20 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                         tma_store_3d(&p.tm_out, smem_u32(ost) + blk * 8192, j0 + blk * 64, c * C, bh);
                     bulk_commit_group();
                 }
-            } else if (store_col) {
-                float* o = static_cast<float*>(p.out) + ((long)bh * L + (long)c * C) * dv + j0 + jl;
-#pragma unroll
-                for (int t = 0; t < 32; t++) {
-                    float x0 = __uint_as_float(r0[t]), x1 = __uint_as_float(r1[t]);
-                    if (norm) {
-                        x0 = x0 / den[t];
-                        x1 = x1 / den[t + 32];
-                    }
-                    if (t < nval) o[(long)t * dv] = x0;
-                    if (t + 32 < nval) o[(long)(t + 32) * dv] = x1;
-                }
             }
-            if (norm) named_bar_sync(3, 128);  // den is rewritten next chunk
             if (warp == W_OUT0 && lane == 0) GLA_TRACE_POINT(13, c);
         }
         if (leader && !p.out_f32) bulk_wait_group0();
