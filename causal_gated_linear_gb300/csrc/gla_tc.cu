@@ -154,8 +154,11 @@ template <int DK, int DVT, bool GATE>
 __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __grid_constant__ TcParams p) {
     using Ly = Layout<DK, DVT>;
     constexpr int NV = Ly::NV;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte aligned base for the swizzled tiles.  The offset is added to the
+    // shared array itself so that every access below stays in the shared
+    // address space (an integer round trip would turn them into generic ones).
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Ly::off_bar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Ly::off_misc);
@@ -351,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_LA_EMPTY + l));
             }
+            if (threadIdx.x == 0) GLA_TRACE_POINT(14, c);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_QK_GATED + s));
@@ -544,6 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                     *reinterpret_cast<uint4*>(P + sw128_offset(t, h * 32 + k8 * 8)) = w;
                 }
             }
+            if (t == 0) GLA_TRACE_POINT(15, c);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_P_FULL));
@@ -594,64 +599,90 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             const uint32_t Ps = sbase + Ly::off_p;
             auto qs_of = [&](int c) { return sbase + Ly::off_qk + (c % NS) * Ly::STAGE_QK; };
             auto vs_of = [&](int c) { return sbase + Ly::off_v + (c % NV) * Ly::VB; };
-            // dS(c) = V_c^T Kh_c into its own TMEM buffer
-            auto issue_ds = [&](int c) -> bool {
-                if (!mbar_wait(bar(B_QK_GATED + c % NS), (c / NS) & 1, abort_flag, p.err)) return false;
-                if (!mbar_wait(bar(B_V_FULL + c % NV), (c / NV) & 1, abort_flag, p.err)) return false;
-                if (!mbar_wait(bar(B_DS_EMPTY), (c & 1) ^ 1, abort_flag, p.err)) return false;
-                tc_fence_after();
-                const uint32_t Ks = qs_of(c) + Ly::QB, Vs = vs_of(c);
+            // Issue each chunk's four products as soon as their inputs are ready
+            // (never waiting on one product while another could go): dS(c) and
+            // A(c) run ahead of the state chain, O_i(c) follows the state update,
+            // O_a(c) follows P(c).  The q/k stage is released as soon as A(c),
+            // dS(c) and O_i(c) have been issued (O_a(c) reads only V and P).
+            int nd = 0, na = 0, ni = 0, no = 0, nq = 0;
+            unsigned long long t_last = globaltimer();
+            uint32_t idle = 0;
+            while (no < N) {
+                bool prog = false;
+                if (no < ni && mbar_test(bar(B_P_FULL), no & 1)) {
+                    tc_fence_after();
+                    const uint32_t Vs = vs_of(no);
 #pragma unroll
-                for (int kk = 0; kk < C / 16; kk++)
-                    mma_ss(tmem + TM_DS, make_sdesc(Vs + kk * 2048, 8192, 1024),
-                           make_sdesc(Ks + kk * 2048, 8192, 1024), idS, kk > 0);
-                mma_commit(bar(B_DS_FULL));
-                return true;
-            };
-            // A(c) = Qh_c Kh_c^T (rows 64..127 of the M=128 tile read past the Q tile and are ignored)
-            auto issue_a = [&](int c) -> bool {
-                if (!mbar_wait(bar(B_A_EMPTY), (c & 1) ^ 1, abort_flag, p.err)) return false;
-                tc_fence_after();
-                const uint32_t Qs = qs_of(c), Ks = Qs + Ly::QB;
-#pragma unroll
-                for (int kk = 0; kk < DK / 16; kk++) {
-                    const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-                    mma_ss(tmem + TM_A, make_sdesc(Qs + off, 16, 1024), make_sdesc(Ks + off, 16, 1024), idA, kk > 0);
+                    for (int kk = 0; kk < C / 16; kk++)
+                        mma_ss(tmem + TM_O, make_sdesc(Vs + kk * 2048, 8192, 1024), make_sdesc(Ps + kk * 32, 16, 1024),
+                               idOa, 1);
+                    mma_commit(bar(B_O_FULL));
+                    mma_commit(bar(B_P_EMPTY));
+                    mma_commit(bar(B_V_EMPTY + no % NV));
+                    GLA_TRACE_POINT(6, no);
+                    no++;
+                    prog = true;
                 }
-                mma_commit(bar(B_A_FULL));
-                return true;
-            };
-            bool ok = N == 0 || (issue_ds(0) && issue_a(0));
-            for (int c = 0; ok && c < N; c++) {
-                if (c + 1 < N && !issue_ds(c + 1)) break;
-                if (!mbar_wait(bar(B_S_READY), c & 1, abort_flag, p.err)) break;
-                if (!mbar_wait(bar(B_O_EMPTY), (c & 1) ^ 1, abort_flag, p.err)) break;
-                tc_fence_after();
-                GLA_TRACE_POINT(7, c);
-                const uint32_t Qs = qs_of(c), Vs = vs_of(c);
-                // O^T = S'^T Qh^T  (A operand: bf16 copy of the decayed state in TMEM)
+                if (ni < N && ni == no && ni < nd && mbar_test(bar(B_S_READY), ni & 1) &&
+                    mbar_test(bar(B_O_EMPTY), (ni & 1) ^ 1)) {
+                    tc_fence_after();
+                    GLA_TRACE_POINT(7, ni);
+                    const uint32_t Qs = qs_of(ni);
+                    // O^T = S'^T Qh^T  (A operand: bf16 copy of the decayed state in TMEM)
 #pragma unroll
-                for (int kk = 0; kk < DK / 16; kk++) {
-                    const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-                    mma_ts(tmem + TM_O, tmem + TM_SB + (c & 1) * (DK / 2) + kk * 8, make_sdesc(Qs + off, 16, 1024),
-                           idOi, kk > 0);
+                    for (int kk = 0; kk < DK / 16; kk++) {
+                        const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+                        mma_ts(tmem + TM_O, tmem + TM_SB + (ni & 1) * (DK / 2) + kk * 8, make_sdesc(Qs + off, 16, 1024),
+                               idOi, kk > 0);
+                    }
+                    mma_commit(bar(B_SB_EMPTY + (ni & 1)));
+                    ni++;
+                    prog = true;
                 }
-                mma_commit(bar(B_SB_EMPTY + (c & 1)));
-                GLA_TRACE_POINT(8, c);
-                if (c + 1 < N && !issue_a(c + 1)) break;
-                if (!mbar_wait(bar(B_P_FULL), c & 1, abort_flag, p.err)) break;
-                tc_fence_after();
-                GLA_TRACE_POINT(9, c);
-                // O^T += V^T P^T
+                if (nd < N && mbar_test(bar(B_QK_GATED + nd % NS), (nd / NS) & 1) &&
+                    mbar_test(bar(B_V_FULL + nd % NV), (nd / NV) & 1) && mbar_test(bar(B_DS_EMPTY), (nd & 1) ^ 1)) {
+                    tc_fence_after();
+                    const uint32_t Ks = qs_of(nd) + Ly::QB, Vs = vs_of(nd);
+                    // dS(c) = V_c^T Kh_c into its own TMEM buffer
 #pragma unroll
-                for (int kk = 0; kk < C / 16; kk++)
-                    mma_ss(tmem + TM_O, make_sdesc(Vs + kk * 2048, 8192, 1024), make_sdesc(Ps + kk * 32, 16, 1024),
-                           idOa, 1);
-                mma_commit(bar(B_O_FULL));
-                mma_commit(bar(B_P_EMPTY));
-                mma_commit(bar(B_V_EMPTY + c % NV));
-                mma_commit(bar(B_QK_EMPTY + c % NS));
-                GLA_TRACE_POINT(6, c);
+                    for (int kk = 0; kk < C / 16; kk++)
+                        mma_ss(tmem + TM_DS, make_sdesc(Vs + kk * 2048, 8192, 1024),
+                               make_sdesc(Ks + kk * 2048, 8192, 1024), idS, kk > 0);
+                    mma_commit(bar(B_DS_FULL));
+                    nd++;
+                    prog = true;
+                }
+                if (na < N && mbar_test(bar(B_QK_GATED + na % NS), (na / NS) & 1) &&
+                    mbar_test(bar(B_A_EMPTY), (na & 1) ^ 1)) {
+                    tc_fence_after();
+                    const uint32_t Qs = qs_of(na), Ks = Qs + Ly::QB;
+                    // A(c) = Qh_c Kh_c^T (rows 64..127 of the M=128 tile read past the Q tile and are ignored)
+#pragma unroll
+                    for (int kk = 0; kk < DK / 16; kk++) {
+                        const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+                        mma_ss(tmem + TM_A, make_sdesc(Qs + off, 16, 1024), make_sdesc(Ks + off, 16, 1024), idA,
+                               kk > 0);
+                    }
+                    mma_commit(bar(B_A_FULL));
+                    na++;
+                    prog = true;
+                }
+                while (nq < ni && nq < na) {  // dS(nq) precedes O_i(nq), so all three were issued
+                    mma_commit(bar(B_QK_EMPTY + nq % NS));
+                    nq++;
+                }
+                if (prog) {
+                    idle = 0;
+                } else if ((++idle & 255u) == 0) {
+                    if (*abort_flag) break;
+                    const unsigned long long now = globaltimer();
+                    if (idle == 256) t_last = now;
+                    else if (now - t_last > kWaitLimitNs) {
+                        *abort_flag = 1;
+                        atomicOr(p.err, kErrTimeout);
+                        break;
+                    }
+                }
             }
             // drain: every issued tcgen05 op has finished before TMEM is released
             mma_commit(bar(B_DRAIN));
