@@ -32,8 +32,8 @@ GLA_OK, GLA_ERR_INVALID, GLA_ERR_UNSUPPORTED, GLA_ERR_MISALIGNED, GLA_ERR_CUDA, 
 BF16, F32 = 0, 1
 FLAG_FEATURE_ELU1, FLAG_NORMALIZE, FLAG_FORCE_SIMT = 1, 2, 4
 
-EXPORTED = ["gla_fwd", "gla_fwd_ex", "gla_decode_step", "gla_device_error", "gla_status_string",
-            "gla_version"]
+EXPORTED = ["gla_fwd", "gla_fwd_ex", "gla_decode_step", "gla_device_error", "gla_device_error_detail",
+            "gla_status_string", "gla_version"]
 
 
 class GlaError(RuntimeError):
@@ -75,6 +75,8 @@ def load(path: str | None = None):
     lib.gla_decode_step.restype = i
     lib.gla_device_error.argtypes = [vp]
     lib.gla_device_error.restype = i
+    lib.gla_device_error_detail.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+    lib.gla_device_error_detail.restype = i
     lib.gla_status_string.argtypes = [i]
     lib.gla_status_string.restype = ctypes.c_char_p
     lib.gla_version.argtypes = []
@@ -137,6 +139,13 @@ def gla_decode_step(q, k, v, log_alpha, state, out, B, H, dk, dv, stream=None) -
 
 def gla_device_error(stream=None) -> int:
     return load().gla_device_error(_stream(stream))
+
+
+def gla_device_error_detail(stream=None):
+    """(status, [flags, first wait, thread, cta]) of the device error record (not cleared)."""
+    buf = (ctypes.c_uint * 4)()
+    st = load().gla_device_error_detail(_stream(stream), buf)
+    return st, list(buf)
 
 
 def gla_status_string(status: int) -> str:

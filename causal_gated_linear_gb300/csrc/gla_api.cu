@@ -10,8 +10,10 @@
 
 namespace gla {
 
-// Set (bitwise OR) by kernels whose bounded pipeline waits ran out.
-__device__ unsigned g_err_word;
+// Device error record.  [0]: flags (bitwise OR) set by kernels whose bounded
+// pipeline waits ran out; [1..3]: details of the first such wait (see
+// gla_device_error_detail in gla.h).
+__device__ unsigned g_err_word[4];
 
 EncodeTiledFn encode_tiled_fn() {
     void* fn = nullptr;
@@ -49,8 +51,8 @@ int read_and_clear_error(cudaStream_t s) {
     unsigned w = 0;
     if (cudaMemcpyFromSymbol(&w, g_err_word, sizeof(w)) != cudaSuccess) return GLA_ERR_CUDA;
     if (w) {
-        const unsigned zero = 0;
-        if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(zero)) != cudaSuccess) return GLA_ERR_CUDA;
+        const unsigned zero[4] = {0, 0, 0, 0};
+        if (cudaMemcpyToSymbol(g_err_word, zero, sizeof(zero)) != cudaSuccess) return GLA_ERR_CUDA;
         return GLA_ERR_TIMEOUT;
     }
     return GLA_OK;
@@ -203,6 +205,13 @@ int gla_decode_step(const void* q, const void* k, const void* v, const float* lo
 }
 
 int gla_device_error(void* stream) { return read_and_clear_error(static_cast<cudaStream_t>(stream)); }
+
+int gla_device_error_detail(void* stream, unsigned* detail4) {
+    if (!detail4) return GLA_ERR_INVALID;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GLA_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(detail4, g_err_word, 4 * sizeof(unsigned)) != cudaSuccess) return GLA_ERR_CUDA;
+    return GLA_OK;
+}
 
 const char* gla_status_string(int status) {
     switch (status) {

@@ -70,6 +70,16 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Record a wait that ran out: flag word, then (first timeout only) which
+// barrier (shared address | parity << 31), which thread and which CTA.
+__device__ __forceinline__ void record_timeout(unsigned* err_word, uint32_t what, uint32_t parity) {
+    atomicOr(err_word, kErrTimeout);
+    if (atomicCAS(err_word + 1, 0u, what | (parity << 31) | 1u) == 0u) {
+        err_word[2] = threadIdx.x;
+        err_word[3] = blockIdx.x;
+    }
+}
+
 // Wait until the phase with the given parity has completed.  Returns false
 // (and raises the CTA's abort flag and the device error word) if it does not
 // complete within kWaitLimitNs, or if another role already aborted.
@@ -83,7 +93,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
             if (*abort_flag) return false;
             if (globaltimer() - t0 > kWaitLimitNs) {
                 *abort_flag = 1;
-                if (err_word) atomicOr(err_word, kErrTimeout);
+                if (err_word) record_timeout(err_word, bar, parity);
                 return false;
             }
         }

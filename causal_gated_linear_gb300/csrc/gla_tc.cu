@@ -94,8 +94,8 @@ enum {
     B_P_EMPTY,
     B_DS_FULL,
     B_DS_EMPTY,
-    B_S_READY,
-    B_SB_EMPTY,  // 2
+    B_S_READY,   // 2 (the state role may run two chunks ahead of O_i)
+    B_SB_EMPTY = B_S_READY + 2,  // 2
     B_O_FULL = B_SB_EMPTY + 2,
     B_O_EMPTY,
     B_DRAIN,
@@ -150,6 +150,77 @@ __device__ __forceinline__ int lane_to_col(int warp_quarter, int lane) {
     return lane < 16 ? warp_quarter * 16 + lane : -1;
 }
 
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Gate factor phase of one gate thread: TPS tokens (its segment) x 4 key
+// channels.  `off` holds (prefix of earlier segments - chunk total) in natural
+// log units; the running value is kept in log2 units so that each factor is a
+// single ex2:  Qh = q * 2^{(b_t - b_C) log2 e},  Kh = k * 2^{-(b_t - b_C) log2 e}.
+// The feature map and the gate are compile-time branches so that the token
+// loop stays one basic block the scheduler can interleave.
+template <int DK, int TPS, int G, bool GATE, bool ELU>
+__device__ __forceinline__ void gate_factors(uint8_t* qt, uint8_t* kt, const float* la, int seg, int col, int nval,
+                                             const float (&off)[4]) {
+    constexpr float kLog2e = 1.4426950408889634f;
+    float run[4];
+#pragma unroll
+    for (int e = 0; e < 4; e++) run[e] = off[e] * kLog2e;
+#pragma unroll
+    for (int i0 = 0; i0 < TPS; i0 += G) {
+        uint2 qr[G], kr[G];
+        float4 lx[G];
+#pragma unroll
+        for (int u = 0; u < G; u++) {
+            const int t = seg * TPS + i0 + u;
+            const uint32_t o = sw128_offset(t, col);
+            qr[u] = *reinterpret_cast<const uint2*>(qt + o);
+            kr[u] = *reinterpret_cast<const uint2*>(kt + o);
+            if (GATE) lx[u] = *reinterpret_cast<const float4*>(la + t * DK);
+        }
+#pragma unroll
+        for (int u = 0; u < G; u++) {
+            const int t = seg * TPS + i0 + u;
+            const float keep = t < nval ? 1.f : 0.f;  // padding tokens must not write the state
+            const float2 q01 = unpack_bf16x2(qr[u].x), q23 = unpack_bf16x2(qr[u].y);
+            const float2 k01 = unpack_bf16x2(kr[u].x), k23 = unpack_bf16x2(kr[u].y);
+            float qv[4] = {q01.x, q01.y, q23.x, q23.y};
+            float kv[4] = {k01.x, k01.y, k23.x, k23.y};
+            if (GATE) {
+                run[0] = fmaf(lx[u].x, kLog2e, run[0]);
+                run[1] = fmaf(lx[u].y, kLog2e, run[1]);
+                run[2] = fmaf(lx[u].z, kLog2e, run[2]);
+                run[3] = fmaf(lx[u].w, kLog2e, run[3]);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                if (ELU) {
+                    qv[e] = elu1(qv[e]);
+                    kv[e] = elu1(kv[e]);
+                }
+                float fq = keep, fk = keep;
+                if (GATE) {  // run = (b_t - b_C) log2 e >= 0
+                    fq *= ex2_approx(run[e]);
+                    fk *= ex2_approx(-run[e]);
+                }
+                qv[e] *= fq;
+                kv[e] *= fk;
+            }
+            qr[u] = make_uint2(pack_bf16x2(qv[0], qv[1]), pack_bf16x2(qv[2], qv[3]));
+            kr[u] = make_uint2(pack_bf16x2(kv[0], kv[1]), pack_bf16x2(kv[2], kv[3]));
+        }
+#pragma unroll
+        for (int u = 0; u < G; u++) {
+            const uint32_t o = sw128_offset(seg * TPS + i0 + u, col);
+            *reinterpret_cast<uint2*>(qt + o) = qr[u];
+            *reinterpret_cast<uint2*>(kt + o) = kr[u];
+        }
+    }
+}
+
 template <int DK, int DVT, bool GATE>
 __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __grid_constant__ TcParams p) {
     using Ly = Layout<DK, DVT>;
@@ -202,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
         mbar_init(bar(B_DS_FULL), 1);
         mbar_init(bar(B_DS_EMPTY), 8);
         mbar_init(bar(B_S_READY), 8);
+        mbar_init(bar(B_S_READY + 1), 8);
         mbar_init(bar(B_SB_EMPTY), 1);
         mbar_init(bar(B_SB_EMPTY + 1), 1);
         mbar_init(bar(B_O_FULL), 1);
@@ -297,58 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             if (GATE || elu || nval < C) {
                 uint8_t* qt = sm + Ly::off_qk + s * Ly::STAGE_QK + atom * 8192;
                 uint8_t* kt = qt + Ly::QB;
-                float run[4] = {off[0], off[1], off[2], off[3]};
-#pragma unroll
-                for (int i0 = 0; i0 < TPS; i0 += G) {
-                    uint2 qr[G], kr[G];
-                    float4 lx[G];
-#pragma unroll
-                    for (int u = 0; u < G; u++) {
-                        const int t = seg * TPS + i0 + u;
-                        const uint32_t o = sw128_offset(t, col);
-                        qr[u] = *reinterpret_cast<const uint2*>(qt + o);
-                        kr[u] = *reinterpret_cast<const uint2*>(kt + o);
-                        if (GATE) lx[u] = *reinterpret_cast<const float4*>(la + t * DK);
-                    }
-#pragma unroll
-                    for (int u = 0; u < G; u++) {
-                        const int t = seg * TPS + i0 + u;
-                        const float2 q01 = unpack_bf16x2(qr[u].x), q23 = unpack_bf16x2(qr[u].y);
-                        const float2 k01 = unpack_bf16x2(kr[u].x), k23 = unpack_bf16x2(kr[u].y);
-                        float qv[4] = {q01.x, q01.y, q23.x, q23.y};
-                        float kv[4] = {k01.x, k01.y, k23.x, k23.y};
-                        if (GATE) {
-                            run[0] += lx[u].x;
-                            run[1] += lx[u].y;
-                            run[2] += lx[u].z;
-                            run[3] += lx[u].w;
-                        }
-#pragma unroll
-                        for (int e = 0; e < 4; e++) {
-                            if (elu) {
-                                qv[e] = elu1(qv[e]);
-                                kv[e] = elu1(kv[e]);
-                            }
-                            if (GATE) {
-                                const float d = run[e];  // b_t - b_C >= 0
-                                qv[e] *= __expf(d);
-                                kv[e] *= __expf(-d);
-                            }
-                            if (t >= nval) {  // padding tokens must not write the state (elu(0)+1 != 0)
-                                qv[e] = 0.f;
-                                kv[e] = 0.f;
-                            }
-                        }
-                        qr[u] = make_uint2(pack_bf16x2(qv[0], qv[1]), pack_bf16x2(qv[2], qv[3]));
-                        kr[u] = make_uint2(pack_bf16x2(kv[0], kv[1]), pack_bf16x2(kv[2], kv[3]));
-                    }
-#pragma unroll
-                    for (int u = 0; u < G; u++) {
-                        const uint32_t o = sw128_offset(seg * TPS + i0 + u, col);
-                        *reinterpret_cast<uint2*>(qt + o) = qr[u];
-                        *reinterpret_cast<uint2*>(kt + o) = kr[u];
-                    }
-                }
+                if (elu)
+                    gate_factors<DK, TPS, G, GATE, true>(qt, kt, la, seg, col, nval, off);
+                else
+                    gate_factors<DK, TPS, G, GATE, false>(qt, kt, la, seg, col, nval, off);
             }
             if (GATE) {
                 __syncwarp();
@@ -426,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(bar(B_DS_EMPTY));
-                mbar_arrive(bar(B_S_READY));
+                mbar_arrive(bar(B_S_READY + (c & 1)));
             }
             if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(5, c);
         }
@@ -484,11 +508,12 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                 if (!p.out_f32) {
                     __nv_bfloat16* o =
                         reinterpret_cast<__nv_bfloat16*>(ost + (jl >> 6) * 8192) + (jl & 63) + h * 32 * 64;
+                    if (norm) {
 #pragma unroll
-                    for (int t = 0; t < 32; t++) {
-                        float x = __uint_as_float(r[t]);
-                        if (norm) x = x / den[h * 32 + t];
-                        o[t * 64] = __float2bfloat16_rn(x);
+                        for (int t = 0; t < 32; t++) o[t * 64] = __float2bfloat16_rn(__uint_as_float(r[t]) / den[h * 32 + t]);
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < 32; t++) o[t * 64] = __float2bfloat16_rn(__uint_as_float(r[t]));
                     }
                 } else {
                     float* o = static_cast<float*>(p.out) + ((long)bh * L + (long)c * C + h * 32) * dv + j0 + jl;
@@ -623,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                     no++;
                     prog = true;
                 }
-                if (ni < N && ni == no && ni < nd && mbar_test(bar(B_S_READY), ni & 1) &&
+                if (ni < N && ni == no && ni < nd && mbar_test(bar(B_S_READY + (ni & 1)), (ni >> 1) & 1) &&
                     mbar_test(bar(B_O_EMPTY), (ni & 1) ^ 1)) {
                     tc_fence_after();
                     GLA_TRACE_POINT(7, ni);
@@ -679,7 +704,9 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                     if (idle == 256) t_last = now;
                     else if (now - t_last > kWaitLimitNs) {
                         *abort_flag = 1;
-                        atomicOr(p.err, kErrTimeout);
+                        // scheduler progress at the time: next dS, A, O_i, O_a chunk (8 bits each)
+                        record_timeout(p.err, 0x40000000u | ((nd & 0xff) << 22) | ((na & 0xff) << 14) |
+                                                  ((ni & 0xff) << 6) | ((no & 0x1f) << 1), 0);
                         break;
                     }
                 }

@@ -69,7 +69,10 @@ def run_prefill(w: synth.Workload, x: dict, out_f32=False, flags=0, final_z=Fals
                         stream=stream)
     gla.check(st)
     torch.cuda.synchronize()
-    gla.check(gla.gla_device_error())
+    _, detail = gla.gla_device_error_detail()
+    if detail[0]:
+        gla.gla_device_error()
+        raise gla.GlaError(f"device wait timed out: {[hex(x) for x in detail]}")
     return (out.float().cpu().numpy().astype(np.float64), fs.cpu().numpy().astype(np.float64),
             None if fz is None else fz.cpu().numpy().astype(np.float64))
 
