@@ -70,8 +70,8 @@ constexpr int kGateThreads = 256;
 // tensor-memory column map (512 columns allocated)
 constexpr uint32_t TM_S = 0;     // S^T fp32, dk columns
 constexpr uint32_t TM_DS = 128;  // dS^T fp32, dk columns
-constexpr uint32_t TM_SB = 256;  // 2 x bf16 copies of S'^T, dk/2 columns each
-constexpr uint32_t TM_O = 384;   // O^T fp32, 64 columns
+constexpr uint32_t TM_SB = 256;  // bf16 copy of S'^T, dk/2 columns
+constexpr uint32_t TM_O = 320;   // 2 x O^T fp32, 64 columns each
 constexpr uint32_t TM_A = 448;   // A fp32, 64 columns
 constexpr uint32_t TM_COLS = 512;
 
@@ -94,11 +94,11 @@ enum {
     B_P_EMPTY,
     B_DS_FULL,
     B_DS_EMPTY,
-    B_S_READY,   // 2 (the state role may run two chunks ahead of O_i)
-    B_SB_EMPTY = B_S_READY + 2,  // 2
-    B_O_FULL = B_SB_EMPTY + 2,
-    B_O_EMPTY,
-    B_DRAIN,
+    B_S_READY,   // 2
+    B_SB_EMPTY = B_S_READY + 2,
+    B_O_FULL,    // 2
+    B_O_EMPTY = B_O_FULL + 2,  // 2
+    B_DRAIN = B_O_EMPTY + 2,
     B_COUNT
 };
 
@@ -124,7 +124,7 @@ struct Layout {
     static constexpr int off_den = off_segtot + 2 * SEG * DK * 4;
     static constexpr int off_bar = off_den + C * 4;
     static constexpr int off_misc = off_bar + B_COUNT * 8;
-    static constexpr int total = off_misc + 16;
+    static constexpr int total = off_misc + 8;  // TMEM base address, abort flag
     static constexpr int alloc = total + 1008;  // round-up to 1024 from a >= 16-byte aligned base
     static_assert(alloc <= 232448, "shared memory budget");
 };
@@ -275,9 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
         mbar_init(bar(B_S_READY), 8);
         mbar_init(bar(B_S_READY + 1), 8);
         mbar_init(bar(B_SB_EMPTY), 1);
-        mbar_init(bar(B_SB_EMPTY + 1), 1);
         mbar_init(bar(B_O_FULL), 1);
+        mbar_init(bar(B_O_FULL + 1), 1);
         mbar_init(bar(B_O_EMPTY), 4);
+        mbar_init(bar(B_O_EMPTY + 1), 4);
         mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0;
         mbar_fence_init();
@@ -418,11 +419,12 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             const int s = c % NS;
             ok = mbar_wait_warp(bar(B_DS_FULL), c & 1, abort_flag, p.err);
             if (ok && GATE) ok = mbar_wait_warp(bar(B_QK_GATED + s), (c / NS) & 1, abort_flag, p.err);
-            if (ok) ok = mbar_wait_warp(bar(B_SB_EMPTY + (c & 1)), ((c >> 1) & 1) ^ 1, abort_flag, p.err);
+            // the single bf16 copy of S' is free once O_i(c-1) has completed
+            if (ok) ok = mbar_wait_warp(bar(B_SB_EMPTY), (c & 1) ^ 1, abort_flag, p.err);
             if (!ok) break;
             tc_fence_after();
             if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(4, c);
-            const uint32_t tSB = tmem + lane_field + TM_SB + (c & 1) * (DK / 2);
+            const uint32_t tSB = tmem + lane_field + TM_SB;
 #pragma unroll 1
             for (int g = 0; g < COLS / 16; g++) {
                 const int c0 = cbase + g * 16;
@@ -479,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
         const bool leader = warp == W_OUT0 && lane == 0;
         uint8_t* ost = sm + Ly::off_ost;
         for (int c = 0; c < N; c++) {
-            bool ok = mbar_wait_warp(bar(B_O_FULL), c & 1, abort_flag, p.err);
+            bool ok = mbar_wait_warp(bar(B_O_FULL + (c & 1)), (c >> 1) & 1, abort_flag, p.err);
             // staging may be rewritten once the previous bulk store has read it
             if (leader && !p.out_f32) bulk_wait_group_read0();
             ok = bar_red_and(2, 128, ok);
@@ -490,12 +492,12 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
 #pragma unroll 1
             for (int h = 0; h < 2; h++) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_field + TM_O + h * 32, r);
+                tmem_ld32(tmem + lane_field + TM_O + (c & 1) * 64 + h * 32, r);
                 tmem_wait_ld();
                 if (h == 1) {
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(B_O_EMPTY));
+                    if (lane == 0) mbar_arrive(bar(B_O_EMPTY + (c & 1)));
                 }
                 if (norm) {
                     if (jl == 64) {
@@ -639,17 +641,18 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                     const uint32_t Vs = vs_of(no);
 #pragma unroll
                     for (int kk = 0; kk < C / 16; kk++)
-                        mma_ss(tmem + TM_O, make_sdesc(Vs + kk * 2048, 8192, 1024), make_sdesc(Ps + kk * 32, 16, 1024),
+                        mma_ss(tmem + TM_O + (no & 1) * 64, make_sdesc(Vs + kk * 2048, 8192, 1024),
+                               make_sdesc(Ps + kk * 32, 16, 1024),
                                idOa, 1);
-                    mma_commit(bar(B_O_FULL));
+                    mma_commit(bar(B_O_FULL + (no & 1)));
                     mma_commit(bar(B_P_EMPTY));
                     mma_commit(bar(B_V_EMPTY + no % NV));
                     GLA_TRACE_POINT(6, no);
                     no++;
                     prog = true;
                 }
-                if (ni < N && ni == no && ni < nd && mbar_test(bar(B_S_READY + (ni & 1)), (ni >> 1) & 1) &&
-                    mbar_test(bar(B_O_EMPTY), (ni & 1) ^ 1)) {
+                if (ni < N && ni < nd && mbar_test(bar(B_S_READY + (ni & 1)), (ni >> 1) & 1) &&
+                    mbar_test(bar(B_O_EMPTY + (ni & 1)), ((ni >> 1) & 1) ^ 1)) {
                     tc_fence_after();
                     GLA_TRACE_POINT(7, ni);
                     const uint32_t Qs = qs_of(ni);
@@ -657,10 +660,10 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
 #pragma unroll
                     for (int kk = 0; kk < DK / 16; kk++) {
                         const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-                        mma_ts(tmem + TM_O, tmem + TM_SB + (ni & 1) * (DK / 2) + kk * 8, make_sdesc(Qs + off, 16, 1024),
+                        mma_ts(tmem + TM_O + (ni & 1) * 64, tmem + TM_SB + kk * 8, make_sdesc(Qs + off, 16, 1024),
                                idOi, kk > 0);
                     }
-                    mma_commit(bar(B_SB_EMPTY + (ni & 1)));
+                    mma_commit(bar(B_SB_EMPTY));
                     ni++;
                     prog = true;
                 }
