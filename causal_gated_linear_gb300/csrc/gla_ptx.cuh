@@ -80,6 +80,16 @@ __device__ __forceinline__ void record_timeout(unsigned* err_word, uint32_t what
     }
 }
 
+// Record a polling loop that made no progress for too long (code: caller-defined
+// bit pattern with bit 29 or 30 set, see gla_device_error_detail).
+__device__ __forceinline__ void record_timeout_code(unsigned* err_word, uint32_t code) {
+    atomicOr(err_word, kErrTimeout);
+    if (atomicCAS(err_word + 1, 0u, code | 1u) == 0u) {
+        err_word[2] = threadIdx.x;
+        err_word[3] = blockIdx.x;
+    }
+}
+
 // Wait until the phase with the given parity has completed.  Returns false
 // (and raises the CTA's abort flag and the device error word) if it does not
 // complete within kWaitLimitNs, or if another role already aborted.

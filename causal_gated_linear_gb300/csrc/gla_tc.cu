@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
     const uint32_t tmem = *tmem_slot;
     const uint32_t lane_field = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
-    int last_issued = -1;  // producer: last chunk whose loads were issued
+    int pl_n = 0, pq_n = 0, pv_n = 0;  // producer: chunks whose log-alpha / q,k / v loads were issued
 
     if (warp < W_STATE0) {
         // ============================================================ gate
@@ -589,31 +589,56 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             tma_prefetch_desc(&p.tm_v);
             if (GATE) tma_prefetch_desc(&p.tm_la);
             if (!p.out_f32) tma_prefetch_desc(&p.tm_out);
-            for (int c = 0; c < N; c++) {
-                const int row = c * C;
-                GLA_TRACE_POINT(0, c);
-                if (GATE) {
-                    const int l = c % NL;
-                    if (!mbar_wait(bar(B_LA_EMPTY + l), ((c / NL) & 1) ^ 1, abort_flag, p.err)) break;
+            // The three rings are refilled independently (a full V ring must not hold
+            // back the next chunk's q/k and log alpha loads).
+            uint32_t idle = 0;
+            unsigned long long t_last = 0;
+            const int nl_end = GATE ? N : 0;
+            while (pl_n < nl_end || pq_n < N || pv_n < N) {
+                bool prog = false;
+                if (pl_n < nl_end && pl_n <= pq_n + 1 &&
+                    mbar_test(bar(B_LA_EMPTY + pl_n % NL), ((pl_n / NL) & 1) ^ 1)) {
+                    const int l = pl_n % NL;
                     mbar_arrive_expect_tx(bar(B_LA_FULL + l), Ly::LAB);
-                    tma_load_3d(sbase + Ly::off_la + l * Ly::LAB, &p.tm_la, bar(B_LA_FULL + l), 0, row, bh);
+                    tma_load_3d(sbase + Ly::off_la + l * Ly::LAB, &p.tm_la, bar(B_LA_FULL + l), 0, pl_n * C, bh);
+                    pl_n++;
+                    prog = true;
                 }
-                const int s = c % NS;
-                if (!mbar_wait(bar(B_QK_EMPTY + s), ((c / NS) & 1) ^ 1, abort_flag, p.err)) break;
-                mbar_arrive_expect_tx(bar(B_QK_FULL + s), 2 * Ly::QB);
-                const uint32_t qdst = sbase + Ly::off_qk + s * Ly::STAGE_QK;
-                for (int a = 0; a < DK / 64; a++) {
-                    tma_load_3d(qdst + a * 8192, &p.tm_q, bar(B_QK_FULL + s), a * 64, row, bh);
-                    tma_load_3d(qdst + Ly::QB + a * 8192, &p.tm_k, bar(B_QK_FULL + s), a * 64, row, bh);
+                if (pq_n < N && mbar_test(bar(B_QK_EMPTY + pq_n % NS), ((pq_n / NS) & 1) ^ 1)) {
+                    const int s = pq_n % NS;
+                    GLA_TRACE_POINT(1, pq_n);
+                    mbar_arrive_expect_tx(bar(B_QK_FULL + s), 2 * Ly::QB);
+                    const uint32_t qdst = sbase + Ly::off_qk + s * Ly::STAGE_QK;
+                    for (int a = 0; a < DK / 64; a++) {
+                        tma_load_3d(qdst + a * 8192, &p.tm_q, bar(B_QK_FULL + s), a * 64, pq_n * C, bh);
+                        tma_load_3d(qdst + Ly::QB + a * 8192, &p.tm_k, bar(B_QK_FULL + s), a * 64, pq_n * C, bh);
+                    }
+                    pq_n++;
+                    prog = true;
                 }
-                const int v = c % NV;
-                if (!mbar_wait(bar(B_V_EMPTY + v), ((c / NV) & 1) ^ 1, abort_flag, p.err)) break;
-                mbar_arrive_expect_tx(bar(B_V_FULL + v), nvb * 8192);
-                for (int blk = 0; blk < nvb; blk++)
-                    tma_load_3d(sbase + Ly::off_v + v * Ly::VB + blk * 8192, &p.tm_v, bar(B_V_FULL + v),
-                                j0 + blk * 64, row, bh);
-                last_issued = c;
-                GLA_TRACE_POINT(1, c);
+                if (pv_n < N && mbar_test(bar(B_V_EMPTY + pv_n % NV), ((pv_n / NV) & 1) ^ 1)) {
+                    const int v = pv_n % NV;
+                    mbar_arrive_expect_tx(bar(B_V_FULL + v), nvb * 8192);
+                    for (int blk = 0; blk < nvb; blk++)
+                        tma_load_3d(sbase + Ly::off_v + v * Ly::VB + blk * 8192, &p.tm_v, bar(B_V_FULL + v),
+                                    j0 + blk * 64, pv_n * C, bh);
+                    pv_n++;
+                    prog = true;
+                }
+                if (prog) {
+                    idle = 0;
+                } else if ((++idle & 255u) == 0) {
+                    if (*abort_flag) break;
+                    const unsigned long long now = globaltimer();
+                    if (idle == 256) {
+                        t_last = now;
+                    } else if (now - t_last > kWaitLimitNs) {
+                        *abort_flag = 1;
+                        record_timeout_code(p.err, 0x20000000u | ((pl_n & 0xff) << 16) | ((pq_n & 0xff) << 8) |
+                                                       (pv_n & 0xff));
+                        break;
+                    }
+                }
             }
         }
     } else {
@@ -708,8 +733,8 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                     else if (now - t_last > kWaitLimitNs) {
                         *abort_flag = 1;
                         // scheduler progress at the time: next dS, A, O_i, O_a chunk (8 bits each)
-                        record_timeout(p.err, 0x40000000u | ((nd & 0xff) << 22) | ((na & 0xff) << 14) |
-                                                  ((ni & 0xff) << 6) | ((no & 0x1f) << 1), 0);
+                        record_timeout_code(p.err, 0x40000000u | ((nd & 0xff) << 22) | ((na & 0xff) << 14) |
+                                                       ((ni & 0xff) << 6) | ((no & 0x1f) << 1));
                         break;
                     }
                 }
@@ -722,14 +747,12 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
     }
 
     // ---------------------------------------------------------------- teardown
-    if (warp == W_TMA && lane == 0 && *abort_flag && last_issued >= 0) {
+    if (warp == W_TMA && lane == 0 && *abort_flag) {
         // wait (bounded) for loads that may still be in flight
         volatile int no_abort = 0;
-        for (int c = max(0, last_issued - NS + 1); c <= last_issued; c++) {
-            mbar_wait(bar(B_QK_FULL + c % NS), (c / NS) & 1, &no_abort, p.err);
-            mbar_wait(bar(B_V_FULL + c % NV), (c / NV) & 1, &no_abort, p.err);
-            if (GATE) mbar_wait(bar(B_LA_FULL + c % NL), (c / NL) & 1, &no_abort, p.err);
-        }
+        for (int c = max(0, pq_n - NS); c < pq_n; c++) mbar_wait(bar(B_QK_FULL + c % NS), (c / NS) & 1, &no_abort, p.err);
+        for (int c = max(0, pv_n - NV); c < pv_n; c++) mbar_wait(bar(B_V_FULL + c % NV), (c / NV) & 1, &no_abort, p.err);
+        for (int c = max(0, pl_n - NL); c < pl_n; c++) mbar_wait(bar(B_LA_FULL + c % NL), (c / NL) & 1, &no_abort, p.err);
     }
     __syncwarp();
     tc_fence_before();

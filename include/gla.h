@@ -132,7 +132,8 @@ int gla_device_error(void* stream);
  * the device error record into detail4[4]: [0] flags (bit 0 = a bounded wait
  * timed out), [1] the first timed-out wait (shared-memory barrier address,
  * bit 31 = awaited parity, bit 0 set; bit 30 set = the MMA issuer's
- * readiness loop, with its chunk counters in bits 1-29), [2] thread index,
+ * readiness loop, with its chunk counters in bits 1-29; bit 29 set = the TMA
+ * producer's loop, with its chunk counters in bits 0-23), [2] thread index,
  * [3] CTA index.  For diagnosing a GLA_ERR_TIMEOUT; gla_device_error clears it.
  */
 int gla_device_error_detail(void* stream, unsigned* detail4);
