@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
         for (int i = 0; i < NS; i++) {
             mbar_init(bar(B_QK_FULL + i), 1);
             mbar_init(bar(B_QK_GATED + i), 8);
-            mbar_init(bar(B_QK_EMPTY + i), 1);
+            mbar_init(bar(B_QK_EMPTY + i), 2);  // released by the A issuer and the O_i issuer
         }
         for (int i = 0; i < NL; i++) {
             mbar_init(bar(B_LA_FULL + i), 1);
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
         mbar_init(bar(B_O_FULL + 1), 1);
         mbar_init(bar(B_O_EMPTY), 4);
         mbar_init(bar(B_O_EMPTY + 1), 4);
-        mbar_init(bar(B_DRAIN), 1);
+        mbar_init(bar(B_DRAIN), 2);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -591,11 +591,31 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             if (!p.out_f32) tma_prefetch_desc(&p.tm_out);
             // The three rings are refilled independently (a full V ring must not hold
             // back the next chunk's q/k and log alpha loads).
+            // This thread also issues A(c) = Qh_c Kh_c^T: a single thread issues one
+            // MMA per ~90 cycles, so the products are split over two issuers.
+            constexpr uint32_t idA = make_idesc_bf16(128, 64, 0, 0);
+            int na = 0;
             uint32_t idle = 0;
             unsigned long long t_last = 0;
             const int nl_end = GATE ? N : 0;
-            while (pl_n < nl_end || pq_n < N || pv_n < N) {
+            while (pl_n < nl_end || pq_n < N || pv_n < N || na < N) {
                 bool prog = false;
+                if (na < pq_n && mbar_test(bar(B_QK_GATED + na % NS), (na / NS) & 1) &&
+                    mbar_test(bar(B_A_EMPTY), (na & 1) ^ 1)) {
+                    tc_fence_after();
+                    const uint32_t Qs = sbase + Ly::off_qk + (na % NS) * Ly::STAGE_QK, Ks = Qs + Ly::QB;
+                    // rows 64..127 of the M=128 tile read past the Q tile and are ignored
+#pragma unroll
+                    for (int kk = 0; kk < DK / 16; kk++) {
+                        const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+                        mma_ss(tmem + TM_A, make_sdesc(Qs + off, 16, 1024), make_sdesc(Ks + off, 16, 1024), idA,
+                               kk > 0);
+                    }
+                    mma_commit(bar(B_A_FULL));
+                    mma_commit(bar(B_QK_EMPTY + na % NS));
+                    na++;
+                    prog = true;
+                }
                 if (pl_n < nl_end && pl_n <= pq_n + 1 &&
                     mbar_test(bar(B_LA_EMPTY + pl_n % NL), ((pl_n / NL) & 1) ^ 1)) {
                     const int l = pl_n % NL;
@@ -640,11 +660,11 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                     }
                 }
             }
+            mma_commit(bar(B_DRAIN));
         }
     } else {
         // ============================================================ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idA = make_idesc_bf16(128, 64, 0, 0);
             constexpr uint32_t idS = make_idesc_bf16(DVT, DK, 1, 1);
             constexpr uint32_t idOi = make_idesc_bf16(DVT, 64, 0, 0);
             constexpr uint32_t idOa = make_idesc_bf16(DVT, 64, 1, 0);
@@ -705,22 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                     nd++;
                     prog = true;
                 }
-                if (na < N && mbar_test(bar(B_QK_GATED + na % NS), (na / NS) & 1) &&
-                    mbar_test(bar(B_A_EMPTY), (na & 1) ^ 1)) {
-                    tc_fence_after();
-                    const uint32_t Qs = qs_of(na), Ks = Qs + Ly::QB;
-                    // A(c) = Qh_c Kh_c^T (rows 64..127 of the M=128 tile read past the Q tile and are ignored)
-#pragma unroll
-                    for (int kk = 0; kk < DK / 16; kk++) {
-                        const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-                        mma_ss(tmem + TM_A, make_sdesc(Qs + off, 16, 1024), make_sdesc(Ks + off, 16, 1024), idA,
-                               kk > 0);
-                    }
-                    mma_commit(bar(B_A_FULL));
-                    na++;
-                    prog = true;
-                }
-                while (nq < ni && nq < na) {  // dS(nq) precedes O_i(nq), so all three were issued
+                while (nq < ni) {  // dS(nq) precedes O_i(nq); A(nq) is released by its own issuer
                     mma_commit(bar(B_QK_EMPTY + nq % NS));
                     nq++;
                 }
