@@ -169,7 +169,7 @@ __device__ __forceinline__ void gate_factors(uint8_t* qt, uint8_t* kt, const flo
     float run[4];
 #pragma unroll
     for (int e = 0; e < 4; e++) run[e] = off[e] * kLog2e;
-#pragma unroll
+#pragma unroll 1
     for (int i0 = 0; i0 < TPS; i0 += G) {
         uint2 qr[G], kr[G];
         float4 lx[G];
@@ -549,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             if (!mbar_wait_warp(bar(B_P_EMPTY), (c & 1) ^ 1, abort_flag, p.err)) break;
             tc_fence_after();
             if (t == 0) GLA_TRACE_POINT(10, c);
-#pragma unroll
+#pragma unroll 1
             for (int h = 0; h < 2; h++) {
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_field + TM_A + h * 32, r);
