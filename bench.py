@@ -245,6 +245,8 @@ def bench_prefill(args, device, rank, world):
 
     import causal_gated_linear_gb300 as gla
     w = synth.with_shape(PREFILL, seed=PREFILL.seed + 1000 * rank)
+    if args.L:  # reduced sequence length (profiling a small case); the line names it
+        w = synth.with_shape(w, L=args.L, name=f"{PREFILL.name}_L{args.L}")
     x = synth.make_prefill(w)
     BH = w.B * w.H
     q, k, v = (to_dev(x[n], device) for n in ("q", "k", "v"))
@@ -439,6 +441,8 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--ref-seconds", type=float, default=10.0)
+    ap.add_argument("--L", type=int, default=0,
+                    help="override the prefill sequence length (small cases for ncu captures)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # timing rule: at least 3 warm-up steps
     if args.impl == "reference":
