@@ -121,10 +121,9 @@ struct Layout {
     static constexpr int off_ost = off_p + PB;
     static constexpr int off_gamma = off_ost + OSB;
     static constexpr int off_segtot = off_gamma + NS * DK * 4;
-    static constexpr int off_den = off_segtot + 2 * SEG * DK * 4;
-    static constexpr int off_bar = off_den + C * 4;
+    static constexpr int off_bar = off_segtot + 2 * SEG * DK * 4;
     static constexpr int off_misc = off_bar + B_COUNT * 8;
-    static constexpr int total = off_misc + 8;  // TMEM base address, abort flag
+    static constexpr int total = off_misc + 12;  // TMEM base address, abort flag, O_i count
     static constexpr int alloc = total + 1008;  // round-up to 1024 from a >= 16-byte aligned base
     static_assert(alloc <= 232448, "shared memory budget");
 };
@@ -234,9 +233,13 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Ly::off_bar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Ly::off_misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Ly::off_misc + 4);
+    // number of O_i products issued so far (written by the MMA thread, read by the A issuer)
+    volatile int* oi_issued = reinterpret_cast<volatile int*>(sm + Ly::off_misc + 8);
     float* gamma = reinterpret_cast<float*>(sm + Ly::off_gamma);
     float* segtot = reinterpret_cast<float*>(sm + Ly::off_segtot);
-    float* den = reinterpret_cast<float*>(sm + Ly::off_den);
+    // normaliser denominators: only with GLA_FLAG_NORMALIZE (dv == 64 on a 128-column
+    // tile), when the second 64-column block of the output staging is unused
+    float* den = reinterpret_cast<float*>(sm + Ly::off_ost + 8192);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
     const int warp = threadIdx.x >> 5;
@@ -281,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
         mbar_init(bar(B_O_EMPTY + 1), 4);
         mbar_init(bar(B_DRAIN), 2);
         *abort_flag = 0;
+        *oi_issued = 0;
         mbar_fence_init();
     }
     if (warp == W_MMA) {
@@ -600,7 +604,9 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             const int nl_end = GATE ? N : 0;
             while (pl_n < nl_end || pq_n < N || pv_n < N || na < N) {
                 bool prog = false;
-                if (na < pq_n && mbar_test(bar(B_QK_GATED + na % NS), (na / NS) & 1) &&
+                // A(c) goes into the tensor pipe only after O_i(c-1): the state chain
+                // waits on O_i(c-1), which must not queue behind A(c).
+                if (na < pq_n && na <= *oi_issued && mbar_test(bar(B_QK_GATED + na % NS), (na / NS) & 1) &&
                     mbar_test(bar(B_A_EMPTY), (na & 1) ^ 1)) {
                     tc_fence_after();
                     const uint32_t Qs = sbase + Ly::off_qk + (na % NS) * Ly::STAGE_QK, Ks = Qs + Ly::QB;
@@ -710,6 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                     }
                     mma_commit(bar(B_SB_EMPTY));
                     ni++;
+                    *oi_issued = ni;
                     prog = true;
                 }
                 if (nd < N && mbar_test(bar(B_QK_GATED + nd % NS), (nd / NS) & 1) &&
