@@ -68,9 +68,13 @@ constexpr int W_STATE0 = 8, W_OUT0 = 16, W_P0 = 20, W_TMA = 22, W_MMA = 23;
 constexpr int kGateThreads = 256;
 
 // tensor-memory column map (512 columns allocated)
-constexpr uint32_t TM_S = 0;     // S^T fp32, dk columns
+constexpr uint32_t TM_S = 0;     // S^T fp32, dk columns (128-column tile)
 constexpr uint32_t TM_DS = 128;  // dS^T fp32, dk columns
-constexpr uint32_t TM_SB = 256;  // bf16 copy of S'^T, dk/2 columns
+constexpr uint32_t TM_SB = 256;  // bf16 copy of S'^T, dk/2 columns (128-column tile)
+// With the 64-column tile (M = 64) S^T is held in the state warps'
+// registers instead, and columns 0..127 hold two bf16 copies of S'^T (one
+// per chunk parity), so the state update of chunk c+1 need not wait for
+// O_i(c) to finish reading its copy.
 constexpr uint32_t TM_O = 320;   // 2 x O^T fp32, 64 columns each
 constexpr uint32_t TM_A = 448;   // A fp32, 64 columns
 constexpr uint32_t TM_COLS = 512;
@@ -90,13 +94,13 @@ enum {
     B_V_EMPTY = B_V_FULL + 3,
     B_A_FULL = B_V_EMPTY + 3,
     B_A_EMPTY,
-    B_P_FULL,
-    B_P_EMPTY,
-    B_DS_FULL,
+    B_P_FULL,    // 2
+    B_P_EMPTY = B_P_FULL + 2,  // 2
+    B_DS_FULL = B_P_EMPTY + 2,
     B_DS_EMPTY,
     B_S_READY,   // 2
-    B_SB_EMPTY = B_S_READY + 2,
-    B_O_FULL,    // 2
+    B_SB_EMPTY = B_S_READY + 2,  // 2
+    B_O_FULL = B_SB_EMPTY + 2,   // 2
     B_O_EMPTY = B_O_FULL + 2,  // 2
     B_DRAIN = B_O_EMPTY + 2,
     B_COUNT
@@ -117,8 +121,13 @@ struct Layout {
     static constexpr int off_qk = 0;
     static constexpr int off_la = off_qk + NS * STAGE_QK;
     static constexpr int off_v = off_la + NL * LAB;
+    // a second P buffer where it fits: P(c+1) need not wait for O_a(c)
+    static constexpr int NP = NS * STAGE_QK + NL * LAB + NV * VB + 2 * PB + OSB + NS * DK * 4 + 2 * SEG * DK * 4 +
+                                      B_COUNT * 8 + 12 + 1008 <= 232448
+                                  ? 2
+                                  : 1;
     static constexpr int off_p = off_v + NV * VB;
-    static constexpr int off_ost = off_p + PB;
+    static constexpr int off_ost = off_p + NP * PB;
     static constexpr int off_gamma = off_ost + OSB;
     static constexpr int off_segtot = off_gamma + NS * DK * 4;
     static constexpr int off_bar = off_segtot + 2 * SEG * DK * 4;
@@ -271,13 +280,15 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
         }
         mbar_init(bar(B_A_FULL), 1);
         mbar_init(bar(B_A_EMPTY), 2);
-        mbar_init(bar(B_P_FULL), 2);
-        mbar_init(bar(B_P_EMPTY), 1);
+        for (int i = 0; i < 2; i++) {
+            mbar_init(bar(B_P_FULL + i), 2);
+            mbar_init(bar(B_P_EMPTY + i), 1);
+            mbar_init(bar(B_SB_EMPTY + i), 1);
+        }
         mbar_init(bar(B_DS_FULL), 1);
         mbar_init(bar(B_DS_EMPTY), 8);
         mbar_init(bar(B_S_READY), 8);
         mbar_init(bar(B_S_READY + 1), 8);
-        mbar_init(bar(B_SB_EMPTY), 1);
         mbar_init(bar(B_O_FULL), 1);
         mbar_init(bar(B_O_FULL + 1), 1);
         mbar_init(bar(B_O_EMPTY), 4);
@@ -325,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             bool ok = true;
             if (GATE) ok = mbar_wait(bar(B_LA_FULL + l), (c / NL) & 1, abort_flag, p.err);
             if (ok) ok = mbar_wait(bar(B_QK_FULL + s), (c / NS) & 1, abort_flag, p.err);
+            if (threadIdx.x == 0) GLA_TRACE_POINT(0, c);
             // Phase 1: per-segment cumulative sums of log alpha, exchanged across the
             // gate warps to give each thread the prefix before its segment (off) and
             // the chunk total b_C (tot).  Phase 2 re-reads log alpha from shared
@@ -394,87 +406,171 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
         constexpr int COLS = DK / 2;  // key channels per warp (two warps per lane quarter)
         const int half = (warp - W_STATE0) >> 2;
         const int cbase = half * COLS;
-        const int jl = lane_to_col<DVT>(warp & 3, lane);  // column in the slice, -1 if unused lane
-        const int j = j0 + jl;
-        const uint32_t tS = tmem + lane_field + TM_S;
-        const uint32_t tD = tmem + lane_field + TM_DS;
-        {
-            const float* s0 =
-                (p.init_state && jl >= 0 && jl < jvalid) ? p.init_state + (long)bh * DK * dv + j : nullptr;
-            const bool zl = norm && jl == 64;
-            for (int g = 0; g < COLS / 16; g++) {
-                uint32_t r[16];
+        if constexpr (DVT == 64) {
+            // S^T in registers.  M = 64 rows sit in lanes 0-15 of each quarter; with the
+            // 16x32bx2 TMEM shape threads 0-15 and 16-31 take the same 16 rows at two
+            // column offsets, so the whole warp works: thread (r, hi) owns row r and the
+            // key channels cbase + 32 g + 16 hi + [0, 16).
+            constexpr int NG = COLS / 32;
+            const int hi = lane >> 4;
+            const int jl = lane_to_col<DVT>(warp & 3, lane & 15);
+            const int j = j0 + jl;
+            const bool jv = jl < jvalid;
+            const uint32_t tD = tmem + lane_field + TM_DS;
+            float S[NG * 16];
+            {
+                const float* s0 = (p.init_state && jv) ? p.init_state + (long)bh * DK * dv + j : nullptr;
 #pragma unroll
-                for (int i = 0; i < 16; i++) {
-                    const int d = cbase + g * 16 + i;
-                    float x = 0.f;
-                    if (s0)
-                        x = s0[(long)d * dv];
-                    else if (zl && p.init_z)
-                        x = p.init_z[(long)bh * DK + d];
-                    r[i] = __float_as_uint(x);
-                }
-                tmem_st16(tS + cbase + g * 16, r);
+                for (int g = 0; g < NG; g++)
+#pragma unroll
+                    for (int i = 0; i < 16; i++)
+                        S[g * 16 + i] = s0 ? s0[(long)(cbase + g * 32 + hi * 16 + i) * dv] : 0.f;
+                // first phase of the dS buffer's release (the protocol shared with the
+                // 128-column tile, whose state initialisation writes TMEM)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_DS_EMPTY));
             }
-            tmem_wait_st();
-        }
-        bool ok = true;
-        for (int c = 0; c < N; c++) {
-            const int s = c % NS;
-            ok = mbar_wait_warp(bar(B_DS_FULL), c & 1, abort_flag, p.err);
-            if (ok && GATE) ok = mbar_wait_warp(bar(B_QK_GATED + s), (c / NS) & 1, abort_flag, p.err);
-            // the single bf16 copy of S' is free once O_i(c-1) has completed
-            if (ok) ok = mbar_wait_warp(bar(B_SB_EMPTY), (c & 1) ^ 1, abort_flag, p.err);
-            if (!ok) break;
-            tc_fence_after();
-            if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(4, c);
-            const uint32_t tSB = tmem + lane_field + TM_SB;
-#pragma unroll 1
-            for (int g = 0; g < COLS / 16; g++) {
-                const int c0 = cbase + g * 16;
-                uint32_t rs[16], rd[16];
-                tmem_ld16(tS + c0, rs);
-                tmem_ld16(tD + c0, rd);
-                tmem_wait_ld();
-                uint32_t pk[8];
+            bool ok = true;
+            for (int c = 0; c < N; c++) {
+                const int s = c % NS;
+                const int sb = c & 1;
+                ok = mbar_wait_warp(bar(B_DS_FULL), c & 1, abort_flag, p.err);
+                if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(16, c);
+                if (ok && GATE) ok = mbar_wait_warp(bar(B_QK_GATED + s), (c / NS) & 1, abort_flag, p.err);
+                if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(17, c);
+                // this chunk's bf16 copy of S' is free once O_i(c-2) has completed
+                if (ok) ok = mbar_wait_warp(bar(B_SB_EMPTY + sb), ((c >> 1) & 1) ^ 1, abort_flag, p.err);
+                if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(18, c);
+                if (!ok) break;
+                tc_fence_after();
+                if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(4, c);
+                const uint32_t tSB = tmem + lane_field + (uint32_t)sb * 64u;
 #pragma unroll
-                for (int i = 0; i < 16; i += 2) {
-                    float s0v = __uint_as_float(rs[i]), s1v = __uint_as_float(rs[i + 1]);
-                    if (GATE) {
-                        s0v *= gamma[s * DK + c0 + i];
-                        s1v *= gamma[s * DK + c0 + i + 1];
+                for (int g = 0; g < NG * 2; g++) {
+                    // 8 key channels per half-warp: c0 + [0, 8) for threads 0-15, c0 + 16 + [0, 8)
+                    // for threads 16-31 (S index g/2 * 16 + (g&1) * 8 + i)
+                    const int c0 = cbase + (g >> 1) * 32 + (g & 1) * 8;
+                    uint32_t d[8];
+                    tmem_ld16x2_x8<16>(tD + c0, d);
+                    tmem_wait_ld();
+                    const float* gm = gamma + s * DK + c0 + hi * 16;
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int i = 0; i < 8; i += 4) {
+                        float4 gv = make_float4(1.f, 1.f, 1.f, 1.f);
+                        if (GATE) gv = *reinterpret_cast<const float4*>(gm + i);
+                        float* sv = S + g * 8 + i;
+                        const float a0 = sv[0] * gv.x, a1 = sv[1] * gv.y, a2 = sv[2] * gv.z, a3 = sv[3] * gv.w;
+                        pk[i / 2] = pack_bf16x2(a0, a1);
+                        pk[i / 2 + 1] = pack_bf16x2(a2, a3);
+                        sv[0] = a0 + __uint_as_float(d[i]);
+                        sv[1] = a1 + __uint_as_float(d[i + 1]);
+                        sv[2] = a2 + __uint_as_float(d[i + 2]);
+                        sv[3] = a3 + __uint_as_float(d[i + 3]);
                     }
-                    pk[i / 2] = pack_bf16x2(s0v, s1v);
-                    rs[i] = __float_as_uint(s0v + __uint_as_float(rd[i]));
-                    rs[i + 1] = __float_as_uint(s1v + __uint_as_float(rd[i + 1]));
+                    tmem_st16x2_x4<8>(tSB + c0 / 2, pk);
                 }
-                tmem_st16(tS + c0, rs);
-                tmem_st8(tSB + c0 / 2, pk);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(B_DS_EMPTY));
+                    mbar_arrive(bar(B_S_READY + (c & 1)));
+                }
+                if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(5, c);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(bar(B_DS_EMPTY));
-                mbar_arrive(bar(B_S_READY + (c & 1)));
-            }
-            if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(5, c);
-        }
-        if (ok) {
-            tc_fence_after();
-            float* fs = (p.final_state && jl >= 0 && jl < jvalid) ? p.final_state + (long)bh * DK * dv + j : nullptr;
-            const bool zl = norm && jl == 64 && p.final_z;
-            for (int g = 0; g < COLS / 16; g++) {
-                uint32_t r[16];
-                tmem_ld16(tS + cbase + g * 16, r);
-                tmem_wait_ld();
+            if (ok && p.final_state && jv) {
+                float* fs = p.final_state + (long)bh * DK * dv + j;
 #pragma unroll
-                for (int i = 0; i < 16; i++) {
-                    const int d = cbase + g * 16 + i;
-                    if (fs)
-                        fs[(long)d * dv] = __uint_as_float(r[i]);
-                    else if (zl)
-                        p.final_z[(long)bh * DK + d] = __uint_as_float(r[i]);
+                for (int g = 0; g < NG; g++)
+#pragma unroll
+                    for (int i = 0; i < 16; i++) fs[(long)(cbase + g * 32 + hi * 16 + i) * dv] = S[g * 16 + i];
+            }
+        } else {
+            const int jl = lane_to_col<DVT>(warp & 3, lane);  // column in the slice
+            const int j = j0 + jl;
+            const uint32_t tS = tmem + lane_field + TM_S;
+            const uint32_t tD = tmem + lane_field + TM_DS;
+            {
+                const float* s0 =
+                    (p.init_state && jl < jvalid) ? p.init_state + (long)bh * DK * dv + j : nullptr;
+                const bool zl = norm && jl == 64;
+                for (int g = 0; g < COLS / 16; g++) {
+                    uint32_t r[16];
+#pragma unroll
+                    for (int i = 0; i < 16; i++) {
+                        const int d = cbase + g * 16 + i;
+                        float x = 0.f;
+                        if (s0)
+                            x = s0[(long)d * dv];
+                        else if (zl && p.init_z)
+                            x = p.init_z[(long)bh * DK + d];
+                        r[i] = __float_as_uint(x);
+                    }
+                    tmem_st16(tS + cbase + g * 16, r);
+                }
+                tmem_wait_st();
+                // first phase of the dS buffer's release
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_DS_EMPTY));
+            }
+            bool ok = true;
+            for (int c = 0; c < N; c++) {
+                const int s = c % NS;
+                ok = mbar_wait_warp(bar(B_DS_FULL), c & 1, abort_flag, p.err);
+                if (ok && GATE) ok = mbar_wait_warp(bar(B_QK_GATED + s), (c / NS) & 1, abort_flag, p.err);
+                // the single bf16 copy of S' is free once O_i(c-1) has completed
+                if (ok) ok = mbar_wait_warp(bar(B_SB_EMPTY), (c & 1) ^ 1, abort_flag, p.err);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t tSB = tmem + lane_field + TM_SB;
+#pragma unroll 1
+                for (int g = 0; g < COLS / 16; g++) {
+                    const int c0 = cbase + g * 16;
+                    uint32_t rs[16], rd[16];
+                    tmem_ld16(tS + c0, rs);
+                    tmem_ld16(tD + c0, rd);
+                    tmem_wait_ld();
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int i = 0; i < 16; i += 2) {
+                        float s0v = __uint_as_float(rs[i]), s1v = __uint_as_float(rs[i + 1]);
+                        if (GATE) {
+                            s0v *= gamma[s * DK + c0 + i];
+                            s1v *= gamma[s * DK + c0 + i + 1];
+                        }
+                        pk[i / 2] = pack_bf16x2(s0v, s1v);
+                        rs[i] = __float_as_uint(s0v + __uint_as_float(rd[i]));
+                        rs[i + 1] = __float_as_uint(s1v + __uint_as_float(rd[i + 1]));
+                    }
+                    tmem_st16(tS + c0, rs);
+                    tmem_st8(tSB + c0 / 2, pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(B_DS_EMPTY));
+                    mbar_arrive(bar(B_S_READY + (c & 1)));
+                }
+            }
+            if (ok) {
+                tc_fence_after();
+                float* fs = (p.final_state && jl < jvalid) ? p.final_state + (long)bh * DK * dv + j : nullptr;
+                const bool zl = norm && jl == 64 && p.final_z;
+                for (int g = 0; g < COLS / 16; g++) {
+                    uint32_t r[16];
+                    tmem_ld16(tS + cbase + g * 16, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; i++) {
+                        const int d = cbase + g * 16 + i;
+                        if (fs)
+                            fs[(long)d * dv] = __uint_as_float(r[i]);
+                        else if (zl)
+                            p.final_z[(long)bh * DK + d] = __uint_as_float(r[i]);
+                    }
                 }
             }
         }
@@ -547,10 +643,11 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
     } else if (warp < W_TMA) {
         // ============================================================ P = tril(A) -> bf16
         const int t = threadIdx.x - W_P0 * 32;  // token row 0..63 (TMEM lanes 0..63)
-        uint8_t* P = sm + Ly::off_p;
         for (int c = 0; c < N; c++) {
+            const int pb = c % Ly::NP;
+            uint8_t* P = sm + Ly::off_p + pb * Ly::PB;
             if (!mbar_wait_warp(bar(B_A_FULL), c & 1, abort_flag, p.err)) break;
-            if (!mbar_wait_warp(bar(B_P_EMPTY), (c & 1) ^ 1, abort_flag, p.err)) break;
+            if (!mbar_wait_warp(bar(B_P_EMPTY + pb), ((c / Ly::NP) & 1) ^ 1, abort_flag, p.err)) break;
             tc_fence_after();
             if (t == 0) GLA_TRACE_POINT(10, c);
 #pragma unroll 1
@@ -562,6 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(B_A_EMPTY));
+                    if (t == 0) GLA_TRACE_POINT(23, c);
                 }
 #pragma unroll
                 for (int k8 = 0; k8 < 4; k8++) {
@@ -582,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             if (t == 0) GLA_TRACE_POINT(15, c);
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_P_FULL));
+            if (lane == 0) mbar_arrive(bar(B_P_FULL + pb));
             if (t == 0) GLA_TRACE_POINT(11, c);
         }
     } else if (warp == W_TMA) {
@@ -609,6 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                 if (na < pq_n && na <= *oi_issued && mbar_test(bar(B_QK_GATED + na % NS), (na / NS) & 1) &&
                     mbar_test(bar(B_A_EMPTY), (na & 1) ^ 1)) {
                     tc_fence_after();
+                    GLA_TRACE_POINT(19, na);
                     const uint32_t Qs = sbase + Ly::off_qk + (na % NS) * Ly::STAGE_QK, Ks = Qs + Ly::QB;
                     // rows 64..127 of the M=128 tile read past the Q tile and are ignored
 #pragma unroll
@@ -619,6 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                     }
                     mma_commit(bar(B_A_FULL));
                     mma_commit(bar(B_QK_EMPTY + na % NS));
+                    GLA_TRACE_POINT(9, na);
                     na++;
                     prog = true;
                 }
@@ -674,7 +774,6 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             constexpr uint32_t idS = make_idesc_bf16(DVT, DK, 1, 1);
             constexpr uint32_t idOi = make_idesc_bf16(DVT, 64, 0, 0);
             constexpr uint32_t idOa = make_idesc_bf16(DVT, 64, 1, 0);
-            const uint32_t Ps = sbase + Ly::off_p;
             auto qs_of = [&](int c) { return sbase + Ly::off_qk + (c % NS) * Ly::STAGE_QK; };
             auto vs_of = [&](int c) { return sbase + Ly::off_v + (c % NV) * Ly::VB; };
             // Issue each chunk's four products as soon as their inputs are ready
@@ -687,16 +786,17 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             uint32_t idle = 0;
             while (no < N) {
                 bool prog = false;
-                if (no < ni && mbar_test(bar(B_P_FULL), no & 1)) {
+                if (no < ni && mbar_test(bar(B_P_FULL + no % Ly::NP), (no / Ly::NP) & 1)) {
                     tc_fence_after();
-                    const uint32_t Vs = vs_of(no);
+                    GLA_TRACE_POINT(22, no);
+                    const uint32_t Vs = vs_of(no), Ps = sbase + Ly::off_p + (no % Ly::NP) * Ly::PB;
 #pragma unroll
                     for (int kk = 0; kk < C / 16; kk++)
                         mma_ss(tmem + TM_O + (no & 1) * 64, make_sdesc(Vs + kk * 2048, 8192, 1024),
                                make_sdesc(Ps + kk * 32, 16, 1024),
                                idOa, 1);
                     mma_commit(bar(B_O_FULL + (no & 1)));
-                    mma_commit(bar(B_P_EMPTY));
+                    mma_commit(bar(B_P_EMPTY + no % Ly::NP));
                     mma_commit(bar(B_V_EMPTY + no % NV));
                     GLA_TRACE_POINT(6, no);
                     no++;
@@ -707,21 +807,24 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                     tc_fence_after();
                     GLA_TRACE_POINT(7, ni);
                     const uint32_t Qs = qs_of(ni);
+                    const uint32_t tsb = tmem + (DVT == 64 ? (uint32_t)(ni & 1) * 64u : TM_SB);
                     // O^T = S'^T Qh^T  (A operand: bf16 copy of the decayed state in TMEM)
 #pragma unroll
                     for (int kk = 0; kk < DK / 16; kk++) {
                         const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-                        mma_ts(tmem + TM_O + (ni & 1) * 64, tmem + TM_SB + kk * 8, make_sdesc(Qs + off, 16, 1024),
+                        mma_ts(tmem + TM_O + (ni & 1) * 64, tsb + kk * 8, make_sdesc(Qs + off, 16, 1024),
                                idOi, kk > 0);
                     }
-                    mma_commit(bar(B_SB_EMPTY));
+                    mma_commit(bar(B_SB_EMPTY + (DVT == 64 ? (ni & 1) : 0)));
+                    GLA_TRACE_POINT(21, ni);
                     ni++;
                     *oi_issued = ni;
                     prog = true;
                 }
                 if (nd < N && mbar_test(bar(B_QK_GATED + nd % NS), (nd / NS) & 1) &&
-                    mbar_test(bar(B_V_FULL + nd % NV), (nd / NV) & 1) && mbar_test(bar(B_DS_EMPTY), (nd & 1) ^ 1)) {
+                    mbar_test(bar(B_V_FULL + nd % NV), (nd / NV) & 1) && mbar_test(bar(B_DS_EMPTY), nd & 1)) {
                     tc_fence_after();
+                    GLA_TRACE_POINT(20, nd);
                     const uint32_t Ks = qs_of(nd) + Ly::QB, Vs = vs_of(nd);
                     // dS(c) = V_c^T Kh_c into its own TMEM buffer
 #pragma unroll
@@ -729,6 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                         mma_ss(tmem + TM_DS, make_sdesc(Vs + kk * 2048, 8192, 1024),
                                make_sdesc(Ks + kk * 2048, 8192, 1024), idS, kk > 0);
                     mma_commit(bar(B_DS_FULL));
+                    GLA_TRACE_POINT(8, nd);
                     nd++;
                     prog = true;
                 }
