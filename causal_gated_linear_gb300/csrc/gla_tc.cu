@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
     if (warp < W_STATE0) {
         // ============================================================ gate
         constexpr int QUADS = Ly::QUADS, SEG = Ly::SEG, TPS = Ly::TPS;
-        constexpr int G = TPS < 4 ? TPS : 4;  // tokens per factor group
+        constexpr int G = TPS < 2 ? TPS : 2;  // tokens per factor group (2: no register spills)
         const int gt = threadIdx.x;
         const int quad = gt % QUADS, seg = gt / QUADS;
         const int ch = 4 * quad;
