@@ -354,6 +354,14 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t start, uint32_t lbo, uin
     return d;
 }
 
+// The same descriptor split into its constant part and the start address:
+// desc = sdesc_const(lbo, sbo) | (addr >> 4) for a shared address below
+// 256 KB, so stepping along K or to another stage is one add on the low word.
+__host__ __device__ constexpr uint64_t sdesc_const(uint32_t lbo, uint32_t sbo) {
+    return (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) | (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) |
+           (static_cast<uint64_t>(1u) << 46) | (static_cast<uint64_t>(kSwizzle128B) << 61);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
 // a_mn / b_mn: 1 if that operand is MN-major (transposed), 0 if K-major.
 __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, int a_mn, int b_mn) {
@@ -376,6 +384,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
     __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&u);
     return __bfloat1622float2(h);
+}
+
+// Packed fp32 pair fused multiply-add (one instruction for two IEEE
+// round-to-nearest results, bit-identical to two scalar fmaf).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
 }
 
 __device__ __forceinline__ float elu1(float x) { return x > 0.f ? x + 1.f : __expf(x); }

@@ -174,9 +174,8 @@ template <int DK, int TPS, int G, bool GATE, bool ELU>
 __device__ __forceinline__ void gate_factors(uint8_t* qt, uint8_t* kt, const float* la, int seg, int col, int nval,
                                              const float (&off)[4]) {
     constexpr float kLog2e = 1.4426950408889634f;
-    float run[4];
-#pragma unroll
-    for (int e = 0; e < 4; e++) run[e] = off[e] * kLog2e;
+    const float2 l2e = make_float2(kLog2e, kLog2e);
+    float2 run01 = make_float2(off[0] * kLog2e, off[1] * kLog2e), run23 = make_float2(off[2] * kLog2e, off[3] * kLog2e);
 #pragma unroll 1
     for (int i0 = 0; i0 < TPS; i0 += G) {
         uint2 qr[G], kr[G];
@@ -191,34 +190,34 @@ __device__ __forceinline__ void gate_factors(uint8_t* qt, uint8_t* kt, const flo
         }
 #pragma unroll
         for (int u = 0; u < G; u++) {
-            const int t = seg * TPS + i0 + u;
-            const float keep = t < nval ? 1.f : 0.f;  // padding tokens must not write the state
-            const float2 q01 = unpack_bf16x2(qr[u].x), q23 = unpack_bf16x2(qr[u].y);
-            const float2 k01 = unpack_bf16x2(kr[u].x), k23 = unpack_bf16x2(kr[u].y);
-            float qv[4] = {q01.x, q01.y, q23.x, q23.y};
-            float kv[4] = {k01.x, k01.y, k23.x, k23.y};
+            float2 q01 = unpack_bf16x2(qr[u].x), q23 = unpack_bf16x2(qr[u].y);
+            float2 k01 = unpack_bf16x2(kr[u].x), k23 = unpack_bf16x2(kr[u].y);
+            if (ELU) {
+                q01 = make_float2(elu1(q01.x), elu1(q01.y));
+                q23 = make_float2(elu1(q23.x), elu1(q23.y));
+                k01 = make_float2(elu1(k01.x), elu1(k01.y));
+                k23 = make_float2(elu1(k23.x), elu1(k23.y));
+            }
+            float2 fq01 = make_float2(1.f, 1.f), fq23 = fq01, fk01 = fq01, fk23 = fq01;
+            if (GATE) {  // run = (b_t - b_C) log2 e >= 0
+                run01 = fma2(make_float2(lx[u].x, lx[u].y), l2e, run01);
+                run23 = fma2(make_float2(lx[u].z, lx[u].w), l2e, run23);
+                fq01 = make_float2(ex2_approx(run01.x), ex2_approx(run01.y));
+                fq23 = make_float2(ex2_approx(run23.x), ex2_approx(run23.y));
+                fk01 = make_float2(ex2_approx(-run01.x), ex2_approx(-run01.y));
+                fk23 = make_float2(ex2_approx(-run23.x), ex2_approx(-run23.y));
+            }
             if (GATE) {
-                run[0] = fmaf(lx[u].x, kLog2e, run[0]);
-                run[1] = fmaf(lx[u].y, kLog2e, run[1]);
-                run[2] = fmaf(lx[u].z, kLog2e, run[2]);
-                run[3] = fmaf(lx[u].w, kLog2e, run[3]);
+                // scalar products: packed pairs here need aligned register pairs and spill
+                q01 = make_float2(q01.x * fq01.x, q01.y * fq01.y);
+                q23 = make_float2(q23.x * fq23.x, q23.y * fq23.y);
+                k01 = make_float2(k01.x * fk01.x, k01.y * fk01.y);
+                k23 = make_float2(k23.x * fk23.x, k23.y * fk23.y);
             }
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                if (ELU) {
-                    qv[e] = elu1(qv[e]);
-                    kv[e] = elu1(kv[e]);
-                }
-                float fq = keep, fk = keep;
-                if (GATE) {  // run = (b_t - b_C) log2 e >= 0
-                    fq *= ex2_approx(run[e]);
-                    fk *= ex2_approx(-run[e]);
-                }
-                qv[e] *= fq;
-                kv[e] *= fk;
-            }
-            qr[u] = make_uint2(pack_bf16x2(qv[0], qv[1]), pack_bf16x2(qv[2], qv[3]));
-            kr[u] = make_uint2(pack_bf16x2(kv[0], kv[1]), pack_bf16x2(kv[2], kv[3]));
+            qr[u] = make_uint2(pack_bf16x2(q01.x, q01.y), pack_bf16x2(q23.x, q23.y));
+            kr[u] = make_uint2(pack_bf16x2(k01.x, k01.y), pack_bf16x2(k23.x, k23.y));
+            // rows past the sequence end arrive zero-filled; only phi(0) = 1 needs masking
+            if (ELU && seg * TPS + i0 + u >= nval) qr[u] = kr[u] = make_uint2(0u, 0u);
         }
 #pragma unroll
         for (int u = 0; u < G; u++) {
@@ -383,7 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             }
             if (threadIdx.x == 0) GLA_TRACE_POINT(2, c);
             const int nval = min(C, L - c * C);
-            if (GATE || elu || nval < C) {
+            // Rows past the sequence end arrive zero-filled (q, k and log alpha), so they
+            // add nothing to A, dS or O; only the feature map (phi(0) = 1) needs them masked.
+            if (GATE || elu) {
                 uint8_t* qt = sm + Ly::off_qk + s * Ly::STAGE_QK + atom * 8192;
                 uint8_t* kt = qt + Ly::QB;
                 if (elu)
