@@ -22,16 +22,18 @@
 //   MMA_dS  dS^T    = V^T Kh           M=DVT, N=dk, K=64  (V, Kh MN-major; own buffer)
 //   MMA_Oi  O^T     = S'^T_bf16 Qh^T   M=DVT, N=64, K=dk  (A operand from TMEM)
 //   MMA_Oa  O^T    += V^T P^T          M=DVT, N=64, K=64  (P = tril(A) in bf16)
-// The state warps apply S' = Diag(e^{b_C}) S, write the bf16 copy of S' and
-// S = S' + dS in fp32, entirely in TMEM; no state ever leaves the chip
-// between chunks.  With M = 64 the accumulator rows live in TMEM lanes
+// The state warps apply S' = Diag(e^{b_C}) S, write the bf16 copy of S' into
+// TMEM and S = S' + dS in fp32 (in TMEM for the 128-column tile, in their
+// registers for the 64-column tile); no state ever leaves the chip between
+// chunks.  With M = 64 the accumulator rows live in TMEM lanes
 // 16q + r -> lane 32q + r (r < 16) of each 32-lane quarter q.
 //
 // Warp roles (24 warps): 0-7 gate (cumsum with a cross-warp segment
 // exchange, factors written in place over the TMA-landed q/k tiles), 8-15
 // state, 16-19 output (TMEM -> shared staging -> TMA bulk store), 20-21 P
-// (mask A -> bf16 P), 22 TMA producer, 23 MMA issuer and TMEM owner.  Every
-// pipeline wait is bounded (gla_ptx.cuh).
+// (mask A -> bf16 P), 22 TMA producer (and A issuer with the 128-column
+// tile), 23 MMA issuer and TMEM owner.  Every pipeline wait is bounded
+// (gla_ptx.cuh).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -252,6 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // A(c) comes from the TMA producer thread (128-column tile) or, with the
+    // 64-column tile, from the MMA thread together with the other three products
+    constexpr bool kTwoIssuers = DVT == 128;
     const int tile = blockIdx.x % p.ntile;
     const int bh = blockIdx.x / p.ntile;
     const int j0 = tile * DVT;
@@ -267,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
         for (int i = 0; i < NS; i++) {
             mbar_init(bar(B_QK_FULL + i), 1);
             mbar_init(bar(B_QK_GATED + i), 8);
-            mbar_init(bar(B_QK_EMPTY + i), 2);  // released by the A issuer and the O_i issuer
+            mbar_init(bar(B_QK_EMPTY + i), kTwoIssuers ? 2 : 1);  // released by the issuer(s) of A, dS, O_i
         }
         for (int i = 0; i < NL; i++) {
             mbar_init(bar(B_LA_FULL + i), 1);
@@ -694,10 +699,11 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             if (!p.out_f32) tma_prefetch_desc(&p.tm_out);
             // The three rings are refilled independently (a full V ring must not hold
             // back the next chunk's q/k and log alpha loads).
-            // This thread also issues A(c) = Qh_c Kh_c^T: a single thread issues one
-            // MMA per ~90 cycles, so the products are split over two issuers.
+            // With the 128-column tile this thread also issues A(c) = Qh_c Kh_c^T: its
+            // M = 128 products take twice as long as the 64-column tile's, and one
+            // issuing thread would then hold back the other products.
             constexpr uint32_t idA = make_idesc_bf16(128, 64, 0, 0);
-            int na = 0;
+            int na = kTwoIssuers ? 0 : N;
             uint32_t idle = 0;
             unsigned long long t_last = 0;
             const int nl_end = GATE ? N : 0;
@@ -705,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                 bool prog = false;
                 // A(c) goes into the tensor pipe only after O_i(c-1): the state chain
                 // waits on O_i(c-1), which must not queue behind A(c).
-                if (na < pq_n && na <= *oi_issued && mbar_test(bar(B_QK_GATED + na % NS), (na / NS) & 1) &&
+                if (kTwoIssuers && na < pq_n && na <= *oi_issued && mbar_test(bar(B_QK_GATED + na % NS), (na / NS) & 1) &&
                     mbar_test(bar(B_A_EMPTY), (na & 1) ^ 1)) {
                     tc_fence_after();
                     GLA_TRACE_POINT(19, na);
@@ -772,72 +778,98 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
     } else {
         // ============================================================ MMA issuer
         if (lane == 0) {
+            constexpr uint32_t idA = make_idesc_bf16(128, 64, 0, 0);
             constexpr uint32_t idS = make_idesc_bf16(DVT, DK, 1, 1);
             constexpr uint32_t idOi = make_idesc_bf16(DVT, 64, 0, 0);
             constexpr uint32_t idOa = make_idesc_bf16(DVT, 64, 1, 0);
+            constexpr uint64_t kK = sdesc_const(16, 1024);     // K-major, 128-byte swizzle
+            constexpr uint64_t kMN = sdesc_const(8192, 1024);  // MN-major, 64-column blocks 8 KB apart
             auto qs_of = [&](int c) { return sbase + Ly::off_qk + (c % NS) * Ly::STAGE_QK; };
             auto vs_of = [&](int c) { return sbase + Ly::off_v + (c % NV) * Ly::VB; };
-            // Issue each chunk's four products as soon as their inputs are ready
-            // (never waiting on one product while another could go): dS(c) and
-            // A(c) run ahead of the state chain, O_i(c) follows the state update,
-            // O_a(c) follows P(c).  The q/k stage is released as soon as A(c),
-            // dS(c) and O_i(c) have been issued (O_a(c) reads only V and P).
+            // Issue each chunk's products as soon as their inputs are ready (A only with
+            // the 64-column tile).  A phase that has completed stays complete until the
+            // product waiting on it is issued, so each barrier is polled only until it
+            // first passes.
             int nd = 0, na = 0, ni = 0, no = 0, nq = 0;
+            bool d_e = false, d_g = false, d_v = false;  // dS(nd): dS buffer free, gated, V landed
+            bool a_e = false, a_g = false;               // A(na): A buffer free, gated
+            bool i_s = false, i_o = false;               // O_i(ni): state written, O buffer free
             unsigned long long t_last = globaltimer();
             uint32_t idle = 0;
             while (no < N) {
                 bool prog = false;
                 if (no < ni && mbar_test(bar(B_P_FULL + no % Ly::NP), (no / Ly::NP) & 1)) {
                     tc_fence_after();
-                    GLA_TRACE_POINT(22, no);
-                    const uint32_t Vs = vs_of(no), Ps = sbase + Ly::off_p + (no % Ly::NP) * Ly::PB;
+                    const uint64_t vd = kMN | (vs_of(no) >> 4);
+                    const uint64_t pd = kK | ((sbase + Ly::off_p + (no % Ly::NP) * Ly::PB) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < C / 16; kk++)
-                        mma_ss(tmem + TM_O + (no & 1) * 64, make_sdesc(Vs + kk * 2048, 8192, 1024),
-                               make_sdesc(Ps + kk * 32, 16, 1024),
-                               idOa, 1);
+                        mma_ss(tmem + TM_O + (no & 1) * 64, vd + kk * (2048 >> 4), pd + kk * (32 >> 4), idOa, 1);
                     mma_commit(bar(B_O_FULL + (no & 1)));
                     mma_commit(bar(B_P_EMPTY + no % Ly::NP));
                     mma_commit(bar(B_V_EMPTY + no % NV));
-                    GLA_TRACE_POINT(6, no);
                     no++;
                     prog = true;
                 }
-                if (ni < N && ni < nd && mbar_test(bar(B_S_READY + (ni & 1)), (ni >> 1) & 1) &&
-                    mbar_test(bar(B_O_EMPTY + (ni & 1)), ((ni >> 1) & 1) ^ 1)) {
-                    tc_fence_after();
-                    GLA_TRACE_POINT(7, ni);
-                    const uint32_t Qs = qs_of(ni);
-                    const uint32_t tsb = tmem + (DVT == 64 ? (uint32_t)(ni & 1) * 64u : TM_SB);
-                    // O^T = S'^T Qh^T  (A operand: bf16 copy of the decayed state in TMEM)
+                if (ni < nd) {
+                    if (!i_s) i_s = mbar_test(bar(B_S_READY + (ni & 1)), (ni >> 1) & 1);
+                    if (i_s && !i_o) i_o = mbar_test(bar(B_O_EMPTY + (ni & 1)), ((ni >> 1) & 1) ^ 1);
+                    if (i_s && i_o) {
+                        tc_fence_after();
+                        // O^T = S'^T Qh^T  (A operand: bf16 copy of the decayed state in TMEM)
+                        const uint64_t qd = kK | (qs_of(ni) >> 4);
+                        const uint32_t tsb = tmem + (DVT == 64 ? (uint32_t)(ni & 1) * 64u : TM_SB);
 #pragma unroll
-                    for (int kk = 0; kk < DK / 16; kk++) {
-                        const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-                        mma_ts(tmem + TM_O + (ni & 1) * 64, tsb + kk * 8, make_sdesc(Qs + off, 16, 1024),
-                               idOi, kk > 0);
+                        for (int kk = 0; kk < DK / 16; kk++) {
+                            const uint32_t off = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+                            mma_ts(tmem + TM_O + (ni & 1) * 64, tsb + kk * 8, qd + off, idOi, kk > 0);
+                        }
+                        mma_commit(bar(B_SB_EMPTY + (DVT == 64 ? (ni & 1) : 0)));
+                        ni++;
+                        *oi_issued = ni;
+                        i_s = i_o = false;
+                        prog = true;
                     }
-                    mma_commit(bar(B_SB_EMPTY + (DVT == 64 ? (ni & 1) : 0)));
-                    GLA_TRACE_POINT(21, ni);
-                    ni++;
-                    *oi_issued = ni;
-                    prog = true;
                 }
-                if (nd < N && mbar_test(bar(B_QK_GATED + nd % NS), (nd / NS) & 1) &&
-                    mbar_test(bar(B_V_FULL + nd % NV), (nd / NV) & 1) && mbar_test(bar(B_DS_EMPTY), nd & 1)) {
-                    tc_fence_after();
-                    GLA_TRACE_POINT(20, nd);
-                    const uint32_t Ks = qs_of(nd) + Ly::QB, Vs = vs_of(nd);
-                    // dS(c) = V_c^T Kh_c into its own TMEM buffer
+                if (nd < N) {
+                    if (!d_e) d_e = mbar_test(bar(B_DS_EMPTY), nd & 1);
+                    if (d_e && !d_g) d_g = mbar_test(bar(B_QK_GATED + nd % NS), (nd / NS) & 1);
+                    if (d_g && !d_v) d_v = mbar_test(bar(B_V_FULL + nd % NV), (nd / NV) & 1);
+                    if (d_v) {
+                        tc_fence_after();
+                        // dS(c) = V_c^T Kh_c into its own TMEM buffer
+                        const uint64_t vd = kMN | (vs_of(nd) >> 4), kd = kMN | ((qs_of(nd) + Ly::QB) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < C / 16; kk++)
-                        mma_ss(tmem + TM_DS, make_sdesc(Vs + kk * 2048, 8192, 1024),
-                               make_sdesc(Ks + kk * 2048, 8192, 1024), idS, kk > 0);
-                    mma_commit(bar(B_DS_FULL));
-                    GLA_TRACE_POINT(8, nd);
-                    nd++;
-                    prog = true;
+                        for (int kk = 0; kk < C / 16; kk++)
+                            mma_ss(tmem + TM_DS, vd + kk * (2048 >> 4), kd + kk * (2048 >> 4), idS, kk > 0);
+                        mma_commit(bar(B_DS_FULL));
+                        nd++;
+                        d_e = d_g = d_v = false;
+                        prog = true;
+                    }
                 }
-                while (nq < ni) {  // dS(nq) precedes O_i(nq); A(nq) is released by its own issuer
+                // A(c) enters the tensor pipe only after O_i(c-1), which the state chain waits on
+                if (!kTwoIssuers && na < N && na <= ni) {
+                    if (!a_e) a_e = mbar_test(bar(B_A_EMPTY), (na & 1) ^ 1);
+                    if (a_e && !a_g) a_g = mbar_test(bar(B_QK_GATED + na % NS), (na / NS) & 1);
+                    if (a_g) {
+                        tc_fence_after();
+                        // rows 64..127 of the M = 128 tile read past the Q tile and are ignored
+                        const uint64_t qd = kK | (qs_of(na) >> 4), kd = kK | ((qs_of(na) + Ly::QB) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < DK / 16; kk++) {
+                            const uint32_t off = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+                            mma_ss(tmem + TM_A, qd + off, kd + off, idA, kk > 0);
+                        }
+                        mma_commit(bar(B_A_FULL));
+                        na++;
+                        a_e = a_g = false;
+                        prog = true;
+                    }
+                }
+                // the q/k stage of chunk nq is free once A (from this thread), dS and O_i
+                // of nq have finished
+                while (nq < ni && (kTwoIssuers || nq < na)) {
                     mma_commit(bar(B_QK_EMPTY + nq % NS));
                     nq++;
                 }
