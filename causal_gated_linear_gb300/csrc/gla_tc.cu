@@ -595,6 +595,30 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             tc_fence_after();
             if (warp == W_OUT0 && lane == 0) GLA_TRACE_POINT(12, c);
             const int nval = min(C, L - c * C);
+            if constexpr (DVT == 64) {
+                // M = 64 rows sit in lanes 0-15 of each quarter: the 16x32bx2 shape gives
+                // threads 0-15 tokens 0-31 and threads 16-31 tokens 32-63 of the same rows
+                const int jr = lane_to_col<DVT>(warp & 3, lane & 15);
+                const int t0 = (lane >> 4) * 32;
+                uint32_t r[32];
+                tmem_ld16x2_x32<32>(tmem + lane_field + TM_O + (c & 1) * 64, r);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_O_EMPTY + (c & 1)));
+                if (jr < jvalid) {
+                    if (!p.out_f32) {
+                        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(ost) + jr + t0 * 64;
+#pragma unroll
+                        for (int t = 0; t < 32; t++) o[t * 64] = __float2bfloat16_rn(__uint_as_float(r[t]));
+                    } else {
+                        float* o = static_cast<float*>(p.out) + ((long)bh * L + (long)c * C + t0) * dv + j0 + jr;
+#pragma unroll
+                        for (int t = 0; t < 32; t++)
+                            if (t0 + t < nval) o[(long)t * dv] = __uint_as_float(r[t]);
+                    }
+                }
+            } else {
 #pragma unroll 1
             for (int h = 0; h < 2; h++) {
                 uint32_t r[32];
@@ -632,6 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                         if (h * 32 + t < nval) o[(long)t * dv] = x;
                     }
                 }
+            }
             }
             if (!p.out_f32) {
                 fence_proxy_async_smem();
