@@ -53,6 +53,11 @@ def prefill_bytes(w) -> float:
     return float(BH * (L * per_tok + states))
 
 
+def decode_multi_bytes(w) -> float:
+    """Per call: fp32 state read + write once, and per token bf16 q/k/v, fp32 log alpha, bf16 out."""
+    return float(w.B * w.H * (2 * w.dk * w.dv * 4 + w.L * (2 * w.dk * 2 + w.dv * 2 + w.dk * 4 + w.dv * 2)))
+
+
 def decode_bytes(NS, H, dk, dv) -> float:
     """Per step: fp32 state read + write, bf16 q/k/v, fp32 log alpha, fp32 out."""
     return float(NS * H * (2 * dk * dv * 4 + 2 * dk * 2 + dv * 2 + dk * 4 + dv * 4))
@@ -69,9 +74,16 @@ def load_peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
-def kernel_source_hash() -> str:
+KERNEL_SOURCES = {
+    "gla_prefill_tc_kernel": ("gla_tc.cu", "gla_ptx.cuh"),
+    "gla_decode_kernel": ("gla_decode.cu",),
+    "gla_prefill_short_kernel": ("gla_short.cu",),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for f in ("gla_tc.cu", "gla_ptx.cuh", "gla_decode.cu"):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "causal_gated_linear_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -85,7 +97,7 @@ def recorded_traffic(kernel: str):
     with open(p) as f:
         d = json.load(f)
     e = d.get(kernel)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(kernel):
         return None
     return e.get("bytes_per_launch")
 
@@ -361,6 +373,38 @@ def bench_decode(args, device, rank):
     return dict(ms_per_step=ms, steps=n, NS=NS, H=H, dk=dk, dv=dv)
 
 
+def bench_decode_multi(args, device, rank):
+    """Several tokens per sequence per call (the prefill -> decode hand-off) through gla_fwd with
+    the state advanced in place."""
+    import torch
+
+    import causal_gated_linear_gb300 as gla
+    w = synth.with_shape(synth.DECODE_MULTI, seed=synth.DECODE_MULTI.seed + 1000 * rank)
+    x = synth.make_prefill(w)
+    q, k, v = (to_dev(x[n], device) for n in ("q", "k", "v"))
+    la, st = to_dev(x["log_alpha"], device), to_dev(x["init_state"], device)
+    out = torch.empty((w.B, w.H, w.L, w.dv), dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def call():
+        r = gla.gla_fwd(q, k, v, la, st, out, st, w.B, w.H, w.L, w.dk, w.dv, C, stream=stream)
+        if r != 0:
+            raise RuntimeError(gla.gla_status_string(r))
+
+    for _ in range(4):
+        call()
+    torch.cuda.synchronize(device)
+    n = args.multi_calls
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(n):
+        call()
+    ev1.record(stream)
+    torch.cuda.synchronize(device)
+    gla.check(gla.gla_device_error(stream))
+    return dict(w=w, ms_per_call=ev0.elapsed_time(ev1) / n, calls=n)
+
+
 def run_gla(args):
     import torch
     rank, world, local = dist_env()
@@ -375,6 +419,7 @@ def run_gla(args):
 
     w, BH, pre = bench_prefill(args, device, rank, world)
     dec = bench_decode(args, device, rank) if args.decode_steps > 0 else None
+    mdec = bench_decode_multi(args, device, rank) if args.multi_calls > 0 else None
 
     ms = pre["total_ms"] / args.steps
     tokens = w.B * w.L
@@ -412,6 +457,18 @@ def run_gla(args):
                                        "kernel": "gla_decode_kernel", "alg_bytes_per_launch": dbytes},
                           "tokens_per_s": dec["NS"] * dec["H"] / (dec["ms_per_step"] / 1e3) / dec["H"],
                           "token_pool": f"{args.decode_pool} distinct token sets reused cyclically"}
+    if mdec is not None:
+        mw = mdec["w"]
+        mbytes = decode_multi_bytes(mw)
+        mgbs = mbytes / (mdec["ms_per_call"] / 1e3) / 1e9
+        line["decode_multi"] = {
+            "workload": mw.name, "tokens_per_call": mw.L, "ms_per_call": mdec["ms_per_call"],
+            "calls": mdec["calls"], "tokens_per_s": mw.B * mw.L / (mdec["ms_per_call"] / 1e3),
+            "state_hbm_gbs": mgbs, "unit": "GB/s",
+            "roofline": {"bound": "hbm", "achieved": mgbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": mgbs / peaks["hbm_gbs"],
+                         "traffic": recorded_traffic("gla_prefill_short_kernel"),
+                         "kernel": "gla_prefill_short_kernel", "alg_bytes_per_launch": mbytes}}
     if "e2e" in pre:
         e = pre["e2e"]
         line["e2e"] = {"value": tokens * world / (e["ms_per_step"] / 1e3), "unit": "tokens/s",
@@ -438,6 +495,8 @@ def main():
     ap.add_argument("--impl", default="gla", choices=["gla", "reference"])
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--decode-pool", type=int, default=8)
+    ap.add_argument("--multi-calls", type=int, default=64,
+                    help="timed calls of the 8-tokens-per-sequence hand-off workload (0: skip)")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--ref-seconds", type=float, default=10.0)

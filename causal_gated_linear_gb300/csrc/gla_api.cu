@@ -72,7 +72,7 @@ int validate_prefill(const gla_fwd_args* a) {
     if (a->B < 1 || a->H < 1 || a->L < 0 || a->dk < 1 || a->dv < 1) return GLA_ERR_INVALID;
     if (a->in_dtype != GLA_DTYPE_BF16 && a->in_dtype != GLA_DTYPE_F32) return GLA_ERR_INVALID;
     if (a->out_dtype != GLA_DTYPE_BF16 && a->out_dtype != GLA_DTYPE_F32) return GLA_ERR_INVALID;
-    if (a->flags & ~7u) return GLA_ERR_INVALID;
+    if (a->flags & ~15u) return GLA_ERR_INVALID;
     if (a->L > 0 && (!a->q || !a->k || !a->v || !a->out)) return GLA_ERR_INVALID;
     if (a->chunk != 64) return GLA_ERR_UNSUPPORTED;
     if (a->dk > 256) return GLA_ERR_UNSUPPORTED;
@@ -142,7 +142,9 @@ int gla_fwd_ex(const gla_fwd_args* a, void* stream) {
     pa.err_word = err_word_ptr();
     if (!pa.err_word) return GLA_ERR_CUDA;
     cudaError_t e;
-    if (prefill_tc_supported(pa)) {
+    if (prefill_short_supported(pa)) {
+        e = launch_prefill_short(pa, s);
+    } else if (prefill_tc_supported(pa)) {
         e = launch_prefill_tc(pa, s);
     } else {
         if (BH > 65535) return GLA_ERR_UNSUPPORTED;

@@ -45,6 +45,11 @@ bool prefill_tc_supported(const PrefillArgs& a);
 // Returns cudaSuccess, or an error from encoding the tensor maps / launching.
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
 
+// Whether the short-sequence kernel (1..16 tokens, state read and written
+// once per call) handles this call.
+bool prefill_short_supported(const PrefillArgs& a);
+cudaError_t launch_prefill_short(const PrefillArgs& a, cudaStream_t s);
+
 // Memory-bound decode step.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 

@@ -1,0 +1,154 @@
+// gla_short.cu -- sequences of 1..16 tokens per call, memory-bound.
+//
+// "linear-attention" blog, Linear attention: with a fixed-size state, new
+// tokens need only that state and themselves, and "Attention is recurrent":
+// decoding-sized work is bound by memory bandwidth.  "Gated Linear
+// Attention", GLA Recurrent Form:  S_t = Diag(alpha_t) S_{t-1} + k_t v_t^T,
+// o_t = S_t^T q_t, applied token by token (exactly the chunk form's result).
+//
+// This is the hand-off from prefill to multi-token decode: the fp32 state of
+// one (batch*head) is read into registers once, the L <= 16 tokens are applied
+// in order and the state is written back once, so a call costs one pass over
+// the state -- the traffic of a single decode step -- for up to 16 tokens.
+// Each thread owns one float4 of value columns for kRows key rows (64 floats);
+// the per-token partial outputs over those rows go to shared memory and are
+// summed over the row groups after the token loop (one barrier per call).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gla_internal.h"
+
+namespace gla {
+namespace {
+
+constexpr int kRows = 16;     // key rows per thread
+constexpr int kMaxTokens = 16;
+constexpr int kMaxThreads = 512;
+
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <bool GATE>
+__global__ void __launch_bounds__(kMaxThreads) gla_prefill_short_kernel(const PrefillArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    const int dk = a.dk, dv = a.dv, L = a.L;
+    const int cols4 = dv >> 2, rows_par = dk / kRows;
+    const long bh = blockIdx.x;
+    const int tid = threadIdx.x, nthr = blockDim.x;  // nthr == cols4 * rows_par
+    float* s_q = sm;                 // [L][dk]
+    float* s_k = s_q + L * dk;       // [L][dk]
+    float* s_a = s_k + L * dk;       // [L][dk]  alpha = e^{log alpha}
+    float* s_v = s_a + L * dk;       // [L][dv]
+    float4* s_red = reinterpret_cast<float4*>(s_v + L * dv);  // [L][rows_par][cols4]
+
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + bh * L * dk;
+    const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k) + bh * L * dk;
+    const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v) + bh * L * dv;
+    for (int i = tid; i < L * dk; i += nthr) {
+        s_q[i] = __bfloat162float(q[i]);
+        s_k[i] = __bfloat162float(k[i]);
+        s_a[i] = GATE ? __expf(a.log_alpha[bh * L * dk + i]) : 1.f;
+    }
+    for (int i = tid; i < L * dv; i += nthr) s_v[i] = __bfloat162float(v[i]);
+
+    // this thread's rows r = rg + j * rows_par (consecutive threads: consecutive float4 of a row)
+    const int c4 = tid % cols4, rg = tid / cols4;
+    float4 S[kRows];
+    if (a.init_state) {
+        const float4* S0 = reinterpret_cast<const float4*>(a.init_state + bh * (long)dk * dv);
+#pragma unroll
+        for (int j = 0; j < kRows; j++) S[j] = __ldcs(&S0[(long)(rg + j * rows_par) * cols4 + c4]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < kRows; j++) S[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();
+
+    for (int t = 0; t < L; t++) {
+        const float4 vv = reinterpret_cast<const float4*>(s_v + t * dv)[c4];
+        const float* qt = s_q + t * dk;
+        const float* kt = s_k + t * dk;
+        const float* at = s_a + t * dk;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < kRows; j++) {
+            const int r = rg + j * rows_par;
+            const float al = at[r], kk = kt[r], qq = qt[r];
+            S[j].x = fmaf(al, S[j].x, kk * vv.x);
+            S[j].y = fmaf(al, S[j].y, kk * vv.y);
+            S[j].z = fmaf(al, S[j].z, kk * vv.z);
+            S[j].w = fmaf(al, S[j].w, kk * vv.w);
+            acc.x = fmaf(qq, S[j].x, acc.x);
+            acc.y = fmaf(qq, S[j].y, acc.y);
+            acc.z = fmaf(qq, S[j].z, acc.z);
+            acc.w = fmaf(qq, S[j].w, acc.w);
+        }
+        s_red[(t * rows_par + rg) * cols4 + c4] = acc;
+    }
+    if (a.final_state) {  // may alias init_state: this CTA read its whole slice above
+        float4* Sf = reinterpret_cast<float4*>(a.final_state + bh * (long)dk * dv);
+#pragma unroll
+        for (int j = 0; j < kRows; j++) __stcs(&Sf[(long)(rg + j * rows_par) * cols4 + c4], S[j]);
+    }
+    __syncthreads();
+
+    for (int idx = tid; idx < L * cols4; idx += nthr) {
+        const int t = idx / cols4, cc = idx % cols4;
+        float4 o = s_red[(t * rows_par) * cols4 + cc];
+        for (int rr = 1; rr < rows_par; rr++) {
+            const float4 p = s_red[(t * rows_par + rr) * cols4 + cc];
+            o.x += p.x;
+            o.y += p.y;
+            o.z += p.z;
+            o.w += p.w;
+        }
+        const long oi = (bh * L + t) * (long)cols4 + cc;
+        if (a.out_dtype == GLA_DTYPE_F32)
+            reinterpret_cast<float4*>(a.out)[oi] = o;
+        else
+            reinterpret_cast<uint2*>(a.out)[oi] = make_uint2(pack_bf16x2_rn(o.x, o.y), pack_bf16x2_rn(o.z, o.w));
+    }
+}
+
+size_t short_smem_bytes(const PrefillArgs& a) {
+    return (size_t)a.L * (3 * a.dk + a.dv) * sizeof(float) + (size_t)a.L * a.dk * a.dv / 4;
+}
+
+}  // namespace
+
+bool prefill_short_supported(const PrefillArgs& a) {
+    if (a.L < 1 || a.L > kMaxTokens) return false;
+    if (a.in_dtype != GLA_DTYPE_BF16) return false;
+    if (a.flags & (GLA_FLAG_FEATURE_ELU1 | GLA_FLAG_NORMALIZE | GLA_FLAG_FORCE_SIMT | GLA_FLAG_FORCE_CHUNK))
+        return false;
+    if (a.dk % kRows != 0 || a.dv % 4 != 0) return false;
+    const long threads = (long)a.dk * a.dv / (4 * kRows);
+    if (threads < 32 || threads > kMaxThreads || threads % 32 != 0) return false;
+    if ((long)a.B * a.H > 0x7fffffffL) return false;
+    return short_smem_bytes(a) <= 227 * 1024;
+}
+
+cudaError_t launch_prefill_short(const PrefillArgs& a, cudaStream_t s) {
+    const int threads = a.dk * a.dv / (4 * kRows);
+    const size_t smem = short_smem_bytes(a);
+    const unsigned grid = (unsigned)((long)a.B * a.H);
+    cudaError_t e;
+    if (a.log_alpha) {
+        e = cudaFuncSetAttribute(gla_prefill_short_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        gla_prefill_short_kernel<true><<<grid, threads, smem, s>>>(a);
+    } else {
+        e = cudaFuncSetAttribute(gla_prefill_short_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        gla_prefill_short_kernel<false><<<grid, threads, smem, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace gla

@@ -59,7 +59,8 @@ enum { GLA_DTYPE_BF16 = 0, GLA_DTYPE_F32 = 1 };
 enum {
     GLA_FLAG_FEATURE_ELU1 = 1u,  /* apply phi(x) = elu(x) + 1 to q and k */
     GLA_FLAG_NORMALIZE = 2u,     /* o_t = phi(q_t)^T S_t / phi(q_t)^T z_t */
-    GLA_FLAG_FORCE_SIMT = 4u     /* use the fp32 SIMT chunk kernel even for bf16 */
+    GLA_FLAG_FORCE_SIMT = 4u,    /* use the fp32 SIMT chunk kernel even for bf16 */
+    GLA_FLAG_FORCE_CHUNK = 8u    /* use a chunk kernel even for a sequence of <= 16 tokens */
 };
 
 /*
@@ -76,6 +77,11 @@ enum {
  *   stream      cudaStream_t (NULL = legacy default stream)
  * Supported: dk in {64, 128}, dv a multiple of 64 (tensor-core kernel); any
  * other dk, dv in [1, 256] runs on the SIMT kernel.  L >= 0, B, H >= 1.
+ * A call of 1..16 tokens (the prefill-to-decode hand-off: several new tokens
+ * per sequence on top of init_state) runs the recurrence token by token in
+ * fp32 on a kernel that reads and writes each head's state once, when
+ * dk % 16 == 0, dv % 4 == 0 and 2048 <= dk*dv <= 32768 with dk*dv a multiple
+ * of 2048 (no feature map or normaliser); GLA_FLAG_FORCE_CHUNK turns this off.
  * out must not alias any input.
  */
 int gla_fwd(const void* q, const void* k, const void* v, const float* log_alpha,

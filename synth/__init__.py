@@ -162,6 +162,12 @@ CONFIGS = {
                 init_std=0.1, seed=BASE_SEED + 3),
 }
 
+# several new tokens per sequence on top of a decode-sized state (the prefill -> decode
+# hand-off): decode distributions (q, k, v ~ N(0,1), log alpha = logsigmoid(N(4, 1.5)),
+# S ~ N(0, 0.1)), 8 tokens per call
+DECODE_MULTI = Workload("gla_decode_multi_256seqH32d128T8", 256, 32, 8, 128, 128, qk_scale=False,
+                        gate_temp=1.0, init_std=0.1, seed=BASE_SEED + 5)
+
 DECODE = dict(name="gla_decode_256seqH32d128x1024", NS=256, H=32, dk=128, dv=128, steps=1024,
               gate_mean=4.0, gate_std=1.5, state_std=0.1, seed=BASE_SEED + 4)
 
