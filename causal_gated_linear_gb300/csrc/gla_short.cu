@@ -10,9 +10,11 @@
 // one (batch*head) is read into registers once, the L <= 16 tokens are applied
 // in order and the state is written back once, so a call costs one pass over
 // the state -- the traffic of a single decode step -- for up to 16 tokens.
-// Each thread owns one float4 of value columns for kRows key rows (64 floats);
-// the per-token partial outputs over those rows go to shared memory and are
-// summed over the row groups after the token loop (one barrier per call).
+// Each thread owns one float4 of value columns for kRows consecutive key rows
+// (64 floats), so its per-token alpha, k and q come in as float4 shared loads;
+// the updates run as packed fp32 pairs.  The per-token partial outputs over
+// those rows go to shared memory and are summed over the row groups after the
+// token loop (one barrier per call).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -30,6 +32,25 @@ constexpr int kMaxThreads = 512;
 __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// d = a * b + c on fp32 pairs (one instruction, two IEEE round-to-nearest results)
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
 }
 
 template <bool GATE>
@@ -55,13 +76,14 @@ __global__ void __launch_bounds__(kMaxThreads) gla_prefill_short_kernel(const Pr
     }
     for (int i = tid; i < L * dv; i += nthr) s_v[i] = __bfloat162float(v[i]);
 
-    // this thread's rows r = rg + j * rows_par (consecutive threads: consecutive float4 of a row)
+    // this thread's rows r = rg * kRows + j (consecutive threads: consecutive float4 of a row)
     const int c4 = tid % cols4, rg = tid / cols4;
+    const int r0 = rg * kRows;
     float4 S[kRows];
     if (a.init_state) {
         const float4* S0 = reinterpret_cast<const float4*>(a.init_state + bh * (long)dk * dv);
 #pragma unroll
-        for (int j = 0; j < kRows; j++) S[j] = __ldcs(&S0[(long)(rg + j * rows_par) * cols4 + c4]);
+        for (int j = 0; j < kRows; j++) S[j] = __ldcs(&S0[(long)(r0 + j) * cols4 + c4]);
     } else {
 #pragma unroll
         for (int j = 0; j < kRows; j++) S[j] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -70,29 +92,35 @@ __global__ void __launch_bounds__(kMaxThreads) gla_prefill_short_kernel(const Pr
 
     for (int t = 0; t < L; t++) {
         const float4 vv = reinterpret_cast<const float4*>(s_v + t * dv)[c4];
-        const float* qt = s_q + t * dk;
-        const float* kt = s_k + t * dk;
-        const float* at = s_a + t * dk;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float2 v01 = make_float2(vv.x, vv.y), v23 = make_float2(vv.z, vv.w);
+        const float4* q4 = reinterpret_cast<const float4*>(s_q + t * dk + r0);
+        const float4* k4 = reinterpret_cast<const float4*>(s_k + t * dk + r0);
+        const float4* a4 = reinterpret_cast<const float4*>(s_a + t * dk + r0);
+        float2 acc01 = make_float2(0.f, 0.f), acc23 = acc01;
 #pragma unroll
-        for (int j = 0; j < kRows; j++) {
-            const int r = rg + j * rows_par;
-            const float al = at[r], kk = kt[r], qq = qt[r];
-            S[j].x = fmaf(al, S[j].x, kk * vv.x);
-            S[j].y = fmaf(al, S[j].y, kk * vv.y);
-            S[j].z = fmaf(al, S[j].z, kk * vv.z);
-            S[j].w = fmaf(al, S[j].w, kk * vv.w);
-            acc.x = fmaf(qq, S[j].x, acc.x);
-            acc.y = fmaf(qq, S[j].y, acc.y);
-            acc.z = fmaf(qq, S[j].z, acc.z);
-            acc.w = fmaf(qq, S[j].w, acc.w);
+        for (int g = 0; g < kRows / 4; g++) {
+            const float4 al4 = a4[g], kk4 = k4[g], qq4 = q4[g];
+            const float al[4] = {al4.x, al4.y, al4.z, al4.w}, kk[4] = {kk4.x, kk4.y, kk4.z, kk4.w},
+                        qq[4] = {qq4.x, qq4.y, qq4.z, qq4.w};
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                float4& sj = S[g * 4 + e];
+                const float2 al2 = make_float2(al[e], al[e]), kk2 = make_float2(kk[e], kk[e]),
+                             qq2 = make_float2(qq[e], qq[e]);
+                // S = alpha S + k v^T (the recurrence's order: decay, then write), then o += q S
+                const float2 s01 = fma2(al2, make_float2(sj.x, sj.y), mul2(kk2, v01));
+                const float2 s23 = fma2(al2, make_float2(sj.z, sj.w), mul2(kk2, v23));
+                sj = make_float4(s01.x, s01.y, s23.x, s23.y);
+                acc01 = fma2(qq2, s01, acc01);
+                acc23 = fma2(qq2, s23, acc23);
+            }
         }
-        s_red[(t * rows_par + rg) * cols4 + c4] = acc;
+        s_red[(t * rows_par + rg) * cols4 + c4] = make_float4(acc01.x, acc01.y, acc23.x, acc23.y);
     }
     if (a.final_state) {  // may alias init_state: this CTA read its whole slice above
         float4* Sf = reinterpret_cast<float4*>(a.final_state + bh * (long)dk * dv);
 #pragma unroll
-        for (int j = 0; j < kRows; j++) __stcs(&Sf[(long)(rg + j * rows_par) * cols4 + c4], S[j]);
+        for (int j = 0; j < kRows; j++) __stcs(&Sf[(long)(r0 + j) * cols4 + c4], S[j]);
     }
     __syncthreads();
 
