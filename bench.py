@@ -48,7 +48,8 @@ def prefill_flops(w) -> float:
 def prefill_bytes(w) -> float:
     """Algorithmic bytes: q, k, v, log alpha read once, out written once, init/final state."""
     BH, L = w.B * w.H, w.L
-    per_tok = 2 * w.dk + 2 * w.dk + 2 * w.dv + 4 * w.dk + 2 * w.dv
+    la_bytes = 4 if getattr(w, "scalar_gate", False) else 4 * w.dk  # one gate per token, or per channel
+    per_tok = 2 * w.dk + 2 * w.dk + 2 * w.dv + la_bytes + 2 * w.dv
     states = (2 if w.init_std > 0 else 1) * w.dk * w.dv * 4
     return float(BH * (L * per_tok + states))
 
@@ -78,6 +79,7 @@ KERNEL_SOURCES = {
     "gla_prefill_tc_kernel": ("gla_tc.cu", "gla_ptx.cuh"),
     "gla_decode_kernel": ("gla_decode.cu",),
     "gla_prefill_short_kernel": ("gla_short.cu",),
+    "gla_prefill_tc_kernel_scalar_gate": ("gla_tc.cu", "gla_ptx.cuh"),
 }
 
 
@@ -300,6 +302,33 @@ def bench_prefill(args, device, rank, world):
     total_ms = max_over_ranks(total_ms, world, device)
     res = dict(total_ms=total_ms, per_launch_ms=statistics.mean(per), wall_s=wall, clocks=clk.summary())
 
+    # the same workload with one gate per token (GLA_FLAG_SCALAR_GATE): q, k, v and states reused
+    if args.scalar_calls > 0:
+        ws = synth.with_shape(w, scalar_gate=True, name=w.name + "_scalar_gate")
+        las = to_dev(synth.gate_log_alpha(ws), device)
+
+        def sstep():
+            st = gla.gla_fwd_ex(q, k, v, out, w.B, w.H, w.L, w.dk, w.dv, log_alpha=las, init_state=s0,
+                                final_state=fs, flags=gla.FLAG_SCALAR_GATE, stream=stream)
+            if st != 0:
+                raise RuntimeError(gla.gla_status_string(st))
+
+        for _ in range(2):
+            sstep()
+        torch.cuda.synchronize(device)
+        sev = []
+        for _ in range(args.scalar_calls):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            sstep()
+            b.record(stream)
+            sev.append((a, b))
+        torch.cuda.synchronize(device)
+        gla.check(gla.gla_device_error(stream))
+        res["scalar"] = dict(w=ws, per_launch_ms=statistics.mean(a.elapsed_time(b) for a, b in sev),
+                             calls=args.scalar_calls)
+        del las
+
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     if args.e2e:
         hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
@@ -457,6 +486,17 @@ def run_gla(args):
                                        "kernel": "gla_decode_kernel", "alg_bytes_per_launch": dbytes},
                           "tokens_per_s": dec["NS"] * dec["H"] / (dec["ms_per_step"] / 1e3) / dec["H"],
                           "token_pool": f"{args.decode_pool} distinct token sets reused cyclically"}
+    if "scalar" in pre:
+        sw = pre["scalar"]["w"]
+        sbytes = prefill_bytes(sw)
+        sgbs = sbytes / (pre["scalar"]["per_launch_ms"] / 1e3) / 1e9
+        line["scalar_gate"] = {
+            "workload": sw.name, "ms_per_launch": pre["scalar"]["per_launch_ms"], "calls": pre["scalar"]["calls"],
+            "tokens_per_s": sw.B * sw.L / (pre["scalar"]["per_launch_ms"] / 1e3),
+            "roofline": {"bound": "hbm", "achieved": sgbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": sgbs / peaks["hbm_gbs"],
+                         "traffic": recorded_traffic("gla_prefill_tc_kernel_scalar_gate"),
+                         "kernel": "gla_prefill_tc_kernel (per-token gate)", "alg_bytes_per_launch": sbytes}}
     if mdec is not None:
         mw = mdec["w"]
         mbytes = decode_multi_bytes(mw)
@@ -495,6 +535,8 @@ def main():
     ap.add_argument("--impl", default="gla", choices=["gla", "reference"])
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--decode-pool", type=int, default=8)
+    ap.add_argument("--scalar-calls", type=int, default=5,
+                    help="timed launches of the long-context workload with one gate per token (0: skip)")
     ap.add_argument("--multi-calls", type=int, default=64,
                     help="timed calls of the 8-tokens-per-sequence hand-off workload (0: skip)")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")

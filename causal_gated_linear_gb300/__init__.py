@@ -30,7 +30,7 @@ from . import _build
 
 GLA_OK, GLA_ERR_INVALID, GLA_ERR_UNSUPPORTED, GLA_ERR_MISALIGNED, GLA_ERR_CUDA, GLA_ERR_TIMEOUT = range(6)
 BF16, F32 = 0, 1
-FLAG_FEATURE_ELU1, FLAG_NORMALIZE, FLAG_FORCE_SIMT, FLAG_FORCE_CHUNK = 1, 2, 4, 8
+FLAG_FEATURE_ELU1, FLAG_NORMALIZE, FLAG_FORCE_SIMT, FLAG_FORCE_CHUNK, FLAG_SCALAR_GATE = 1, 2, 4, 8, 16
 
 EXPORTED = ["gla_fwd", "gla_fwd_ex", "gla_decode_step", "gla_device_error", "gla_device_error_detail",
             "gla_status_string", "gla_version"]

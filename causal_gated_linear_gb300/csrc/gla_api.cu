@@ -72,7 +72,7 @@ int validate_prefill(const gla_fwd_args* a) {
     if (a->B < 1 || a->H < 1 || a->L < 0 || a->dk < 1 || a->dv < 1) return GLA_ERR_INVALID;
     if (a->in_dtype != GLA_DTYPE_BF16 && a->in_dtype != GLA_DTYPE_F32) return GLA_ERR_INVALID;
     if (a->out_dtype != GLA_DTYPE_BF16 && a->out_dtype != GLA_DTYPE_F32) return GLA_ERR_INVALID;
-    if (a->flags & ~15u) return GLA_ERR_INVALID;
+    if (a->flags & ~31u) return GLA_ERR_INVALID;
     if (a->L > 0 && (!a->q || !a->k || !a->v || !a->out)) return GLA_ERR_INVALID;
     if (a->chunk != 64) return GLA_ERR_UNSUPPORTED;
     if (a->dk > 256) return GLA_ERR_UNSUPPORTED;
@@ -83,7 +83,8 @@ int validate_prefill(const gla_fwd_args* a) {
     const size_t BH = (size_t)a->B * a->H, L = (size_t)a->L;
     const size_t es = a->in_dtype == GLA_DTYPE_F32 ? 4 : 2, eo = a->out_dtype == GLA_DTYPE_F32 ? 4 : 2;
     const size_t nq = BH * L * a->dk * es, nv = BH * L * a->dv * es, no = BH * L * a->dv * eo;
-    const size_t nla = BH * L * a->dk * 4, ns = BH * a->dk * a->dv * 4, nz = BH * a->dk * 4;
+    const size_t nla = BH * L * ((a->flags & GLA_FLAG_SCALAR_GATE) ? 1 : a->dk) * 4;
+    const size_t ns = BH * a->dk * a->dv * 4, nz = BH * a->dk * 4;
     if (overlaps(a->out, no, a->q, nq) || overlaps(a->out, no, a->k, nq) || overlaps(a->out, no, a->v, nv) ||
         overlaps(a->out, no, a->log_alpha, nla) || overlaps(a->out, no, a->init_state, ns) ||
         overlaps(a->out, no, a->final_state, ns))

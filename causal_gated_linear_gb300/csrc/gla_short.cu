@@ -69,10 +69,15 @@ __global__ void __launch_bounds__(kMaxThreads) gla_prefill_short_kernel(const Pr
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + bh * L * dk;
     const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k) + bh * L * dk;
     const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v) + bh * L * dv;
+    // per-channel gate: [L][dk]; per-token gate (GLA_FLAG_SCALAR_GATE): [L], shared by all channels
+    const bool scalar_gate = a.flags & GLA_FLAG_SCALAR_GATE;
     for (int i = tid; i < L * dk; i += nthr) {
         s_q[i] = __bfloat162float(q[i]);
         s_k[i] = __bfloat162float(k[i]);
-        s_a[i] = GATE ? __expf(a.log_alpha[bh * L * dk + i]) : 1.f;
+        if (GATE)
+            s_a[i] = __expf(scalar_gate ? a.log_alpha[bh * L + i / dk] : a.log_alpha[bh * L * dk + i]);
+        else
+            s_a[i] = 1.f;
     }
     for (int i = tid; i < L * dv; i += nthr) s_v[i] = __bfloat162float(v[i]);
 

@@ -71,7 +71,10 @@ __global__ void __launch_bounds__(kThreads) gla_prefill_simt_kernel(PrefillArgs 
     const TI* q = static_cast<const TI*>(a.q) + bh * (long)L * dk;
     const TI* k = static_cast<const TI*>(a.k) + bh * (long)L * dk;
     const TI* v = static_cast<const TI*>(a.v) + bh * (long)L * dv;
-    const float* la = a.log_alpha ? a.log_alpha + bh * (long)L * dk : nullptr;
+    // per-channel gate: [L][dk]; per-token gate (GLA_FLAG_SCALAR_GATE): [L], shared by all channels
+    const bool scalar_gate = a.flags & GLA_FLAG_SCALAR_GATE;
+    const long la_t = scalar_gate ? 1 : dk, la_d = scalar_gate ? 0 : 1;
+    const float* la = a.log_alpha ? a.log_alpha + bh * (long)L * la_t : nullptr;
     TO* out = static_cast<TO*>(a.out) + bh * (long)L * dv;
 
     for (int idx = tid; idx < dk * NC; idx += kThreads) {
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(kThreads) gla_prefill_simt_kernel(PrefillArgs 
                     xq = phi_elu1_exact(xq);
                     xk = phi_elu1_exact(xk);
                 }
-                if (la) xl = la[g];
+                if (la) xl = la[(long)(t0 + t) * la_t + d * la_d];
             }
             qf[idx] = xq;
             kf[idx] = xk;

@@ -62,7 +62,8 @@ namespace gla {
 namespace {
 
 constexpr int C = 64;  // chunk length (tokens)
-constexpr int NS = 3;  // q/k stages (hold Qh/Kh until the chunk's MMAs finish)
+constexpr int NS_MAX = 4;  // q/k stages at most (hold Qh/Kh until the chunk's MMAs finish)
+constexpr int NV_MAX = 4;  // V stages at most
 constexpr int NL = 2;  // log-alpha stages
 constexpr int kWarps = 24;
 constexpr int kThreads = kWarps * 32;
@@ -88,13 +89,13 @@ struct VRing {
 
 enum {
     B_QK_FULL = 0,
-    B_QK_GATED = B_QK_FULL + NS,
-    B_QK_EMPTY = B_QK_GATED + NS,
-    B_LA_FULL = B_QK_EMPTY + NS,
+    B_QK_GATED = B_QK_FULL + NS_MAX,
+    B_QK_EMPTY = B_QK_GATED + NS_MAX,
+    B_LA_FULL = B_QK_EMPTY + NS_MAX,
     B_LA_EMPTY = B_LA_FULL + NL,
     B_V_FULL = B_LA_EMPTY + NL,
-    B_V_EMPTY = B_V_FULL + 3,
-    B_A_FULL = B_V_EMPTY + 3,
+    B_V_EMPTY = B_V_FULL + NV_MAX,
+    B_A_FULL = B_V_EMPTY + NV_MAX,
     B_A_EMPTY,
     B_P_FULL,    // 2
     B_P_EMPTY = B_P_FULL + 2,  // 2
@@ -108,12 +109,17 @@ enum {
     B_COUNT
 };
 
-template <int DK, int DVT>
+// SCALAR: one log alpha per token (shared by all channels): its tile is 256
+// bytes instead of DK * 256, and the shared memory it frees buys a fourth q/k
+// stage and a deeper V ring.
+template <int DK, int DVT, bool SCALAR = false>
 struct Layout {
-    static constexpr int NV = VRing<DVT>::N;
+    static constexpr int NS = SCALAR ? 4 : 3;
+    static constexpr int NV = SCALAR ? (DVT == 64 ? 4 : 3) : VRing<DVT>::N;
     static constexpr int QB = DK * C * 2;        // one bf16 [64][DK] tile (DK/64 swizzle atoms)
     static constexpr int STAGE_QK = 2 * QB;
-    static constexpr int LAB = DK * C * 4;       // fp32 [64][DK]
+    static constexpr int LAB = SCALAR ? C * 4 : DK * C * 4;  // fp32 [64][DK], or [64] with SCALAR
+    static constexpr int LA_REGION = (NL * LAB + 1023) / 1024 * 1024;  // the V tiles stay 1024-aligned
     static constexpr int VB = DVT * C * 2;       // bf16 [64][DVT] as DVT/64 atoms of 64 columns
     static constexpr int PB = C * C * 2;         // bf16 [64][64]
     static constexpr int OSB = C * DVT * 2;      // output staging, DVT/64 blocks of [64][64] bf16
@@ -122,9 +128,9 @@ struct Layout {
     static constexpr int TPS = C / SEG;               // tokens per segment
     static constexpr int off_qk = 0;
     static constexpr int off_la = off_qk + NS * STAGE_QK;
-    static constexpr int off_v = off_la + NL * LAB;
+    static constexpr int off_v = off_la + LA_REGION;
     // a second P buffer where it fits: P(c+1) need not wait for O_a(c)
-    static constexpr int NP = NS * STAGE_QK + NL * LAB + NV * VB + 2 * PB + OSB + NS * DK * 4 + 2 * SEG * DK * 4 +
+    static constexpr int NP = NS * STAGE_QK + LA_REGION + NV * VB + 2 * PB + OSB + NS * DK * 4 + 2 * SEG * DK * 4 +
                                       B_COUNT * 8 + 12 + 1008 <= 232448
                                   ? 2
                                   : 1;
@@ -172,12 +178,15 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // single ex2:  Qh = q * 2^{(b_t - b_C) log2 e},  Kh = k * 2^{-(b_t - b_C) log2 e}.
 // The feature map and the gate are compile-time branches so that the token
 // loop stays one basic block the scheduler can interleave.
-template <int DK, int TPS, int G, bool GATE, bool ELU>
+// With SCALAR (one log alpha per token) all four channels share one running
+// value, so a token costs one pair of ex2 instead of four.
+template <int DK, int TPS, int G, bool GATE, bool ELU, bool SCALAR>
 __device__ __forceinline__ void gate_factors(uint8_t* qt, uint8_t* kt, const float* la, int seg, int col, int nval,
                                              const float (&off)[4]) {
     constexpr float kLog2e = 1.4426950408889634f;
     const float2 l2e = make_float2(kLog2e, kLog2e);
     float2 run01 = make_float2(off[0] * kLog2e, off[1] * kLog2e), run23 = make_float2(off[2] * kLog2e, off[3] * kLog2e);
+    float run_s = off[0] * kLog2e;
 #pragma unroll 1
     for (int i0 = 0; i0 < TPS; i0 += G) {
         uint2 qr[G], kr[G];
@@ -188,7 +197,7 @@ __device__ __forceinline__ void gate_factors(uint8_t* qt, uint8_t* kt, const flo
             const uint32_t o = sw128_offset(t, col);
             qr[u] = *reinterpret_cast<const uint2*>(qt + o);
             kr[u] = *reinterpret_cast<const uint2*>(kt + o);
-            if (GATE) lx[u] = *reinterpret_cast<const float4*>(la + t * DK);
+            if (GATE) lx[u] = SCALAR ? make_float4(la[t], 0.f, 0.f, 0.f) : *reinterpret_cast<const float4*>(la + t * DK);
         }
 #pragma unroll
         for (int u = 0; u < G; u++) {
@@ -201,7 +210,12 @@ __device__ __forceinline__ void gate_factors(uint8_t* qt, uint8_t* kt, const flo
                 k23 = make_float2(elu1(k23.x), elu1(k23.y));
             }
             float2 fq01 = make_float2(1.f, 1.f), fq23 = fq01, fk01 = fq01, fk23 = fq01;
-            if (GATE) {  // run = (b_t - b_C) log2 e >= 0
+            if (GATE && SCALAR) {  // run = (b_t - b_C) log2 e >= 0, the same for every channel
+                run_s = fmaf(lx[u].x, kLog2e, run_s);
+                const float fq = ex2_approx(run_s), fk = ex2_approx(-run_s);
+                fq01 = fq23 = make_float2(fq, fq);
+                fk01 = fk23 = make_float2(fk, fk);
+            } else if (GATE) {  // run = (b_t - b_C) log2 e >= 0
                 run01 = fma2(make_float2(lx[u].x, lx[u].y), l2e, run01);
                 run23 = fma2(make_float2(lx[u].z, lx[u].w), l2e, run23);
                 fq01 = make_float2(ex2_approx(run01.x), ex2_approx(run01.y));
@@ -230,9 +244,10 @@ __device__ __forceinline__ void gate_factors(uint8_t* qt, uint8_t* kt, const flo
     }
 }
 
-template <int DK, int DVT, bool GATE>
+template <int DK, int DVT, bool GATE, bool SCALAR>
 __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __grid_constant__ TcParams p) {
-    using Ly = Layout<DK, DVT>;
+    using Ly = Layout<DK, DVT, SCALAR>;
+    constexpr int NS = Ly::NS;
     constexpr int NV = Ly::NV;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base for the swizzled tiles.  The offset is added to the
@@ -278,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             mbar_init(bar(B_LA_FULL + i), 1);
             mbar_init(bar(B_LA_EMPTY + i), 8);
         }
-        for (int i = 0; i < 3; i++) {
+        for (int i = 0; i < NV; i++) {
             mbar_init(bar(B_V_FULL + i), 1);
             mbar_init(bar(B_V_EMPTY + i), 1);
         }
@@ -346,14 +361,17 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             // the chunk total b_C (tot).  Phase 2 re-reads log alpha from shared
             // memory and re-accumulates, so no per-token sums are held in registers.
             float off[4] = {0.f, 0.f, 0.f, 0.f}, tot[4] = {0.f, 0.f, 0.f, 0.f};
-            const float* la = reinterpret_cast<const float*>(sm + Ly::off_la + l * Ly::LAB) + ch;
+            // per-channel: this thread's 4 channels of row t at la + t*DK; SCALAR: row t at la[t]
+            const float* la = reinterpret_cast<const float*>(sm + Ly::off_la + l * Ly::LAB) + (SCALAR ? 0 : ch);
             if (GATE) {
                 float* st = segtot + (c & 1) * SEG * DK;
                 if (ok) {
                     float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                     for (int i = 0; i < TPS; i++) {
-                        const float4 x = *reinterpret_cast<const float4*>(la + (seg * TPS + i) * DK);
+                        const float4 x = SCALAR ? make_float4(la[seg * TPS + i], la[seg * TPS + i], la[seg * TPS + i],
+                                                              la[seg * TPS + i])
+                                                : *reinterpret_cast<const float4*>(la + (seg * TPS + i) * DK);
                         r.x += x.x;
                         r.y += x.y;
                         r.z += x.z;
@@ -393,9 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                 uint8_t* qt = sm + Ly::off_qk + s * Ly::STAGE_QK + atom * 8192;
                 uint8_t* kt = qt + Ly::QB;
                 if (elu)
-                    gate_factors<DK, TPS, G, GATE, true>(qt, kt, la, seg, col, nval, off);
+                    gate_factors<DK, TPS, G, GATE, true, SCALAR>(qt, kt, la, seg, col, nval, off);
                 else
-                    gate_factors<DK, TPS, G, GATE, false>(qt, kt, la, seg, col, nval, off);
+                    gate_factors<DK, TPS, G, GATE, false, SCALAR>(qt, kt, la, seg, col, nval, off);
             }
             if (GATE) {
                 __syncwarp();
@@ -758,7 +776,10 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                     mbar_test(bar(B_LA_EMPTY + pl_n % NL), ((pl_n / NL) & 1) ^ 1)) {
                     const int l = pl_n % NL;
                     mbar_arrive_expect_tx(bar(B_LA_FULL + l), Ly::LAB);
-                    tma_load_3d(sbase + Ly::off_la + l * Ly::LAB, &p.tm_la, bar(B_LA_FULL + l), 0, pl_n * C, bh);
+                    if (SCALAR)  // [B*H][L] fp32, box 64 tokens x 1
+                        tma_load_3d(sbase + Ly::off_la + l * Ly::LAB, &p.tm_la, bar(B_LA_FULL + l), pl_n * C, bh, 0);
+                    else
+                        tma_load_3d(sbase + Ly::off_la + l * Ly::LAB, &p.tm_la, bar(B_LA_FULL + l), 0, pl_n * C, bh);
                     pl_n++;
                     prog = true;
                 }
@@ -949,7 +970,7 @@ CUresult encode_3d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <int DK, int DVT, bool GATE>
+template <int DK, int DVT, bool GATE, bool SCALAR>
 cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
     TcParams p;
     memset(&p, 0, sizeof(p));
@@ -961,8 +982,14 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
         encode_3d(&p.tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, a.dv, a.L, BH, 64, C,
                   CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    if (GATE && encode_3d(&p.tm_la, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.log_alpha, DK, a.L, BH, DK, C,
-                          CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+    if (GATE && !SCALAR &&
+        encode_3d(&p.tm_la, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.log_alpha, DK, a.L, BH, DK, C,
+                  CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    // one log alpha per token: [B*H][L] (row stride L*4 bytes, a multiple of 16 when L % 4 == 0)
+    if (GATE && SCALAR &&
+        encode_3d(&p.tm_la, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.log_alpha, a.L, BH, 1, C, 1,
+                  CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     p.out_f32 = a.out_dtype == GLA_DTYPE_F32;
     if (!p.out_f32 && encode_3d(&p.tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out, a.dv, a.L, BH, 64, C,
@@ -979,8 +1006,8 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
     p.nchunks = (a.L + C - 1) / C;
     p.ntile = (a.dv + DVT - 1) / DVT;
     p.flags = a.flags;
-    auto kern = gla_prefill_tc_kernel<DK, DVT, GATE>;
-    const int smem = Layout<DK, DVT>::alloc;
+    auto kern = gla_prefill_tc_kernel<DK, DVT, GATE, SCALAR>;
+    const int smem = Layout<DK, DVT, SCALAR>::alloc;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const long grid = (long)BH * p.ntile;
@@ -1007,7 +1034,8 @@ int choose_dvt(const PrefillArgs& a) {
 
 template <int DK, int DVT>
 cudaError_t launch_g(const PrefillArgs& a, cudaStream_t s) {
-    return a.log_alpha ? launch_t<DK, DVT, true>(a, s) : launch_t<DK, DVT, false>(a, s);
+    if (!a.log_alpha) return launch_t<DK, DVT, false, false>(a, s);
+    return (a.flags & GLA_FLAG_SCALAR_GATE) ? launch_t<DK, DVT, true, true>(a, s) : launch_t<DK, DVT, true, false>(a, s);
 }
 
 }  // namespace
@@ -1019,6 +1047,8 @@ bool prefill_tc_supported(const PrefillArgs& a) {
     if (a.dv < 64 || a.dv % 64 != 0) return false;
     if ((a.flags & GLA_FLAG_NORMALIZE) && a.dv != 64) return false;
     if (a.L < 1) return false;
+    // the per-token gate's tensor map needs a 16-byte row stride
+    if (a.log_alpha && (a.flags & GLA_FLAG_SCALAR_GATE) && a.L % 4 != 0) return false;
     const long grid = (long)a.B * a.H * (a.dv / 64);
     if (grid > INT_MAX) return false;
     return true;

@@ -60,7 +60,10 @@ enum {
     GLA_FLAG_FEATURE_ELU1 = 1u,  /* apply phi(x) = elu(x) + 1 to q and k */
     GLA_FLAG_NORMALIZE = 2u,     /* o_t = phi(q_t)^T S_t / phi(q_t)^T z_t */
     GLA_FLAG_FORCE_SIMT = 4u,    /* use the fp32 SIMT chunk kernel even for bf16 */
-    GLA_FLAG_FORCE_CHUNK = 8u    /* use a chunk kernel even for a sequence of <= 16 tokens */
+    GLA_FLAG_FORCE_CHUNK = 8u,   /* use a chunk kernel even for a sequence of <= 16 tokens */
+    GLA_FLAG_SCALAR_GATE = 16u   /* log_alpha is fp32 [B][H][L]: one gate per token, shared by all
+                                    key channels ("Gated Linear Attention", the scalar special case
+                                    of the gate matrix G_t = alpha_t 1^T with alpha_t = gamma_t 1) */
 };
 
 /*

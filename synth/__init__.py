@@ -147,6 +147,7 @@ class Workload:
     qk_scale: bool = True        # q, k multiplied by dk^-1/2 at generation
     feature_elu1: bool = False
     normalize: bool = False
+    scalar_gate: bool = False    # log alpha [B,H,L]: one gate per token, shared by the channels
     init_std: float = 0.0        # 0 -> zero initial state
     seed: int = BASE_SEED
     extra: dict = field(default_factory=dict)
@@ -209,8 +210,7 @@ def make_prefill(w: Workload, heads=None):
     out = dict(q=q.reshape(shp_k), k=k.reshape(shp_k), v=v.reshape(shp_v), log_alpha=None,
                init_state=None)
     if w.gate:
-        g = gen(T_G, dk, std=w.gate_std, mean=w.gate_mean)
-        out["log_alpha"] = to_f32(log_sigmoid(g) / w.gate_temp).reshape(shp_k)
+        out["log_alpha"] = gate_log_alpha(w, heads)
     if w.init_std > 0:
         per = dk * dv
         if heads is not None:
@@ -221,6 +221,23 @@ def make_prefill(w: Workload, heads=None):
             out["init_state"] = to_f32(normals(w.seed, T_S0, (B * H * per,), std=w.init_std)
                                        ).reshape(B, H, dk, dv)
     return out
+
+
+def gate_log_alpha(w: Workload, heads=None):
+    """log alpha of a gated prefill workload, float32 [B,H,L,dk] ([B,H,L] with scalar_gate);
+    the values make_prefill returns for it."""
+    B, H, L, dk = w.B, w.H, w.L, w.dk
+    sel = list(range(B * H)) if heads is None else list(heads)
+    gd = 1 if w.scalar_gate else dk
+    per = L * gd
+    if heads is None:
+        g = normals(w.seed, T_G, (B * H * per,), mean=w.gate_mean, std=w.gate_std)
+    else:
+        g = np.concatenate([normals(w.seed, T_G, (per,), start=hh * per, mean=w.gate_mean, std=w.gate_std)
+                            for hh in sel])
+    lead = (len(sel),) if heads is not None else (B, H)
+    shp = lead + ((L,) if w.scalar_gate else (L, dk))
+    return to_f32(log_sigmoid(g) / w.gate_temp).reshape(shp)
 
 
 def decode_state(NS, H, dk, dv, std, seed, heads=None):

@@ -61,7 +61,8 @@ def run_prefill(w: synth.Workload, x: dict, out_f32=False, flags=0, final_z=Fals
     fs = torch.full((B, H, dk, dv), float("nan"), dtype=torch.float32, device=dev())
     fz = torch.full((B, H, dk), float("nan"), dtype=torch.float32, device=dev()) if final_z else None
     fl = flags | (gla.FLAG_FEATURE_ELU1 if w.feature_elu1 else 0) | \
-        (gla.FLAG_NORMALIZE if w.normalize else 0) | (gla.FLAG_FORCE_SIMT if force_simt else 0)
+        (gla.FLAG_NORMALIZE if w.normalize else 0) | (gla.FLAG_FORCE_SIMT if force_simt else 0) | \
+        (gla.FLAG_SCALAR_GATE if w.scalar_gate else 0)
     st = gla.gla_fwd_ex(q, k, v, out, B, H, L, dk, dv, chunk=w.chunk, log_alpha=la, init_state=s0,
                         init_z=z0, final_state=fs, final_z=fz,
                         in_dtype=gla.F32 if f32in else gla.BF16,
@@ -78,7 +79,11 @@ def run_prefill(w: synth.Workload, x: dict, out_f32=False, flags=0, final_z=Fals
 
 
 def oracle_prefill(w: synth.Workload, x: dict, init_z=None, nthreads=0):
+    la = synth.as_f64(x["log_alpha"])
+    if w.scalar_gate and la is not None:
+        # a per-token gate is the per-channel gate with the same value on every channel
+        la = np.repeat(la[..., None], w.dk, axis=-1)
     return oracle.gla_fwd(synth.as_f64(x["q"]), synth.as_f64(x["k"]), synth.as_f64(x["v"]),
-                          synth.as_f64(x["log_alpha"]), synth.as_f64(x["init_state"]),
+                          la, synth.as_f64(x["init_state"]),
                           None if init_z is None else np.asarray(init_z, np.float64),
                           feature_elu1=w.feature_elu1, normalize=w.normalize, nthreads=nthreads)
