@@ -62,6 +62,8 @@ def _load(plant: int = 0, build_dir: str | None = None):
         lib.oracle_gla_fwd_chunked.argtypes = [D, D, D, D, D, D, D, L, L, L, L, L, L,
                                                ctypes.c_int]
         lib.oracle_gla_fwd_chunked.restype = ctypes.c_int
+        lib.oracle_delta_fwd.argtypes = [D, D, D, D, D, D, D, D, L, L, L, L, ctypes.c_int]
+        lib.oracle_delta_fwd.restype = ctypes.c_int
         lib.oracle_max_threads.restype = ctypes.c_int
         _LIBS[key] = lib
         return lib
@@ -160,3 +162,29 @@ def gla_decode_step(q, k, v, log_alpha, state, nthreads=0, plant=0, build_dir=No
     if rc != 0:
         raise RuntimeError(f"oracle_gla_decode_step failed ({rc})")
     return out.reshape(*lead, dv), st.reshape(*lead, dk, dv)
+
+
+def delta_fwd(q, k, v, beta, log_alpha=None, init_state=None, nthreads=0, plant=0, build_dir=None):
+    """Delta rule, token by token ("linear-attention" blog, Delta attention; gated when
+    log_alpha is given).  q, k, log_alpha: [..., L, dk]; v: [..., L, dv]; beta: [..., L].
+
+    Returns (out, final_state) as float64 arrays.
+    """
+    q = _f64(q)
+    lead = q.shape[:-2]
+    L, dk = q.shape[-2:]
+    dv = np.shape(v)[-1]
+    BH = int(np.prod(lead)) if lead else 1
+    q = q.reshape(BH, L, dk)
+    k = _f64(k).reshape(BH, L, dk)
+    v = _f64(v).reshape(BH, L, dv)
+    b = _f64(beta).reshape(BH, L)
+    la = _f64(log_alpha).reshape(BH, L, dk) if log_alpha is not None else None
+    s0 = _f64(init_state).reshape(BH, dk, dv) if init_state is not None else None
+    out = np.empty((BH, L, dv), dtype=np.float64)
+    fs = np.empty((BH, dk, dv), dtype=np.float64)
+    rc = _load(plant, build_dir).oracle_delta_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(la), _ptr(s0),
+                                                  _ptr(out), _ptr(fs), BH, L, dk, dv, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_delta_fwd failed ({rc})")
+    return out.reshape(*lead, L, dv), fs.reshape(*lead, dk, dv)

@@ -21,6 +21,10 @@
  *  [CHK]  "Gated Linear Attention", "Summary" / "Chunk-Wise Block-Parallel":
  *         the chunk-wise form that interpolates between the parallel and the
  *         recurrent form (used only by oracle_gla_fwd_chunked).
+ *  [DLT]  "linear-attention" blog, "Delta attention": before writing, ask
+ *         what the memory already predicts for the key and write only the
+ *         error, with a write strength beta_n; the gated variant decays the
+ *         state first (used only by oracle_delta_fwd).
  *
  * Readings taken where the pages are silent or garbled:
  *  - state S is d_k x d_v, the update is k_t v_t^T, the decay scales the d_k
@@ -29,6 +33,11 @@
  *  - the normaliser z_t is carried like one extra all-ones value column of
  *    the state, so it decays with the same Diag(alpha_t) when a gate is
  *    present; no epsilon is added (phi > 0 keeps the denominator positive).
+ *
+ *  - delta rule: p_n = S_{n-1}^T k_n (the memory's prediction for k_n),
+ *    u_n = beta_n (v_n - p_n) (the error, written with strength beta_n),
+ *    S_n = S_{n-1} + k_n u_n^T, o_n = S_n^T q_n; with a gate the decay
+ *    Diag(alpha_n) is applied to S_{n-1} before the prediction.
  *
  * Planted mistakes: compiling with -DORACLE_PLANT=n (n >= 1) builds a
  * deliberately wrong variant that the pinning tests must reject.  The normal
@@ -274,6 +283,84 @@ int oracle_gla_fwd_chunked(const double *q, const double *k, const double *v,
         }
         if (final_state) memcpy(final_state + bh * dk * dv, S, (size_t)(dk * dv) * sizeof(double));
         free(S); free(b);
+    }
+    return err;
+}
+
+/*
+ * Delta rule [DLT], token by token, for every (b, h):
+ *   S <- Diag(alpha_n) S            (gated variant; log_alpha may be NULL)
+ *   p  = S^T k_n                    (what the memory predicts for k_n)
+ *   u  = beta_n (v_n - p)           (the error, written with strength beta_n)
+ *   S <- S + k_n u^T
+ *   o_n = S^T q_n
+ * Layouts: q, k, log_alpha [BH][L][dk]; v, out [BH][L][dv]; beta [BH][L];
+ * init_state, final_state [BH][dk][dv] (init_state may be NULL: zero).
+ */
+int oracle_delta_fwd(const double *q, const double *k, const double *v, const double *beta,
+                     const double *log_alpha, const double *init_state, double *out,
+                     double *final_state, long BH, long L, long dk, long dv, int nthreads) {
+    set_threads(nthreads);
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long h = 0; h < BH; h++) {
+        double *S = malloc(sizeof(double) * dk * dv);
+        double *p = malloc(sizeof(double) * dv);
+        double *u = malloc(sizeof(double) * dv);
+        if (!S || !p || !u) {
+#pragma omp atomic write
+            err = 1;
+            free(S);
+            free(p);
+            free(u);
+            continue;
+        }
+        for (long i = 0; i < dk * dv; i++) S[i] = init_state ? init_state[h * dk * dv + i] : 0.0;
+        for (long t = 0; t < L; t++) {
+            const double *qt = q + (h * L + t) * dk, *kt = k + (h * L + t) * dk;
+            const double *vt = v + (h * L + t) * dv;
+            const double bt = beta[h * L + t];
+            if (log_alpha)
+                for (long i = 0; i < dk; i++) {
+                    const double a = exp(log_alpha[(h * L + t) * dk + i]);
+                    for (long j = 0; j < dv; j++) S[i * dv + j] *= a;
+                }
+            for (long j = 0; j < dv; j++) {
+                double acc = 0.0;
+                for (long i = 0; i < dk; i++) acc += S[i * dv + j] * kt[i];
+                p[j] = acc;
+            }
+            for (long j = 0; j < dv; j++) {
+#if ORACLE_PLANT == 5
+                u[j] = bt * vt[j]; /* planted: prediction dropped (plain linear attention) */
+#else
+                u[j] = bt * (vt[j] - p[j]);
+#endif
+            }
+            double *ot = out + (h * L + t) * dv;
+#if ORACLE_PLANT == 6
+            /* planted: output read before the write */
+            for (long j = 0; j < dv; j++) {
+                double acc = 0.0;
+                for (long i = 0; i < dk; i++) acc += S[i * dv + j] * qt[i];
+                ot[j] = acc;
+            }
+#endif
+            for (long i = 0; i < dk; i++)
+                for (long j = 0; j < dv; j++) S[i * dv + j] += kt[i] * u[j];
+#if ORACLE_PLANT != 6
+            for (long j = 0; j < dv; j++) {
+                double acc = 0.0;
+                for (long i = 0; i < dk; i++) acc += S[i * dv + j] * qt[i];
+                ot[j] = acc;
+            }
+#endif
+        }
+        if (final_state)
+            for (long i = 0; i < dk * dv; i++) final_state[h * dk * dv + i] = S[i];
+        free(S);
+        free(p);
+        free(u);
     }
     return err;
 }

@@ -18,7 +18,7 @@ from test_oracle_pins import _close, _golden, _inputs, _phi, quadratic_masked
 @pytest.fixture(scope="module")
 def plant_dir(tmp_path_factory):
     d = str(tmp_path_factory.mktemp("plants"))
-    for n in (1, 2, 3, 4):
+    for n in (1, 2, 3, 4, 5, 6):
         oracle.build(plant=n, build_dir=d)
     return d
 
@@ -61,3 +61,23 @@ def test_plant4_exclusive_output_is_caught(plant_dir):
     out, _, _ = _fwd(4, plant_dir, q, k, v)
     S = np.cumsum(np.einsum("bld,blj->bldj", k, v), axis=1)
     assert not _close(out, np.einsum("bld,bldj->blj", q, S))
+
+
+def test_plant5_delta_prediction_dropped_is_caught(plant_dir):
+    from test_oracle_delta_pins import _close as dclose, _inputs as dinputs, triangular_form
+    q, k, v, beta = dinputs(1, 40, 6, 5)
+    out, fs = oracle.delta_fwd(q, k, v, beta, plant=5, build_dir=plant_dir)
+    O, S = triangular_form(q[0], k[0], v[0], beta[0], np.zeros((6, 5)))
+    assert not dclose(out[0], O)
+    g = _golden("delta_2x2.json")
+    o, _ = oracle.delta_fwd(*(np.array(g[n], float)[None] for n in ("q", "k", "v", "beta")),
+                            plant=5, build_dir=plant_dir)
+    assert not dclose(o[0], g["expect_out"], 1e-14)
+
+
+def test_plant6_delta_output_before_write_is_caught(plant_dir):
+    from test_oracle_delta_pins import _close as dclose
+    g = _golden("delta_2x2.json")
+    o, _ = oracle.delta_fwd(*(np.array(g[n], float)[None] for n in ("q", "k", "v", "beta")),
+                            plant=6, build_dir=plant_dir)
+    assert not dclose(o[0], g["expect_out"], 1e-14)
