@@ -59,6 +59,19 @@ def decode_multi_bytes(w) -> float:
     return float(w.B * w.H * (2 * w.dk * w.dv * 4 + w.L * (2 * w.dk * 2 + w.dv * 2 + w.dk * 4 + w.dv * 2)))
 
 
+def delta_flops(w) -> float:
+    """Delta rule per token and head: prediction S^T k, write k u^T, output S^T q (2 dk dv flops
+    each), plus the gate's decay (dk dv)."""
+    return float(w.B * w.H * w.L * (6 + (1 if w.gate else 0)) * w.dk * w.dv)
+
+
+def fp32_alu_peak_tflops(peaks) -> float:
+    """FP32 FMA peak from unit counts: SMs x 128 FP32 lanes x 2 flops x max SM clock."""
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return sms * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+
+
 def decode_bytes(NS, H, dk, dv) -> float:
     """Per step: fp32 state read + write, bf16 q/k/v, fp32 log alpha, fp32 out."""
     return float(NS * H * (2 * dk * dv * 4 + 2 * dk * 2 + dv * 2 + dk * 4 + dv * 4))
@@ -71,8 +84,9 @@ def load_peaks():
             d = json.load(f)
         return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
                     bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
-                    source="measured")
-    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+                    sm_max_mhz=float(d.get("sm_max_mhz", 2070.0)), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, sm_max_mhz=2070.0,
+                source="fallback")
 
 
 KERNEL_SOURCES = {
@@ -80,6 +94,7 @@ KERNEL_SOURCES = {
     "gla_decode_kernel": ("gla_decode.cu",),
     "gla_prefill_short_kernel": ("gla_short.cu",),
     "gla_prefill_tc_kernel_scalar_gate": ("gla_tc.cu", "gla_ptx.cuh"),
+    "gla_delta_kernel": ("gla_delta.cu",),
 }
 
 
@@ -434,6 +449,40 @@ def bench_decode_multi(args, device, rank):
     return dict(w=w, ms_per_call=ev0.elapsed_time(ev1) / n, calls=n)
 
 
+def bench_delta(args, device, rank):
+    """The delta rule (gla_delta_fwd) on its workload: B8 H16 L4096 dk = dv = 128, gated."""
+    import torch
+
+    import causal_gated_linear_gb300 as gla
+    w = synth.with_shape(synth.DELTA, seed=synth.DELTA.seed + 1000 * rank)
+    x = synth.make_delta(w)
+    q, k, v, b = (to_dev(x[n], device) for n in ("q", "k", "v", "beta"))
+    la = to_dev(x["log_alpha"], device)
+    out = torch.empty((w.B, w.H, w.L, w.dv), dtype=torch.bfloat16, device=device)
+    fs = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def call():
+        r = gla.gla_delta_fwd(q, k, v, b, out, w.B, w.H, w.L, w.dk, w.dv, log_alpha=la, final_state=fs,
+                              stream=stream)
+        if r != 0:
+            raise RuntimeError(gla.gla_status_string(r))
+
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize(device)
+    evs = []
+    for _ in range(args.delta_calls):
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        e.record(stream)
+        evs.append((a, e))
+    torch.cuda.synchronize(device)
+    gla.check(gla.gla_device_error(stream))
+    return dict(w=w, ms=statistics.mean(a.elapsed_time(e) for a, e in evs), calls=args.delta_calls)
+
+
 def run_gla(args):
     import torch
     rank, world, local = dist_env()
@@ -449,6 +498,7 @@ def run_gla(args):
     w, BH, pre = bench_prefill(args, device, rank, world)
     dec = bench_decode(args, device, rank) if args.decode_steps > 0 else None
     mdec = bench_decode_multi(args, device, rank) if args.multi_calls > 0 else None
+    dlt = bench_delta(args, device, rank) if args.delta_calls > 0 else None
 
     ms = pre["total_ms"] / args.steps
     tokens = w.B * w.L
@@ -497,6 +547,18 @@ def run_gla(args):
                          "frac": sgbs / peaks["hbm_gbs"],
                          "traffic": recorded_traffic("gla_prefill_tc_kernel_scalar_gate"),
                          "kernel": "gla_prefill_tc_kernel (per-token gate)", "alg_bytes_per_launch": sbytes}}
+    if dlt is not None:
+        dw = dlt["w"]
+        dfl = delta_flops(dw)
+        dtf = dfl / (dlt["ms"] / 1e3) / 1e12
+        apk = fp32_alu_peak_tflops(peaks)
+        line["delta"] = {
+            "workload": dw.name, "ms_per_launch": dlt["ms"], "calls": dlt["calls"],
+            "tokens_per_s": dw.B * dw.L / (dlt["ms"] / 1e3),
+            "roofline": {"bound": "alu", "achieved": dtf, "peak": apk, "unit": "TFLOP/s", "frac": dtf / apk,
+                         "traffic": recorded_traffic("gla_delta_kernel"), "kernel": "gla_delta_kernel",
+                         "alg_flops_per_launch": dfl,
+                         "peak_source": "FP32 FMA: SMs x 128 lanes x 2 flops x max SM clock"}}
     if mdec is not None:
         mw = mdec["w"]
         mbytes = decode_multi_bytes(mw)
@@ -535,6 +597,8 @@ def main():
     ap.add_argument("--impl", default="gla", choices=["gla", "reference"])
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--decode-pool", type=int, default=8)
+    ap.add_argument("--delta-calls", type=int, default=3,
+                    help="timed launches of the delta-rule workload (0: skip)")
     ap.add_argument("--scalar-calls", type=int, default=5,
                     help="timed launches of the long-context workload with one gate per token (0: skip)")
     ap.add_argument("--multi-calls", type=int, default=64,

@@ -13,6 +13,8 @@ The functions mirror the C entry points:
                init_state=None, init_z=None, final_state=None, final_z=None,
                in_dtype=BF16, out_dtype=BF16, flags=0, stream=None) -> int
     gla_decode_step(q, k, v, log_alpha, state, out, B, H, dk, dv, stream=None)
+    gla_delta_fwd(q, k, v, beta, out, B, H, L, dk, dv, log_alpha=None, init_state=None,
+                  final_state=None, out_dtype=BF16, stream=None) -> int
     gla_device_error(stream=None) -> int
     gla_status_string(status) -> str
     gla_version() -> str
@@ -32,8 +34,8 @@ GLA_OK, GLA_ERR_INVALID, GLA_ERR_UNSUPPORTED, GLA_ERR_MISALIGNED, GLA_ERR_CUDA, 
 BF16, F32 = 0, 1
 FLAG_FEATURE_ELU1, FLAG_NORMALIZE, FLAG_FORCE_SIMT, FLAG_FORCE_CHUNK, FLAG_SCALAR_GATE = 1, 2, 4, 8, 16
 
-EXPORTED = ["gla_fwd", "gla_fwd_ex", "gla_decode_step", "gla_device_error", "gla_device_error_detail",
-            "gla_status_string", "gla_version"]
+EXPORTED = ["gla_fwd", "gla_fwd_ex", "gla_decode_step", "gla_delta_fwd", "gla_device_error",
+            "gla_device_error_detail", "gla_status_string", "gla_version"]
 
 
 class GlaError(RuntimeError):
@@ -73,6 +75,8 @@ def load(path: str | None = None):
     lib.gla_fwd_ex.restype = i
     lib.gla_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, vp]
     lib.gla_decode_step.restype = i
+    lib.gla_delta_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
+    lib.gla_delta_fwd.restype = i
     lib.gla_device_error.argtypes = [vp]
     lib.gla_device_error.restype = i
     lib.gla_device_error_detail.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
@@ -135,6 +139,12 @@ def gla_fwd_ex(q, k, v, out, B, H, L, dk, dv, chunk=64, log_alpha=None, init_sta
 def gla_decode_step(q, k, v, log_alpha, state, out, B, H, dk, dv, stream=None) -> int:
     return load().gla_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(state),
                                   _ptr(out), B, H, dk, dv, _stream(stream))
+
+
+def gla_delta_fwd(q, k, v, beta, out, B, H, L, dk, dv, log_alpha=None, init_state=None, final_state=None,
+                  out_dtype=BF16, stream=None) -> int:
+    return load().gla_delta_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(log_alpha), _ptr(init_state),
+                                _ptr(out), _ptr(final_state), B, H, L, dk, dv, out_dtype, _stream(stream))
 
 
 def gla_device_error(stream=None) -> int:

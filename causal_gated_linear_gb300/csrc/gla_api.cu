@@ -207,6 +207,52 @@ int gla_decode_step(const void* q, const void* k, const void* v, const float* lo
     return finish(launch_decode(a, s), s);
 }
 
+int gla_delta_fwd(const void* q, const void* k, const void* v, const float* beta, const float* log_alpha,
+                  const float* init_state, void* out, float* final_state, int B, int H, int L, int dk, int dv,
+                  int out_dtype, void* stream) {
+    if (B < 1 || H < 1 || L < 0 || dk < 1 || dv < 1) return GLA_ERR_INVALID;
+    if (out_dtype != GLA_DTYPE_BF16 && out_dtype != GLA_DTYPE_F32) return GLA_ERR_INVALID;
+    if (L > 0 && (!q || !k || !v || !beta || !out)) return GLA_ERR_INVALID;
+    if (!delta_supported(dk, dv)) return GLA_ERR_UNSUPPORTED;
+    if ((size_t)B * H > 0x7fffffffu || (dv + 63) / 64 > 65535) return GLA_ERR_UNSUPPORTED;
+    const void* ptrs[] = {q, k, v, beta, log_alpha, init_state, out, final_state};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return GLA_ERR_MISALIGNED;
+    const size_t BH = (size_t)B * H, Ls = (size_t)L;
+    const size_t no = BH * Ls * dv * (out_dtype == GLA_DTYPE_F32 ? 4 : 2), ns = BH * dk * dv * 4;
+    if (overlaps(out, no, q, BH * Ls * dk * 2) || overlaps(out, no, k, BH * Ls * dk * 2) ||
+        overlaps(out, no, v, BH * Ls * dv * 2) || overlaps(out, no, beta, BH * Ls * 4) ||
+        overlaps(out, no, log_alpha, BH * Ls * dk * 4) || overlaps(out, no, init_state, ns) ||
+        overlaps(out, no, final_state, ns))
+        return GLA_ERR_INVALID;
+    if (final_state && init_state && final_state != init_state && overlaps(final_state, ns, init_state, ns))
+        return GLA_ERR_INVALID;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (L == 0) {
+        cudaError_t e = cudaSuccess;
+        if (final_state && final_state != init_state)
+            e = init_state ? cudaMemcpyAsync(final_state, init_state, ns, cudaMemcpyDeviceToDevice, s)
+                           : cudaMemsetAsync(final_state, 0, ns, s);
+        return finish(e, s);
+    }
+    DeltaArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.beta = beta;
+    a.log_alpha = log_alpha;
+    a.init_state = init_state;
+    a.out = out;
+    a.final_state = final_state;
+    a.B = B;
+    a.H = H;
+    a.L = L;
+    a.dk = dk;
+    a.dv = dv;
+    a.out_dtype = out_dtype;
+    return finish(launch_delta(a, s), s);
+}
+
 int gla_device_error(void* stream) { return read_and_clear_error(static_cast<cudaStream_t>(stream)); }
 
 int gla_device_error_detail(void* stream, unsigned* detail4) {

@@ -50,6 +50,23 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
 bool prefill_short_supported(const PrefillArgs& a);
 cudaError_t launch_prefill_short(const PrefillArgs& a, cudaStream_t s);
 
+struct DeltaArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* beta;
+    const float* log_alpha;
+    const float* init_state;
+    void* out;
+    float* final_state;
+    int B, H, L, dk, dv;
+    int out_dtype;
+};
+
+// Delta rule, token by token (one warp per 16 value columns of a head).
+bool delta_supported(int dk, int dv);
+cudaError_t launch_delta(const DeltaArgs& a, cudaStream_t s);
+
 // Memory-bound decode step.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 

@@ -131,6 +131,29 @@ int gla_decode_step(const void* q, const void* k, const void* v, const float* lo
                     float* state, float* out, int B, int H, int dk, int dv, void* stream);
 
 /*
+ * gla_delta_fwd -- the delta rule ("linear-attention" blog, Delta attention):
+ * before each write the memory's prediction for the key is taken and only the
+ * error is written, with strength beta_n; the gated variant decays the state
+ * first ("Gated Linear Attention", GLA Recurrent Form):
+ *   S <- Diag(alpha_n) S;  p = S^T k_n;  u = beta_n (v_n - p);  S <- S + k_n u^T;
+ *   o_n = S^T q_n.
+ *
+ *   q, k        bf16 [B][H][L][dk]
+ *   v           bf16 [B][H][L][dv]
+ *   beta        fp32 [B][H][L]  (write strength per token)
+ *   log_alpha   fp32 [B][H][L][dk], or NULL for no gate
+ *   init_state  fp32 [B][H][dk][dv], or NULL for S_{-1} = 0
+ *   out         [B][H][L][dv], bf16 or fp32 (out_dtype = GLA_DTYPE_BF16 / _F32)
+ *   final_state fp32 [B][H][dk][dv], or NULL; may alias init_state
+ * The recurrence runs token by token in fp32.  Supported: dk in {32, 64, 128},
+ * dv a multiple of 16.  Pointers 16-byte aligned; out must not alias an input.
+ * Validation failures return before any launch.
+ */
+int gla_delta_fwd(const void* q, const void* k, const void* v, const float* beta, const float* log_alpha,
+                  const float* init_state, void* out, float* final_state, int B, int H, int L, int dk, int dv,
+                  int out_dtype, void* stream);
+
+/*
  * gla_device_error -- synchronise `stream`, read and clear the device error
  * word that bounded waits set.  Returns GLA_OK, GLA_ERR_TIMEOUT or GLA_ERR_CUDA.
  */

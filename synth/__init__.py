@@ -32,7 +32,7 @@ _MIX1 = np.uint64(0xBF58476D1CE4E5B9)
 _MIX2 = np.uint64(0x94D049BB133111EB)
 
 # tensor ids (the "tensor" part of the counter key)
-T_Q, T_K, T_V, T_G, T_S0 = 1, 2, 3, 4, 5
+T_Q, T_K, T_V, T_G, T_S0, T_BETA = 1, 2, 3, 4, 5, 6
 
 BASE_SEED = 20261202
 
@@ -238,6 +238,33 @@ def gate_log_alpha(w: Workload, heads=None):
     lead = (len(sel),) if heads is not None else (B, H)
     shp = lead + ((L,) if w.scalar_gate else (L, dk))
     return to_f32(log_sigmoid(g) / w.gate_temp).reshape(shp)
+
+
+# delta-rule workload: the config-2 shape; q and k rows of unit length, v ~ N(0,1),
+# beta = sigmoid(N(0,1)) per token, the config-2 gate (logsigmoid(N(4, 1.5)) / 16)
+DELTA = Workload("gla_delta_B8H16L4096d128", 8, 16, 4096, 128, 128, qk_scale=False,
+                 seed=BASE_SEED + 6)
+
+
+def make_delta(w: Workload, heads=None):
+    """Inputs of a delta-rule workload: q, k (rows scaled to unit length, then bf16 bits),
+    v (bf16 bits), beta float32 [.., L], log_alpha float32 [.., L, dk] or None, init_state
+    float32 or None.  `heads` selects flat (b*H+h) indices, as in make_prefill."""
+    x = make_prefill(w, heads)
+    B, H, L, dk = w.B, w.H, w.L, w.dk
+    sel = list(range(B * H)) if heads is None else list(heads)
+    for n, tid in (("q", T_Q), ("k", T_K)):
+        parts = [normals(w.seed, tid, (L, dk), start=hh * L * dk) for hh in sel] if heads is not None \
+            else [normals(w.seed, tid, (B * H * L * dk,))]
+        a = np.concatenate([p.reshape(-1) for p in parts]).reshape(-1, dk)
+        a = a / np.linalg.norm(a, axis=1, keepdims=True)
+        x[n] = to_bf16_bits(a).reshape(x[n].shape)
+    bparts = [normals(w.seed, T_BETA, (L,), start=hh * L) for hh in sel] if heads is not None \
+        else [normals(w.seed, T_BETA, (B * H * L,))]
+    g = np.concatenate([p.reshape(-1) for p in bparts])
+    lead = (len(sel),) if heads is not None else (B, H)
+    x["beta"] = to_f32(1.0 / (1.0 + np.exp(-g))).reshape(lead + (L,))
+    return x
 
 
 def decode_state(NS, H, dk, dv, std, seed, heads=None):
