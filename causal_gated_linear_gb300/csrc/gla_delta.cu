@@ -8,14 +8,15 @@
 // the gated variant first decays the state, S_{n-1} <- Diag(alpha_n) S_{n-1}.
 //
 // Each value column of the state evolves on its own (p_n, u_n and the write
-// are column-wise given k_n and beta_n), so a warp owns 16 value columns of
-// one head for the whole sequence and needs no block-wide synchronisation per
-// token: lane (rg, cq) holds rows [rg * RPL, (rg + 1) * RPL) of columns
-// [4 cq, 4 cq + 4) (RPL = dk / 8 rows, 4 * RPL fp32 registers), and the two
-// reductions over dk per token (the prediction and the output) are three
-// butterfly shuffles across the eight row groups.  Tokens are staged in shared
-// memory 32 at a time by the whole CTA (4 warps = 64 value columns); rows are
-// padded so that the eight row groups' float4 reads fall in distinct banks.
+// are column-wise given k_n and beta_n), so a warp owns 4 value columns of one
+// head for the whole sequence and needs no block-wide synchronisation per
+// token: lane (rg, cp) holds rows [rg * RPL, (rg + 1) * RPL) of the column
+// pair 2 cp (RPL = dk / 16 rows, as packed fp32 pairs), and the two
+// reductions over dk per token (the prediction and the output) are four
+// butterfly shuffles across the sixteen row groups.  A CTA of 16 warps covers
+// 64 value columns; tokens are staged in shared memory 16 at a time, double
+// buffered: the next round's global loads are in flight while the current
+// round is computed.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -26,17 +27,22 @@
 namespace gla {
 namespace {
 
-constexpr int kWarps = 4;             // 16 value columns each
-constexpr int kCols = 16 * kWarps;    // value columns per CTA
-constexpr int kTB = 32;               // tokens staged per round
+constexpr int kWarps = 16;            // 4 value columns each
+constexpr int kCols = 4 * kWarps;     // value columns per CTA
+constexpr int kThreads = kWarps * 32;
+constexpr int kTB = 16;               // tokens staged per round
 
 template <int RPL>
 struct DeltaLayout {
-    static constexpr int DK = RPL * 8;
-    static constexpr int STRIDE = RPL == 4 ? 12 : RPL + 4;  // padded floats per row group
-    static constexpr int ROW = 8 * STRIDE;                  // padded floats per token
+    static constexpr int DK = RPL * 16;
+    static constexpr int STRIDE = RPL + 4;   // padded floats per row group (16-byte aligned for RPL >= 4)
+    static constexpr int ROW = 16 * STRIDE;  // padded floats per token
     __host__ __device__ static constexpr int pidx(int r) { return (r / RPL) * STRIDE + r % RPL; }
-    static constexpr size_t bytes = sizeof(float) * (size_t)kTB * (3 * ROW + kCols + 1);
+    static constexpr int BUF = kTB * (3 * ROW + kCols + 4);  // floats per staging buffer
+    static constexpr size_t bytes = sizeof(float) * 2 * (size_t)BUF;
+    // elements of one round each thread loads: q, k, log alpha (DK per token) and v (kCols per token)
+    static constexpr int NQ = (kTB * DK + kThreads - 1) / kThreads;
+    static constexpr int NV = (kTB * kCols + kThreads - 1) / kThreads;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
@@ -44,33 +50,66 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// sum over the eight row groups (lane bits 2..4)
-__device__ __forceinline__ float rowgroup_sum(float x) {
-    x += __shfl_xor_sync(0xffffffffu, x, 4);
-    x += __shfl_xor_sync(0xffffffffu, x, 8);
-    x += __shfl_xor_sync(0xffffffffu, x, 16);
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// sum over the sixteen row groups (lane bits 1..4)
+__device__ __forceinline__ float2 rowgroup_sum(float2 x) {
+#pragma unroll
+    for (int m = 2; m <= 16; m <<= 1) {
+        x.x += __shfl_xor_sync(0xffffffffu, x.x, m);
+        x.y += __shfl_xor_sync(0xffffffffu, x.y, m);
+    }
     return x;
 }
 
+// RPL consecutive floats of a staged row group (16-byte aligned when RPL >= 4)
+template <int RPL>
+__device__ __forceinline__ void load_rows(const float* p, float (&r)[RPL]) {
+    if constexpr (RPL >= 4) {
+#pragma unroll
+        for (int i = 0; i < RPL; i += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(p + i);
+            r[i] = x.x, r[i + 1] = x.y, r[i + 2] = x.z, r[i + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < RPL; i += 2) {
+            const float2 x = *reinterpret_cast<const float2*>(p + i);
+            r[i] = x.x, r[i + 1] = x.y;
+        }
+    }
+}
+
 template <int RPL, bool GATE, bool OUT_F32>
-__global__ void __launch_bounds__(kWarps * 32) gla_delta_kernel(const DeltaArgs a) {
+__global__ void __launch_bounds__(kThreads) gla_delta_kernel(const DeltaArgs a) {
     using Ly = DeltaLayout<RPL>;
     constexpr int DK = Ly::DK;
     extern __shared__ __align__(16) float sm[];
-    float* s_q = sm;                        // [kTB][ROW]
-    float* s_k = s_q + kTB * Ly::ROW;       // [kTB][ROW]
-    float* s_a = s_k + kTB * Ly::ROW;       // [kTB][ROW]  alpha = e^{log alpha}
-    float* s_v = s_a + kTB * Ly::ROW;       // [kTB][kCols]
-    float* s_b = s_v + kTB * kCols;         // [kTB]
 
     const int L = a.L, dv = a.dv;
     const long bh = blockIdx.x;
     const int col0 = blockIdx.y * kCols;
     const int ncols = min(kCols, dv - col0);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rg = lane >> 2, cq = lane & 3;
-    const int c = warp * 16 + cq * 4;       // this lane's first column within the CTA's block
-    const bool active = c < ncols;          // dv is a multiple of 16, so warps are all or nothing
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rg = lane >> 1, cp = lane & 1;
+    const int c = warp * 4 + cp * 2;        // this lane's first column within the CTA's block
+    const bool active = c < ncols;          // dv is a multiple of 16: a warp is all or nothing
     const int r0 = rg * RPL;
 
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + bh * (long)L * DK;
@@ -79,101 +118,130 @@ __global__ void __launch_bounds__(kWarps * 32) gla_delta_kernel(const DeltaArgs 
     const float* la = GATE ? a.log_alpha + bh * (long)L * DK : nullptr;
     const float* beta = a.beta + bh * (long)L;
 
-    float S[RPL][4];
+    // one round of tokens [t0, t0 + n): global -> registers, registers -> a staging buffer
+    __nv_bfloat16 rq[Ly::NQ], rk[Ly::NQ];
+    float ra[Ly::NQ];
+    __nv_bfloat16 rv[Ly::NV];
+    float rb = 0.f;
+    auto fetch = [&](int t0) {
+        const int n = min(kTB, L - t0);
+#pragma unroll
+        for (int m = 0; m < Ly::NQ; m++) {
+            const int idx = tid + m * kThreads;
+            if (idx < n * DK) {
+                const long g = (long)t0 * DK + idx;
+                rq[m] = q[g];
+                rk[m] = k[g];
+                if (GATE) ra[m] = la[g];
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < Ly::NV; m++) {
+            const int idx = tid + m * kThreads;
+            const int t = idx / kCols, j = idx % kCols;
+            if (t < n && j < ncols) rv[m] = v[(long)(t0 + t) * dv + col0 + j];
+        }
+        if (tid < n) rb = beta[t0 + tid];
+    };
+    auto stage = [&](int t0, float* buf) {
+        const int n = min(kTB, L - t0);
+        float* s_q = buf;
+        float* s_k = s_q + kTB * Ly::ROW;
+        float* s_a = s_k + kTB * Ly::ROW;
+        float* s_v = s_a + kTB * Ly::ROW;
+        float* s_b = s_v + kTB * kCols;
+#pragma unroll
+        for (int m = 0; m < Ly::NQ; m++) {
+            const int idx = tid + m * kThreads;
+            if (idx < n * DK) {
+                const int o = (idx / DK) * Ly::ROW + Ly::pidx(idx % DK);
+                s_q[o] = __bfloat162float(rq[m]);
+                s_k[o] = __bfloat162float(rk[m]);
+                if (GATE) s_a[o] = __expf(ra[m]);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < Ly::NV; m++) {
+            const int idx = tid + m * kThreads;
+            const int t = idx / kCols, j = idx % kCols;
+            if (t < n && j < ncols) s_v[t * kCols + j] = __bfloat162float(rv[m]);
+        }
+        if (tid < n) s_b[tid] = rb;
+    };
+
+    float2 S[RPL];
     if (active && a.init_state) {
         const float* s0 = a.init_state + bh * (long)DK * dv + col0 + c;
 #pragma unroll
-        for (int i = 0; i < RPL; i++) {
-            const float4 x = *reinterpret_cast<const float4*>(s0 + (long)(r0 + i) * dv);
-            S[i][0] = x.x, S[i][1] = x.y, S[i][2] = x.z, S[i][3] = x.w;
-        }
+        for (int i = 0; i < RPL; i++) S[i] = *reinterpret_cast<const float2*>(s0 + (long)(r0 + i) * dv);
     } else {
 #pragma unroll
-        for (int i = 0; i < RPL; i++) S[i][0] = S[i][1] = S[i][2] = S[i][3] = 0.f;
+        for (int i = 0; i < RPL; i++) S[i] = make_float2(0.f, 0.f);
     }
 
-    for (int t0 = 0; t0 < L; t0 += kTB) {
+    fetch(0);
+    stage(0, sm);
+    __syncthreads();
+    for (int t0 = 0, rnd = 0; t0 < L; t0 += kTB, rnd++) {
         const int n = min(kTB, L - t0);
-        __syncthreads();  // the previous round's tokens are consumed
-        for (int idx = threadIdx.x; idx < n * DK; idx += kWarps * 32) {
-            const int t = idx / DK, r = idx % DK;
-            const long g = (long)(t0 + t) * DK + r;
-            const int o = t * Ly::ROW + Ly::pidx(r);
-            s_q[o] = __bfloat162float(q[g]);
-            s_k[o] = __bfloat162float(k[g]);
-            if (GATE) s_a[o] = __expf(la[g]);
-        }
-        for (int idx = threadIdx.x; idx < n * ncols; idx += kWarps * 32) {
-            const int t = idx / ncols, j = idx % ncols;
-            s_v[t * kCols + j] = __bfloat162float(v[(long)(t0 + t) * dv + col0 + j]);
-        }
-        for (int t = threadIdx.x; t < n; t += kWarps * 32) s_b[t] = beta[t0 + t];
-        __syncthreads();
-        if (!active) continue;
-        for (int t = 0; t < n; t++) {
-            const float* kt = s_k + t * Ly::ROW + rg * Ly::STRIDE;
-            const float* qt = s_q + t * Ly::ROW + rg * Ly::STRIDE;
-            const float* at = s_a + t * Ly::ROW + rg * Ly::STRIDE;
-            // the gate decays the state before the prediction
-            if (GATE) {
+        const bool more = t0 + kTB < L;
+        if (more) fetch(t0 + kTB);  // in flight while this round is computed
+        const float* buf = sm + (rnd & 1) * Ly::BUF;
+        const float* s_q = buf;
+        const float* s_k = s_q + kTB * Ly::ROW;
+        const float* s_a = s_k + kTB * Ly::ROW;
+        const float* s_v = s_a + kTB * Ly::ROW;
+        const float* s_b = s_v + kTB * kCols;
+        if (active) {
+            for (int t = 0; t < n; t++) {
+                const int ro = t * Ly::ROW + rg * Ly::STRIDE;
+                float kr[RPL], qr[RPL];
+                load_rows<RPL>(s_k + ro, kr);
+                // the gate decays the state before the prediction
+                if (GATE) {
+                    float ar[RPL];
+                    load_rows<RPL>(s_a + ro, ar);
 #pragma unroll
-                for (int i4 = 0; i4 < RPL; i4 += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4*>(at + i4);
-                    const float al[4] = {a4.x, a4.y, a4.z, a4.w};
+                    for (int i = 0; i < RPL; i++) S[i] = mul2(S[i], make_float2(ar[i], ar[i]));
+                }
+                // prediction p = S^T k for this lane's column pair (two chains)
+                float2 p0 = make_float2(0.f, 0.f), p1 = p0;
 #pragma unroll
-                    for (int e = 0; e < 4; e++)
+                for (int i = 0; i < RPL; i += 2) {
+                    p0 = fma2(S[i], make_float2(kr[i], kr[i]), p0);
+                    p1 = fma2(S[i + 1], make_float2(kr[i + 1], kr[i + 1]), p1);
+                }
+                const float2 p = rowgroup_sum(make_float2(p0.x + p1.x, p0.y + p1.y));
+                // the error, written with strength beta: S += k u^T; then o = S^T q
+                const float2 v2 = *reinterpret_cast<const float2*>(s_v + t * kCols + c);
+                const float b = s_b[t];
+                const float2 u = make_float2(b * (v2.x - p.x), b * (v2.y - p.y));
+                load_rows<RPL>(s_q + ro, qr);
+                float2 o0 = make_float2(0.f, 0.f), o1 = o0;
 #pragma unroll
-                        for (int j = 0; j < 4; j++) S[i4 + e][j] *= al[e];
+                for (int i = 0; i < RPL; i += 2) {
+                    S[i] = fma2(make_float2(kr[i], kr[i]), u, S[i]);
+                    S[i + 1] = fma2(make_float2(kr[i + 1], kr[i + 1]), u, S[i + 1]);
+                    o0 = fma2(make_float2(qr[i], qr[i]), S[i], o0);
+                    o1 = fma2(make_float2(qr[i + 1], qr[i + 1]), S[i + 1], o1);
+                }
+                const float2 o = rowgroup_sum(make_float2(o0.x + o1.x, o0.y + o1.y));
+                if (rg == 0) {
+                    const long oi = (bh * L + t0 + t) * (long)dv + col0 + c;
+                    if (OUT_F32)
+                        *reinterpret_cast<float2*>(static_cast<float*>(a.out) + oi) = o;
+                    else
+                        *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + oi) = pack_bf16x2_rn(o.x, o.y);
                 }
             }
-            // prediction p = S^T k for this lane's four columns
-            float kr[RPL];
-#pragma unroll
-            for (int i4 = 0; i4 < RPL; i4 += 4) {
-                const float4 k4 = *reinterpret_cast<const float4*>(kt + i4);
-                kr[i4] = k4.x, kr[i4 + 1] = k4.y, kr[i4 + 2] = k4.z, kr[i4 + 3] = k4.w;
-            }
-            float p[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int i = 0; i < RPL; i++)
-#pragma unroll
-                for (int j = 0; j < 4; j++) p[j] = fmaf(S[i][j], kr[i], p[j]);
-#pragma unroll
-            for (int j = 0; j < 4; j++) p[j] = rowgroup_sum(p[j]);
-            // the error, written with strength beta: S += k u^T
-            const float4 v4 = *reinterpret_cast<const float4*>(s_v + t * kCols + c);
-            const float b = s_b[t];
-            const float u[4] = {b * (v4.x - p[0]), b * (v4.y - p[1]), b * (v4.z - p[2]), b * (v4.w - p[3])};
-            float o[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int i4 = 0; i4 < RPL; i4 += 4) {
-                const float4 q4 = *reinterpret_cast<const float4*>(qt + i4);
-                const float qr[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-                for (int e = 0; e < 4; e++)
-#pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        S[i4 + e][j] = fmaf(kr[i4 + e], u[j], S[i4 + e][j]);
-                        o[j] = fmaf(qr[e], S[i4 + e][j], o[j]);
-                    }
-            }
-#pragma unroll
-            for (int j = 0; j < 4; j++) o[j] = rowgroup_sum(o[j]);
-            if (rg == 0) {
-                const long oi = (bh * L + t0 + t) * (long)dv + col0 + c;
-                if (OUT_F32)
-                    *reinterpret_cast<float4*>(static_cast<float*>(a.out) + oi) = make_float4(o[0], o[1], o[2], o[3]);
-                else
-                    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + oi) =
-                        make_uint2(pack_bf16x2_rn(o[0], o[1]), pack_bf16x2_rn(o[2], o[3]));
-            }
         }
+        if (more) stage(t0 + kTB, sm + ((rnd + 1) & 1) * Ly::BUF);
+        __syncthreads();
     }
     if (active && a.final_state) {  // may alias init_state: each lane read its own entries first
         float* fs = a.final_state + bh * (long)DK * dv + col0 + c;
 #pragma unroll
-        for (int i = 0; i < RPL; i++)
-            *reinterpret_cast<float4*>(fs + (long)(r0 + i) * dv) = make_float4(S[i][0], S[i][1], S[i][2], S[i][3]);
+        for (int i = 0; i < RPL; i++) *reinterpret_cast<float2*>(fs + (long)(r0 + i) * dv) = S[i];
     }
 }
 
@@ -184,7 +252,7 @@ cudaError_t launch_rpl(const DeltaArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((long)a.B * a.H), (unsigned)((a.dv + kCols - 1) / kCols));
-    kern<<<grid, kWarps * 32, smem, s>>>(a);
+    kern<<<grid, kThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -203,9 +271,9 @@ bool delta_supported(int dk, int dv) {
 
 cudaError_t launch_delta(const DeltaArgs& a, cudaStream_t s) {
     if ((long)a.B * a.H == 0 || a.L == 0) return cudaSuccess;
-    if (a.dk == 32) return launch_g<4>(a, s);
-    if (a.dk == 64) return launch_g<8>(a, s);
-    return launch_g<16>(a, s);
+    if (a.dk == 32) return launch_g<2>(a, s);
+    if (a.dk == 64) return launch_g<4>(a, s);
+    return launch_g<8>(a, s);
 }
 
 }  // namespace gla
