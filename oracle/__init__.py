@@ -64,6 +64,8 @@ def _load(plant: int = 0, build_dir: str | None = None):
         lib.oracle_gla_fwd_chunked.restype = ctypes.c_int
         lib.oracle_delta_fwd.argtypes = [D, D, D, D, D, D, D, D, L, L, L, L, ctypes.c_int]
         lib.oracle_delta_fwd.restype = ctypes.c_int
+        lib.oracle_gla_bwd.argtypes = [D, D, D, D, D, D, D, D, D, D, D, D, L, L, L, L, ctypes.c_int]
+        lib.oracle_gla_bwd.restype = ctypes.c_int
         lib.oracle_max_threads.restype = ctypes.c_int
         _LIBS[key] = lib
         return lib
@@ -188,3 +190,37 @@ def delta_fwd(q, k, v, beta, log_alpha=None, init_state=None, nthreads=0, plant=
     if rc != 0:
         raise RuntimeError(f"oracle_delta_fwd failed ({rc})")
     return out.reshape(*lead, L, dv), fs.reshape(*lead, dk, dv)
+
+
+def gla_bwd(q, k, v, dout, log_alpha=None, init_state=None, dfinal=None, nthreads=0, plant=0,
+            build_dir=None):
+    """Reverse mode of the recurrence ("Gated Linear Attention", GLA Recurrent Form).
+    q, k, log_alpha: [..., L, dk]; v, dout: [..., L, dv]; init_state, dfinal: [..., dk, dv].
+
+    Returns (dq, dk, dv, dlog_alpha or None, dinit) as float64 arrays.  Keeps every state:
+    memory L * dk * dv doubles per head.
+    """
+    q = _f64(q)
+    lead = q.shape[:-2]
+    L, dk = q.shape[-2:]
+    dv = np.shape(v)[-1]
+    BH = int(np.prod(lead)) if lead else 1
+    q = q.reshape(BH, L, dk)
+    k = _f64(k).reshape(BH, L, dk)
+    v = _f64(v).reshape(BH, L, dv)
+    do = _f64(dout).reshape(BH, L, dv)
+    la = _f64(log_alpha).reshape(BH, L, dk) if log_alpha is not None else None
+    s0 = _f64(init_state).reshape(BH, dk, dv) if init_state is not None else None
+    df = _f64(dfinal).reshape(BH, dk, dv) if dfinal is not None else None
+    dq = np.empty((BH, L, dk))
+    dkk = np.empty((BH, L, dk))
+    dvv = np.empty((BH, L, dv))
+    dla = np.empty((BH, L, dk)) if la is not None else None
+    dinit = np.empty((BH, dk, dv))
+    rc = _load(plant, build_dir).oracle_gla_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(s0), _ptr(do),
+                                                _ptr(df), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dla),
+                                                _ptr(dinit), BH, L, dk, dv, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gla_bwd failed ({rc})")
+    r = lambda a, *s: None if a is None else a.reshape(*lead, *s)
+    return r(dq, L, dk), r(dkk, L, dk), r(dvv, L, dv), r(dla, L, dk), r(dinit, dk, dv)

@@ -39,6 +39,10 @@
  *    S_n = S_{n-1} + k_n u_n^T, o_n = S_n^T q_n; with a gate the decay
  *    Diag(alpha_n) is applied to S_{n-1} before the prediction.
  *
+ *  - backward: reverse mode through the recurrence with every state kept
+ *    (dL/dS_t = Diag(alpha_{t+1}) dL/dS_{t+1} + q_t dout_t^T), pinned by
+ *    finite differences of the forward oracle.
+ *
  * Planted mistakes: compiling with -DORACLE_PLANT=n (n >= 1) builds a
  * deliberately wrong variant that the pinning tests must reject.  The normal
  * build has ORACLE_PLANT = 0 and none of those branches.
@@ -361,6 +365,102 @@ int oracle_delta_fwd(const double *q, const double *k, const double *v, const do
         free(S);
         free(p);
         free(u);
+    }
+    return err;
+}
+
+/*
+ * Backward of the recurrence [GLA Recurrent Form], reverse mode, for every
+ * (b, h), given dout = dL/do_t and dfinal = dL/dS_{L-1} (may be NULL):
+ *   forward:  S_t = Diag(alpha_t) S_{t-1} + k_t v_t^T  (every S_t kept),
+ *             dq_t = S_t dout_t
+ *   reverse:  H = dfinal (or 0); for t = L-1 .. 0:
+ *               G   = H + q_t dout_t^T              (dL/dS_t, total)
+ *               dk_t = G v_t,  dv_t = G^T k_t
+ *               dlog_alpha_t[i] = alpha_t[i] sum_j G[i][j] S_{t-1}[i][j]
+ *               H   = Diag(alpha_t) G               (dL/dS_{t-1} so far)
+ *             dinit = H.
+ * Layouts as oracle_gla_fwd; dout [BH][L][dv]; dq, dk, dla [BH][L][dk];
+ * dv [BH][L][dv]; dfinal, dinit [BH][dk][dv].  dla and dinit may be NULL.
+ */
+int oracle_gla_bwd(const double *q, const double *k, const double *v, const double *log_alpha,
+                   const double *init_state, const double *dout, const double *dfinal, double *dq,
+                   double *dk_out, double *dv_out, double *dla, double *dinit, long BH, long L, long dk,
+                   long dv, int nthreads) {
+    set_threads(nthreads);
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long h = 0; h < BH; h++) {
+        /* states[t + 1] = S_t, states[0] = S_{-1} */
+        double *states = malloc(sizeof(double) * (size_t)(L + 1) * dk * dv);
+        double *G = malloc(sizeof(double) * dk * dv);
+        double *Hs = malloc(sizeof(double) * dk * dv);
+        if (!states || !G || !Hs) {
+#pragma omp atomic write
+            err = 1;
+            free(states);
+            free(G);
+            free(Hs);
+            continue;
+        }
+        for (long i = 0; i < dk * dv; i++) states[i] = init_state ? init_state[h * dk * dv + i] : 0.0;
+        for (long t = 0; t < L; t++) {
+            const double *Sp = states + (size_t)t * dk * dv;
+            double *S = states + (size_t)(t + 1) * dk * dv;
+            const double *kt = k + (h * L + t) * dk, *vt = v + (h * L + t) * dv;
+            const double *dot = dout + (h * L + t) * dv;
+            for (long i = 0; i < dk; i++) {
+                const double a = log_alpha ? exp(log_alpha[(h * L + t) * dk + i]) : 1.0;
+                for (long j = 0; j < dv; j++) S[i * dv + j] = a * Sp[i * dv + j] + kt[i] * vt[j];
+            }
+            for (long i = 0; i < dk; i++) {
+                double acc = 0.0;
+                for (long j = 0; j < dv; j++) acc += S[i * dv + j] * dot[j];
+                dq[(h * L + t) * dk + i] = acc;
+            }
+        }
+        for (long i = 0; i < dk * dv; i++) Hs[i] = dfinal ? dfinal[h * dk * dv + i] : 0.0;
+        for (long t = L - 1; t >= 0; t--) {
+            const double *Sp = states + (size_t)t * dk * dv;
+            const double *qt = q + (h * L + t) * dk, *kt = k + (h * L + t) * dk, *vt = v + (h * L + t) * dv;
+            const double *dot = dout + (h * L + t) * dv;
+            for (long i = 0; i < dk; i++)
+                for (long j = 0; j < dv; j++) G[i * dv + j] = Hs[i * dv + j] + qt[i] * dot[j];
+            for (long i = 0; i < dk; i++) {
+                double acc = 0.0;
+                for (long j = 0; j < dv; j++) acc += G[i * dv + j] * vt[j];
+                dk_out[(h * L + t) * dk + i] = acc;
+            }
+            for (long j = 0; j < dv; j++) {
+                double acc = 0.0;
+                for (long i = 0; i < dk; i++) acc += G[i * dv + j] * kt[i];
+                dv_out[(h * L + t) * dv + j] = acc;
+            }
+            for (long i = 0; i < dk; i++) {
+                const double a = log_alpha ? exp(log_alpha[(h * L + t) * dk + i]) : 1.0;
+                if (dla) {
+                    double acc = 0.0;
+#if ORACLE_PLANT == 7
+                    /* planted: gate gradient paired with S_t instead of S_{t-1} */
+                    for (long j = 0; j < dv; j++) acc += G[i * dv + j] * Sp[dk * dv + i * dv + j];
+#else
+                    for (long j = 0; j < dv; j++) acc += G[i * dv + j] * Sp[i * dv + j];
+#endif
+                    dla[(h * L + t) * dk + i] = a * acc;
+                }
+#if ORACLE_PLANT == 8
+                /* planted: state gradient carried back without the decay */
+                for (long j = 0; j < dv; j++) Hs[i * dv + j] = G[i * dv + j];
+#else
+                for (long j = 0; j < dv; j++) Hs[i * dv + j] = a * G[i * dv + j];
+#endif
+            }
+        }
+        if (dinit)
+            for (long i = 0; i < dk * dv; i++) dinit[h * dk * dv + i] = Hs[i];
+        free(states);
+        free(G);
+        free(Hs);
     }
     return err;
 }

@@ -18,7 +18,7 @@ from test_oracle_pins import _close, _golden, _inputs, _phi, quadratic_masked
 @pytest.fixture(scope="module")
 def plant_dir(tmp_path_factory):
     d = str(tmp_path_factory.mktemp("plants"))
-    for n in (1, 2, 3, 4, 5, 6):
+    for n in (1, 2, 3, 4, 5, 6, 7, 8):
         oracle.build(plant=n, build_dir=d)
     return d
 
@@ -81,3 +81,22 @@ def test_plant6_delta_output_before_write_is_caught(plant_dir):
     o, _ = oracle.delta_fwd(*(np.array(g[n], float)[None] for n in ("q", "k", "v", "beta")),
                             plant=6, build_dir=plant_dir)
     assert not dclose(o[0], g["expect_out"], 1e-14)
+
+
+def _bwd_vs_fd(plant, d):
+    from test_oracle_bwd_pins import _fd, _inputs as binputs, _loss
+    q, k, v, la, s0, Wo, Wf = binputs(5, L=6, dk=3, dv=2)
+    got = oracle.gla_bwd(q, k, v, Wo, la, s0, Wf, plant=plant, build_dir=d)
+    f = lambda: _loss(q, k, v, la, s0, Wo, Wf)
+    refs = (_fd(f, q), _fd(f, k), _fd(f, v), _fd(f, la), _fd(f, s0))
+    return [float(np.max(np.abs(g - r))) for g, r in zip(got, refs)]
+
+
+def test_plant7_gate_gradient_with_wrong_state_is_caught(plant_dir):
+    err = _bwd_vs_fd(7, plant_dir)
+    assert err[3] > 1e-3, err
+
+
+def test_plant8_undecayed_state_gradient_is_caught(plant_dir):
+    err = _bwd_vs_fd(8, plant_dir)
+    assert max(err[1], err[2], err[4]) > 1e-3, err
