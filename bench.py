@@ -65,6 +65,13 @@ def delta_flops(w) -> float:
     return float(w.B * w.H * w.L * (6 + (1 if w.gate else 0)) * w.dk * w.dv)
 
 
+def bwd_flops(w) -> float:
+    """Backward per token and state element: S_t = alpha S + k v^T (3 flops with the gate, 2
+    without) and dq = S dout (2); G_t += q dout^T (2), dk = G v (2), dv = G^T k (2), and the
+    decay of G in both reverse sweeps (1 each, with the gate)."""
+    return float(w.B * w.H * w.L * (15 if w.gate else 12) * w.dk * w.dv)
+
+
 def fp32_alu_peak_tflops(peaks) -> float:
     """FP32 FMA peak from unit counts: SMs x 128 FP32 lanes x 2 flops x max SM clock."""
     import torch
@@ -95,6 +102,7 @@ KERNEL_SOURCES = {
     "gla_prefill_short_kernel": ("gla_short.cu",),
     "gla_prefill_tc_kernel_scalar_gate": ("gla_tc.cu", "gla_ptx.cuh"),
     "gla_delta_kernel": ("gla_delta.cu",),
+    "gla_bwd_kernel": ("gla_bwd.cu",),
 }
 
 
@@ -483,6 +491,42 @@ def bench_delta(args, device, rank):
     return dict(w=w, ms=statistics.mean(a.elapsed_time(e) for a, e in evs), calls=args.delta_calls)
 
 
+def bench_bwd(args, device, rank):
+    """The backward pass (gla_bwd) on its workload: B8 H16 L4096 dk = dv = 128, bf16, gated;
+    all of dq, dk, dv and dlog_alpha."""
+    import torch
+
+    import causal_gated_linear_gb300 as gla
+    w = synth.with_shape(synth.BWD, seed=synth.BWD.seed + 1000 * rank)
+    x = synth.make_bwd(w)
+    q, k, v, do = (to_dev(x[n], device) for n in ("q", "k", "v", "dout"))
+    la = to_dev(x["log_alpha"], device)
+    f32 = lambda *s: torch.empty(s, dtype=torch.float32, device=device)
+    dq, dk, dv, dla = f32(w.B, w.H, w.L, w.dk), f32(w.B, w.H, w.L, w.dk), f32(w.B, w.H, w.L, w.dv), \
+        f32(w.B, w.H, w.L, w.dk)
+    stream = torch.cuda.current_stream(device)
+
+    def call():
+        r = gla.gla_bwd(q, k, v, do, dq, dk, dv, w.B, w.H, w.L, w.dk, w.dv, log_alpha=la, dlog_alpha=dla,
+                        stream=stream)
+        if r != 0:
+            raise RuntimeError(gla.gla_status_string(r))
+
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize(device)
+    evs = []
+    for _ in range(args.bwd_calls):
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        e.record(stream)
+        evs.append((a, e))
+    torch.cuda.synchronize(device)
+    gla.check(gla.gla_device_error(stream))
+    return dict(w=w, ms=statistics.mean(a.elapsed_time(e) for a, e in evs), calls=args.bwd_calls)
+
+
 def run_gla(args):
     import torch
     rank, world, local = dist_env()
@@ -499,6 +543,7 @@ def run_gla(args):
     dec = bench_decode(args, device, rank) if args.decode_steps > 0 else None
     mdec = bench_decode_multi(args, device, rank) if args.multi_calls > 0 else None
     dlt = bench_delta(args, device, rank) if args.delta_calls > 0 else None
+    bwd = bench_bwd(args, device, rank) if args.bwd_calls > 0 else None
 
     ms = pre["total_ms"] / args.steps
     tokens = w.B * w.L
@@ -559,6 +604,18 @@ def run_gla(args):
                          "traffic": recorded_traffic("gla_delta_kernel"), "kernel": "gla_delta_kernel",
                          "alg_flops_per_launch": dfl,
                          "peak_source": "FP32 FMA: SMs x 128 lanes x 2 flops x max SM clock"}}
+    if bwd is not None:
+        bw = bwd["w"]
+        bfl = bwd_flops(bw)
+        btf = bfl / (bwd["ms"] / 1e3) / 1e12
+        apk = fp32_alu_peak_tflops(peaks)
+        line["backward"] = {
+            "workload": bw.name, "ms_per_launch": bwd["ms"], "calls": bwd["calls"],
+            "tokens_per_s": bw.B * bw.L / (bwd["ms"] / 1e3),
+            "roofline": {"bound": "alu", "achieved": btf, "peak": apk, "unit": "TFLOP/s", "frac": btf / apk,
+                         "traffic": recorded_traffic("gla_bwd_kernel"), "kernel": "gla_bwd_kernel",
+                         "alg_flops_per_launch": bfl,
+                         "peak_source": "FP32 FMA: SMs x 128 lanes x 2 flops x max SM clock"}}
     if mdec is not None:
         mw = mdec["w"]
         mbytes = decode_multi_bytes(mw)
@@ -599,6 +656,8 @@ def main():
     ap.add_argument("--decode-pool", type=int, default=8)
     ap.add_argument("--delta-calls", type=int, default=3,
                     help="timed launches of the delta-rule workload (0: skip)")
+    ap.add_argument("--bwd-calls", type=int, default=3,
+                    help="timed launches of the backward workload (0: skip)")
     ap.add_argument("--scalar-calls", type=int, default=5,
                     help="timed launches of the long-context workload with one gate per token (0: skip)")
     ap.add_argument("--multi-calls", type=int, default=64,

@@ -15,6 +15,8 @@ The functions mirror the C entry points:
     gla_decode_step(q, k, v, log_alpha, state, out, B, H, dk, dv, stream=None)
     gla_delta_fwd(q, k, v, beta, out, B, H, L, dk, dv, log_alpha=None, init_state=None,
                   final_state=None, out_dtype=BF16, stream=None) -> int
+    gla_bwd(q, k, v, dout, dq, dk, dv, B, H, L, dk_dim, dv_dim, log_alpha=None, init_state=None,
+            dfinal=None, dlog_alpha=None, dinit=None, in_dtype=BF16, stream=None) -> int
     gla_device_error(stream=None) -> int
     gla_status_string(status) -> str
     gla_version() -> str
@@ -34,7 +36,7 @@ GLA_OK, GLA_ERR_INVALID, GLA_ERR_UNSUPPORTED, GLA_ERR_MISALIGNED, GLA_ERR_CUDA, 
 BF16, F32 = 0, 1
 FLAG_FEATURE_ELU1, FLAG_NORMALIZE, FLAG_FORCE_SIMT, FLAG_FORCE_CHUNK, FLAG_SCALAR_GATE = 1, 2, 4, 8, 16
 
-EXPORTED = ["gla_fwd", "gla_fwd_ex", "gla_decode_step", "gla_delta_fwd", "gla_device_error",
+EXPORTED = ["gla_fwd", "gla_fwd_ex", "gla_decode_step", "gla_delta_fwd", "gla_bwd", "gla_device_error",
             "gla_device_error_detail", "gla_status_string", "gla_version"]
 
 
@@ -77,6 +79,8 @@ def load(path: str | None = None):
     lib.gla_decode_step.restype = i
     lib.gla_delta_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
     lib.gla_delta_fwd.restype = i
+    lib.gla_bwd.argtypes = [vp] * 12 + [i] * 6 + [vp]
+    lib.gla_bwd.restype = i
     lib.gla_device_error.argtypes = [vp]
     lib.gla_device_error.restype = i
     lib.gla_device_error_detail.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
@@ -145,6 +149,13 @@ def gla_delta_fwd(q, k, v, beta, out, B, H, L, dk, dv, log_alpha=None, init_stat
                   out_dtype=BF16, stream=None) -> int:
     return load().gla_delta_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(log_alpha), _ptr(init_state),
                                 _ptr(out), _ptr(final_state), B, H, L, dk, dv, out_dtype, _stream(stream))
+
+
+def gla_bwd(q, k, v, dout, dq, dk, dv, B, H, L, dk_dim, dv_dim, log_alpha=None, init_state=None, dfinal=None,
+            dlog_alpha=None, dinit=None, in_dtype=BF16, stream=None) -> int:
+    return load().gla_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(init_state), _ptr(dout), _ptr(dfinal),
+                          _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dlog_alpha), _ptr(dinit), B, H, L, dk_dim, dv_dim,
+                          in_dtype, _stream(stream))
 
 
 def gla_device_error(stream=None) -> int:

@@ -253,6 +253,60 @@ int gla_delta_fwd(const void* q, const void* k, const void* v, const float* beta
     return finish(launch_delta(a, s), s);
 }
 
+int gla_bwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* init_state,
+            const void* dout, const float* dfinal, float* dq, float* dk_out, float* dv_out, float* dlog_alpha,
+            float* dinit, int B, int H, int L, int dk, int dv, int in_dtype, void* stream) {
+    if (B < 1 || H < 1 || L < 0 || dk < 1 || dv < 1) return GLA_ERR_INVALID;
+    if (in_dtype != GLA_DTYPE_BF16 && in_dtype != GLA_DTYPE_F32) return GLA_ERR_INVALID;
+    if (L > 0 && (!q || !k || !v || !dout || !dq || !dk_out || !dv_out)) return GLA_ERR_INVALID;
+    if (dlog_alpha && !log_alpha) return GLA_ERR_INVALID;
+    if (!bwd_supported(dk, dv)) return GLA_ERR_UNSUPPORTED;
+    if ((size_t)B * H > 0x7fffffffu) return GLA_ERR_UNSUPPORTED;
+    const void* ptrs[] = {q, k, v, log_alpha, init_state, dout, dfinal, dq, dk_out, dv_out, dlog_alpha, dinit};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return GLA_ERR_MISALIGNED;
+    const size_t BH = (size_t)B * H, Ls = (size_t)L, es = in_dtype == GLA_DTYPE_F32 ? 4 : 2;
+    const size_t nk = BH * Ls * dk, nv = BH * Ls * dv, ns = BH * dk * dv * 4;
+    const void* in_p[] = {q, k, v, dout, log_alpha, init_state, dfinal};
+    const size_t in_n[] = {nk * es, nk * es, nv * es, nv * es, nk * 4, ns, ns};
+    const void* out_p[] = {dq, dk_out, dv_out, dlog_alpha, dinit};
+    const size_t out_n[] = {nk * 4, nk * 4, nv * 4, nk * 4, ns};
+    for (int o = 0; o < 5; o++) {
+        for (int i = 0; i < 7; i++)
+            if (overlaps(out_p[o], out_n[o], in_p[i], in_n[i])) return GLA_ERR_INVALID;
+        for (int p = 0; p < o; p++)
+            if (overlaps(out_p[o], out_n[o], out_p[p], out_n[p])) return GLA_ERR_INVALID;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (L == 0) {
+        cudaError_t e = cudaSuccess;
+        if (dinit)
+            e = dfinal ? cudaMemcpyAsync(dinit, dfinal, ns, cudaMemcpyDeviceToDevice, s)
+                       : cudaMemsetAsync(dinit, 0, ns, s);
+        return finish(e, s);
+    }
+    BwdArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.dout = dout;
+    a.log_alpha = log_alpha;
+    a.init_state = init_state;
+    a.dfinal = dfinal;
+    a.dq = dq;
+    a.dk_out = dk_out;
+    a.dv_out = dv_out;
+    a.dlog_alpha = dlog_alpha;
+    a.dinit = dinit;
+    a.B = B;
+    a.H = H;
+    a.L = L;
+    a.dk = dk;
+    a.dv = dv;
+    a.in_dtype = in_dtype;
+    return finish(launch_bwd(a, s), s);
+}
+
 int gla_device_error(void* stream) { return read_and_clear_error(static_cast<cudaStream_t>(stream)); }
 
 int gla_device_error_detail(void* stream, unsigned* detail4) {

@@ -67,6 +67,28 @@ struct DeltaArgs {
 bool delta_supported(int dk, int dv);
 cudaError_t launch_delta(const DeltaArgs& a, cudaStream_t s);
 
+struct BwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* dout;
+    const float* log_alpha;
+    const float* init_state;
+    const float* dfinal;
+    float* dq;
+    float* dk_out;
+    float* dv_out;
+    float* dlog_alpha;
+    float* dinit;
+    int B, H, L, dk, dv;
+    int in_dtype;
+};
+
+// Gradients of the recurrence (row CTAs: dq, dk, dlog_alpha, dS_init;
+// column CTAs: dv), one launch.
+bool bwd_supported(int dk, int dv);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s);
+
 // Memory-bound decode step.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 

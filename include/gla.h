@@ -154,6 +154,37 @@ int gla_delta_fwd(const void* q, const void* k, const void* v, const float* beta
                   int out_dtype, void* stream);
 
 /*
+ * gla_bwd -- gradients of the recurrence ("Gated Linear Attention", GLA
+ * Recurrent Form: S_t = Diag(alpha_t) S_{t-1} + k_t v_t^T, o_t = S_t^T q_t)
+ * for a loss L with dout = dL/do_t and dfinal = dL/dS_{L-1}.  With
+ * G_t = dL/dS_t = Diag(alpha_{t+1}) G_{t+1} + q_t dout_t^T:
+ *   dq_t = S_t dout_t,  dk_t = G_t v_t,  dv_t = G_t^T k_t,
+ *   dinit = Diag(alpha_0) G_0,
+ *   dlog_alpha_t = sum_{s >= t} (q_s * dq_s - k_s * dk_s) + rowsum(dfinal * S_{L-1})
+ *     (the gate enters only through its cumulative sums, so this equals
+ *      alpha_t * rowsum(G_t * S_{t-1})).
+ *
+ *   q, k        [B][H][L][dk], bf16 or fp32 (in_dtype)
+ *   v, dout     [B][H][L][dv], in_dtype
+ *   log_alpha   fp32 [B][H][L][dk], or NULL for no gate
+ *   init_state  fp32 [B][H][dk][dv], or NULL for S_{-1} = 0
+ *   dfinal      fp32 [B][H][dk][dv], or NULL for dL/dS_{L-1} = 0
+ *   dq, dk_out  fp32 [B][H][L][dk]      (written)
+ *   dv_out      fp32 [B][H][L][dv]      (written)
+ *   dlog_alpha  fp32 [B][H][L][dk], or NULL (needs log_alpha)
+ *   dinit       fp32 [B][H][dk][dv], or NULL
+ * All caller-owned device memory, 16-byte aligned; outputs must not overlap
+ * inputs or each other.  The recurrence runs token by token in fp32 (one
+ * launch: row blocks sweep forward for dq, then backward for dk, dlog_alpha
+ * and dinit; column blocks sweep backward for dv).  Supported: dk, dv in
+ * {32, 64, 128}.  Validation failures return before any launch; L = 0 only
+ * writes dinit (= dfinal, or zero).
+ */
+int gla_bwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* init_state,
+            const void* dout, const float* dfinal, float* dq, float* dk_out, float* dv_out, float* dlog_alpha,
+            float* dinit, int B, int H, int L, int dk, int dv, int in_dtype, void* stream);
+
+/*
  * gla_device_error -- synchronise `stream`, read and clear the device error
  * word that bounded waits set.  Returns GLA_OK, GLA_ERR_TIMEOUT or GLA_ERR_CUDA.
  */

@@ -32,7 +32,7 @@ _MIX1 = np.uint64(0xBF58476D1CE4E5B9)
 _MIX2 = np.uint64(0x94D049BB133111EB)
 
 # tensor ids (the "tensor" part of the counter key)
-T_Q, T_K, T_V, T_G, T_S0, T_BETA = 1, 2, 3, 4, 5, 6
+T_Q, T_K, T_V, T_G, T_S0, T_BETA, T_DOUT, T_DFIN = 1, 2, 3, 4, 5, 6, 7, 8
 
 BASE_SEED = 20261202
 
@@ -264,6 +264,31 @@ def make_delta(w: Workload, heads=None):
     g = np.concatenate([p.reshape(-1) for p in bparts])
     lead = (len(sel),) if heads is not None else (B, H)
     x["beta"] = to_f32(1.0 / (1.0 + np.exp(-g))).reshape(lead + (L,))
+    return x
+
+
+# backward workload: the config-2 prefill (B8 H16 L4096 dk = dv = 128, bf16, its gate
+# and q/k scale) with an output gradient dout ~ N(0, 1) per element
+BWD = Workload("gla_bwd_B8H16L4096d128", 8, 16, 4096, 128, 128, seed=BASE_SEED + 7)
+
+
+def make_bwd(w: Workload, heads=None, dfinal_std=0.0):
+    """Inputs of a backward workload: make_prefill's, plus dout (bf16 bits or float32, like v)
+    and dfinal (float32 [.., dk, dv] ~ N(0, dfinal_std), or None when dfinal_std == 0)."""
+    x = make_prefill(w, heads)
+    B, H, L, dk, dv = w.B, w.H, w.L, w.dk, w.dv
+    sel = list(range(B * H)) if heads is None else list(heads)
+    lead = (len(sel),) if heads is not None else (B, H)
+    parts = [normals(w.seed, T_DOUT, (L * dv,), start=hh * L * dv) for hh in sel] if heads is not None \
+        else [normals(w.seed, T_DOUT, (B * H * L * dv,))]
+    d = np.concatenate([p.reshape(-1) for p in parts])
+    x["dout"] = (to_bf16_bits(d) if w.dtype == "bf16" else to_f32(d)).reshape(lead + (L, dv))
+    x["dfinal"] = None
+    if dfinal_std > 0:
+        per = dk * dv
+        parts = [normals(w.seed, T_DFIN, (per,), start=hh * per, std=dfinal_std) for hh in sel] \
+            if heads is not None else [normals(w.seed, T_DFIN, (B * H * per,), std=dfinal_std)]
+        x["dfinal"] = to_f32(np.concatenate([p.reshape(-1) for p in parts])).reshape(lead + (dk, dv))
     return x
 
 
