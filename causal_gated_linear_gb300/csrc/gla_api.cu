@@ -261,7 +261,7 @@ int gla_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
     if (L > 0 && (!q || !k || !v || !dout || !dq || !dk_out || !dv_out)) return GLA_ERR_INVALID;
     if (dlog_alpha && !log_alpha) return GLA_ERR_INVALID;
     if (!bwd_supported(dk, dv)) return GLA_ERR_UNSUPPORTED;
-    if ((size_t)B * H > 0x7fffffffu) return GLA_ERR_UNSUPPORTED;
+    if ((size_t)B * H * (bwd_blocks(dk) + bwd_blocks(dv)) > 0x7fffffffu) return GLA_ERR_UNSUPPORTED;
     const void* ptrs[] = {q, k, v, log_alpha, init_state, dout, dfinal, dq, dk_out, dv_out, dlog_alpha, dinit};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return GLA_ERR_MISALIGNED;

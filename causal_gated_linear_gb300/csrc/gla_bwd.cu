@@ -19,14 +19,19 @@
 //    their own (S_t[i,:] needs alpha_t[i], k_t[i] and v_t), so a forward sweep
 //    carries S and emits dq (a reduction over the value columns), and a
 //    reverse sweep carries G and emits dk, the running gate sum and dS_{-1}.
-//    Lane (cg, rp) of a warp holds rows warp*4 + 2 rp + {0, 1} as fp32 pairs
-//    over the value columns [cg * CPL, (cg + 1) * CPL).
+//    Lane (cg, rp) of a warp holds rows warp*4 + 2 rp + {0, 1} over the value
+//    columns [cg * CPL, (cg + 1) * CPL), as fp32 pairs of adjacent columns.
 //  * column CTAs own 64 value columns: a reverse sweep carries G column-wise
 //    and emits dv (a reduction over the key rows).  Lane (rg, cp) holds rows
-//    [rg * RPL, (rg + 1) * RPL) of the column pair 2 cp.
-// Reductions are four butterfly shuffles across the sixteen lane groups.
-// Tokens are staged in shared memory 16 at a time, double buffered.  Row CTAs
-// come first in the grid: they do two sweeps, the column CTAs one.
+//    [rg * RPL, (rg + 1) * RPL) of the columns 2 cp + {0, 1}, as fp32 pairs of
+//    adjacent rows.
+// Pairs run along the vectors read from shared memory per token, so they feed
+// the packed fp32 instructions as loaded.  The reductions are output-only (they
+// do not feed the recurrence), so a round of 8 tokens keeps its 16 partial sums
+// per lane and reduce-scatters them across the sixteen lane groups at the end
+// of the round.  Tokens are staged in shared memory a round at a time, double
+// buffered.  Row CTAs come first in the grid: they do two sweeps, the column
+// CTAs one.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -40,8 +45,8 @@ namespace {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kTB = 16;            // tokens staged per round
-constexpr int kBlock = 4 * kWarps; // rows per row CTA, columns per column CTA
+constexpr int kTB = 8;              // tokens staged per round (one batch of reductions)
+constexpr int kBlock = 4 * kWarps;  // rows per row CTA, columns per column CTA
 
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     float2 d;
@@ -63,7 +68,7 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
 
 __device__ __forceinline__ float2 dup(float x) { return make_float2(x, x); }
 
-// sum over the sixteen lane groups (lane bits 1..4)
+// sum over the sixteen lane groups (lane bits 1..4), every lane gets the total
 __device__ __forceinline__ float2 group_sum(float2 x) {
 #pragma unroll
     for (int m = 2; m <= 16; m <<= 1) {
@@ -71,6 +76,45 @@ __device__ __forceinline__ float2 group_sum(float2 x) {
         x.y += __shfl_xor_sync(0xffffffffu, x.y, m);
     }
     return x;
+}
+
+// Reduce-scatter over the sixteen lane groups: v[e] (e = 2 tb + w, 16 partial
+// sums per lane) summed across lane bits 1..4; lane group g = lane >> 1 ends
+// with the total of entry e = g.  Four halving exchanges: 15 shuffles for 16
+// sums instead of 64.
+__device__ __forceinline__ float reduce_scatter16(const float2 (&acc)[kTB], int lane) {
+    float v8[8];
+    {
+        const bool up = lane & 16;
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const float lo = i & 1 ? acc[i >> 1].y : acc[i >> 1].x;
+            const float hi = i & 1 ? acc[4 + (i >> 1)].y : acc[4 + (i >> 1)].x;
+            const float send = up ? lo : hi, mine = up ? hi : lo;
+            v8[i] = mine + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+    }
+    float v4[4];
+    {
+        const bool up = lane & 8;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const float send = up ? v8[i] : v8[4 + i], mine = up ? v8[4 + i] : v8[i];
+            v4[i] = mine + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+    }
+    float v2[2];
+    {
+        const bool up = lane & 4;
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            const float send = up ? v4[i] : v4[2 + i], mine = up ? v4[2 + i] : v4[i];
+            v2[i] = mine + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+    }
+    const bool up = lane & 2;
+    const float send = up ? v2[0] : v2[1], mine = up ? v2[1] : v2[0];
+    return mine + __shfl_xor_sync(0xffffffffu, send, 2);
 }
 
 template <typename T>
@@ -81,27 +125,24 @@ __device__ __forceinline__ float to_f(T x) {
         return __bfloat162float(x);
 }
 
-// N consecutive floats of a staged group (16-byte aligned when N >= 4)
+// N consecutive floats of a staged group as N / 2 pairs (16-byte aligned when N >= 4)
 template <int N>
-__device__ __forceinline__ void load_run(const float* p, float (&r)[N]) {
+__device__ __forceinline__ void load_pairs(const float* p, float2 (&r)[N / 2]) {
     if constexpr (N >= 4) {
 #pragma unroll
         for (int i = 0; i < N; i += 4) {
             const float4 x = *reinterpret_cast<const float4*>(p + i);
-            r[i] = x.x, r[i + 1] = x.y, r[i + 2] = x.z, r[i + 3] = x.w;
+            r[i / 2] = make_float2(x.x, x.y);
+            r[i / 2 + 1] = make_float2(x.z, x.w);
         }
     } else {
-#pragma unroll
-        for (int i = 0; i < N; i += 2) {
-            const float2 x = *reinterpret_cast<const float2*>(p + i);
-            r[i] = x.x, r[i + 1] = x.y;
-        }
+        r[0] = *reinterpret_cast<const float2*>(p);
     }
 }
 
 // Staging of one round of tokens.  "Wide" arrays span the full dimension that
 // the CTA's lanes split in sixteen groups of W floats (padded to W + 4 per
-// group); "narrow" arrays span only the CTA's own 64-entry block.
+// group); "narrow" arrays span only the CTA's own kBlock entries.
 template <int W>
 struct Stage {
     static constexpr int FULL = 16 * W;
@@ -112,22 +153,31 @@ struct Stage {
     static constexpr int NN = (kTB * kBlock + kThreads - 1) / kThreads;  // narrow loads per thread
 };
 
+// rounds of the reverse sweeps: the last kTB tokens first; returns the count, sets t0
+__device__ __forceinline__ int rev_span(int L, int rr, int& t0) {
+    const int hi = L - rr * kTB;
+    t0 = max(0, hi - kTB);
+    return hi - t0;
+}
+
 // ---- row CTAs: dq (forward sweep); dk, dlog_alpha, dS_{-1} (reverse sweep) ----
 // Wide arrays are over the value columns (W = CPL): v, dout.  Narrow arrays over
-// the CTA's 64 key rows: k, alpha, and q, dq in the reverse sweep.
+// the CTA's key rows: k, alpha, and q, dq in the reverse sweep.  A lane's state
+// is S[w][p] = (S[r + w][c_{2p}], S[r + w][c_{2p+1}]), w = 0, 1, c_j = cg CPL + j.
 template <int CPL, bool GATE, typename T>
-__device__ __forceinline__ void rows_body(const BwdArgs& a, float* sm, int blk) {
+__device__ __forceinline__ void rows_body(const BwdArgs& a, float* sm, long bh, int blk) {
     using St = Stage<CPL>;
-    constexpr int DV = St::FULL;
+    constexpr int DV = St::FULL, NP = CPL / 2;
     constexpr int BUF = kTB * (2 * St::ROW + 4 * kBlock);
     const int L = a.L, dk = a.dk;
-    const long bh = blockIdx.x;
     const int row0 = blk * kBlock, nrows = min(kBlock, dk - row0);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cg = lane >> 1, rp = lane & 1;
-    const int rl = warp * 4 + rp * 2;  // this lane's first row within the block
+    const int rl = warp * 4 + rp * 2;      // this lane's first row within the block
     const bool active = warp * 4 < nrows;  // dk is a multiple of 4: a warp is all or nothing
     const int r = row0 + rl;
+    // after a reduce-scatter this lane holds token tb_l of row rl + w_l
+    const int tb_l = cg >> 1, w_l = cg & 1;
 
     const T* q = static_cast<const T*>(a.q) + bh * (long)L * dk;
     const T* k = static_cast<const T*>(a.k) + bh * (long)L * dk;
@@ -138,7 +188,7 @@ __device__ __forceinline__ void rows_body(const BwdArgs& a, float* sm, int blk) 
 
     T rv[St::NW], rd[St::NW], rk[St::NN], rq[St::NN];
     float ra[St::NN], rdq[St::NN];
-    // round [t0, t0 + n): global -> registers; REV also fetches q and dq
+    // round [t0, t0 + n): global -> registers; rev also fetches q and dq
     auto fetch = [&](int t0, int n, bool rev) {
 #pragma unroll
         for (int m = 0; m < St::NW; m++) {
@@ -194,17 +244,16 @@ __device__ __forceinline__ void rows_body(const BwdArgs& a, float* sm, int blk) 
         }
     };
 
-    float2 S[CPL];  // S[j] = (S[r][c_j], S[r + 1][c_j]), c_j = cg * CPL + j
+    float2 S[2][NP];
     if (active && a.init_state) {
         const float* s0 = a.init_state + (bh * dk + r) * (long)DV + cg * CPL;
-        float x0[CPL], x1[CPL];
-        load_run<CPL>(s0, x0);
-        load_run<CPL>(s0 + DV, x1);
-#pragma unroll
-        for (int j = 0; j < CPL; j++) S[j] = make_float2(x0[j], x1[j]);
+        load_pairs<CPL>(s0, S[0]);
+        load_pairs<CPL>(s0 + DV, S[1]);
     } else {
 #pragma unroll
-        for (int j = 0; j < CPL; j++) S[j] = make_float2(0.f, 0.f);
+        for (int w = 0; w < 2; w++)
+#pragma unroll
+            for (int p = 0; p < NP; p++) S[w][p] = make_float2(0.f, 0.f);
     }
 
     // forward sweep: S_t and dq_t = S_t dout_t
@@ -223,77 +272,83 @@ __device__ __forceinline__ void rows_body(const BwdArgs& a, float* sm, int blk) 
             const float* s_k = s_d + kTB * St::ROW;
             const float* s_a = s_k + kTB * kBlock;
             if (active) {
-                for (int t = 0; t < n; t++) {
-                    float vr[CPL], dr[CPL];
-                    load_run<CPL>(s_v + t * St::ROW + cg * St::STRIDE, vr);
-                    load_run<CPL>(s_d + t * St::ROW + cg * St::STRIDE, dr);
-                    const float2 k2 = *reinterpret_cast<const float2*>(s_k + t * kBlock + rl);
-                    float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
-                    if (GATE) {
+                float2 acc[kTB];
+#pragma unroll
+                for (int t = 0; t < kTB; t++) {
+                    acc[t] = make_float2(0.f, 0.f);
+                    if (t < n) {
+                        float2 vp[NP], dp[NP];
+                        load_pairs<CPL>(s_v + t * St::ROW + cg * St::STRIDE, vp);
+                        load_pairs<CPL>(s_d + t * St::ROW + cg * St::STRIDE, dp);
+                        const float2 k2 = *reinterpret_cast<const float2*>(s_k + t * kBlock + rl);
                         const float2 a2 = *reinterpret_cast<const float2*>(s_a + t * kBlock + rl);
+                        float2 pr[2];
 #pragma unroll
-                        for (int j = 0; j < CPL; j++) S[j] = fma2(a2, S[j], mul2(k2, dup(vr[j])));
-                    } else {
+                        for (int w = 0; w < 2; w++) {
+                            const float2 kd = dup(w ? k2.y : k2.x), ad = dup(w ? a2.y : a2.x);
+                            pr[w] = make_float2(0.f, 0.f);
 #pragma unroll
-                        for (int j = 0; j < CPL; j++) S[j] = fma2(k2, dup(vr[j]), S[j]);
+                            for (int p = 0; p < NP; p++) {
+                                S[w][p] = GATE ? fma2(ad, S[w][p], mul2(kd, vp[p])) : fma2(kd, vp[p], S[w][p]);
+                                pr[w] = fma2(S[w][p], dp[p], pr[w]);
+                            }
+                        }
+                        acc[t] = make_float2(pr[0].x + pr[0].y, pr[1].x + pr[1].y);
                     }
-#pragma unroll
-                    for (int j = 0; j < CPL; j += 2) {
-                        acc0 = fma2(S[j], dup(dr[j]), acc0);
-                        acc1 = fma2(S[j + 1], dup(dr[j + 1]), acc1);
-                    }
-                    const float2 d = group_sum(make_float2(acc0.x + acc1.x, acc0.y + acc1.y));
-                    if (cg == 0) *reinterpret_cast<float2*>(dq + (long)(t0 + t) * dk + r) = d;
                 }
+                const float x = reduce_scatter16(acc, lane);
+                if (tb_l < n) dq[(long)(t0 + tb_l) * dk + r + w_l] = x;
             }
             if (nn > 0) stage(nn, false, sm + ((rnd + 1) & 1) * BUF);
             __syncthreads();
         }
     }
 
-    // the boundary term of the gate gradient: rowsum(dfinal * S_{L-1})
-    float2 gsum = make_float2(0.f, 0.f);
+    // the boundary term of the gate gradient, rowsum(dfinal * S_{L-1}), for row rl + w_l
+    float carry = 0.f;
     if (active) {
         const float* df = a.dfinal ? a.dfinal + (bh * dk + r) * (long)DV + cg * CPL : nullptr;
-        float x0[CPL], x1[CPL];
+        float2 F[2][NP];
         if (df) {
-            load_run<CPL>(df, x0);
-            load_run<CPL>(df + DV, x1);
+            load_pairs<CPL>(df, F[0]);
+            load_pairs<CPL>(df + DV, F[1]);
         } else {
 #pragma unroll
-            for (int j = 0; j < CPL; j++) x0[j] = 0.f, x1[j] = 0.f;
+            for (int w = 0; w < 2; w++)
+#pragma unroll
+                for (int p = 0; p < NP; p++) F[w][p] = make_float2(0.f, 0.f);
         }
         if (GATE && df) {
-            float2 c = make_float2(0.f, 0.f);
+            float2 c[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int j = 0; j < CPL; j++) c = fma2(S[j], make_float2(x0[j], x1[j]), c);
-            gsum = group_sum(c);
+            for (int w = 0; w < 2; w++)
+#pragma unroll
+                for (int p = 0; p < NP; p++) c[w] = fma2(S[w][p], F[w][p], c[w]);
+            const float2 cs = group_sum(make_float2(c[0].x + c[0].y, c[1].x + c[1].y));
+            carry = w_l ? cs.y : cs.x;
         }
         // from here S holds G, the gradient reaching the state (dfinal at t = L - 1)
 #pragma unroll
-        for (int j = 0; j < CPL; j++) S[j] = make_float2(x0[j], x1[j]);
+        for (int w = 0; w < 2; w++)
+#pragma unroll
+            for (int p = 0; p < NP; p++) S[w][p] = F[w][p];
     }
 
-    // reverse sweep: G_t, dk_t = G_t v_t, dlog_alpha_t, then G <- Diag(alpha_t) G
+    // reverse sweep: G_t = G + q_t dout_t^T, dk_t = G_t v_t, the gate gradient, G <- Diag(alpha_t) G_t
     float* dkp = a.dk_out + bh * (long)L * dk;
     float* dla = GATE && a.dlog_alpha ? a.dlog_alpha + bh * (long)L * dk : nullptr;
     {
-        const int nr = (L + kTB - 1) / kTB;  // rounds, the last one first
-        auto span = [&](int rr, int& t0) {
-            const int hi = L - rr * kTB;
-            t0 = max(0, hi - kTB);
-            return hi - t0;
-        };
+        const int nr = (L + kTB - 1) / kTB;
         int t0;
-        int n = span(0, t0);
+        int n = rev_span(L, 0, t0);
         fetch(t0, n, true);
         stage(n, true, sm);
         __syncthreads();
         for (int rr = 0; rr < nr; rr++) {
-            n = span(rr, t0);
+            n = rev_span(L, rr, t0);
             int tn = 0, nn = 0;
             if (rr + 1 < nr) {
-                nn = span(rr + 1, tn);
+                nn = rev_span(L, rr + 1, tn);
                 fetch(tn, nn, true);
             }
             const float* buf = sm + (rr & 1) * BUF;
@@ -304,33 +359,47 @@ __device__ __forceinline__ void rows_body(const BwdArgs& a, float* sm, int blk) 
             const float* s_q = s_a + kTB * kBlock;
             const float* s_dq = s_q + kTB * kBlock;
             if (active) {
-                for (int t = n - 1; t >= 0; t--) {
-                    float vr[CPL], dr[CPL];
-                    load_run<CPL>(s_v + t * St::ROW + cg * St::STRIDE, vr);
-                    load_run<CPL>(s_d + t * St::ROW + cg * St::STRIDE, dr);
-                    const float2 q2 = *reinterpret_cast<const float2*>(s_q + t * kBlock + rl);
-                    float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
+                float2 acc[kTB];
 #pragma unroll
-                    for (int j = 0; j < CPL; j += 2) {
-                        S[j] = fma2(q2, dup(dr[j]), S[j]);
-                        S[j + 1] = fma2(q2, dup(dr[j + 1]), S[j + 1]);
-                        acc0 = fma2(S[j], dup(vr[j]), acc0);
-                        acc1 = fma2(S[j + 1], dup(vr[j + 1]), acc1);
-                    }
-                    const float2 d = group_sum(make_float2(acc0.x + acc1.x, acc0.y + acc1.y));
-                    const long o = (long)(t0 + t) * dk + r;
-                    if (cg == 0) *reinterpret_cast<float2*>(dkp + o) = d;
-                    if (GATE) {
+                for (int t = kTB - 1; t >= 0; t--) {
+                    acc[t] = make_float2(0.f, 0.f);
+                    if (t < n) {
+                        float2 vp[NP], dp[NP];
+                        load_pairs<CPL>(s_v + t * St::ROW + cg * St::STRIDE, vp);
+                        load_pairs<CPL>(s_d + t * St::ROW + cg * St::STRIDE, dp);
+                        const float2 q2 = *reinterpret_cast<const float2*>(s_q + t * kBlock + rl);
                         const float2 a2 = *reinterpret_cast<const float2*>(s_a + t * kBlock + rl);
+                        float2 pr[2];
 #pragma unroll
-                        for (int j = 0; j < CPL; j++) S[j] = mul2(a2, S[j]);
-                        const float2 k2 = *reinterpret_cast<const float2*>(s_k + t * kBlock + rl);
-                        const float2 dq2 = *reinterpret_cast<const float2*>(s_dq + t * kBlock + rl);
-                        // running sum over s >= t of q_s dq_s - k_s dk_s
-                        gsum = fma2(q2, dq2, gsum);
-                        gsum = fma2(make_float2(-k2.x, -k2.y), d, gsum);
-                        if (dla && cg == 0) *reinterpret_cast<float2*>(dla + o) = gsum;
+                        for (int w = 0; w < 2; w++) {
+                            const float2 qd = dup(w ? q2.y : q2.x), ad = dup(w ? a2.y : a2.x);
+                            pr[w] = make_float2(0.f, 0.f);
+#pragma unroll
+                            for (int p = 0; p < NP; p++) {
+                                S[w][p] = fma2(qd, dp[p], S[w][p]);
+                                pr[w] = fma2(S[w][p], vp[p], pr[w]);
+                                if (GATE) S[w][p] = mul2(ad, S[w][p]);
+                            }
+                        }
+                        acc[t] = make_float2(pr[0].x + pr[0].y, pr[1].x + pr[1].y);
                     }
+                }
+                const float x = reduce_scatter16(acc, lane);  // dk of token tb_l, row rl + w_l
+                const bool ok = tb_l < n;
+                const long o = (long)(t0 + tb_l) * dk + r + w_l;
+                if (ok) dkp[o] = x;
+                if (GATE) {
+                    // suffix sums over the round's tokens of q dq - k dk, plus the later rounds' total
+                    const int i = tb_l * kBlock + rl + w_l;
+                    float s = ok ? fmaf(s_q[i], s_dq[i], -s_k[i] * x) : 0.f;
+#pragma unroll
+                    for (int d = 1; d < kTB; d <<= 1) {
+                        const float o2 = __shfl_down_sync(0xffffffffu, s, 4 * d);
+                        if (tb_l + d < kTB) s += o2;
+                    }
+                    const float total = __shfl_sync(0xffffffffu, s, lane & 3);  // token 0 of this row
+                    if (dla && ok) dla[o] = s + carry;
+                    carry += total;
                 }
             }
             if (nn > 0) stage(nn, true, sm + ((rr + 1) & 1) * BUF);
@@ -340,29 +409,29 @@ __device__ __forceinline__ void rows_body(const BwdArgs& a, float* sm, int blk) 
     if (active && a.dinit) {
         float* di = a.dinit + (bh * dk + r) * (long)DV + cg * CPL;
 #pragma unroll
-        for (int j = 0; j < CPL; j++) {
-            di[j] = S[j].x;
-            di[DV + j] = S[j].y;
-        }
+        for (int w = 0; w < 2; w++)
+#pragma unroll
+            for (int p = 0; p < NP; p++) *reinterpret_cast<float2*>(di + w * DV + 2 * p) = S[w][p];
     }
 }
 
 // ---- column CTAs: dv (reverse sweep) ----
 // Wide arrays are over the key rows (W = RPL): q, k, alpha.  Narrow arrays over
-// the CTA's 64 value columns: dout.
+// the CTA's value columns: dout.  A lane's state is G[w][p] = (G[r0 + 2p][c + w],
+// G[r0 + 2p + 1][c + w]), w = 0, 1.
 template <int RPL, bool GATE, typename T>
-__device__ __forceinline__ void cols_body(const BwdArgs& a, float* sm, int blk) {
+__device__ __forceinline__ void cols_body(const BwdArgs& a, float* sm, long bh, int blk) {
     using St = Stage<RPL>;
-    constexpr int DK = St::FULL;
+    constexpr int DK = St::FULL, NP = RPL / 2;
     constexpr int BUF = kTB * (3 * St::ROW + kBlock);
     const int L = a.L, dv = a.dv;
-    const long bh = blockIdx.x;
     const int col0 = blk * kBlock, ncols = min(kBlock, dv - col0);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rg = lane >> 1, cp = lane & 1;
     const int c = warp * 4 + cp * 2;
     const bool active = warp * 4 < ncols;  // dv is a multiple of 4
     const int r0 = rg * RPL;
+    const int tb_l = rg >> 1, w_l = rg & 1;
 
     const T* q = static_cast<const T*>(a.q) + bh * (long)L * DK;
     const T* k = static_cast<const T*>(a.k) + bh * (long)L * DK;
@@ -411,33 +480,35 @@ __device__ __forceinline__ void cols_body(const BwdArgs& a, float* sm, int blk) 
         }
     };
 
-    float2 G[RPL];  // G[i] = (G[r0 + i][col0 + c], G[r0 + i][col0 + c + 1])
+    float2 G[2][NP];
     if (active && a.dfinal) {
         const float* df = a.dfinal + bh * (long)DK * dv + col0 + c;
 #pragma unroll
-        for (int i = 0; i < RPL; i++) G[i] = *reinterpret_cast<const float2*>(df + (long)(r0 + i) * dv);
+        for (int p = 0; p < NP; p++) {
+            const float2 x0 = *reinterpret_cast<const float2*>(df + (long)(r0 + 2 * p) * dv);
+            const float2 x1 = *reinterpret_cast<const float2*>(df + (long)(r0 + 2 * p + 1) * dv);
+            G[0][p] = make_float2(x0.x, x1.x);
+            G[1][p] = make_float2(x0.y, x1.y);
+        }
     } else {
 #pragma unroll
-        for (int i = 0; i < RPL; i++) G[i] = make_float2(0.f, 0.f);
+        for (int w = 0; w < 2; w++)
+#pragma unroll
+            for (int p = 0; p < NP; p++) G[w][p] = make_float2(0.f, 0.f);
     }
 
-    float* dvp = a.dv_out + bh * (long)L * dv + col0 + c;
+    float* dvp = a.dv_out + bh * (long)L * dv + col0 + c + w_l;
     const int nr = (L + kTB - 1) / kTB;
-    auto span = [&](int rr, int& t0) {
-        const int hi = L - rr * kTB;
-        t0 = max(0, hi - kTB);
-        return hi - t0;
-    };
     int t0;
-    int n = span(0, t0);
+    int n = rev_span(L, 0, t0);
     fetch(t0, n);
     stage(n, sm);
     __syncthreads();
     for (int rr = 0; rr < nr; rr++) {
-        n = span(rr, t0);
+        n = rev_span(L, rr, t0);
         int tn = 0, nn = 0;
         if (rr + 1 < nr) {
-            nn = span(rr + 1, tn);
+            nn = rev_span(L, rr + 1, tn);
             fetch(tn, nn);
         }
         const float* buf = sm + (rr & 1) * BUF;
@@ -446,29 +517,35 @@ __device__ __forceinline__ void cols_body(const BwdArgs& a, float* sm, int blk) 
         const float* s_a = s_k + kTB * St::ROW;
         const float* s_d = s_a + kTB * St::ROW;
         if (active) {
-            for (int t = n - 1; t >= 0; t--) {
-                const int ro = t * St::ROW + rg * St::STRIDE;
-                float qr[RPL], kr[RPL];
-                load_run<RPL>(s_q + ro, qr);
-                load_run<RPL>(s_k + ro, kr);
-                const float2 d2 = *reinterpret_cast<const float2*>(s_d + t * kBlock + c);
-                float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
+            float2 acc[kTB];
 #pragma unroll
-                for (int i = 0; i < RPL; i += 2) {
-                    G[i] = fma2(dup(qr[i]), d2, G[i]);
-                    G[i + 1] = fma2(dup(qr[i + 1]), d2, G[i + 1]);
-                    acc0 = fma2(dup(kr[i]), G[i], acc0);
-                    acc1 = fma2(dup(kr[i + 1]), G[i + 1], acc1);
-                }
-                const float2 d = group_sum(make_float2(acc0.x + acc1.x, acc0.y + acc1.y));
-                if (rg == 0) *reinterpret_cast<float2*>(dvp + (long)(t0 + t) * dv) = d;
-                if (GATE) {
-                    float ar[RPL];
-                    load_run<RPL>(s_a + ro, ar);
+            for (int t = kTB - 1; t >= 0; t--) {
+                acc[t] = make_float2(0.f, 0.f);
+                if (t < n) {
+                    const int ro = t * St::ROW + rg * St::STRIDE;
+                    float2 qp[NP], kp[NP];
+                    load_pairs<RPL>(s_q + ro, qp);
+                    load_pairs<RPL>(s_k + ro, kp);
+                    const float2 d2 = *reinterpret_cast<const float2*>(s_d + t * kBlock + c);
+                    float2 ap[NP];
+                    if (GATE) load_pairs<RPL>(s_a + ro, ap);
+                    float2 pr[2];
 #pragma unroll
-                    for (int i = 0; i < RPL; i++) G[i] = mul2(G[i], dup(ar[i]));
+                    for (int w = 0; w < 2; w++) {
+                        const float2 dd = dup(w ? d2.y : d2.x);
+                        pr[w] = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int p = 0; p < NP; p++) {
+                            G[w][p] = fma2(qp[p], dd, G[w][p]);
+                            pr[w] = fma2(kp[p], G[w][p], pr[w]);
+                            if (GATE) G[w][p] = mul2(G[w][p], ap[p]);
+                        }
+                    }
+                    acc[t] = make_float2(pr[0].x + pr[0].y, pr[1].x + pr[1].y);
                 }
             }
+            const float x = reduce_scatter16(acc, lane);  // dv of token tb_l, column c + w_l
+            if (tb_l < n) dvp[(long)(t0 + tb_l) * dv] = x;
         }
         if (nn > 0) stage(nn, sm + ((rr + 1) & 1) * BUF);
         __syncthreads();
@@ -482,15 +559,18 @@ constexpr size_t bwd_smem_bytes() {
     return sizeof(float) * 2 * (rows > cols ? rows : cols);
 }
 
-// blockIdx.x: (batch, head); blockIdx.y < row_blocks: a row CTA, else a column CTA
+// 1-D grid: the first B H rb CTAs are row CTAs (the rb row blocks of a head
+// adjacent, so they share its v and dout through L2), then B H cb column CTAs.
 template <int CPL, int RPL, bool GATE, typename T>
 __global__ void __launch_bounds__(kThreads) gla_bwd_kernel(const BwdArgs a) {
     extern __shared__ __align__(16) float sm[];
-    const int row_blocks = (a.dk + kBlock - 1) / kBlock;
-    if ((int)blockIdx.y < row_blocks)
-        rows_body<CPL, GATE, T>(a, sm, blockIdx.y);
+    const long BH = (long)a.B * a.H;
+    const int rb = (a.dk + kBlock - 1) / kBlock, cb = (a.dv + kBlock - 1) / kBlock;
+    const long b = blockIdx.x;
+    if (b < BH * rb)
+        rows_body<CPL, GATE, T>(a, sm, b / rb, (int)(b % rb));
     else
-        cols_body<RPL, GATE, T>(a, sm, blockIdx.y - row_blocks);
+        cols_body<RPL, GATE, T>(a, sm, (b - BH * rb) / cb, (int)((b - BH * rb) % cb));
 }
 
 template <int CPL, int RPL, bool GATE, typename T>
@@ -500,9 +580,8 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t s) {
     static_assert(smem <= 227 * 1024, "staging exceeds shared memory");
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const unsigned rb = (unsigned)((a.dk + kBlock - 1) / kBlock), cb = (unsigned)((a.dv + kBlock - 1) / kBlock);
-    const dim3 grid((unsigned)((long)a.B * a.H), rb + cb);
-    kern<<<grid, kThreads, smem, s>>>(a);
+    const long blocks = (long)a.B * a.H * (bwd_blocks(a.dk) + bwd_blocks(a.dv));
+    kern<<<(unsigned)blocks, kThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -524,6 +603,8 @@ cudaError_t launch_dk(const BwdArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+int bwd_blocks(int d) { return (d + kBlock - 1) / kBlock; }
 
 bool bwd_supported(int dk, int dv) {
     return (dk == 32 || dk == 64 || dk == 128) && (dv == 32 || dv == 64 || dv == 128);

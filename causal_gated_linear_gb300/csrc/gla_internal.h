@@ -87,6 +87,7 @@ struct BwdArgs {
 // Gradients of the recurrence (row CTAs: dq, dk, dlog_alpha, dS_init;
 // column CTAs: dv), one launch.
 bool bwd_supported(int dk, int dv);
+int bwd_blocks(int d);  // CTAs per head along one dimension (row CTAs for dk, column CTAs for dv)
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s);
 
 // Memory-bound decode step.
