@@ -15,23 +15,27 @@
 // are the only place log alpha appears.)
 //
 // Two kinds of CTA share one launch:
-//  * row CTAs own 64 key rows of one head, all value columns.  Rows evolve on
+//  * row CTAs own 32 key rows of one head, all value columns.  Rows evolve on
 //    their own (S_t[i,:] needs alpha_t[i], k_t[i] and v_t), so a forward sweep
 //    carries S and emits dq (a reduction over the value columns), and a
 //    reverse sweep carries G and emits dk, the running gate sum and dS_{-1}.
 //    Lane (cg, rp) of a warp holds rows warp*4 + 2 rp + {0, 1} over the value
 //    columns [cg * CPL, (cg + 1) * CPL), as fp32 pairs of adjacent columns.
-//  * column CTAs own 64 value columns: a reverse sweep carries G column-wise
+//  * column CTAs own 32 value columns: a reverse sweep carries G column-wise
 //    and emits dv (a reduction over the key rows).  Lane (rg, cp) holds rows
 //    [rg * RPL, (rg + 1) * RPL) of the columns 2 cp + {0, 1}, as fp32 pairs of
 //    adjacent rows.
 // Pairs run along the vectors read from shared memory per token, so they feed
-// the packed fp32 instructions as loaded.  The reductions are output-only (they
-// do not feed the recurrence), so a round of 8 tokens keeps its 16 partial sums
-// per lane and reduce-scatters them across the sixteen lane groups at the end
-// of the round.  Tokens are staged in shared memory a round at a time, double
-// buffered.  Row CTAs come first in the grid: they do two sweeps, the column
-// CTAs one.
+// the packed fp32 instructions as loaded; the per-lane scalars (k, alpha, q of
+// a row, dout of a column) are staged as (x, x) pairs.  The reductions are
+// output-only (they do not feed the recurrence), so a batch of 8 tokens keeps
+// its 16 partial sums per lane and reduce-scatters them across the sixteen
+// lane groups.  Rounds of 16 tokens are staged in shared memory, double
+// buffered: the next round's global loads are in flight while the current one
+// is computed.  8 warps and at most 128 registers per thread give two CTAs per
+// SM; row CTAs come first in the grid (they do two sweeps, the column CTAs
+// one), the row blocks of a head adjacent so that they share its v and dout
+// through L2.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -43,9 +47,10 @@
 namespace gla {
 namespace {
 
-constexpr int kWarps = 16;
+constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kTB = 8;              // tokens staged per round (one batch of reductions)
+constexpr int kTB = 16;             // tokens staged per round
+constexpr int kRB = 8;              // tokens per batch of reductions
 constexpr int kBlock = 4 * kWarps;  // rows per row CTA, columns per column CTA
 
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
@@ -82,7 +87,7 @@ __device__ __forceinline__ float2 group_sum(float2 x) {
 // sums per lane) summed across lane bits 1..4; lane group g = lane >> 1 ends
 // with the total of entry e = g.  Four halving exchanges: 15 shuffles for 16
 // sums instead of 64.
-__device__ __forceinline__ float reduce_scatter16(const float2 (&acc)[kTB], int lane) {
+__device__ __forceinline__ float reduce_scatter16(const float2 (&acc)[kRB], int lane) {
     float v8[8];
     {
         const bool up = lane & 16;
@@ -168,7 +173,7 @@ template <int CPL, bool GATE, typename T>
 __device__ __forceinline__ void rows_body(const BwdArgs& a, float* sm, long bh, int blk) {
     using St = Stage<CPL>;
     constexpr int DV = St::FULL, NP = CPL / 2;
-    constexpr int BUF = kTB * (2 * St::ROW + 4 * kBlock);
+    constexpr int BUF = kTB * (2 * St::ROW + 7 * kBlock);
     const int L = a.L, dk = a.dk;
     const int row0 = blk * kBlock, nrows = min(kBlock, dk - row0);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -217,10 +222,10 @@ __device__ __forceinline__ void rows_body(const BwdArgs& a, float* sm, long bh, 
     auto stage = [&](int n, bool rev, float* buf) {
         float* s_v = buf;
         float* s_d = s_v + kTB * St::ROW;
-        float* s_k = s_d + kTB * St::ROW;
-        float* s_a = s_k + kTB * kBlock;
-        float* s_q = s_a + kTB * kBlock;
-        float* s_dq = s_q + kTB * kBlock;
+        float2* s_k = reinterpret_cast<float2*>(s_d + kTB * St::ROW);  // (k, k) per entry
+        float2* s_a = s_k + kTB * kBlock;                               // (alpha, alpha)
+        float2* s_q = s_a + kTB * kBlock;                               // (q, q)
+        float* s_dq = reinterpret_cast<float*>(s_q + kTB * kBlock);
 #pragma unroll
         for (int m = 0; m < St::NW; m++) {
             const int idx = tid + m * kThreads;
@@ -234,10 +239,10 @@ __device__ __forceinline__ void rows_body(const BwdArgs& a, float* sm, long bh, 
         for (int m = 0; m < St::NN; m++) {
             const int idx = tid + m * kThreads;
             if (idx / kBlock < n && idx % kBlock < nrows) {
-                s_k[idx] = to_f(rk[m]);
-                s_a[idx] = GATE ? __expf(ra[m]) : 1.f;
+                s_k[idx] = dup(to_f(rk[m]));
+                s_a[idx] = dup(GATE ? __expf(ra[m]) : 1.f);
                 if (rev) {
-                    s_q[idx] = to_f(rq[m]);
+                    s_q[idx] = dup(to_f(rq[m]));
                     s_dq[idx] = GATE ? rdq[m] : 0.f;
                 }
             }
@@ -270,34 +275,40 @@ __device__ __forceinline__ void rows_body(const BwdArgs& a, float* sm, long bh, 
             const float* s_v = buf;
             const float* s_d = s_v + kTB * St::ROW;
             const float* s_k = s_d + kTB * St::ROW;
-            const float* s_a = s_k + kTB * kBlock;
+            const float* s_a = s_k + 2 * kTB * kBlock;
             if (active) {
-                float2 acc[kTB];
 #pragma unroll
-                for (int t = 0; t < kTB; t++) {
-                    acc[t] = make_float2(0.f, 0.f);
-                    if (t < n) {
-                        float2 vp[NP], dp[NP];
-                        load_pairs<CPL>(s_v + t * St::ROW + cg * St::STRIDE, vp);
-                        load_pairs<CPL>(s_d + t * St::ROW + cg * St::STRIDE, dp);
-                        const float2 k2 = *reinterpret_cast<const float2*>(s_k + t * kBlock + rl);
-                        const float2 a2 = *reinterpret_cast<const float2*>(s_a + t * kBlock + rl);
-                        float2 pr[2];
+                for (int h = 0; h < kTB / kRB; h++) {
+                    float2 acc[kRB];
 #pragma unroll
-                        for (int w = 0; w < 2; w++) {
-                            const float2 kd = dup(w ? k2.y : k2.x), ad = dup(w ? a2.y : a2.x);
-                            pr[w] = make_float2(0.f, 0.f);
+                    for (int u = 0; u < kRB; u++) {
+                        const int t = h * kRB + u;
+                        acc[u] = make_float2(0.f, 0.f);
+                        if (t < n) {
+                            float2 vp[NP], dp[NP];
+                            load_pairs<CPL>(s_v + t * St::ROW + cg * St::STRIDE, vp);
+                            load_pairs<CPL>(s_d + t * St::ROW + cg * St::STRIDE, dp);
+                            const float4 k4 = *reinterpret_cast<const float4*>(s_k + 2 * (t * kBlock + rl));
+                            const float4 a4 = *reinterpret_cast<const float4*>(s_a + 2 * (t * kBlock + rl));
+                            float2 pr[2];
 #pragma unroll
-                            for (int p = 0; p < NP; p++) {
-                                S[w][p] = GATE ? fma2(ad, S[w][p], mul2(kd, vp[p])) : fma2(kd, vp[p], S[w][p]);
-                                pr[w] = fma2(S[w][p], dp[p], pr[w]);
+                            for (int w = 0; w < 2; w++) {
+                                const float2 kd = w ? make_float2(k4.z, k4.w) : make_float2(k4.x, k4.y);
+                                const float2 ad = w ? make_float2(a4.z, a4.w) : make_float2(a4.x, a4.y);
+                                pr[w] = make_float2(0.f, 0.f);
+#pragma unroll
+                                for (int p = 0; p < NP; p++) {
+                                    S[w][p] = GATE ? fma2(ad, S[w][p], mul2(kd, vp[p])) : fma2(kd, vp[p], S[w][p]);
+                                    pr[w] = fma2(S[w][p], dp[p], pr[w]);
+                                }
                             }
+                            acc[u] = make_float2(pr[0].x + pr[0].y, pr[1].x + pr[1].y);
                         }
-                        acc[t] = make_float2(pr[0].x + pr[0].y, pr[1].x + pr[1].y);
                     }
+                    const float x = reduce_scatter16(acc, lane);
+                    const int tt = h * kRB + tb_l;
+                    if (tt < n) dq[(long)(t0 + tt) * dk + r + w_l] = x;
                 }
-                const float x = reduce_scatter16(acc, lane);
-                if (tb_l < n) dq[(long)(t0 + tb_l) * dk + r + w_l] = x;
             }
             if (nn > 0) stage(nn, false, sm + ((rnd + 1) & 1) * BUF);
             __syncthreads();
@@ -355,51 +366,57 @@ __device__ __forceinline__ void rows_body(const BwdArgs& a, float* sm, long bh, 
             const float* s_v = buf;
             const float* s_d = s_v + kTB * St::ROW;
             const float* s_k = s_d + kTB * St::ROW;
-            const float* s_a = s_k + kTB * kBlock;
-            const float* s_q = s_a + kTB * kBlock;
-            const float* s_dq = s_q + kTB * kBlock;
+            const float* s_a = s_k + 2 * kTB * kBlock;
+            const float* s_q = s_a + 2 * kTB * kBlock;
+            const float* s_dq = s_q + 2 * kTB * kBlock;
             if (active) {
-                float2 acc[kTB];
 #pragma unroll
-                for (int t = kTB - 1; t >= 0; t--) {
-                    acc[t] = make_float2(0.f, 0.f);
-                    if (t < n) {
-                        float2 vp[NP], dp[NP];
-                        load_pairs<CPL>(s_v + t * St::ROW + cg * St::STRIDE, vp);
-                        load_pairs<CPL>(s_d + t * St::ROW + cg * St::STRIDE, dp);
-                        const float2 q2 = *reinterpret_cast<const float2*>(s_q + t * kBlock + rl);
-                        const float2 a2 = *reinterpret_cast<const float2*>(s_a + t * kBlock + rl);
-                        float2 pr[2];
+                for (int h = kTB / kRB - 1; h >= 0; h--) {
+                    float2 acc[kRB];
 #pragma unroll
-                        for (int w = 0; w < 2; w++) {
-                            const float2 qd = dup(w ? q2.y : q2.x), ad = dup(w ? a2.y : a2.x);
-                            pr[w] = make_float2(0.f, 0.f);
+                    for (int u = kRB - 1; u >= 0; u--) {
+                        const int t = h * kRB + u;
+                        acc[u] = make_float2(0.f, 0.f);
+                        if (t < n) {
+                            float2 vp[NP], dp[NP];
+                            load_pairs<CPL>(s_v + t * St::ROW + cg * St::STRIDE, vp);
+                            load_pairs<CPL>(s_d + t * St::ROW + cg * St::STRIDE, dp);
+                            const float4 q4 = *reinterpret_cast<const float4*>(s_q + 2 * (t * kBlock + rl));
+                            const float4 a4 = *reinterpret_cast<const float4*>(s_a + 2 * (t * kBlock + rl));
+                            float2 pr[2];
 #pragma unroll
-                            for (int p = 0; p < NP; p++) {
-                                S[w][p] = fma2(qd, dp[p], S[w][p]);
-                                pr[w] = fma2(S[w][p], vp[p], pr[w]);
-                                if (GATE) S[w][p] = mul2(ad, S[w][p]);
+                            for (int w = 0; w < 2; w++) {
+                                const float2 qd = w ? make_float2(q4.z, q4.w) : make_float2(q4.x, q4.y);
+                                const float2 ad = w ? make_float2(a4.z, a4.w) : make_float2(a4.x, a4.y);
+                                pr[w] = make_float2(0.f, 0.f);
+#pragma unroll
+                                for (int p = 0; p < NP; p++) {
+                                    S[w][p] = fma2(qd, dp[p], S[w][p]);
+                                    pr[w] = fma2(S[w][p], vp[p], pr[w]);
+                                    if (GATE) S[w][p] = mul2(ad, S[w][p]);
+                                }
                             }
+                            acc[u] = make_float2(pr[0].x + pr[0].y, pr[1].x + pr[1].y);
                         }
-                        acc[t] = make_float2(pr[0].x + pr[0].y, pr[1].x + pr[1].y);
                     }
-                }
-                const float x = reduce_scatter16(acc, lane);  // dk of token tb_l, row rl + w_l
-                const bool ok = tb_l < n;
-                const long o = (long)(t0 + tb_l) * dk + r + w_l;
-                if (ok) dkp[o] = x;
-                if (GATE) {
-                    // suffix sums over the round's tokens of q dq - k dk, plus the later rounds' total
-                    const int i = tb_l * kBlock + rl + w_l;
-                    float s = ok ? fmaf(s_q[i], s_dq[i], -s_k[i] * x) : 0.f;
+                    const float x = reduce_scatter16(acc, lane);  // dk of token h kRB + tb_l, row rl + w_l
+                    const int tt = h * kRB + tb_l;
+                    const bool ok = tt < n;
+                    const long o = (long)(t0 + tt) * dk + r + w_l;
+                    if (ok) dkp[o] = x;
+                    if (GATE) {
+                        // suffix sums over the batch's tokens of q dq - k dk, plus the later tokens' total
+                        const int i = tt * kBlock + rl + w_l;
+                        float s = ok ? fmaf(s_q[2 * i], s_dq[i], -s_k[2 * i] * x) : 0.f;
 #pragma unroll
-                    for (int d = 1; d < kTB; d <<= 1) {
-                        const float o2 = __shfl_down_sync(0xffffffffu, s, 4 * d);
-                        if (tb_l + d < kTB) s += o2;
+                        for (int d = 1; d < kRB; d <<= 1) {
+                            const float o2 = __shfl_down_sync(0xffffffffu, s, 4 * d);
+                            if (tb_l + d < kRB) s += o2;
+                        }
+                        const float total = __shfl_sync(0xffffffffu, s, lane & 3);  // the batch's first token
+                        if (dla && ok) dla[o] = s + carry;
+                        carry += total;
                     }
-                    const float total = __shfl_sync(0xffffffffu, s, lane & 3);  // token 0 of this row
-                    if (dla && ok) dla[o] = s + carry;
-                    carry += total;
                 }
             }
             if (nn > 0) stage(nn, true, sm + ((rr + 1) & 1) * BUF);
@@ -423,7 +440,7 @@ template <int RPL, bool GATE, typename T>
 __device__ __forceinline__ void cols_body(const BwdArgs& a, float* sm, long bh, int blk) {
     using St = Stage<RPL>;
     constexpr int DK = St::FULL, NP = RPL / 2;
-    constexpr int BUF = kTB * (3 * St::ROW + kBlock);
+    constexpr int BUF = kTB * (3 * St::ROW + 2 * kBlock);
     const int L = a.L, dv = a.dv;
     const int col0 = blk * kBlock, ncols = min(kBlock, dv - col0);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -462,7 +479,7 @@ __device__ __forceinline__ void cols_body(const BwdArgs& a, float* sm, long bh, 
         float* s_q = buf;
         float* s_k = s_q + kTB * St::ROW;
         float* s_a = s_k + kTB * St::ROW;
-        float* s_d = s_a + kTB * St::ROW;
+        float2* s_d = reinterpret_cast<float2*>(s_a + kTB * St::ROW);  // (dout, dout) per entry
 #pragma unroll
         for (int m = 0; m < St::NW; m++) {
             const int idx = tid + m * kThreads;
@@ -476,7 +493,7 @@ __device__ __forceinline__ void cols_body(const BwdArgs& a, float* sm, long bh, 
 #pragma unroll
         for (int m = 0; m < St::NN; m++) {
             const int idx = tid + m * kThreads;
-            if (idx / kBlock < n && idx % kBlock < ncols) s_d[idx] = to_f(rd[m]);
+            if (idx / kBlock < n && idx % kBlock < ncols) s_d[idx] = dup(to_f(rd[m]));
         }
     };
 
@@ -515,37 +532,42 @@ __device__ __forceinline__ void cols_body(const BwdArgs& a, float* sm, long bh, 
         const float* s_q = buf;
         const float* s_k = s_q + kTB * St::ROW;
         const float* s_a = s_k + kTB * St::ROW;
-        const float* s_d = s_a + kTB * St::ROW;
+        const float* s_d = s_a + kTB * St::ROW;  // (dout, dout) pairs
         if (active) {
-            float2 acc[kTB];
 #pragma unroll
-            for (int t = kTB - 1; t >= 0; t--) {
-                acc[t] = make_float2(0.f, 0.f);
-                if (t < n) {
-                    const int ro = t * St::ROW + rg * St::STRIDE;
-                    float2 qp[NP], kp[NP];
-                    load_pairs<RPL>(s_q + ro, qp);
-                    load_pairs<RPL>(s_k + ro, kp);
-                    const float2 d2 = *reinterpret_cast<const float2*>(s_d + t * kBlock + c);
-                    float2 ap[NP];
-                    if (GATE) load_pairs<RPL>(s_a + ro, ap);
-                    float2 pr[2];
+            for (int h = kTB / kRB - 1; h >= 0; h--) {
+                float2 acc[kRB];
 #pragma unroll
-                    for (int w = 0; w < 2; w++) {
-                        const float2 dd = dup(w ? d2.y : d2.x);
-                        pr[w] = make_float2(0.f, 0.f);
+                for (int u = kRB - 1; u >= 0; u--) {
+                    const int t = h * kRB + u;
+                    acc[u] = make_float2(0.f, 0.f);
+                    if (t < n) {
+                        const int ro = t * St::ROW + rg * St::STRIDE;
+                        float2 qp[NP], kp[NP];
+                        load_pairs<RPL>(s_q + ro, qp);
+                        load_pairs<RPL>(s_k + ro, kp);
+                        const float4 d4 = *reinterpret_cast<const float4*>(s_d + 2 * (t * kBlock + c));
+                        float2 ap[NP];
+                        if (GATE) load_pairs<RPL>(s_a + ro, ap);
+                        float2 pr[2];
 #pragma unroll
-                        for (int p = 0; p < NP; p++) {
-                            G[w][p] = fma2(qp[p], dd, G[w][p]);
-                            pr[w] = fma2(kp[p], G[w][p], pr[w]);
-                            if (GATE) G[w][p] = mul2(G[w][p], ap[p]);
+                        for (int w = 0; w < 2; w++) {
+                            const float2 dd = w ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
+                            pr[w] = make_float2(0.f, 0.f);
+#pragma unroll
+                            for (int p = 0; p < NP; p++) {
+                                G[w][p] = fma2(qp[p], dd, G[w][p]);
+                                pr[w] = fma2(kp[p], G[w][p], pr[w]);
+                                if (GATE) G[w][p] = mul2(G[w][p], ap[p]);
+                            }
                         }
+                        acc[u] = make_float2(pr[0].x + pr[0].y, pr[1].x + pr[1].y);
                     }
-                    acc[t] = make_float2(pr[0].x + pr[0].y, pr[1].x + pr[1].y);
                 }
+                const float x = reduce_scatter16(acc, lane);  // dv of token h kRB + tb_l, column c + w_l
+                const int tt = h * kRB + tb_l;
+                if (tt < n) dvp[(long)(t0 + tt) * dv] = x;
             }
-            const float x = reduce_scatter16(acc, lane);  // dv of token tb_l, column c + w_l
-            if (tb_l < n) dvp[(long)(t0 + tb_l) * dv] = x;
         }
         if (nn > 0) stage(nn, sm + ((rr + 1) & 1) * BUF);
         __syncthreads();
@@ -554,15 +576,15 @@ __device__ __forceinline__ void cols_body(const BwdArgs& a, float* sm, long bh, 
 
 template <int CPL, int RPL>
 constexpr size_t bwd_smem_bytes() {
-    constexpr size_t rows = (size_t)kTB * (2 * Stage<CPL>::ROW + 4 * kBlock);
-    constexpr size_t cols = (size_t)kTB * (3 * Stage<RPL>::ROW + kBlock);
+    constexpr size_t rows = (size_t)kTB * (2 * Stage<CPL>::ROW + 7 * kBlock);
+    constexpr size_t cols = (size_t)kTB * (3 * Stage<RPL>::ROW + 2 * kBlock);
     return sizeof(float) * 2 * (rows > cols ? rows : cols);
 }
 
 // 1-D grid: the first B H rb CTAs are row CTAs (the rb row blocks of a head
 // adjacent, so they share its v and dout through L2), then B H cb column CTAs.
 template <int CPL, int RPL, bool GATE, typename T>
-__global__ void __launch_bounds__(kThreads) gla_bwd_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) gla_bwd_kernel(const BwdArgs a) {
     extern __shared__ __align__(16) float sm[];
     const long BH = (long)a.B * a.H;
     const int rb = (a.dk + kBlock - 1) / kBlock, cb = (a.dv + kBlock - 1) / kBlock;
