@@ -11,12 +11,14 @@
 // are column-wise given k_n and beta_n), so a warp owns 4 value columns of one
 // head for the whole sequence and needs no block-wide synchronisation per
 // token: lane (rg, cp) holds rows [rg * RPL, (rg + 1) * RPL) of the column
-// pair 2 cp (RPL = dk / 16 rows, as packed fp32 pairs), and the two
-// reductions over dk per token (the prediction and the output) are four
-// butterfly shuffles across the sixteen row groups.  A CTA of 16 warps covers
-// 64 value columns; tokens are staged in shared memory 16 at a time, double
-// buffered: the next round's global loads are in flight while the current
-// round is computed.
+// pair 2 cp (RPL = dk / 16 rows, as packed fp32 pairs).  The prediction is a
+// reduction over dk that feeds the write, so it takes four butterfly shuffles
+// across the sixteen row groups every token; the output does not feed the
+// recurrence, so a batch of 4 tokens keeps its partial sums and
+// reduce-scatters them (8 shuffles for 4 tokens instead of 32).  A CTA of 16
+// warps covers 64 value columns, two CTAs per SM (64 registers); tokens are
+// staged in shared memory 16 at a time, double buffered: the next round's
+// global loads are in flight while the current round is computed.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -31,6 +33,7 @@ constexpr int kWarps = 16;            // 4 value columns each
 constexpr int kCols = 4 * kWarps;     // value columns per CTA
 constexpr int kThreads = kWarps * 32;
 constexpr int kTB = 16;               // tokens staged per round
+constexpr int kRB = 4;                // tokens per batch of output reductions
 
 template <int RPL>
 struct DeltaLayout {
@@ -44,11 +47,6 @@ struct DeltaLayout {
     static constexpr int NQ = (kTB * DK + kThreads - 1) / kThreads;
     static constexpr int NV = (kTB * kCols + kThreads - 1) / kThreads;
 };
-
-__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
 
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     float2 d;
@@ -78,6 +76,34 @@ __device__ __forceinline__ float2 rowgroup_sum(float2 x) {
     return x;
 }
 
+// Reduce-scatter over the sixteen row groups (lane bits 1..4) of the 2 NB partial
+// sums of a lane (entry e = 2 tb + w): halving exchanges while entries remain,
+// then plain butterfly adds.  NB = 8: row group g ends with entry g; NB = 4:
+// row groups 2e and 2e + 1 both end with entry e.
+template <int NB>
+__device__ __forceinline__ float reduce_scatter(const float2 (&acc)[NB], int lane) {
+    float v[2 * NB];
+#pragma unroll
+    for (int i = 0; i < NB; i++) v[2 * i] = acc[i].x, v[2 * i + 1] = acc[i].y;
+    int n = 2 * NB;
+#pragma unroll
+    for (int mask = 16; mask >= 2; mask >>= 1) {
+        if (n > 1) {
+            const bool up = lane & mask;
+            const int half = n / 2;
+#pragma unroll
+            for (int i = 0; i < half; i++) {
+                const float send = up ? v[i] : v[half + i], mine = up ? v[half + i] : v[i];
+                v[i] = mine + __shfl_xor_sync(0xffffffffu, send, mask);
+            }
+            n = half;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], mask);
+        }
+    }
+    return v[0];
+}
+
 // RPL consecutive floats of a staged row group (16-byte aligned when RPL >= 4)
 template <int RPL>
 __device__ __forceinline__ void load_rows(const float* p, float (&r)[RPL]) {
@@ -97,7 +123,7 @@ __device__ __forceinline__ void load_rows(const float* p, float (&r)[RPL]) {
 }
 
 template <int RPL, bool GATE, bool OUT_F32>
-__global__ void __launch_bounds__(kThreads) gla_delta_kernel(const DeltaArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) gla_delta_kernel(const DeltaArgs a) {
     using Ly = DeltaLayout<RPL>;
     constexpr int DK = Ly::DK;
     extern __shared__ __align__(16) float sm[];
@@ -111,6 +137,9 @@ __global__ void __launch_bounds__(kThreads) gla_delta_kernel(const DeltaArgs a) 
     const int c = warp * 4 + cp * 2;        // this lane's first column within the CTA's block
     const bool active = c < ncols;          // dv is a multiple of 16: a warp is all or nothing
     const int r0 = rg * RPL;
+    // after a reduce-scatter: token tb_l of the batch, column c + w_l (two row groups hold each)
+    const int tb_l = rg >> 2, w_l = (rg >> 1) & 1;
+    const bool writer = (rg & 1) == 0;
 
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + bh * (long)L * DK;
     const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k) + bh * (long)L * DK;
@@ -193,45 +222,53 @@ __global__ void __launch_bounds__(kThreads) gla_delta_kernel(const DeltaArgs a) 
         const float* s_v = s_a + kTB * Ly::ROW;
         const float* s_b = s_v + kTB * kCols;
         if (active) {
-            for (int t = 0; t < n; t++) {
-                const int ro = t * Ly::ROW + rg * Ly::STRIDE;
-                float kr[RPL], qr[RPL];
-                load_rows<RPL>(s_k + ro, kr);
-                // the gate decays the state before the prediction
-                if (GATE) {
-                    float ar[RPL];
-                    load_rows<RPL>(s_a + ro, ar);
 #pragma unroll
-                    for (int i = 0; i < RPL; i++) S[i] = mul2(S[i], make_float2(ar[i], ar[i]));
-                }
-                // prediction p = S^T k for this lane's column pair (two chains)
-                float2 p0 = make_float2(0.f, 0.f), p1 = p0;
+            for (int h = 0; h < kTB / kRB; h++) {
+                float2 acc[kRB];
 #pragma unroll
-                for (int i = 0; i < RPL; i += 2) {
-                    p0 = fma2(S[i], make_float2(kr[i], kr[i]), p0);
-                    p1 = fma2(S[i + 1], make_float2(kr[i + 1], kr[i + 1]), p1);
-                }
-                const float2 p = rowgroup_sum(make_float2(p0.x + p1.x, p0.y + p1.y));
-                // the error, written with strength beta: S += k u^T; then o = S^T q
-                const float2 v2 = *reinterpret_cast<const float2*>(s_v + t * kCols + c);
-                const float b = s_b[t];
-                const float2 u = make_float2(b * (v2.x - p.x), b * (v2.y - p.y));
-                load_rows<RPL>(s_q + ro, qr);
-                float2 o0 = make_float2(0.f, 0.f), o1 = o0;
+                for (int uu = 0; uu < kRB; uu++) {
+                    const int t = h * kRB + uu;
+                    acc[uu] = make_float2(0.f, 0.f);
+                    if (t < n) {
+                        const int ro = t * Ly::ROW + rg * Ly::STRIDE;
+                        float kr[RPL], qr[RPL];
+                        load_rows<RPL>(s_k + ro, kr);
+                        if (GATE) {
+                            float ar[RPL];
+                            load_rows<RPL>(s_a + ro, ar);
 #pragma unroll
-                for (int i = 0; i < RPL; i += 2) {
-                    S[i] = fma2(make_float2(kr[i], kr[i]), u, S[i]);
-                    S[i + 1] = fma2(make_float2(kr[i + 1], kr[i + 1]), u, S[i + 1]);
-                    o0 = fma2(make_float2(qr[i], qr[i]), S[i], o0);
-                    o1 = fma2(make_float2(qr[i + 1], qr[i + 1]), S[i + 1], o1);
+                            for (int i = 0; i < RPL; i++) S[i] = mul2(S[i], make_float2(ar[i], ar[i]));
+                        }
+                        float2 p0 = make_float2(0.f, 0.f), p1 = p0;
+#pragma unroll
+                        for (int i = 0; i < RPL; i += 2) {
+                            p0 = fma2(S[i], make_float2(kr[i], kr[i]), p0);
+                            p1 = fma2(S[i + 1], make_float2(kr[i + 1], kr[i + 1]), p1);
+                        }
+                        const float2 p = rowgroup_sum(make_float2(p0.x + p1.x, p0.y + p1.y));
+                        const float2 v2 = *reinterpret_cast<const float2*>(s_v + t * kCols + c);
+                        const float b = s_b[t];
+                        const float2 u = make_float2(b * (v2.x - p.x), b * (v2.y - p.y));
+                        load_rows<RPL>(s_q + ro, qr);
+                        float2 o0 = make_float2(0.f, 0.f), o1 = o0;
+#pragma unroll
+                        for (int i = 0; i < RPL; i += 2) {
+                            S[i] = fma2(make_float2(kr[i], kr[i]), u, S[i]);
+                            S[i + 1] = fma2(make_float2(kr[i + 1], kr[i + 1]), u, S[i + 1]);
+                            o0 = fma2(make_float2(qr[i], qr[i]), S[i], o0);
+                            o1 = fma2(make_float2(qr[i + 1], qr[i + 1]), S[i + 1], o1);
+                        }
+                        acc[uu] = make_float2(o0.x + o1.x, o0.y + o1.y);
+                    }
                 }
-                const float2 o = rowgroup_sum(make_float2(o0.x + o1.x, o0.y + o1.y));
-                if (rg == 0) {
-                    const long oi = (bh * L + t0 + t) * (long)dv + col0 + c;
+                const float o = reduce_scatter<kRB>(acc, lane);
+                const int tt = h * kRB + tb_l;
+                if (tt < n && writer) {
+                    const long oi = (bh * L + t0 + tt) * (long)dv + col0 + c + w_l;
                     if (OUT_F32)
-                        *reinterpret_cast<float2*>(static_cast<float*>(a.out) + oi) = o;
+                        static_cast<float*>(a.out)[oi] = o;
                     else
-                        *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + oi) = pack_bf16x2_rn(o.x, o.y);
+                        static_cast<__nv_bfloat16*>(a.out)[oi] = __float2bfloat16_rn(o);
                 }
             }
         }
