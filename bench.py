@@ -352,7 +352,8 @@ def bench_prefill(args, device, rank, world):
                              calls=args.scalar_calls)
         del las
 
-    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    # end to end through the public API with host buffers (pinned), copies inside the timed region:
+    # gla_fwd_host copies each head group in, computes it and copies it out, overlapping the groups
     if args.e2e:
         hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
         hla, hs0 = la.cpu().pin_memory(), s0.cpu().pin_memory()
@@ -362,29 +363,31 @@ def bench_prefill(args, device, rank, world):
         d2h = hout.numel() * hout.element_size() + hfs.numel() * hfs.element_size()
         dq, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         dla, ds0 = torch.empty_like(la), torch.empty_like(s0)
+        host = dict(q=hq, k=hk, v=hv, log_alpha=hla, init_state=hs0, out=hout, final_state=hfs)
+        devb = dict(q=dq, k=dk_, v=dv_, log_alpha=dla, init_state=ds0, out=out, final_state=fs)
+        s_in, s_c, s_out = (torch.cuda.Stream(device) for _ in range(3))
 
         def e2e_step():
-            for d, h in ((dq, hq), (dk_, hk), (dv_, hv), (dla, hla), (ds0, hs0)):
-                d.copy_(h, non_blocking=True)
-            st = gla.gla_fwd(dq, dk_, dv_, dla, ds0, out, fs, w.B, w.H, w.L, w.dk, w.dv, C, stream=stream)
+            st = gla.gla_fwd_host(host, devb, w.B, w.H, w.L, w.dk, w.dv, C, groups=args.e2e_groups,
+                                  copy_in=s_in, compute=s_c, copy_out=s_out)
             if st != 0:
                 raise RuntimeError(gla.gla_status_string(st))
-            hout.copy_(out, non_blocking=True)
-            hfs.copy_(fs, non_blocking=True)
 
         e2e_step()
         torch.cuda.synchronize(device)
         ne = max(1, min(args.steps, 3))
         barrier(world)
         torch.cuda.synchronize(device)
-        ev0.record(stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s_in)
         for _ in range(ne):
             e2e_step()
-        ev1.record(stream)
+        e1.record(s_out)
         torch.cuda.synchronize(device)
-        e_ms = max_over_ranks(ev0.elapsed_time(ev1), world, device)
-        res["e2e"] = dict(ms_per_step=e_ms / ne, h2d=h2d, d2h=d2h)
-        del hq, hk, hv, hla, hs0, hout, hfs, dq, dk_, dv_, dla, ds0
+        gla.check(gla.gla_device_error(s_out))
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
+        res["e2e"] = dict(ms_per_step=e_ms / ne, h2d=h2d, d2h=d2h, groups=args.e2e_groups)
+        del hq, hk, hv, hla, hs0, hout, hfs, dq, dk_, dv_, dla, ds0, host, devb
     del q, k, v, la, s0, out, fs
     torch.cuda.empty_cache()
     return w, BH, res
@@ -632,7 +635,7 @@ def run_gla(args):
         e = pre["e2e"]
         line["e2e"] = {"value": tokens * world / (e["ms_per_step"] / 1e3), "unit": "tokens/s",
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
-                       "ms_per_step": e["ms_per_step"]}
+                       "ms_per_step": e["ms_per_step"], "api": "gla_fwd_host", "head_groups": e["groups"]}
     if rank == 0 and world == 1 and args.cpu_baseline:
         tps, cores, desc, dt = oracle_sample(args.ref_seconds)
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
@@ -663,6 +666,8 @@ def main():
     ap.add_argument("--multi-calls", type=int, default=64,
                     help="timed calls of the 8-tokens-per-sequence hand-off workload (0: skip)")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--e2e-groups", type=int, default=4,
+                    help="head groups whose host copies gla_fwd_host overlaps with the computation")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--L", type=int, default=0,

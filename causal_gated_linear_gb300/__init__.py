@@ -12,6 +12,8 @@ The functions mirror the C entry points:
     gla_fwd_ex(q, k, v, out, B, H, L, dk, dv, chunk=64, log_alpha=None,
                init_state=None, init_z=None, final_state=None, final_z=None,
                in_dtype=BF16, out_dtype=BF16, flags=0, stream=None) -> int
+    gla_fwd_host(host, dev, B, H, L, dk, dv, chunk=64, groups=4, in_dtype=BF16,
+                 out_dtype=BF16, flags=0, copy_in=None, compute=None, copy_out=None) -> int
     gla_decode_step(q, k, v, log_alpha, state, out, B, H, dk, dv, stream=None)
     gla_delta_fwd(q, k, v, beta, out, B, H, L, dk, dv, log_alpha=None, init_state=None,
                   final_state=None, out_dtype=BF16, stream=None) -> int
@@ -36,7 +38,7 @@ GLA_OK, GLA_ERR_INVALID, GLA_ERR_UNSUPPORTED, GLA_ERR_MISALIGNED, GLA_ERR_CUDA, 
 BF16, F32 = 0, 1
 FLAG_FEATURE_ELU1, FLAG_NORMALIZE, FLAG_FORCE_SIMT, FLAG_FORCE_CHUNK, FLAG_SCALAR_GATE = 1, 2, 4, 8, 16
 
-EXPORTED = ["gla_fwd", "gla_fwd_ex", "gla_decode_step", "gla_delta_fwd", "gla_bwd", "gla_device_error",
+EXPORTED = ["gla_fwd", "gla_fwd_ex", "gla_fwd_host", "gla_decode_step", "gla_delta_fwd", "gla_bwd", "gla_device_error",
             "gla_device_error_detail", "gla_status_string", "gla_version"]
 
 
@@ -75,6 +77,8 @@ def load(path: str | None = None):
     lib.gla_fwd.restype = i
     lib.gla_fwd_ex.argtypes = [ctypes.POINTER(_FwdArgs), vp]
     lib.gla_fwd_ex.restype = i
+    lib.gla_fwd_host.argtypes = [ctypes.POINTER(_FwdArgs), ctypes.POINTER(_FwdArgs), i, vp, vp, vp]
+    lib.gla_fwd_host.restype = i
     lib.gla_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, vp]
     lib.gla_decode_step.restype = i
     lib.gla_delta_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
@@ -138,6 +142,20 @@ def gla_fwd_ex(q, k, v, out, B, H, L, dk, dv, chunk=64, log_alpha=None, init_sta
                  _ptr(out), _ptr(final_state), _ptr(final_z), B, H, L, dk, dv, chunk, in_dtype,
                  out_dtype, flags)
     return load().gla_fwd_ex(ctypes.byref(a), _stream(stream))
+
+
+def gla_fwd_host(host: dict, dev: dict, B, H, L, dk, dv, chunk=64, groups=4, in_dtype=BF16, out_dtype=BF16,
+                 flags=0, copy_in=None, compute=None, copy_out=None) -> int:
+    """`host` and `dev` map gla_fwd_args field names (q, k, v, log_alpha, init_state, init_z, out,
+    final_state, final_z) to host (pinned) and device tensors; missing names are NULL."""
+    names = ("q", "k", "v", "log_alpha", "init_state", "init_z", "out", "final_state", "final_z")
+
+    def args(m):
+        return _FwdArgs(*(_ptr(m.get(n)) for n in names), B, H, L, dk, dv, chunk, in_dtype, out_dtype, flags)
+
+    ha, da = args(host), args(dev)
+    return load().gla_fwd_host(ctypes.byref(ha), ctypes.byref(da), groups, _stream(copy_in), _stream(compute),
+                               _stream(copy_out))
 
 
 def gla_decode_step(q, k, v, log_alpha, state, out, B, H, dk, dv, stream=None) -> int:

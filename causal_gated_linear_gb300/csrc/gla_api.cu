@@ -154,6 +154,105 @@ int gla_fwd_ex(const gla_fwd_args* a, void* stream) {
     return finish(e, s);
 }
 
+int gla_fwd_host(const gla_fwd_args* host, const gla_fwd_args* dev, int groups, void* copy_in, void* compute,
+                 void* copy_out) {
+    if (!host || !dev || groups < 1) return GLA_ERR_INVALID;
+    int st = validate_prefill(dev);
+    if (st != GLA_OK) return st;
+    if (host->B != dev->B || host->H != dev->H || host->L != dev->L || host->dk != dev->dk || host->dv != dev->dv ||
+        host->chunk != dev->chunk || host->in_dtype != dev->in_dtype || host->out_dtype != dev->out_dtype ||
+        host->flags != dev->flags)
+        return GLA_ERR_INVALID;
+    // every buffer is given on both sides or on neither
+    const void* hp[] = {host->q, host->k, host->v, host->log_alpha, host->init_state, host->init_z,
+                        host->out, host->final_state, host->final_z};
+    const void* dp[] = {dev->q, dev->k, dev->v, dev->log_alpha, dev->init_state, dev->init_z,
+                        dev->out, dev->final_state, dev->final_z};
+    for (int i = 0; i < 9; i++)
+        if ((hp[i] == nullptr) != (dp[i] == nullptr)) return GLA_ERR_INVALID;
+    if (dev->final_state && dev->final_state == dev->init_state) return GLA_ERR_INVALID;  // staged separately
+    if (dev->final_z && dev->final_z == dev->init_z) return GLA_ERR_INVALID;
+    cudaStream_t s_in = static_cast<cudaStream_t>(copy_in), s_c = static_cast<cudaStream_t>(compute),
+                 s_out = static_cast<cudaStream_t>(copy_out);
+    const long BH = (long)dev->B * dev->H;
+    const size_t L = (size_t)dev->L;
+    const size_t es = dev->in_dtype == GLA_DTYPE_F32 ? 4 : 2, eo = dev->out_dtype == GLA_DTYPE_F32 ? 4 : 2;
+    const bool normz = dev->flags & GLA_FLAG_NORMALIZE;
+    // bytes per head of each buffer, in the order of hp / dp
+    const size_t per[] = {L * dev->dk * es, L * dev->dk * es, L * dev->dv * es,
+                          L * ((dev->flags & GLA_FLAG_SCALAR_GATE) ? 1 : dev->dk) * 4, (size_t)dev->dk * dev->dv * 4,
+                          normz ? (size_t)dev->dk * 4 : 0, L * dev->dv * eo, (size_t)dev->dk * dev->dv * 4,
+                          normz ? (size_t)dev->dk * 4 : 0};
+    // group boundaries fall on multiples of `gran` heads, so that every slice of
+    // every buffer starts 16-byte aligned (a head's bytes are a multiple of 2)
+    long gran = 1;
+    for (size_t b : per) {
+        long need = 1;
+        while (b > 0 && (b * need) % 16 != 0) need *= 2;
+        if (need > gran) gran = need;
+    }
+    const long units = (BH + gran - 1) / gran;
+    const int G = (int)(groups < units ? groups : units);
+    cudaEvent_t start_c, start_out;
+    if (cudaEventCreateWithFlags(&start_c, cudaEventDisableTiming) != cudaSuccess) return GLA_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&start_out, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventDestroy(start_c);
+        return GLA_ERR_CUDA;
+    }
+    // inputs are overwritten only after earlier kernels on `compute` have read them, outputs
+    // only after earlier copies on `copy_out` have read them
+    cudaError_t e = cudaEventRecord(start_c, s_c);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s_in, start_c, 0);
+    if (e == cudaSuccess) e = cudaEventRecord(start_out, s_out);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s_c, start_out, 0);
+    cudaEventDestroy(start_c);
+    cudaEventDestroy(start_out);
+    if (e != cudaSuccess) return GLA_ERR_CUDA;
+    for (int g = 0; g < G; g++) {
+        const long u0 = units * g / G, u1 = units * (g + 1) / G;
+        const long h0 = u0 * gran < BH ? u0 * gran : BH, h1 = u1 * gran < BH ? u1 * gran : BH, nh = h1 - h0;
+        const void* hs[9];
+        void* ds[9];
+        for (int i = 0; i < 9; i++) {
+            hs[i] = hp[i] ? static_cast<const char*>(hp[i]) + h0 * per[i] : nullptr;
+            ds[i] = dp[i] ? const_cast<char*>(static_cast<const char*>(dp[i])) + h0 * per[i] : nullptr;
+        }
+        for (int i = 0; i < 6; i++)
+            if (ds[i] && nh * per[i] > 0 &&
+                cudaMemcpyAsync(ds[i], hs[i], nh * per[i], cudaMemcpyHostToDevice, s_in) != cudaSuccess)
+                return GLA_ERR_CUDA;
+        cudaEvent_t landed, done;
+        if (cudaEventCreateWithFlags(&landed, cudaEventDisableTiming) != cudaSuccess) return GLA_ERR_CUDA;
+        e = cudaEventRecord(landed, s_in);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s_c, landed, 0);
+        cudaEventDestroy(landed);
+        if (e != cudaSuccess) return GLA_ERR_CUDA;
+        gla_fwd_args ga = *dev;  // the group's heads as one batch of nh heads
+        ga.B = 1;
+        ga.H = (int)nh;
+        ga.q = ds[0], ga.k = ds[1], ga.v = ds[2];
+        ga.log_alpha = static_cast<const float*>(ds[3]);
+        ga.init_state = static_cast<const float*>(ds[4]);
+        ga.init_z = static_cast<const float*>(ds[5]);
+        ga.out = ds[6];
+        ga.final_state = static_cast<float*>(ds[7]);
+        ga.final_z = static_cast<float*>(ds[8]);
+        st = gla_fwd_ex(&ga, s_c);
+        if (st != GLA_OK) return st;
+        if (cudaEventCreateWithFlags(&done, cudaEventDisableTiming) != cudaSuccess) return GLA_ERR_CUDA;
+        e = cudaEventRecord(done, s_c);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, done, 0);
+        cudaEventDestroy(done);
+        if (e != cudaSuccess) return GLA_ERR_CUDA;
+        for (int i = 6; i < 9; i++)
+            if (ds[i] && nh * per[i] > 0 &&
+                cudaMemcpyAsync(const_cast<void*>(hs[i]), ds[i], nh * per[i], cudaMemcpyDeviceToHost, s_out) !=
+                    cudaSuccess)
+                return GLA_ERR_CUDA;
+    }
+    return finish(cudaSuccess, s_out);
+}
+
 int gla_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* init_state, void* out,
             float* final_state, int B, int H, int L, int dk, int dv, int chunk, void* stream) {
     gla_fwd_args a;

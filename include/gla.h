@@ -116,6 +116,37 @@ typedef struct {
 int gla_fwd_ex(const gla_fwd_args* a, void* stream);
 
 /*
+ * gla_fwd_host -- gla_fwd_ex on host-resident data, with the host<->device
+ * copies overlapped with the computation.  The (batch, head) pairs are
+ * independent problems ("Gated Linear Attention", GLA Recurrent Form: each
+ * head carries its own state), so they are split into `groups` contiguous
+ * groups; group g's inputs are copied host->device on `copy_in`, computed on
+ * `compute` once they have landed, and its outputs copied device->host on
+ * `copy_out` once computed, so the copies of one group overlap the kernels and
+ * the copies of the others.
+ *
+ *   host    gla_fwd_args of HOST pointers (page-locked for the copies to be
+ *           asynchronous): inputs q, k, v, log_alpha, init_state, init_z;
+ *           outputs out, final_state, final_z.
+ *   dev     gla_fwd_args of caller-owned DEVICE buffers with the same shapes
+ *           (the staging area), same B, H, L, dk, dv, chunk, dtypes and flags;
+ *           each buffer given on both sides or on neither; final_state (and
+ *           final_z) must not alias init_state (init_z) here.
+ *   groups  >= 1.  Group boundaries fall on multiples of the smallest head
+ *           count whose bytes in every buffer are a multiple of 16 (so each
+ *           group's slices stay 16-byte aligned); more groups than that allows
+ *           are clamped.
+ * Ordering: the call first makes `copy_in` wait for work already queued on
+ * `compute` and `compute` wait for work already queued on `copy_out`, so
+ * back-to-back calls reuse the staging area safely.  The call returns once
+ * everything is queued; the host outputs are complete when `copy_out` has
+ * drained.  Events it needs are created and released by the call.  Validation
+ * failures return before anything is queued.
+ */
+int gla_fwd_host(const gla_fwd_args* host, const gla_fwd_args* dev, int groups, void* copy_in, void* compute,
+                 void* copy_out);
+
+/*
  * gla_decode_step -- one recurrent step per (sequence, head) ("linear-attention"
  * blog, Linear attention: o_n from S_{n-1}, q_n, k_n, v_n; gate from GLA
  * Recurrent Form).
