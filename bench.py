@@ -375,6 +375,17 @@ def bench_prefill(args, device, rank, world):
 
         e2e_step()
         torch.cuda.synchronize(device)
+        # the host link's own rate on these buffers: one timed copy of v in, one of out back
+        c0, c1, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        with torch.cuda.stream(s_in):
+            c0.record(s_in)
+            dv_.copy_(hv, non_blocking=True)
+            c1.record(s_in)
+            hout.copy_(out, non_blocking=True)
+            c2.record(s_in)
+        torch.cuda.synchronize(device)
+        h2d_gbs = hv.numel() * hv.element_size() / (c0.elapsed_time(c1) / 1e3) / 1e9
+        d2h_gbs = hout.numel() * hout.element_size() / (c1.elapsed_time(c2) / 1e3) / 1e9
         ne = max(1, min(args.steps, 3))
         barrier(world)
         torch.cuda.synchronize(device)
@@ -386,7 +397,8 @@ def bench_prefill(args, device, rank, world):
         torch.cuda.synchronize(device)
         gla.check(gla.gla_device_error(s_out))
         e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
-        res["e2e"] = dict(ms_per_step=e_ms / ne, h2d=h2d, d2h=d2h, groups=args.e2e_groups)
+        res["e2e"] = dict(ms_per_step=e_ms / ne, h2d=h2d, d2h=d2h, groups=args.e2e_groups, h2d_gbs=h2d_gbs,
+                          d2h_gbs=d2h_gbs)
         del hq, hk, hv, hla, hs0, hout, hfs, dq, dk_, dv_, dla, ds0, host, devb
     del q, k, v, la, s0, out, fs
     torch.cuda.empty_cache()
@@ -635,7 +647,9 @@ def run_gla(args):
         e = pre["e2e"]
         line["e2e"] = {"value": tokens * world / (e["ms_per_step"] / 1e3), "unit": "tokens/s",
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
-                       "ms_per_step": e["ms_per_step"], "api": "gla_fwd_host", "head_groups": e["groups"]}
+                       "ms_per_step": e["ms_per_step"], "api": "gla_fwd_host", "head_groups": e["groups"],
+                       "link": {"h2d_gbs": e["h2d_gbs"], "d2h_gbs": e["d2h_gbs"],
+                                "h2d_floor_ms": e["h2d"] / e["h2d_gbs"] / 1e6}}
     if rank == 0 and world == 1 and args.cpu_baseline:
         tps, cores, desc, dt = oracle_sample(args.ref_seconds)
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
