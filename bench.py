@@ -24,6 +24,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -35,7 +36,7 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 METRIC = ("GLA prefill tokens/s & % bf16 tensor peak; decode-step state HBM GB/s (1×GB300)")
-PREFILL = synth.CONFIGS[3]
+HEADLINE = synth.LONGCTX
 DEC = synth.DECODE
 C = 64
 
@@ -137,7 +138,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        # raw samples go to $GLA_BENCH_CLOCKS_DIR (default: the system temp directory)
+        d = os.environ.get("GLA_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(d, f"clocks_bench_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
@@ -223,21 +226,21 @@ def oracle_sample(seconds_target: float = 10.0):
     """
     import oracle
     cores = max(1, oracle.max_threads())
-    nh = min(PREFILL.H, max(1, cores))
+    nh = min(HEADLINE.H, max(1, cores))
     Ls = 256
     # grow the sample until it takes a noticeable fraction of the target
     while True:
-        w = synth.with_shape(PREFILL, B=1, H=nh, L=Ls)
+        w = synth.with_shape(HEADLINE, B=1, H=nh, L=Ls)
         x = synth.make_prefill(w, heads=list(range(nh)))
         args = [synth.as_f64(x[n]) for n in ("q", "k", "v", "log_alpha", "init_state")]
         t0 = time.perf_counter()
         oracle.gla_fwd(*args, nthreads=cores)
         dt = time.perf_counter() - t0
-        if dt >= seconds_target / 4 or Ls >= PREFILL.L:
+        if dt >= seconds_target / 4 or Ls >= HEADLINE.L:
             break
-        Ls = min(PREFILL.L, Ls * max(2, int(math.ceil(seconds_target / 4 / max(dt, 1e-3)))))
+        Ls = min(HEADLINE.L, Ls * max(2, int(math.ceil(seconds_target / 4 / max(dt, 1e-3)))))
     token_heads_per_s = nh * Ls / dt
-    tps = token_heads_per_s / (PREFILL.B * PREFILL.H)   # tokens/s of the B*H workload
+    tps = token_heads_per_s / (HEADLINE.B * HEADLINE.H)   # tokens/s of the B*H workload
     desc = f"{nh} heads x {Ls} tokens of the B1 H32 L65536 dk128 dv256 workload, fp64, {cores} threads"
     return tps, cores, desc, dt
 
@@ -257,8 +260,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": PREFILL.name, "B": PREFILL.B, "H": PREFILL.H, "L": PREFILL.L,
-                   "dk": PREFILL.dk, "dv": PREFILL.dv, "chunk": C},
+        "config": {"workload": HEADLINE.name, "B": HEADLINE.B, "H": HEADLINE.H, "L": HEADLINE.L,
+                   "dk": HEADLINE.dk, "dv": HEADLINE.dv, "chunk": C},
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -281,9 +284,9 @@ def bench_prefill(args, device, rank, world):
     import torch
 
     import causal_gated_linear_gb300 as gla
-    w = synth.with_shape(PREFILL, seed=PREFILL.seed + 1000 * rank)
+    w = synth.with_shape(HEADLINE, seed=HEADLINE.seed + 1000 * rank)
     if args.L:  # reduced sequence length (profiling a small case); the line names it
-        w = synth.with_shape(w, L=args.L, name=f"{PREFILL.name}_L{args.L}")
+        w = synth.with_shape(w, L=args.L, name=f"{HEADLINE.name}_L{args.L}")
     x = synth.make_prefill(w)
     BH = w.B * w.H
     q, k, v = (to_dev(x[n], device) for n in ("q", "k", "v"))

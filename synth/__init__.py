@@ -153,15 +153,18 @@ class Workload:
     extra: dict = field(default_factory=dict)
 
 
-CONFIGS = {
-    0: Workload("gla_fp32_B1H1L256d32", 1, 1, 256, 32, 32, dtype="f32",
-                gate_mean=3.0, gate_std=1.0, gate_temp=1.0, seed=BASE_SEED + 0),
-    1: Workload("linattn_elu1_norm_B4H8L2048d64", 4, 8, 2048, 64, 64, gate=False,
-                qk_scale=False, feature_elu1=True, normalize=True, seed=BASE_SEED + 1),
-    2: Workload("gla_prefill_B8H16L4096d128", 8, 16, 4096, 128, 128, seed=BASE_SEED + 2),
-    3: Workload("gla_longctx_B1H32L65536dk128dv256", 1, 32, 65536, 128, 256,
-                init_std=0.1, seed=BASE_SEED + 3),
-}
+# fp32 SIMT path: B1 H1 L256 dk = dv = 32, gate logsigmoid(N(3, 1))
+FP32_SMALL = Workload("gla_fp32_B1H1L256d32", 1, 1, 256, 32, 32, dtype="f32",
+                      gate_mean=3.0, gate_std=1.0, gate_temp=1.0, seed=BASE_SEED + 0)
+# plain causal linear attention with phi = elu + 1 and the normaliser: B4 H8 L2048 d64
+ELU_NORM = Workload("linattn_elu1_norm_B4H8L2048d64", 4, 8, 2048, 64, 64, gate=False,
+                    qk_scale=False, feature_elu1=True, normalize=True, seed=BASE_SEED + 1)
+# gated prefill: B8 H16 L4096 dk = dv = 128, bf16
+PREFILL = Workload("gla_prefill_B8H16L4096d128", 8, 16, 4096, 128, 128, seed=BASE_SEED + 2)
+# long-context gated prefill with an initial state: B1 H32 L65536 dk128 dv256, bf16
+LONGCTX = Workload("gla_longctx_B1H32L65536dk128dv256", 1, 32, 65536, 128, 256,
+                   init_std=0.1, seed=BASE_SEED + 3)
+PREFILL_WORKLOADS = (FP32_SMALL, ELU_NORM, PREFILL, LONGCTX)
 
 # several new tokens per sequence on top of a decode-sized state (the prefill -> decode
 # hand-off): decode distributions (q, k, v ~ N(0,1), log alpha = logsigmoid(N(4, 1.5)),
@@ -240,8 +243,8 @@ def gate_log_alpha(w: Workload, heads=None):
     return to_f32(log_sigmoid(g) / w.gate_temp).reshape(shp)
 
 
-# delta-rule workload: the config-2 shape; q and k rows of unit length, v ~ N(0,1),
-# beta = sigmoid(N(0,1)) per token, the config-2 gate (logsigmoid(N(4, 1.5)) / 16)
+# delta-rule workload: the B8 H16 L4096 d128 prefill shape; q and k rows of unit length,
+# v ~ N(0,1), beta = sigmoid(N(0,1)) per token, the prefill gate (logsigmoid(N(4, 1.5)) / 16)
 DELTA = Workload("gla_delta_B8H16L4096d128", 8, 16, 4096, 128, 128, qk_scale=False,
                  seed=BASE_SEED + 6)
 
@@ -267,7 +270,7 @@ def make_delta(w: Workload, heads=None):
     return x
 
 
-# backward workload: the config-2 prefill (B8 H16 L4096 dk = dv = 128, bf16, its gate
+# backward workload: the gated prefill (B8 H16 L4096 dk = dv = 128, bf16, its gate
 # and q/k scale) with an output gradient dout ~ N(0, 1) per element
 BWD = Workload("gla_bwd_B8H16L4096d128", 8, 16, 4096, 128, 128, seed=BASE_SEED + 7)
 

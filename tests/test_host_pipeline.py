@@ -57,7 +57,7 @@ def _np(t):
 @pytest.mark.parametrize("groups", [1, 3, 8, 1000])
 def test_host_pipeline_equals_device_call(groups):
     import torch
-    w = synth.with_shape(synth.CONFIGS[2], B=2, H=3, L=200, init_std=0.1)
+    w = synth.with_shape(synth.PREFILL, B=2, H=3, L=200, init_std=0.1)
     x = synth.make_prefill(w)
     st, host, _, _ = run_host(w, x, groups)
     gla.check(st)
@@ -73,14 +73,14 @@ def test_host_pipeline_variants(case):
     import torch
     z0 = None
     if case == "scalar_gate":
-        w = synth.with_shape(synth.CONFIGS[2], B=1, H=4, L=130, scalar_gate=True, init_std=0.1)
+        w = synth.with_shape(synth.PREFILL, B=1, H=4, L=130, scalar_gate=True, init_std=0.1)
     elif case == "elu_norm":
-        w = synth.with_shape(synth.CONFIGS[1], B=2, H=2, L=100)
+        w = synth.with_shape(synth.ELU_NORM, B=2, H=2, L=100)
         z0 = np.abs(synth.to_f32(synth.normals(5, 9, (2 * 2 * 64,)))).reshape(2, 2, 64)
     elif case == "fp32":
-        w = synth.with_shape(synth.CONFIGS[0], B=1, H=3, L=70, init_std=0.1)
+        w = synth.with_shape(synth.FP32_SMALL, B=1, H=3, L=70, init_std=0.1)
     else:
-        w = synth.with_shape(synth.CONFIGS[2], B=2, H=4, L=8, init_std=0.1)
+        w = synth.with_shape(synth.PREFILL, B=2, H=4, L=8, init_std=0.1)
     x = synth.make_prefill(w)
     st, host, _, _ = run_host(w, x, 3, init_z=z0, final_z=w.normalize)
     gla.check(st)
@@ -98,7 +98,7 @@ def test_host_pipeline_back_to_back_reuses_staging():
     staging buffers and streams, with different inputs: each host output
     matches its own inputs."""
     import torch
-    w = synth.with_shape(synth.CONFIGS[2], B=1, H=6, L=300, init_std=0.1)
+    w = synth.with_shape(synth.PREFILL, B=1, H=6, L=300, init_std=0.1)
     xa = synth.make_prefill(w)
     xb = synth.make_prefill(synth.with_shape(w, seed=w.seed + 1))
     st, ha, dev, s = run_host(w, xa, 4)
@@ -119,7 +119,7 @@ def test_host_pipeline_back_to_back_reuses_staging():
 
 def test_host_pipeline_rejects_bad_calls():
     import torch
-    w = synth.with_shape(synth.CONFIGS[2], B=1, H=2, L=64, init_std=0.1)
+    w = synth.with_shape(synth.PREFILL, B=1, H=2, L=64, init_std=0.1)
     x = synth.make_prefill(w)
     host = dict(q=_host(x["q"]), k=_host(x["k"]), v=_host(x["v"]), log_alpha=_host(x["log_alpha"]),
                 init_state=_host(x["init_state"]),

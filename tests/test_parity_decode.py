@@ -50,7 +50,7 @@ def test_decode_no_gate():
     assert rel_l2(out.cpu().numpy(), ro) <= DEC_REL and rel_l2(st.cpu().numpy(), rs) <= DEC_REL
 
 
-def test_config4_full_1024_steps_sampled():
+def test_decode_full_1024_steps_sampled():
     """Full decode workload: 256 x 32 heads, 1024 steps; every step's output is
     checked on a sample of heads, and the final state on the same sample."""
     import torch
@@ -79,7 +79,7 @@ def test_config4_full_1024_steps_sampled():
 def test_decode_steps_equal_prefill():
     """N decode steps from an initial state reproduce the prefill of the same N tokens."""
     import torch
-    w = synth.with_shape(synth.CONFIGS[2], B=1, H=2, L=40, init_std=0.1, seed=81)
+    w = synth.with_shape(synth.PREFILL, B=1, H=2, L=40, init_std=0.1, seed=81)
     x = synth.make_prefill(w)
     o, s, _ = run_prefill(w, x, out_f32=True)
     st = to_dev(x["init_state"]).clone()

@@ -20,13 +20,13 @@ def _lib():
 
 
 def _cfg(base, **kw):
-    return synth.with_shape(synth.CONFIGS[base], **kw)
+    return synth.with_shape(base, **kw)
 
 
 # ------------------------------------------------------------------ fp32 SIMT path
 
-def test_config0_fp32_full():
-    w = synth.CONFIGS[0]
+def test_fp32_small_full():
+    w = synth.FP32_SMALL
     x = synth.make_prefill(w)
     o, s, _ = run_prefill(w, x)
     ro, rs, _ = oracle_prefill(w, x)
@@ -36,7 +36,7 @@ def test_config0_fp32_full():
 
 @pytest.mark.parametrize("L,dk,dv", [(1, 32, 32), (63, 16, 48), (130, 64, 40), (65, 200, 24)])
 def test_simt_fp32_shapes(L, dk, dv):
-    w = _cfg(0, B=2, H=2, L=L, dk=dk, dv=dv, seed=11 + L)
+    w = _cfg(synth.FP32_SMALL, B=2, H=2, L=L, dk=dk, dv=dv, seed=11 + L)
     x = synth.make_prefill(w)
     o, s, _ = run_prefill(w, x)
     ro, rs, _ = oracle_prefill(w, x)
@@ -45,7 +45,7 @@ def test_simt_fp32_shapes(L, dk, dv):
 
 @pytest.mark.parametrize("L,dk,dv", [(100, 32, 32), (257, 128, 96)])
 def test_simt_bf16_forced(L, dk, dv):
-    w = _cfg(2, B=1, H=3, L=L, dk=dk, dv=dv, init_std=0.1, seed=5 + L)
+    w = _cfg(synth.PREFILL, B=1, H=3, L=L, dk=dk, dv=dv, init_std=0.1, seed=5 + L)
     x = synth.make_prefill(w)
     o, s, _ = run_prefill(w, x, force_simt=True)
     ro, rs, _ = oracle_prefill(w, x)
@@ -69,7 +69,7 @@ TC_SHAPES = [
 
 @pytest.mark.parametrize("B,H,L,dk,dv,gate,init", TC_SHAPES)
 def test_tc_shapes(B, H, L, dk, dv, gate, init):
-    w = _cfg(2, B=B, H=H, L=L, dk=dk, dv=dv, gate=gate, init_std=0.1 if init else 0.0,
+    w = _cfg(synth.PREFILL, B=B, H=H, L=L, dk=dk, dv=dv, gate=gate, init_std=0.1 if init else 0.0,
              seed=100 + L + dk + dv)
     x = synth.make_prefill(w)
     # short sequences go to the token-by-token path unless the chunk kernel is forced
@@ -88,7 +88,7 @@ def test_tc_shapes(B, H, L, dk, dv, gate, init):
 def test_tc_both_tile_widths(monkeypatch, dvt, B, H, L, dk, dv, gate, init):
     """The 64- and 128-column value tiles (M = 64 / M = 128 MMAs) give the same parity."""
     monkeypatch.setenv("GLA_TC_DVT", dvt)
-    w = _cfg(2, B=B, H=H, L=L, dk=dk, dv=dv, gate=gate, init_std=0.1 if init else 0.0,
+    w = _cfg(synth.PREFILL, B=B, H=H, L=L, dk=dk, dv=dv, gate=gate, init_std=0.1 if init else 0.0,
              seed=200 + L + dk + dv)
     x = synth.make_prefill(w)
     o, s, _ = run_prefill(w, x)
@@ -98,7 +98,7 @@ def test_tc_both_tile_widths(monkeypatch, dvt, B, H, L, dk, dv, gate, init):
 
 
 def test_tc_fp32_output():
-    w = _cfg(2, B=1, H=2, L=300, init_std=0.1, seed=77)
+    w = _cfg(synth.PREFILL, B=1, H=2, L=300, init_std=0.1, seed=77)
     x = synth.make_prefill(w)
     o, s, _ = run_prefill(w, x, out_f32=True)
     ro, rs, _ = oracle_prefill(w, x)
@@ -108,7 +108,7 @@ def test_tc_fp32_output():
 
 def test_tc_strong_decay_and_long_chunks():
     """log alpha = logsigmoid(N(3,1)) without temperature: |b_C| reaches ~9 per chunk."""
-    w = _cfg(2, B=1, H=2, L=256, dk=64, dv=64, gate_mean=3.0, gate_std=1.0, gate_temp=1.0, seed=9)
+    w = _cfg(synth.PREFILL, B=1, H=2, L=256, dk=64, dv=64, gate_mean=3.0, gate_std=1.0, gate_temp=1.0, seed=9)
     x = synth.make_prefill(w)
     o, s, _ = run_prefill(w, x)
     ro, rs, _ = oracle_prefill(w, x)
@@ -116,8 +116,8 @@ def test_tc_strong_decay_and_long_chunks():
     assert_bf16_close(s, rs, "state")
 
 
-def test_config1_normalised_full():
-    w = synth.CONFIGS[1]
+def test_elu_norm_full():
+    w = synth.ELU_NORM
     x = synth.make_prefill(w)
     o, s, z = run_prefill(w, x, final_z=True)
     ro, rs, rz = oracle_prefill(w, x)
@@ -125,15 +125,15 @@ def test_config1_normalised_full():
     assert rel_l2(s, rs) <= 1e-2 and rel_l2(z, rz) <= 1e-2
 
 
-def test_config1_normalised_tail_and_resume():
-    w = _cfg(1, B=1, H=2, L=150, seed=31)
+def test_elu_norm_tail_and_resume():
+    w = _cfg(synth.ELU_NORM, B=1, H=2, L=150, seed=31)
     x = synth.make_prefill(w)
     o, s, z = run_prefill(w, x, final_z=True)
     ro, rs, rz = oracle_prefill(w, x)
     assert_bf16_close(o, ro, "out")
     assert rel_l2(z, rz) <= 1e-2, rel_l2(z, rz)
     # resume from (S, z) on a second segment
-    w2 = _cfg(1, B=1, H=2, L=70, seed=32)
+    w2 = _cfg(synth.ELU_NORM, B=1, H=2, L=70, seed=32)
     x2 = synth.make_prefill(w2)
     x2["init_state"] = s.astype(np.float32)
     o2, _, _ = run_prefill(w2, x2, init_z=z.astype(np.float32))
@@ -141,8 +141,8 @@ def test_config1_normalised_tail_and_resume():
     assert_bf16_close(o2, ro2, "resumed out")
 
 
-def test_config2_full_sampled():
-    w = synth.CONFIGS[2]
+def test_prefill_full_sampled():
+    w = synth.PREFILL
     x = synth.make_prefill(w)
     o, s, _ = run_prefill(w, x)
     heads = [0, 37, 64, 127]
@@ -154,9 +154,9 @@ def test_config2_full_sampled():
     assert_bf16_close(s, rs, "state")
 
 
-def test_config3_full_sampled():
+def test_longctx_full_sampled():
     import torch
-    w = synth.CONFIGS[3]
+    w = synth.LONGCTX
     x = synth.make_prefill(w)
     q, k, v = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"])
     la, s0 = to_dev(x["log_alpha"]), to_dev(x["init_state"])
@@ -178,14 +178,14 @@ def test_config3_full_sampled():
 # ------------------------------------------------------------------ properties
 
 def test_split_resume_on_gpu():
-    w = _cfg(2, B=1, H=2, L=300, init_std=0.1, seed=41)
+    w = _cfg(synth.PREFILL, B=1, H=2, L=300, init_std=0.1, seed=41)
     x = synth.make_prefill(w)
     o, s, _ = run_prefill(w, x)
     for L1 in (128, 77):
-        w1 = _cfg(2, B=1, H=2, L=L1)
+        w1 = _cfg(synth.PREFILL, B=1, H=2, L=L1)
         x1 = {kk: (vv[:, :, :L1] if kk in ("q", "k", "v", "log_alpha") else vv) for kk, vv in x.items()}
         o1, s1, _ = run_prefill(w1, x1)
-        w2 = _cfg(2, B=1, H=2, L=300 - L1)
+        w2 = _cfg(synth.PREFILL, B=1, H=2, L=300 - L1)
         x2 = {kk: (vv[:, :, L1:] if kk in ("q", "k", "v", "log_alpha") else vv) for kk, vv in x.items()}
         x2["init_state"] = s1.astype(np.float32)
         o2, s2, _ = run_prefill(w2, x2)
@@ -194,7 +194,7 @@ def test_split_resume_on_gpu():
 
 
 def test_deterministic_bitwise():
-    w = _cfg(2, B=2, H=2, L=333, init_std=0.1, seed=51)
+    w = _cfg(synth.PREFILL, B=2, H=2, L=333, init_std=0.1, seed=51)
     x = synth.make_prefill(w)
     a = run_prefill(w, x)
     b = run_prefill(w, x)
@@ -203,7 +203,7 @@ def test_deterministic_bitwise():
 
 def test_final_state_may_alias_initial_state():
     import torch
-    w = _cfg(2, B=1, H=2, L=100, init_std=0.1, seed=61)
+    w = _cfg(synth.PREFILL, B=1, H=2, L=100, init_std=0.1, seed=61)
     x = synth.make_prefill(w)
     ro, rs, _ = oracle_prefill(w, x)
     q, k, v, la = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"]), to_dev(x["log_alpha"])
@@ -229,7 +229,7 @@ def test_empty_sequence_copies_state():
 
 def test_no_gate_matches_cumsum_closed_form():
     """alpha == 1 on the GPU: the final state equals K^T V in fp64 (closed form)."""
-    w = _cfg(2, B=1, H=2, L=192, gate=False, seed=71)
+    w = _cfg(synth.PREFILL, B=1, H=2, L=192, gate=False, seed=71)
     x = synth.make_prefill(w)
     _, s, _ = run_prefill(w, x)
     k = synth.as_f64(x["k"]).reshape(2, 192, 128)

@@ -19,7 +19,7 @@ def _lib():
 
 
 def _w(base, **kw):
-    return synth.with_shape(synth.CONFIGS[base], scalar_gate=True, **kw)
+    return synth.with_shape(base, scalar_gate=True, **kw)
 
 
 @pytest.mark.parametrize("dvt", ["64", "128"])
@@ -32,7 +32,7 @@ def _w(base, **kw):
 ])
 def test_scalar_gate_tc(monkeypatch, dvt, B, H, L, dk, dv, init):
     monkeypatch.setenv("GLA_TC_DVT", dvt)
-    w = _w(2, B=B, H=H, L=L, dk=dk, dv=dv, init_std=0.1 if init else 0.0, seed=300 + L + dk + dv)
+    w = _w(synth.PREFILL, B=B, H=H, L=L, dk=dk, dv=dv, init_std=0.1 if init else 0.0, seed=300 + L + dk + dv)
     x = synth.make_prefill(w)
     o, s, _ = run_prefill(w, x, flags=gla.FLAG_FORCE_CHUNK)
     ro, rs, _ = oracle_prefill(w, x)
@@ -42,7 +42,7 @@ def test_scalar_gate_tc(monkeypatch, dvt, B, H, L, dk, dv, init):
 
 def test_scalar_gate_strong_decay():
     """log gamma = logsigmoid(N(3,1)) without temperature: ~ -0.05 per token, -3 per chunk."""
-    w = _w(2, B=1, H=2, L=256, dk=64, dv=64, gate_mean=3.0, gate_std=1.0, gate_temp=1.0, seed=17)
+    w = _w(synth.PREFILL, B=1, H=2, L=256, dk=64, dv=64, gate_mean=3.0, gate_std=1.0, gate_temp=1.0, seed=17)
     x = synth.make_prefill(w)
     o, s, _ = run_prefill(w, x)
     ro, rs, _ = oracle_prefill(w, x)
@@ -52,7 +52,7 @@ def test_scalar_gate_strong_decay():
 
 def test_scalar_gate_ragged_length_runs_simt():
     """L % 4 != 0: the per-token gate's rows are not 16-byte aligned for TMA; the SIMT kernel runs."""
-    w = _w(2, B=1, H=2, L=130, init_std=0.1, seed=19)
+    w = _w(synth.PREFILL, B=1, H=2, L=130, init_std=0.1, seed=19)
     x = synth.make_prefill(w)
     o, s, _ = run_prefill(w, x)
     ro, rs, _ = oracle_prefill(w, x)
@@ -61,7 +61,7 @@ def test_scalar_gate_ragged_length_runs_simt():
 
 
 def test_scalar_gate_fp32_inputs():
-    w = _w(0, B=2, H=2, L=100, seed=21)
+    w = _w(synth.FP32_SMALL, B=2, H=2, L=100, seed=21)
     x = synth.make_prefill(w)
     o, s, _ = run_prefill(w, x)
     ro, rs, _ = oracle_prefill(w, x)
@@ -80,7 +80,7 @@ def test_scalar_gate_equals_broadcast_channel_gate():
     """The per-token gate and the per-channel gate holding the same value on every channel run
     through their own kernel variants and give the same result (bf16 bar)."""
     import numpy as np
-    w = _w(2, B=1, H=2, L=192, init_std=0.1, seed=25)
+    w = _w(synth.PREFILL, B=1, H=2, L=192, init_std=0.1, seed=25)
     x = synth.make_prefill(w)
     o1, s1, _ = run_prefill(w, x)
     w2 = synth.with_shape(w, scalar_gate=False)
@@ -94,7 +94,7 @@ def test_scalar_gate_equals_broadcast_channel_gate():
 def test_scalar_gate_long_context_sampled():
     """Long-context shape (B1 H32 L65536 dk128 dv256, nonzero initial state), sampled heads."""
     import torch
-    w = _w(3, seed=synth.CONFIGS[3].seed + 50)
+    w = _w(synth.LONGCTX, seed=synth.LONGCTX.seed + 50)
     x = synth.make_prefill(w)
     q, k, v = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"])
     la, s0 = to_dev(x["log_alpha"]), to_dev(x["init_state"])

@@ -47,7 +47,7 @@ def test_short_bf16_out():
     # prefill-config distributions (q, k scaled by dk^-1/2, log alpha / 16): outputs of order 1,
     # the scale the bf16 bar (max-abs 5e-2) is stated for; decode-style unscaled inputs give
     # outputs near 100, where rounding the output to bf16 alone moves it by ~0.4
-    w = synth.with_shape(synth.CONFIGS[2], B=2, H=4, L=11, init_std=0.1, seed=3)
+    w = synth.with_shape(synth.PREFILL, B=2, H=4, L=11, init_std=0.1, seed=3)
     x = synth.make_prefill(w)
     o, s, _ = run_prefill(w, x)
     ro, rs, _ = oracle_prefill(w, x)
@@ -78,7 +78,7 @@ def test_short_equals_decode_steps():
 def test_short_matches_chunk_kernel():
     """The same call forced through the chunk kernel agrees within the bf16 bar (prefill-config
     distributions, outputs of order 1 as the bar assumes)."""
-    w = synth.with_shape(synth.CONFIGS[3], B=2, H=2, L=16, seed=7)
+    w = synth.with_shape(synth.LONGCTX, B=2, H=2, L=16, seed=7)
     x = synth.make_prefill(w)
     o1, s1, _ = run_prefill(w, x, out_f32=True)
     o2, s2, _ = run_prefill(w, x, out_f32=True, flags=gla.FLAG_FORCE_CHUNK)

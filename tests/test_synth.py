@@ -35,7 +35,7 @@ def test_bf16_rounding_ties_to_even():
 
 
 def test_head_sampling_matches_full_tensors():
-    w = synth.with_shape(synth.CONFIGS[3], B=1, H=4, L=96, init_std=0.1)
+    w = synth.with_shape(synth.LONGCTX, B=1, H=4, L=96, init_std=0.1)
     full = synth.make_prefill(w)
     part = synth.make_prefill(w, heads=[1, 3])
     for name in ("q", "k", "v", "log_alpha"):
@@ -45,7 +45,7 @@ def test_head_sampling_matches_full_tensors():
 
 
 def test_log_alpha_recipe_range():
-    w = synth.with_shape(synth.CONFIGS[2], B=1, H=2, L=256)
+    w = synth.with_shape(synth.PREFILL, B=1, H=2, L=256)
     x = synth.make_prefill(w)
     la = x["log_alpha"]
     assert la.dtype == np.float32 and np.all(la < 0) and np.all(la > -1.0)
