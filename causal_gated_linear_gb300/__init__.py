@@ -18,7 +18,7 @@ The functions mirror the C entry points:
     gla_delta_fwd(q, k, v, beta, out, B, H, L, dk, dv, log_alpha=None, init_state=None,
                   final_state=None, out_dtype=BF16, stream=None) -> int
     gla_bwd(q, k, v, dout, dq, dk, dv, B, H, L, dk_dim, dv_dim, log_alpha=None, init_state=None,
-            dfinal=None, dlog_alpha=None, dinit=None, in_dtype=BF16, stream=None) -> int
+            dfinal=None, dlog_alpha=None, dinit=None, in_dtype=BF16, flags=0, stream=None) -> int
     gla_device_error(stream=None) -> int
     gla_status_string(status) -> str
     gla_version() -> str
@@ -83,7 +83,7 @@ def load(path: str | None = None):
     lib.gla_decode_step.restype = i
     lib.gla_delta_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
     lib.gla_delta_fwd.restype = i
-    lib.gla_bwd.argtypes = [vp] * 12 + [i] * 6 + [vp]
+    lib.gla_bwd.argtypes = [vp] * 12 + [i] * 6 + [ctypes.c_uint, vp]
     lib.gla_bwd.restype = i
     lib.gla_device_error.argtypes = [vp]
     lib.gla_device_error.restype = i
@@ -170,10 +170,10 @@ def gla_delta_fwd(q, k, v, beta, out, B, H, L, dk, dv, log_alpha=None, init_stat
 
 
 def gla_bwd(q, k, v, dout, dq, dk, dv, B, H, L, dk_dim, dv_dim, log_alpha=None, init_state=None, dfinal=None,
-            dlog_alpha=None, dinit=None, in_dtype=BF16, stream=None) -> int:
+            dlog_alpha=None, dinit=None, in_dtype=BF16, flags=0, stream=None) -> int:
     return load().gla_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(init_state), _ptr(dout), _ptr(dfinal),
                           _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dlog_alpha), _ptr(dinit), B, H, L, dk_dim, dv_dim,
-                          in_dtype, _stream(stream))
+                          in_dtype, flags, _stream(stream))
 
 
 def gla_device_error(stream=None) -> int:

@@ -354,9 +354,11 @@ int gla_delta_fwd(const void* q, const void* k, const void* v, const float* beta
 
 int gla_bwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* init_state,
             const void* dout, const float* dfinal, float* dq, float* dk_out, float* dv_out, float* dlog_alpha,
-            float* dinit, int B, int H, int L, int dk, int dv, int in_dtype, void* stream) {
+            float* dinit, int B, int H, int L, int dk, int dv, int in_dtype, unsigned flags, void* stream) {
     if (B < 1 || H < 1 || L < 0 || dk < 1 || dv < 1) return GLA_ERR_INVALID;
     if (in_dtype != GLA_DTYPE_BF16 && in_dtype != GLA_DTYPE_F32) return GLA_ERR_INVALID;
+    if (flags & ~(unsigned)GLA_FLAG_SCALAR_GATE) return GLA_ERR_INVALID;
+    const bool scalar = flags & GLA_FLAG_SCALAR_GATE;
     if (L > 0 && (!q || !k || !v || !dout || !dq || !dk_out || !dv_out)) return GLA_ERR_INVALID;
     if (dlog_alpha && !log_alpha) return GLA_ERR_INVALID;
     if (!bwd_supported(dk, dv)) return GLA_ERR_UNSUPPORTED;
@@ -365,11 +367,11 @@ int gla_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return GLA_ERR_MISALIGNED;
     const size_t BH = (size_t)B * H, Ls = (size_t)L, es = in_dtype == GLA_DTYPE_F32 ? 4 : 2;
-    const size_t nk = BH * Ls * dk, nv = BH * Ls * dv, ns = BH * dk * dv * 4;
+    const size_t nk = BH * Ls * dk, nv = BH * Ls * dv, ns = BH * dk * dv * 4, nla = scalar ? BH * Ls : nk;
     const void* in_p[] = {q, k, v, dout, log_alpha, init_state, dfinal};
-    const size_t in_n[] = {nk * es, nk * es, nv * es, nv * es, nk * 4, ns, ns};
+    const size_t in_n[] = {nk * es, nk * es, nv * es, nv * es, nla * 4, ns, ns};
     const void* out_p[] = {dq, dk_out, dv_out, dlog_alpha, dinit};
-    const size_t out_n[] = {nk * 4, nk * 4, nv * 4, nk * 4, ns};
+    const size_t out_n[] = {nk * 4, nk * 4, nv * 4, nla * 4, ns};
     for (int o = 0; o < 5; o++) {
         for (int i = 0; i < 7; i++)
             if (overlaps(out_p[o], out_n[o], in_p[i], in_n[i])) return GLA_ERR_INVALID;
@@ -403,6 +405,9 @@ int gla_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
     a.dk = dk;
     a.dv = dv;
     a.in_dtype = in_dtype;
+    a.flags = flags;
+    // a per-token gate's gradient is accumulated across the row blocks of a head
+    if (scalar && dlog_alpha && cudaMemsetAsync(dlog_alpha, 0, nla * 4, s) != cudaSuccess) return GLA_ERR_CUDA;
     return finish(launch_bwd(a, s), s);
 }
 

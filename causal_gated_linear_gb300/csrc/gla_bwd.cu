@@ -188,7 +188,9 @@ __device__ __forceinline__ void rows_body(const BwdArgs& a, float* sm, long bh, 
     const T* k = static_cast<const T*>(a.k) + bh * (long)L * dk;
     const T* v = static_cast<const T*>(a.v) + bh * (long)L * DV;
     const T* dout = static_cast<const T*>(a.dout) + bh * (long)L * DV;
-    const float* la = GATE ? a.log_alpha + bh * (long)L * dk : nullptr;
+    // per-channel gate [L][dk]; per-token gate (GLA_FLAG_SCALAR_GATE) [L], shared by all rows
+    const bool scalar = a.flags & GLA_FLAG_SCALAR_GATE;
+    const float* la = GATE ? a.log_alpha + bh * (long)L * (scalar ? 1 : dk) : nullptr;
     float* dq = a.dq + bh * (long)L * dk;
 
     T rv[St::NW], rd[St::NW], rk[St::NN], rq[St::NN];
@@ -211,7 +213,7 @@ __device__ __forceinline__ void rows_body(const BwdArgs& a, float* sm, long bh, 
             if (t < n && i < nrows) {
                 const long g = (long)(t0 + t) * dk + row0 + i;
                 rk[m] = k[g];
-                if (GATE) ra[m] = la[g];
+                if (GATE) ra[m] = scalar ? la[t0 + t] : la[g];
                 if (rev) {
                     rq[m] = q[g];
                     if (GATE) rdq[m] = dq[g];
@@ -347,7 +349,7 @@ __device__ __forceinline__ void rows_body(const BwdArgs& a, float* sm, long bh, 
 
     // reverse sweep: G_t = G + q_t dout_t^T, dk_t = G_t v_t, the gate gradient, G <- Diag(alpha_t) G_t
     float* dkp = a.dk_out + bh * (long)L * dk;
-    float* dla = GATE && a.dlog_alpha ? a.dlog_alpha + bh * (long)L * dk : nullptr;
+    float* dla = GATE && a.dlog_alpha ? a.dlog_alpha + bh * (long)L * (scalar ? 1 : dk) : nullptr;
     {
         const int nr = (L + kTB - 1) / kTB;
         int t0;
@@ -414,7 +416,16 @@ __device__ __forceinline__ void rows_body(const BwdArgs& a, float* sm, long bh, 
                             if (tb_l + d < kRB) s += o2;
                         }
                         const float total = __shfl_sync(0xffffffffu, s, lane & 3);  // the batch's first token
-                        if (dla && ok) dla[o] = s + carry;
+                        if (!scalar) {
+                            if (dla && ok) dla[o] = s + carry;
+                        } else if (dla) {
+                            // a per-token gate's gradient is the sum over all rows: this warp's four
+                            // rows here (lanes 4 tb + {0..3}), the row blocks through atomics
+                            float g4 = s + carry;
+                            g4 += __shfl_xor_sync(0xffffffffu, g4, 1);
+                            g4 += __shfl_xor_sync(0xffffffffu, g4, 2);
+                            if (ok && (lane & 3) == 0) atomicAdd(dla + t0 + tt, g4);
+                        }
                         carry += total;
                     }
                 }
@@ -453,7 +464,8 @@ __device__ __forceinline__ void cols_body(const BwdArgs& a, float* sm, long bh, 
     const T* q = static_cast<const T*>(a.q) + bh * (long)L * DK;
     const T* k = static_cast<const T*>(a.k) + bh * (long)L * DK;
     const T* dout = static_cast<const T*>(a.dout) + bh * (long)L * dv;
-    const float* la = GATE ? a.log_alpha + bh * (long)L * DK : nullptr;
+    const bool scalar = a.flags & GLA_FLAG_SCALAR_GATE;
+    const float* la = GATE ? a.log_alpha + bh * (long)L * (scalar ? 1 : DK) : nullptr;
 
     T rq[St::NW], rk[St::NW], rd[St::NN];
     float ra[St::NW];
@@ -465,7 +477,7 @@ __device__ __forceinline__ void cols_body(const BwdArgs& a, float* sm, long bh, 
                 const long g = (long)t0 * DK + idx;
                 rq[m] = q[g];
                 rk[m] = k[g];
-                if (GATE) ra[m] = la[g];
+                if (GATE) ra[m] = scalar ? la[t0 + idx / DK] : la[g];
             }
         }
 #pragma unroll

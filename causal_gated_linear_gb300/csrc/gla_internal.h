@@ -82,6 +82,7 @@ struct BwdArgs {
     float* dinit;
     int B, H, L, dk, dv;
     int in_dtype;
+    unsigned flags;  // GLA_FLAG_SCALAR_GATE: log_alpha and dlog_alpha are [B][H][L]
 };
 
 // Gradients of the recurrence (row CTAs: dq, dk, dlog_alpha, dS_init;

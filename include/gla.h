@@ -197,13 +197,18 @@ int gla_delta_fwd(const void* q, const void* k, const void* v, const float* beta
  *
  *   q, k        [B][H][L][dk], bf16 or fp32 (in_dtype)
  *   v, dout     [B][H][L][dv], in_dtype
- *   log_alpha   fp32 [B][H][L][dk], or NULL for no gate
+ *   log_alpha   fp32 [B][H][L][dk], or NULL for no gate; [B][H][L] with
+ *               GLA_FLAG_SCALAR_GATE (one gate per token, all channels)
  *   init_state  fp32 [B][H][dk][dv], or NULL for S_{-1} = 0
  *   dfinal      fp32 [B][H][dk][dv], or NULL for dL/dS_{L-1} = 0
  *   dq, dk_out  fp32 [B][H][L][dk]      (written)
  *   dv_out      fp32 [B][H][L][dv]      (written)
- *   dlog_alpha  fp32 [B][H][L][dk], or NULL (needs log_alpha)
+ *   dlog_alpha  fp32 [B][H][L][dk], or NULL (needs log_alpha); [B][H][L]
+ *               with GLA_FLAG_SCALAR_GATE: the sum of the per-channel
+ *               gradients, accumulated across row blocks with fp32 atomics
+ *               (the order of that sum is not fixed)
  *   dinit       fp32 [B][H][dk][dv], or NULL
+ *   flags       0 or GLA_FLAG_SCALAR_GATE
  * All caller-owned device memory, 16-byte aligned; outputs must not overlap
  * inputs or each other.  The recurrence runs token by token in fp32 (one
  * launch: row blocks sweep forward for dq, then backward for dk, dlog_alpha
@@ -213,7 +218,7 @@ int gla_delta_fwd(const void* q, const void* k, const void* v, const float* beta
  */
 int gla_bwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* init_state,
             const void* dout, const float* dfinal, float* dq, float* dk_out, float* dv_out, float* dlog_alpha,
-            float* dinit, int B, int H, int L, int dk, int dv, int in_dtype, void* stream);
+            float* dinit, int B, int H, int L, int dk, int dv, int in_dtype, unsigned flags, void* stream);
 
 /*
  * gla_device_error -- synchronise `stream`, read and clear the device error

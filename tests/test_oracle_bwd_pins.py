@@ -88,3 +88,17 @@ def test_two_token_scalar_worked_by_hand():
     assert np.allclose(dv.ravel(), [6, 2], atol=1e-14)
     assert np.allclose(dla.ravel(), [0, 6], atol=1e-14)
     assert np.allclose(ds0.ravel(), [1], atol=1e-14)
+
+
+def test_per_token_gate_gradient_is_the_channel_sum():
+    """One gate per token shared by all channels (log alpha_t[i] = g_t): by the
+    chain rule dL/dg_t is the sum over channels of the per-channel gradient;
+    checked against finite differences in g through the forward oracle."""
+    q, k, v, _, s0, Wo, Wf = _inputs(6, L=6, dk=3, dv=2)
+    g = np.random.default_rng(7).uniform(-0.5, -0.05, (1, 6))
+    wide = lambda: np.repeat(g[..., None], 3, axis=-1)
+    _, _, _, dla, _ = oracle.gla_bwd(q, k, v, Wo, wide(), s0, Wf)
+    f = lambda: _loss(q, k, v, wide(), s0, Wo, Wf)
+    ref = _fd(f, g)
+    got = dla.sum(axis=-1)
+    assert np.max(np.abs(got - ref)) <= 1e-6 * max(1.0, np.max(np.abs(ref)))

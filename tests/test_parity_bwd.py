@@ -37,8 +37,11 @@ def run_bwd(w, x, want_dla=True, want_dinit=True):
     dq, dk_, dv_ = nan(B, H, L, dk), nan(B, H, L, dk), nan(B, H, L, dv)
     dla = nan(B, H, L, dk) if (want_dla and la is not None) else None
     di = nan(B, H, dk, dv) if want_dinit else None
+    if dla is not None and w.scalar_gate:
+        dla = nan(B, H, L)
     gla.check(gla.gla_bwd(q, k, v, do, dq, dk_, dv_, B, H, L, dk, dv, log_alpha=la, init_state=s0, dfinal=df,
-                          dlog_alpha=dla, dinit=di, in_dtype=gla.F32 if w.dtype == "f32" else gla.BF16))
+                          dlog_alpha=dla, dinit=di, in_dtype=gla.F32 if w.dtype == "f32" else gla.BF16,
+                          flags=gla.FLAG_SCALAR_GATE if w.scalar_gate else 0))
     torch.cuda.synchronize()
     gla.check(gla.gla_device_error())
     c = lambda t: None if t is None else t.cpu().numpy().astype(np.float64)
@@ -72,6 +75,20 @@ def test_bwd_shapes(B, H, L, dk, dv, gate, init, dfin, dtype):
     w = _w(B, H, L, dk, dv, gate, init, dtype, seed=L + dk + 3 * dv)
     x = synth.make_bwd(w, dfinal_std=0.5 if dfin else 0.0)
     _check(run_bwd(w, x), oracle_bwd(x), gate)
+
+
+@pytest.mark.parametrize("B,H,L,dk,dv", [(1, 2, 77, 128, 128), (2, 1, 200, 64, 32), (1, 1, 16, 32, 64)])
+def test_bwd_per_token_gate(B, H, L, dk, dv):
+    """One gate per token (GLA_FLAG_SCALAR_GATE): the oracle runs on the gate
+    broadcast to every channel, and the per-token gradient is the sum of its
+    per-channel gradients."""
+    w = synth.with_shape(_w(B, H, L, dk, dv, seed=L + 5), scalar_gate=True)
+    x = synth.make_bwd(w, dfinal_std=0.5)
+    got = run_bwd(w, x)
+    xo = dict(x, log_alpha=np.repeat(x["log_alpha"][..., None], dk, axis=-1))
+    ref = list(oracle_bwd(xo))
+    ref[3] = ref[3].sum(axis=-1)
+    _check(got, ref, True)
 
 
 def test_bwd_optional_outputs_absent():
@@ -111,6 +128,8 @@ def test_bwd_rejects_bad_calls():
     assert gla.gla_bwd(q, k, v, do, q, dk, dv, 1, 1, 8, 64, 64, in_dtype=F) == gla.GLA_ERR_INVALID
     assert gla.gla_bwd(q, k, v, do, dq.data_ptr() + 4, dk, dv, 1, 1, 8, 64, 64,
                        in_dtype=F) == gla.GLA_ERR_MISALIGNED
+    assert gla.gla_bwd(q, k, v, do, dq, dk, dv, 1, 1, 8, 64, 64, in_dtype=F,
+                       flags=gla.FLAG_NORMALIZE) == gla.GLA_ERR_INVALID
 
 
 def test_bwd_full_sampled_and_homogeneity():
