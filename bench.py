@@ -129,15 +129,17 @@ def recorded_traffic(kernel: str):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """nvidia-smi sampling of SM clocks and throttle reasons; summary() keeps the
+    samples whose timestamps fall inside the timed region (mark() brackets it)."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
+        self.window = None
         # raw samples go to $GLA_BENCH_CLOCKS_DIR (default: the system temp directory)
         d = os.environ.get("GLA_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
         self.path = os.path.join(d, f"clocks_bench_{os.getpid()}.csv")
@@ -148,10 +150,18 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            # give nvidia-smi time to start sampling before the timed region
+            t0 = time.perf_counter()
+            while time.perf_counter() - t0 < 1.5 and os.path.getsize(self.path) == 0:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self
+
+    def mark(self, start: float, end: float):
+        """Host wall-clock bounds (time.time()) of the timed region."""
+        self.window = (start, end)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -167,21 +177,28 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        lo, hi = self.window if self.window else (-math.inf, math.inf)
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
+                    ts = parts[0]
+                    frac = float("0." + ts.rsplit(".", 1)[1]) if "." in ts else 0.0
+                    t = time.mktime(time.strptime(ts.rsplit(".", 1)[0], "%Y/%m/%d %H:%M:%S")) + frac
+                    if not (lo - 0.02 <= t <= hi + 0.02):
+                        continue
+                    sm.append(float(parts[2]))
+                    mx.append(float(parts[3]))
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
+                for n, v in zip(names, parts[6:10]):
                     if v.lower() == "active":
                         reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in the timed region"],
+                    "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
                 "samples": len(sm)}
 
@@ -310,6 +327,7 @@ def bench_prefill(args, device, rank, world):
         barrier(world)
         torch.cuda.synchronize(device)
         t_wall = time.perf_counter()
+        t_epoch = time.time()
         ev0.record(stream)
         evs = []
         for _ in range(args.steps):
@@ -320,6 +338,7 @@ def bench_prefill(args, device, rank, world):
             evs.append((a, b))
         ev1.record(stream)
         torch.cuda.synchronize(device)
+        clk.mark(t_epoch, time.time())
         barrier(world)
         wall = time.perf_counter() - t_wall
     gla.check(gla.gla_device_error(stream))
@@ -669,7 +688,7 @@ def run_gla(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gla", choices=["gla", "reference"])
     ap.add_argument("--decode-steps", type=int, default=256)
