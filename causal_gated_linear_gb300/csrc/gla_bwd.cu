@@ -12,7 +12,10 @@
 // and log alpha_t enters every b_s with s >= t:
 //   dlog_alpha_t = sum_{s >= t} (q_s * dq_s - k_s * dk_s) + rowsum(dfinal * S_{L-1}).
 // (The same chunk-form reading the forward uses: the gate's cumulative sums
-// are the only place log alpha appears.)
+// are the only place log alpha appears.)  With one gate per token
+// (GLA_FLAG_SCALAR_GATE) every row stages the token's alpha, and the token's
+// gradient is the sum of the rows' (warp shuffles, then fp32 atomics across
+// the row CTAs of a head).
 //
 // Two kinds of CTA share one launch:
 //  * row CTAs own 32 key rows of one head, all value columns.  Rows evolve on
