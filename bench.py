@@ -21,6 +21,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -108,10 +109,15 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_hash(kernel: str) -> str:
+    """Hash of a kernel's sources with comments and blank space removed (a comment edit
+    does not change the kernel, so it does not void a recorded capture)."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "causal_gated_linear_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "causal_gated_linear_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 
