@@ -127,6 +127,7 @@ int gla_fwd_ex(const gla_fwd_args* a, void* stream) {
     pa.in_dtype = a->in_dtype;
     pa.out_dtype = a->out_dtype;
     pa.flags = a->flags;
+    pa.pf_dist = 0;
     const size_t BH = (size_t)a->B * a->H;
     if (a->L == 0) {
         // no tokens: the final state is the initial one

@@ -23,6 +23,7 @@ struct PrefillArgs {
     int in_dtype, out_dtype;
     unsigned flags;
     unsigned* err_word;  // device address of the error word
+    int pf_dist;         // short-sequence kernel: CTAs ahead whose inputs it prefetches into L2
 };
 
 struct DecodeArgs {

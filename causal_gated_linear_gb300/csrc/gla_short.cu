@@ -12,7 +12,8 @@
 // the state -- the traffic of a single decode step -- for up to 16 tokens.
 // Each thread owns one float4 of value columns for kRows consecutive key rows
 // (64 floats), so its per-token alpha, k and q come in as float4 shared loads;
-// the updates run as packed fp32 pairs.  The per-token partial outputs over
+// the updates run as packed fp32 pairs.  Each CTA also prefetches the state
+// and tokens of the head about one wave of CTAs ahead into L2.  The per-token partial outputs over
 // those rows go to shared memory and are summed over the row groups after the
 // token loop (one barrier per call).
 #include <cuda_bf16.h>
@@ -44,6 +45,10 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     return d;
 }
 
+__device__ __forceinline__ void l2_prefetch(const void* p, int bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
     float2 d;
     asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
@@ -71,6 +76,16 @@ __global__ void __launch_bounds__(kMaxThreads) gla_prefill_short_kernel(const Pr
     const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v) + bh * L * dv;
     // per-channel gate: [L][dk]; per-token gate (GLA_FLAG_SCALAR_GATE): [L], shared by all channels
     const bool scalar_gate = a.flags & GLA_FLAG_SCALAR_GATE;
+    // the head pf_dist CTAs ahead: its state and tokens into L2 while this one is processed
+    if (tid == 0 && bh + a.pf_dist < (long)a.B * a.H) {
+        const long nb = bh + a.pf_dist;
+        if (a.init_state) l2_prefetch(a.init_state + nb * (long)dk * dv, dk * dv * 4);
+        l2_prefetch(static_cast<const __nv_bfloat16*>(a.q) + nb * L * dk, L * dk * 2);
+        l2_prefetch(static_cast<const __nv_bfloat16*>(a.k) + nb * L * dk, L * dk * 2);
+        if ((L * dv * 2) % 16 == 0)  // bulk prefetches take 16-byte multiples (dv % 4 == 0 here)
+            l2_prefetch(static_cast<const __nv_bfloat16*>(a.v) + nb * L * dv, L * dv * 2);
+        if (GATE && !scalar_gate) l2_prefetch(a.log_alpha + nb * L * dk, L * dk * 4);
+    }
     for (int i = tid; i < L * dk; i += nthr) {
         s_q[i] = __bfloat162float(q[i]);
         s_k[i] = __bfloat162float(k[i]);
@@ -165,7 +180,12 @@ bool prefill_short_supported(const PrefillArgs& a) {
     return short_smem_bytes(a) <= 227 * 1024;
 }
 
-cudaError_t launch_prefill_short(const PrefillArgs& a, cudaStream_t s) {
+cudaError_t launch_prefill_short(const PrefillArgs& a_in, cudaStream_t s) {
+    PrefillArgs a = a_in;
+    // prefetch distance: about the CTAs resident at once (two per SM)
+    int sms = 148, dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    a.pf_dist = 2 * sms;
     const int threads = a.dk * a.dv / (4 * kRows);
     const size_t smem = short_smem_bytes(a);
     const unsigned grid = (unsigned)((long)a.B * a.H);
