@@ -21,12 +21,17 @@ constexpr int kThreads = 256;
 constexpr int kMaxDk = 512;
 constexpr int kUnroll = 8;
 
-__global__ void __launch_bounds__(kThreads) gla_decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads) gla_decode_kernel(DecodeArgs a, int pf_dist) {
     __shared__ float s_q[kMaxDk], s_k[kMaxDk], s_a[kMaxDk];
     __shared__ float4 s_red[kThreads];
     const int dk = a.dk, dv = a.dv;
     const long hs = blockIdx.x;
     const int tid = threadIdx.x;
+    // the state pf_dist CTAs ahead into L2 while this one streams (16-byte multiples only)
+    if (tid == 0 && hs + pf_dist < (long)gridDim.x && (dk * dv) % 4 == 0) {
+        const float* nxt = a.state + (hs + pf_dist) * (long)dk * dv;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(nxt), "r"(dk * dv * 4) : "memory");
+    }
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + hs * dk;
     const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k) + hs * dk;
     const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v) + hs * dv;
@@ -105,7 +110,9 @@ __global__ void __launch_bounds__(kThreads) gla_decode_kernel(DecodeArgs a) {
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
     const long n = (long)a.B * a.H;
     if (n == 0) return cudaSuccess;
-    gla_decode_kernel<<<dim3((unsigned)n), kThreads, 0, s>>>(a);
+    int sms = 148, dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    gla_decode_kernel<<<dim3((unsigned)n), kThreads, 0, s>>>(a, 3 * sms);  // about the CTAs resident at once
     return cudaGetLastError();
 }
 
