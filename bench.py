@@ -108,12 +108,12 @@ KERNEL_SOURCES = {
 }
 
 
-def kernel_source_hash(kernel: str) -> str:
+def kernel_source_hash(kernel: str, csrc: str | None = None) -> str:
     """Hash of a kernel's sources with comments and blank space removed (a comment edit
     does not change the kernel, so it does not void a recorded capture)."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "causal_gated_linear_gb300", "csrc", f)) as fh:
+        with open(os.path.join(csrc or os.path.join(ROOT, "causal_gated_linear_gb300", "csrc"), f)) as fh:
             src = fh.read()
         src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
         src = re.sub(r"//[^\n]*", " ", src)
