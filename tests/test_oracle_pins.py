@@ -147,6 +147,24 @@ def test_split_resume(L1):
     assert _close(f2, fs)
 
 
+@pytest.mark.parametrize("L1", [64, 37])
+def test_split_from_zero_state_plus_correction(L1):
+    """Linearity in the initial state: the second part run from a zero state,
+    plus the decayed first-part state read by each query,
+    o_t = o'_t + (q_t * e^{B_t})^T S_A and S = Diag(e^{B_end}) S_A + S',
+    with B_t the gate's cumulative sum from the split point (inclusive).  This
+    is the identity a split of the sequence across independent chains uses."""
+    q, k, v, la = _inputs(9, 160, 4, 3)
+    s0 = _rng(10).standard_normal((2, 4, 3))
+    out, fs, _ = oracle.gla_fwd(q, k, v, la, init_state=s0)
+    o1, sa, _ = oracle.gla_fwd(q[:, :L1], k[:, :L1], v[:, :L1], la[:, :L1], init_state=s0)
+    o2, sb, _ = oracle.gla_fwd(q[:, L1:], k[:, L1:], v[:, L1:], la[:, L1:])
+    B = np.cumsum(la[:, L1:], axis=1)
+    corr = np.einsum("btd,bdj->btj", q[:, L1:] * np.exp(B), sa)
+    assert _close(np.concatenate([o1, o2 + corr], axis=1), out)
+    assert _close(np.exp(B[:, -1])[..., None] * sa + sb, fs)
+
+
 @pytest.mark.parametrize("C", [1, 16, 64, 100, 200])
 def test_chunk_form_equals_recurrence(C):
     """The chunk-wise form is an exact refactoring for every chunk size C."""
