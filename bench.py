@@ -4,8 +4,11 @@ Headline (value): long-context GLA prefill, B=1 H=32 L=65536 dk=128 dv=256,
 chunk 64, bf16 q/k/v, fp32 log alpha, fp32 initial state ~N(0, 0.1), returns
 the final state -- tokens/s for the whole job (all ranks).  One step is one
 gla_fwd call over the whole batch (the fused cumsum-gate / intra-chunk /
-inter-chunk / output kernel).  The same run also measures the decode step
-(256 sequences x H32, d128, fp32 state) as achieved state HBM GB/s.
+inter-chunk / output kernel).  The same run also measures, each in its own
+JSON object: the decode step (256 sequences x H32, d128, fp32 state) as
+state HBM GB/s; the 8-token hand-off on that state; the long-context prefill
+with one gate per token; the delta rule and the backward pass (FP32-ALU
+rooflines); and the end-to-end step through gla_fwd_host with host buffers.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gla|reference]
 
