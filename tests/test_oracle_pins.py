@@ -126,6 +126,43 @@ def test_normaliser_with_gate_decays_z():
     assert _close(out, num / den)
 
 
+def test_normaliser_with_initial_state_and_z_bruteforce():
+    """Resuming the normalised form from a given (S_0, z_0): numerator and denominator each
+    carry their initial value decayed to t, o_t = phi(q_t)^T (D_t S_0 + sum_i W_ti phi(k_i) v_i^T)
+    / phi(q_t)^T (D_t z_0 + sum_i W_ti phi(k_i)), with D_t = e^{B_t} and W_ti = e^{B_t - B_i} per
+    channel ("Transformers are RNNs" notes, normalised kernel form; z is the all-ones value
+    column of the state, so it decays like S)."""
+    q, k, v, la = _inputs(16, 40, 3, 2)
+    r = _rng(17)
+    s0 = r.standard_normal((2, 3, 2))
+    z0 = r.uniform(0.5, 2.0, (2, 3))
+    out, fs, fz = oracle.gla_fwd(q, k, v, la, init_state=s0, init_z=z0, feature_elu1=True, normalize=True)
+    pq, pk = _phi(q), _phi(k)
+    for bh in range(2):
+        Bc = np.cumsum(la[bh], axis=0)
+        for t in range(40):
+            w = np.exp(Bc[t][None, :] - Bc[: t + 1])  # [i, d]
+            num = pq[bh, t] @ (np.exp(Bc[t])[:, None] * s0[bh] + (w * pk[bh, : t + 1]).T @ v[bh, : t + 1])
+            den = pq[bh, t] @ (np.exp(Bc[t]) * z0[bh] + (w * pk[bh, : t + 1]).sum(axis=0))
+            assert _close(out[bh, t], num / den)
+        wL = np.exp(Bc[-1][None, :] - Bc)
+        assert _close(fz[bh], np.exp(Bc[-1]) * z0[bh] + (wL * pk[bh]).sum(axis=0))
+        assert _close(fs[bh], np.exp(Bc[-1])[:, None] * s0[bh] + (wL * pk[bh]).T @ v[bh])
+
+
+@pytest.mark.parametrize("L1", [64, 29])
+def test_normalised_split_resume(L1):
+    """The normalised form split anywhere and resumed from the first part's (S, z) equals the
+    whole sequence: the pair (S, z) is a sufficient summary of the prefix."""
+    q, k, v, la = _inputs(18, 120, 4, 3)
+    out, fs, fz = oracle.gla_fwd(q, k, v, la, feature_elu1=True, normalize=True)
+    o1, s1, z1 = oracle.gla_fwd(q[:, :L1], k[:, :L1], v[:, :L1], la[:, :L1], feature_elu1=True, normalize=True)
+    o2, s2, z2 = oracle.gla_fwd(q[:, L1:], k[:, L1:], v[:, L1:], la[:, L1:], init_state=s1, init_z=z1,
+                                feature_elu1=True, normalize=True)
+    assert _close(np.concatenate([o1, o2], axis=1), out)
+    assert _close(s2, fs) and _close(z2, fz)
+
+
 def test_decode_equals_prefill():
     q, k, v, la = _inputs(7, 20, 5, 4)
     s0 = _rng(77).standard_normal((2, 5, 4))
