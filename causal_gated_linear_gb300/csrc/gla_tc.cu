@@ -34,12 +34,20 @@
 // (mask A -> bf16 P), 22 TMA producer (and A issuer with the 128-column
 // tile), 23 MMA issuer and TMEM owner.  Every pipeline wait is bounded
 // (gla_ptx.cuh).
+//
+// Strong gates: alpha has no lower bound, and once a channel decays by more
+// than e^-64 over a chunk the factor e^{b_t - b_C} could overflow.  The pass
+// every call runs only detects such a chunk; the CTA then skips its final-state
+// write and runs its slice a second time (exact_pass) in which strong channels
+// take q e^{b_t} against the unscaled state and their intra-chunk scores are
+// added on the P warps with exponents <= 0.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <climits>
 #include <cstdlib>
 #include <cstring>
+#include <type_traits>
 
 #include "gla_internal.h"
 #include "gla_ptx.cuh"
@@ -69,6 +77,16 @@ constexpr int kWarps = 24;
 constexpr int kThreads = kWarps * 32;
 constexpr int W_STATE0 = 8, W_OUT0 = 16, W_P0 = 20, W_TMA = 22, W_MMA = 23;
 constexpr int kGateThreads = 256;
+
+// A key channel whose gate decays by more than e^-64 over one chunk is "strong"
+// for that chunk: the factorisation relative to the chunk end (q e^{b_t - b_C},
+// k e^{b_C - b_i}) would overflow, so such channels take factors relative to
+// the chunk start on the q side and their intra-chunk scores are added on the
+// P warps with exponents <= 0 (see gate_factors_strong, strong_scores).  The
+// test is made on e^{b_C} exactly as the gate writes it, so every role agrees.
+constexpr float kStrongGamma = 1.6038109e-28f;  // e^-64
+constexpr float kStrongLog = -64.f;
+constexpr int kRing = 8;  // chunks whose strong-channel masks are kept (ring slots)
 
 // tensor-memory column map (512 columns allocated)
 constexpr uint32_t TM_S = 0;     // S^T fp32, dk columns (128-column tile)
@@ -131,7 +149,7 @@ struct Layout {
     static constexpr int off_v = off_la + LA_REGION;
     // a second P buffer where it fits: P(c+1) need not wait for O_a(c)
     static constexpr int NP = NS * STAGE_QK + LA_REGION + NV * VB + 2 * PB + OSB + NS * DK * 4 + 2 * SEG * DK * 4 +
-                                      B_COUNT * 8 + 12 + 1008 <= 232448
+                                      B_COUNT * 8 + 16 + kRing * 20 + 1008 <= 232448
                                   ? 2
                                   : 1;
     static constexpr int off_p = off_v + NV * VB;
@@ -140,13 +158,18 @@ struct Layout {
     static constexpr int off_segtot = off_gamma + NS * DK * 4;
     static constexpr int off_bar = off_segtot + 2 * SEG * DK * 4;
     static constexpr int off_misc = off_bar + B_COUNT * 8;
-    static constexpr int total = off_misc + 12;  // TMEM base address, abort flag, O_i count
+    // ring of per-chunk strong-channel masks: {sequence, 4 x 32-bit masks} per slot
+    static constexpr int off_ring = off_misc + 16;
+    static constexpr int total = off_ring + kRing * 20;  // misc: TMEM base address, abort flag, O_i count
     static constexpr int alloc = total + 1008;  // round-up to 1024 from a >= 16-byte aligned base
     static_assert(alloc <= 232448, "shared memory budget");
 };
 
 struct TcParams {
     CUtensorMap tm_q, tm_k, tm_la, tm_v, tm_out;
+    const uint16_t* q_raw;  // the same inputs as plain pointers (strong-channel scores)
+    const uint16_t* k_raw;
+    const float* la_raw;
     const float* init_state;
     const float* init_z;
     void* out;
@@ -244,12 +267,171 @@ __device__ __forceinline__ void gate_factors(uint8_t* qt, uint8_t* kt, const flo
     }
 }
 
-template <int DK, int DVT, bool GATE, bool SCALAR>
-__global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __grid_constant__ TcParams p) {
+// The four log gates of this thread's channels at token t (one shared gate with SCALAR).
+template <int DK, bool SCALAR>
+__device__ __forceinline__ float4 load_la4(const float* la, int t) {
+    if (SCALAR) {
+        const float x = la[t];
+        return make_float4(x, x, x, x);
+    }
+    return *reinterpret_cast<const float4*>(la + t * DK);
+}
+
+// Gate factors of a thread that owns at least one strong channel in this chunk
+// (its gate decays by more than e^-64 over the chunk, so e^{b_t - b_C} could
+// overflow).  On strong channels q takes the factor e^{b_t} (relative to the
+// chunk start, <= 1); k always takes e^{b_C - b_t} (<= 1), here accumulated as a
+// suffix sum from the chunk end so that it stays exact however large |b_C| is.
+// Channels of the thread that are not strong keep q e^{b_t - b_C}.
+//   pre: sum of log alpha over the segments before this thread's, suf: over the
+//   segments after it, tot: over the whole chunk (b_C).
+template <int DK, int TPS, bool ELU, bool SCALAR>
+__device__ __noinline__ void gate_factors_strong(uint8_t* qt, uint8_t* kt, const float* la, int seg, int col,
+                                                 int nval, float4 pre, float4 tot, float4 suf, unsigned strong4) {
+    constexpr float kLog2e = 1.4426950408889634f;
+    float rq[4] = {(strong4 & 1u) ? pre.x : pre.x - tot.x, (strong4 & 2u) ? pre.y : pre.y - tot.y,
+                   (strong4 & 4u) ? pre.z : pre.z - tot.z, (strong4 & 8u) ? pre.w : pre.w - tot.w};
+    float rk[4] = {suf.x, suf.y, suf.z, suf.w};
+#pragma unroll 1
+    for (int i = 0; i < TPS; i++) {  // q: forward running sum b_t (- b_C on the other channels)
+        const int t = seg * TPS + i;
+        const float4 x = load_la4<DK, SCALAR>(la, t);
+        rq[0] += x.x;
+        rq[1] += x.y;
+        rq[2] += x.z;
+        rq[3] += x.w;
+        const uint32_t o = sw128_offset(t, col);
+        const uint2 qr = *reinterpret_cast<const uint2*>(qt + o);
+        float2 q01 = unpack_bf16x2(qr.x), q23 = unpack_bf16x2(qr.y);
+        if (ELU) {
+            q01 = make_float2(elu1(q01.x), elu1(q01.y));
+            q23 = make_float2(elu1(q23.x), elu1(q23.y));
+        }
+        q01.x *= ex2_approx(rq[0] * kLog2e);
+        q01.y *= ex2_approx(rq[1] * kLog2e);
+        q23.x *= ex2_approx(rq[2] * kLog2e);
+        q23.y *= ex2_approx(rq[3] * kLog2e);
+        uint2 w = make_uint2(pack_bf16x2(q01.x, q01.y), pack_bf16x2(q23.x, q23.y));
+        if (ELU && t >= nval) w = make_uint2(0u, 0u);
+        *reinterpret_cast<uint2*>(qt + o) = w;
+    }
+#pragma unroll 1
+    for (int i = TPS - 1; i >= 0; i--) {  // k: suffix sum b_C - b_t, from the chunk end
+        const int t = seg * TPS + i;
+        const uint32_t o = sw128_offset(t, col);
+        const uint2 kr = *reinterpret_cast<const uint2*>(kt + o);
+        float2 k01 = unpack_bf16x2(kr.x), k23 = unpack_bf16x2(kr.y);
+        if (ELU) {
+            k01 = make_float2(elu1(k01.x), elu1(k01.y));
+            k23 = make_float2(elu1(k23.x), elu1(k23.y));
+        }
+        k01.x *= ex2_approx(rk[0] * kLog2e);
+        k01.y *= ex2_approx(rk[1] * kLog2e);
+        k23.x *= ex2_approx(rk[2] * kLog2e);
+        k23.y *= ex2_approx(rk[3] * kLog2e);
+        uint2 w = make_uint2(pack_bf16x2(k01.x, k01.y), pack_bf16x2(k23.x, k23.y));
+        if (ELU && t >= nval) w = make_uint2(0u, 0u);
+        *reinterpret_cast<uint2*>(kt + o) = w;
+        const float4 x = load_la4<DK, SCALAR>(la, t);
+        rk[0] += x.x;
+        rk[1] += x.y;
+        rk[2] += x.z;
+        rk[3] += x.w;
+    }
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+
+// Intra-chunk scores of the strong channels of a chunk, added in place to row t
+// of the A tile in tensor memory (both 32-column halves):
+//   A[t][i] += sum_{d strong} q_td k_id e^{b_td - b_id}   for i <= t.
+// (The tensor-core product carries these channels with the factors e^{b_t} and
+// e^{b_C - b_i}, whose product is below e^-64 |q_td k_id|: nothing.)  The
+// exponent is a running sum of log alpha walked from i = t downwards, so it is
+// <= 0 and exact for any gate; the walk stops once it is below -88.  Raw q, k
+// and log alpha are read from global memory (the chunk was loaded a moment ago,
+// so they come from L2).  Called by whole warps (the tensor-memory accesses are
+// warp-collective) and only for chunks with a strong channel.
+template <int DK, bool SCALAR>
+__device__ __noinline__ void strong_scores(uint32_t taddr, int t, int nval, uint4 mask4, const uint16_t* qc,
+                                           const uint16_t* kc, const float* lac, bool elu) {
+    const uint32_t mask[4] = {mask4.x, mask4.y, mask4.z, mask4.w};
+    auto lag = [&](int j, int d) { return SCALAR ? lac[j] : lac[(long)j * DK + d]; };
+#pragma unroll 1
+    for (int h = 0; h < 2; h++) {
+        uint32_t r[32];
+        tmem_ld32(taddr + h * 32, r);
+        tmem_wait_ld();
+        const int top = min(t, 32 * h + 31);
+        // rows past the sequence end are never stored; columns above the diagonal are masked
+        if (t < nval && top >= 32 * h) {
+#pragma unroll 1
+            for (int e4 = 0; e4 < 4; e4++) {
+                uint32_t m = mask[e4];  // bit `quad` set: channel 4 quad + e4 is strong
+#pragma unroll 1
+                while (m) {
+                    const int quad = __ffs(m) - 1;
+                    m &= m - 1;
+                    const int d = 4 * quad + e4;
+                    float qd = bf16_bits_to_float(qc[(long)t * DK + d]);
+                    if (elu) qd = elu1(qd);
+                    float s = 0.f;  // b_t - b_i for i = top
+#pragma unroll 1
+                    for (int j = t; j > top && s >= -88.f; j--) s += lag(j, d);
+                    if (s < -88.f) continue;
+#pragma unroll
+                    for (int e = 31; e >= 0; e--) {
+                        const int i = 32 * h + e;
+                        if (i <= top) {
+                            float kd = bf16_bits_to_float(kc[(long)i * DK + d]);
+                            if (elu) kd = elu1(kd);
+                            r[e] = __float_as_uint(
+                                fmaf(qd * kd, ex2_approx(s * 1.4426950408889634f), __uint_as_float(r[e])));
+                            s += lag(i, d);
+                            if (s < -88.f) break;
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        tmem_st32(taddr + h * 32, r);
+        tmem_wait_st();
+    }
+}
+
+// Wait (bounded) until the gate has published the strong-channel masks of chunk c.
+__device__ __forceinline__ bool ring_wait(const volatile uint32_t* slot, uint32_t c, volatile int* abort_flag,
+                                          unsigned* err_word) {
+    if (slot[0] == c) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (slot[0] == c) return true;
+        if ((it & 255u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                if (err_word) record_timeout_code(err_word, 0x10000000u | ((c & 0xffffu) << 1));
+                return false;
+            }
+        }
+    }
+}
+
+// One pass of a CTA over its (batch*head, value slice).
+// SAFE = false: the pass every call makes.  A chunk whose gate decays by more
+// than e^-64 on some channel is not computed exactly by the factorisation
+// relative to the chunk end; such a chunk only raises a flag, the pass then
+// skips the final-state write and returns true (its outputs are rewritten).
+// SAFE = true: the pass that follows in the same CTA when the first returned
+// true; it recomputes the slice with strong channels handled exactly
+// (gate_factors_strong, strong_scores).  Tensor memory is allocated once by
+// the kernel for both passes.
+template <int DK, int DVT, bool GATE, bool SCALAR, bool SAFE>
+__device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_raw) {
     using Ly = Layout<DK, DVT, SCALAR>;
     constexpr int NS = Ly::NS;
     constexpr int NV = Ly::NV;
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base for the swizzled tiles.  The offset is added to the
     // shared array itself so that every access below stays in the shared
     // address space (an integer round trip would turn them into generic ones).
@@ -260,7 +442,11 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Ly::off_misc + 4);
     // number of O_i products issued so far (written by the MMA thread, read by the A issuer)
     volatile int* oi_issued = reinterpret_cast<volatile int*>(sm + Ly::off_misc + 8);
+    // fast pass: set once some chunk of this slice has a strong channel
+    volatile int* strong_flag = reinterpret_cast<volatile int*>(sm + Ly::off_misc + 12);
     float* gamma = reinterpret_cast<float*>(sm + Ly::off_gamma);
+    // slot c % kRing: {chunk index, strong-channel masks m[4]}; bit `quad` of m[e] is channel 4 quad + e
+    uint32_t* ring = reinterpret_cast<uint32_t*>(sm + Ly::off_ring);
     float* segtot = reinterpret_cast<float*>(sm + Ly::off_segtot);
     // normaliser denominators: only with GLA_FLAG_NORMALIZE (dv == 64 on a 128-column
     // tile), when the second 64-column block of the output staging is unused
@@ -284,6 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
 
     // ---------------------------------------------------------------- setup
     if (threadIdx.x == 0) {
+        if (SAFE)  // the first pass's barriers are re-initialised
+            for (int i = 0; i < B_COUNT; i++) mbar_inval(bar(i));
         for (int i = 0; i < NS; i++) {
             mbar_init(bar(B_QK_FULL + i), 1);
             mbar_init(bar(B_QK_GATED + i), 8);
@@ -315,9 +503,11 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
         mbar_init(bar(B_DRAIN), 2);
         *abort_flag = 0;
         *oi_issued = 0;
+        *strong_flag = 0;
+        for (int i = 0; i < kRing; i++) ring[i * 5] = 0xffffffffu;
         mbar_fence_init();
     }
-    if (warp == W_MMA) {
+    if (!SAFE && warp == W_MMA) {
         tmem_alloc(smem_u32(tmem_slot), TM_COLS);
         tmem_relinquish();
     }
@@ -360,7 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             // gate warps to give each thread the prefix before its segment (off) and
             // the chunk total b_C (tot).  Phase 2 re-reads log alpha from shared
             // memory and re-accumulates, so no per-token sums are held in registers.
-            float off[4] = {0.f, 0.f, 0.f, 0.f}, tot[4] = {0.f, 0.f, 0.f, 0.f};
+            float off[4] = {0.f, 0.f, 0.f, 0.f}, tot[4] = {0.f, 0.f, 0.f, 0.f}, pre[4] = {0.f, 0.f, 0.f, 0.f};
+            unsigned strong4 = 0;  // strong channels among this thread's four
             // per-channel: this thread's 4 channels of row t at la + t*DK; SCALAR: row t at la[t]
             const float* la = reinterpret_cast<const float*>(sm + Ly::off_la + l * Ly::LAB) + (SCALAR ? 0 : ch);
             if (GATE) {
@@ -395,11 +586,35 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                     tot[2] += u.z;
                     tot[3] += u.w;
                 }
-                if (seg == 0)
-                    *reinterpret_cast<float4*>(gamma + s * DK + ch) =
-                        make_float4(__expf(tot[0]), __expf(tot[1]), __expf(tot[2]), __expf(tot[3]));
+                if constexpr (SAFE) {
+                    // e^{b_C} per channel: the state's decay; below e^-64 the channel is strong
+                    const float4 gm4 = make_float4(__expf(tot[0]), __expf(tot[1]), __expf(tot[2]), __expf(tot[3]));
+                    strong4 = (gm4.x < kStrongGamma ? 1u : 0u) | (gm4.y < kStrongGamma ? 2u : 0u) |
+                              (gm4.z < kStrongGamma ? 4u : 0u) | (gm4.w < kStrongGamma ? 8u : 0u);
+                    if (seg == 0) *reinterpret_cast<float4*>(gamma + s * DK + ch) = gm4;
+                    if (warp == 0) {  // every segment-0 thread (one per channel quad) is in warp 0
+                        uint32_t m[4];
+    #pragma unroll
+                        for (int e = 0; e < 4; e++) m[e] = __ballot_sync(0xffffffffu, seg == 0 && ((strong4 >> e) & 1u));
+                        if (lane == 0) {
+                            uint32_t* slot = ring + (c % kRing) * 5;
+    #pragma unroll
+                            for (int e = 0; e < 4; e++) slot[1 + e] = m[e];
+                            __threadfence_block();
+                            *reinterpret_cast<volatile uint32_t*>(slot) = static_cast<uint32_t>(c);
+                        }
+                    }
+                } else {
+                    if (seg == 0)
+                        *reinterpret_cast<float4*>(gamma + s * DK + ch) =
+                            make_float4(__expf(tot[0]), __expf(tot[1]), __expf(tot[2]), __expf(tot[3]));
+                    if (fminf(fminf(tot[0], tot[1]), fminf(tot[2], tot[3])) < kStrongLog) *strong_flag = 1;
+                }
 #pragma unroll
-                for (int e = 0; e < 4; e++) off[e] -= tot[e];  // running value is now b_t - b_C
+                for (int e = 0; e < 4; e++) {
+                    pre[e] = off[e];
+                    off[e] -= tot[e];  // running value is now b_t - b_C
+                }
             } else {
                 if (!bar_red_and(1, kGateThreads, ok)) break;
             }
@@ -410,10 +625,30 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             if (GATE || elu) {
                 uint8_t* qt = sm + Ly::off_qk + s * Ly::STAGE_QK + atom * 8192;
                 uint8_t* kt = qt + Ly::QB;
-                if (elu)
+                if (SAFE && GATE && strong4) {  // only the exact pass sets strong4
+                    // suffix of the chunk after this thread's segment (still in segtot)
+                    const float* st = segtot + (c & 1) * SEG * DK;
+                    float4 suf = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int g = seg + 1; g < SEG; g++) {
+                        const float4 u = *reinterpret_cast<const float4*>(st + g * DK + ch);
+                        suf.x += u.x;
+                        suf.y += u.y;
+                        suf.z += u.z;
+                        suf.w += u.w;
+                    }
+                    const float4 pre4 = make_float4(pre[0], pre[1], pre[2], pre[3]);
+                    const float4 tot4 = make_float4(tot[0], tot[1], tot[2], tot[3]);
+                    if (elu)
+                        gate_factors_strong<DK, TPS, true, SCALAR>(qt, kt, la, seg, col, nval, pre4, tot4, suf,
+                                                                   SAFE ? strong4 : 0u);
+                    else
+                        gate_factors_strong<DK, TPS, false, SCALAR>(qt, kt, la, seg, col, nval, pre4, tot4, suf,
+                                                                    SAFE ? strong4 : 0u);
+                } else if (elu) {
                     gate_factors<DK, TPS, G, GATE, true, SCALAR>(qt, kt, la, seg, col, nval, off);
-                else
+                } else {
                     gate_factors<DK, TPS, G, GATE, false, SCALAR>(qt, kt, la, seg, col, nval, off);
+                }
             }
             if (GATE) {
                 __syncwarp();
@@ -469,31 +704,48 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                 tc_fence_after();
                 if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(4, c);
                 const uint32_t tSB = tmem + lane_field + (uint32_t)sb * 64u;
+                // a chunk with a strong channel: that channel's copy feeding O_i is S itself
+                // (its q carries e^{b_t}), every other channel's is e^{b_C} S as usual
+                const uint32_t* slot = ring + (c % kRing) * 5;
+                const bool sgc = SAFE && GATE && ((slot[1] | slot[2] | slot[3] | slot[4]) != 0u);
+                auto update = [&](auto strong_tag) {
+                    constexpr bool ST = decltype(strong_tag)::value;
 #pragma unroll
-                for (int g = 0; g < NG * 2; g++) {
-                    // 8 key channels per half-warp: c0 + [0, 8) for threads 0-15, c0 + 16 + [0, 8)
-                    // for threads 16-31 (S index g/2 * 16 + (g&1) * 8 + i)
-                    const int c0 = cbase + (g >> 1) * 32 + (g & 1) * 8;
-                    uint32_t d[8];
-                    tmem_ld16x2_x8<16>(tD + c0, d);
-                    tmem_wait_ld();
-                    const float* gm = gamma + s * DK + c0 + hi * 16;
-                    uint32_t pk[4];
+                    for (int g = 0; g < NG * 2; g++) {
+                        // 8 key channels per half-warp: c0 + [0, 8) for threads 0-15, c0 + 16 + [0, 8)
+                        // for threads 16-31 (S index g/2 * 16 + (g&1) * 8 + i)
+                        const int c0 = cbase + (g >> 1) * 32 + (g & 1) * 8;
+                        uint32_t d[8];
+                        tmem_ld16x2_x8<16>(tD + c0, d);
+                        tmem_wait_ld();
+                        const float* gm = gamma + s * DK + c0 + hi * 16;
+                        uint32_t pk[4];
 #pragma unroll
-                    for (int i = 0; i < 8; i += 4) {
-                        float4 gv = make_float4(1.f, 1.f, 1.f, 1.f);
-                        if (GATE) gv = *reinterpret_cast<const float4*>(gm + i);
-                        float* sv = S + g * 8 + i;
-                        const float a0 = sv[0] * gv.x, a1 = sv[1] * gv.y, a2 = sv[2] * gv.z, a3 = sv[3] * gv.w;
-                        pk[i / 2] = pack_bf16x2(a0, a1);
-                        pk[i / 2 + 1] = pack_bf16x2(a2, a3);
-                        sv[0] = a0 + __uint_as_float(d[i]);
-                        sv[1] = a1 + __uint_as_float(d[i + 1]);
-                        sv[2] = a2 + __uint_as_float(d[i + 2]);
-                        sv[3] = a3 + __uint_as_float(d[i + 3]);
+                        for (int i = 0; i < 8; i += 4) {
+                            float4 gv = make_float4(1.f, 1.f, 1.f, 1.f);
+                            if (GATE) gv = *reinterpret_cast<const float4*>(gm + i);
+                            float* sv = S + g * 8 + i;
+                            const float a0 = sv[0] * gv.x, a1 = sv[1] * gv.y, a2 = sv[2] * gv.z, a3 = sv[3] * gv.w;
+                            if (ST) {
+                                pk[i / 2] = pack_bf16x2(gv.x < kStrongGamma ? sv[0] : a0, gv.y < kStrongGamma ? sv[1] : a1);
+                                pk[i / 2 + 1] =
+                                    pack_bf16x2(gv.z < kStrongGamma ? sv[2] : a2, gv.w < kStrongGamma ? sv[3] : a3);
+                            } else {
+                                pk[i / 2] = pack_bf16x2(a0, a1);
+                                pk[i / 2 + 1] = pack_bf16x2(a2, a3);
+                            }
+                            sv[0] = a0 + __uint_as_float(d[i]);
+                            sv[1] = a1 + __uint_as_float(d[i + 1]);
+                            sv[2] = a2 + __uint_as_float(d[i + 2]);
+                            sv[3] = a3 + __uint_as_float(d[i + 3]);
+                        }
+                        tmem_st16x2_x4<8>(tSB + c0 / 2, pk);
                     }
-                    tmem_st16x2_x4<8>(tSB + c0 / 2, pk);
-                }
+                };
+                if (sgc)
+                    update(std::true_type{});
+                else
+                    update(std::false_type{});
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -503,7 +755,8 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                 }
                 if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(5, c);
             }
-            if (ok && p.final_state && jv) {
+            // a marked slice leaves its final state to the exact pass (init_state may alias it)
+            if (ok && p.final_state && jv && !(GATE && !SAFE && *strong_flag)) {
                 float* fs = p.final_state + (long)bh * DK * dv + j;
 #pragma unroll
                 for (int g = 0; g < NG; g++)
@@ -549,6 +802,9 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t tSB = tmem + lane_field + TM_SB;
+                // a chunk with a strong channel: that channel's copy feeding O_i is S itself
+                const uint32_t* slot = ring + (c % kRing) * 5;
+                const bool sgc = SAFE && GATE && ((slot[1] | slot[2] | slot[3] | slot[4]) != 0u);
 #pragma unroll 1
                 for (int g = 0; g < COLS / 16; g++) {
                     const int c0 = cbase + g * 16;
@@ -557,16 +813,28 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                     tmem_ld16(tD + c0, rd);
                     tmem_wait_ld();
                     uint32_t pk[8];
+                    if (sgc) {
 #pragma unroll
-                    for (int i = 0; i < 16; i += 2) {
-                        float s0v = __uint_as_float(rs[i]), s1v = __uint_as_float(rs[i + 1]);
-                        if (GATE) {
-                            s0v *= gamma[s * DK + c0 + i];
-                            s1v *= gamma[s * DK + c0 + i + 1];
+                        for (int i = 0; i < 16; i += 2) {
+                            const float s0v = __uint_as_float(rs[i]), s1v = __uint_as_float(rs[i + 1]);
+                            const float g0 = gamma[s * DK + c0 + i], g1 = gamma[s * DK + c0 + i + 1];
+                            const float a0 = s0v * g0, a1 = s1v * g1;
+                            pk[i / 2] = pack_bf16x2(g0 < kStrongGamma ? s0v : a0, g1 < kStrongGamma ? s1v : a1);
+                            rs[i] = __float_as_uint(a0 + __uint_as_float(rd[i]));
+                            rs[i + 1] = __float_as_uint(a1 + __uint_as_float(rd[i + 1]));
                         }
-                        pk[i / 2] = pack_bf16x2(s0v, s1v);
-                        rs[i] = __float_as_uint(s0v + __uint_as_float(rd[i]));
-                        rs[i + 1] = __float_as_uint(s1v + __uint_as_float(rd[i + 1]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; i += 2) {
+                            float s0v = __uint_as_float(rs[i]), s1v = __uint_as_float(rs[i + 1]);
+                            if (GATE) {
+                                s0v *= gamma[s * DK + c0 + i];
+                                s1v *= gamma[s * DK + c0 + i + 1];
+                            }
+                            pk[i / 2] = pack_bf16x2(s0v, s1v);
+                            rs[i] = __float_as_uint(s0v + __uint_as_float(rd[i]));
+                            rs[i + 1] = __float_as_uint(s1v + __uint_as_float(rd[i + 1]));
+                        }
                     }
                     tmem_st16(tS + c0, rs);
                     tmem_st8(tSB + c0 / 2, pk);
@@ -579,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                     mbar_arrive(bar(B_S_READY + (c & 1)));
                 }
             }
-            if (ok) {
+            if (ok && !(GATE && !SAFE && *strong_flag)) {
                 tc_fence_after();
                 float* fs = (p.final_state && jl < jvalid) ? p.final_state + (long)bh * DK * dv + j : nullptr;
                 const bool zl = norm && jl == 64 && p.final_z;
@@ -699,6 +967,21 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
             if (!mbar_wait_warp(bar(B_P_EMPTY + pb), ((c / Ly::NP) & 1) ^ 1, abort_flag, p.err)) break;
             tc_fence_after();
             if (t == 0) GLA_TRACE_POINT(10, c);
+            // strong channels of this chunk (published by the gate before the chunk's A product)
+            uint32_t smask[4] = {0u, 0u, 0u, 0u};
+            if constexpr (SAFE && GATE) {
+                const volatile uint32_t* slot = ring + (c % kRing) * 5;
+                if (!__all_sync(0xffffffffu, ring_wait(slot, static_cast<uint32_t>(c), abort_flag, p.err))) break;
+                __threadfence_block();
+#pragma unroll
+                for (int e = 0; e < 4; e++) smask[e] = slot[1 + e];
+            }
+            if (SAFE && GATE && (smask[0] | smask[1] | smask[2] | smask[3]) != 0u) {
+                const long row0 = (long)bh * L + (long)c * C;  // first token of the chunk in the raw inputs
+                strong_scores<DK, SCALAR>(tmem + lane_field + TM_A, t, min(C, L - c * C),
+                                          make_uint4(smask[0], smask[1], smask[2], smask[3]), p.q_raw + row0 * DK,
+                                          p.k_raw + row0 * DK, p.la_raw + (SCALAR ? row0 : row0 * DK), elu);
+            }
 #pragma unroll 1
             for (int h = 0; h < 2; h++) {
                 uint32_t r[32];
@@ -710,6 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
                     if (lane == 0) mbar_arrive(bar(B_A_EMPTY));
                     if (t == 0) GLA_TRACE_POINT(23, c);
                 }
+
 #pragma unroll
                 for (int k8 = 0; k8 < 4; k8++) {
                     float x[8];
@@ -952,9 +1236,28 @@ __global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __gri
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == W_MMA) {
+    // every role has finished and every copy has landed: the exact pass may reuse the CTA
+    return GATE && !SAFE && *strong_flag && !*abort_flag;
+}
+
+// The exact pass as a function of its own: its code and register allocation stay
+// out of the pass that every call runs.
+template <int DK, int DVT, bool SCALAR>
+__device__ __noinline__ void exact_pass(const TcParams& p, uint8_t* smem_raw) {
+    prefill_pass<DK, DVT, true, SCALAR, true>(p, smem_raw);
+}
+
+template <int DK, int DVT, bool GATE, bool SCALAR>
+__global__ void __launch_bounds__(kThreads, 1) gla_prefill_tc_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const bool redo = prefill_pass<DK, DVT, GATE, SCALAR, false>(p, smem_raw);
+    if constexpr (GATE) {
+        if (redo) exact_pass<DK, DVT, SCALAR>(p, smem_raw);
+    }
+    if ((threadIdx.x >> 5) == W_MMA) {
+        const uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
         tc_fence_after();
-        tmem_dealloc(tmem, TM_COLS);
+        tmem_dealloc(*reinterpret_cast<const uint32_t*>(sm + Layout<DK, DVT, SCALAR>::off_misc), TM_COLS);
     }
 }
 
@@ -995,6 +1298,9 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
     if (!p.out_f32 && encode_3d(&p.tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out, a.dv, a.L, BH, 64, C,
                                 CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    p.q_raw = static_cast<const uint16_t*>(a.q);
+    p.k_raw = static_cast<const uint16_t*>(a.k);
+    p.la_raw = a.log_alpha;
     p.init_state = a.init_state;
     p.init_z = a.init_z;
     p.out = a.out;

@@ -8,7 +8,7 @@
  *   and its flowchart: o_t is q_t applied to the updated state, o_t = S_t^T q_t.
  *   "linear-attention" blog, Linear attention: the fixed-size state replaces
  *   the KV cache, o_n = o_n(S_{n-1}, q_n, k_n, v_n); with alpha == 1 the state
- *   is a running sum of k_i v_i^T (section Prefill: "just a cumulative sum").
+ *   is a running sum of k_i v_i^T (section Prefill).
  *   "Gated Linear Attention", Summary / Chunk-Wise Block-Parallel: prefill
  *   evaluates the same function chunk by chunk, O(L C d + L d^2).
  *   "Transformers are RNNs" notes, kernel derivation: optional feature map
@@ -19,8 +19,14 @@
  *     channels), stored fp32 row-major per (batch, head).
  *   - Inputs are head-major: q, k, log_alpha [B][H][L][d_k]; v, out
  *     [B][H][L][d_v]; states [B][H][d_k][d_v].  All contiguous.
- *   - log_alpha is the natural log of the gate (fp32, <= 0); the library never
- *     applies a sigmoid or a temperature: the caller passes log alpha.
+ *   - log_alpha is the natural log of the gate (fp32, finite, <= 0, i.e.
+ *     alpha in (0, 1]); the library never applies a sigmoid or a temperature:
+ *     the caller passes log alpha.  Every such gate is computed exactly, with
+ *     no lower bound on alpha ("Gated Linear Attention", GLA Recurrent Form).
+ *     On the tensor-core path a chunk over which some key channel decays by
+ *     more than e^-64 makes its CTA compute its (head, value slice) a second
+ *     time with that channel's intra-chunk scores evaluated with exponents
+ *     <= 0 -- exact, but slower for such slices.
  *   - phi(x) = elu(x) + 1 when GLA_FLAG_FEATURE_ELU1 is set; the normaliser
  *     z (GLA_FLAG_NORMALIZE) is carried like one extra all-ones value column
  *     of the state, so it is decayed by alpha exactly like S.
