@@ -5,10 +5,12 @@ chunk 64, bf16 q/k/v, fp32 log alpha, fp32 initial state ~N(0, 0.1), returns
 the final state -- tokens/s for the whole job (all ranks).  One step is one
 gla_fwd call over the whole batch (the fused cumsum-gate / intra-chunk /
 inter-chunk / output kernel).  The same run also measures, each in its own
-JSON object: the decode step (256 sequences x H32, d128, fp32 state) as
-state HBM GB/s; the 8-token hand-off on that state; the long-context prefill
-with one gate per token; the delta rule and the backward pass (FP32-ALU
-rooflines); and the end-to-end step through gla_fwd_host with host buffers.
+JSON object: the other prefill workloads ("configs": fp32 B1 H1 L256 d32,
+elu+1 normalised B4 H8 L2048 d64, gated B8 H16 L4096 d128); the decode step
+(256 sequences x H32, d128, fp32 state, 1024 consecutive steps on fresh
+tokens) as state HBM GB/s; the 8-token hand-off on that state; the
+long-context prefill with one gate per token; the delta rule and the backward
+pass; and the end-to-end step through gla_fwd_host with host buffers.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gla|reference]
 
@@ -50,12 +52,14 @@ def prefill_flops(w) -> float:
     return per_head * w.B * w.H
 
 
-def prefill_bytes(w) -> float:
-    """Algorithmic bytes: q, k, v, log alpha read once, out written once, init/final state."""
+def prefill_bytes(w, final_state=True) -> float:
+    """Algorithmic bytes: q, k, v, log alpha read once, out written once, init/final state
+    (fp32 inputs and output for the fp32 workload, bf16 otherwise; no log alpha without a gate)."""
     BH, L = w.B * w.H, w.L
-    la_bytes = 4 if getattr(w, "scalar_gate", False) else 4 * w.dk  # one gate per token, or per channel
-    per_tok = 2 * w.dk + 2 * w.dk + 2 * w.dv + la_bytes + 2 * w.dv
-    states = (2 if w.init_std > 0 else 1) * w.dk * w.dv * 4
+    es = 4 if w.dtype == "f32" else 2
+    la_bytes = 0 if not w.gate else (4 if getattr(w, "scalar_gate", False) else 4 * w.dk)
+    per_tok = es * (2 * w.dk + w.dv) + la_bytes + es * w.dv
+    states = ((1 if w.init_std > 0 else 0) + (1 if final_state else 0)) * w.dk * w.dv * 4
     return float(BH * (L * per_tok + states))
 
 
@@ -271,6 +275,25 @@ def oracle_sample(seconds_target: float = 10.0):
     return tps, cores, desc, dt
 
 
+def oracle_single_thread(seconds_target: float = 3.0):
+    """The oracle on one host thread: one head of the long-context shape for a bounded number of
+    tokens, extrapolated to the whole B*H workload's tokens/s (labelled as extrapolated)."""
+    import oracle
+    Ls = 256
+    while True:
+        w = synth.with_shape(HEADLINE, B=1, H=1, L=Ls)
+        x = synth.make_prefill(w, heads=[0])
+        args = [synth.as_f64(x[n]) for n in ("q", "k", "v", "log_alpha", "init_state")]
+        t0 = time.perf_counter()
+        oracle.gla_fwd(*args, nthreads=1)
+        dt = time.perf_counter() - t0
+        if dt >= seconds_target / 4 or Ls >= HEADLINE.L:
+            break
+        Ls = min(HEADLINE.L, Ls * max(2, int(math.ceil(seconds_target / 4 / max(dt, 1e-3)))))
+    tps = Ls / dt / (HEADLINE.B * HEADLINE.H)
+    return tps, f"1 head x {Ls} tokens, 1 thread, extrapolated to the 32-head workload", dt
+
+
 def run_reference(args):
     rank, world, local = dist_env()
     if rank != 0:
@@ -417,7 +440,7 @@ def bench_prefill(args, device, rank, world):
         torch.cuda.synchronize(device)
         h2d_gbs = hv.numel() * hv.element_size() / (c0.elapsed_time(c1) / 1e3) / 1e9
         d2h_gbs = hout.numel() * hout.element_size() / (c1.elapsed_time(c2) / 1e3) / 1e9
-        ne = max(1, min(args.steps, 3))
+        ne = args.steps
         barrier(world)
         torch.cuda.synchronize(device)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -428,12 +451,67 @@ def bench_prefill(args, device, rank, world):
         torch.cuda.synchronize(device)
         gla.check(gla.gla_device_error(s_out))
         e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
-        res["e2e"] = dict(ms_per_step=e_ms / ne, h2d=h2d, d2h=d2h, groups=args.e2e_groups, h2d_gbs=h2d_gbs,
-                          d2h_gbs=d2h_gbs)
+        res["e2e"] = dict(ms_per_step=e_ms / ne, steps=ne, h2d=h2d, d2h=d2h, groups=args.e2e_groups,
+                          h2d_gbs=h2d_gbs, d2h_gbs=d2h_gbs)
         del hq, hk, hv, hla, hs0, hout, hfs, dq, dk_, dv_, dla, ds0, host, devb
     del q, k, v, la, s0, out, fs
     torch.cuda.empty_cache()
     return w, BH, res
+
+
+CONFIG_LEGS = (  # (key, workload, writes the final state)
+    ("fp32_small", synth.FP32_SMALL, True),
+    ("elu_norm", synth.ELU_NORM, False),
+    ("prefill", synth.PREFILL, True),
+)
+
+
+def bench_configs(args, device, rank):
+    """The other prefill workloads, each timed launch by launch with CUDA events on the launching
+    stream; L2 (129 MB) is flushed before every timed launch by writing a 256 MB buffer, so the
+    workloads smaller than L2 (the fp32 and elu+1 ones) read their inputs from HBM too."""
+    import torch
+
+    import causal_gated_linear_gb300 as gla
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=device)
+    res = {}
+    for key, w0, final in CONFIG_LEGS:
+        w = synth.with_shape(w0, seed=w0.seed + 1000 * rank)
+        x = synth.make_prefill(w)
+        q, k, v = (to_dev(x[n], device) for n in ("q", "k", "v"))
+        la, s0 = to_dev(x["log_alpha"], device), to_dev(x["init_state"], device)
+        f32 = w.dtype == "f32"
+        out = torch.empty((w.B, w.H, w.L, w.dv), dtype=torch.float32 if f32 else torch.bfloat16, device=device)
+        fs = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=device) if final else None
+        flags = (gla.FLAG_FEATURE_ELU1 if w.feature_elu1 else 0) | (gla.FLAG_NORMALIZE if w.normalize else 0)
+        dt = gla.F32 if f32 else gla.BF16
+
+        def call():
+            r = gla.gla_fwd_ex(q, k, v, out, w.B, w.H, w.L, w.dk, w.dv, log_alpha=la, init_state=s0,
+                               final_state=fs, in_dtype=dt, out_dtype=dt, flags=flags, stream=stream)
+            if r != 0:
+                raise RuntimeError(gla.gla_status_string(r))
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize(device)
+        evs = []
+        for _ in range(args.config_calls):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize(device)
+        gla.check(gla.gla_device_error(stream))
+        res[key] = dict(w=w, final=final, ms=statistics.mean(a.elapsed_time(b) for a, b in evs),
+                        calls=args.config_calls)
+        del q, k, v, la, s0, out, fs, x
+    del flush
+    torch.cuda.empty_cache()
+    return res
 
 
 def bench_decode(args, device, rank):
@@ -443,23 +521,28 @@ def bench_decode(args, device, rank):
     NS, H, dk, dv = DEC["NS"], DEC["H"], DEC["dk"], DEC["dv"]
     seed = DEC["seed"] + 1000 * rank
     st = to_dev(synth.decode_state(NS, H, dk, dv, DEC["state_std"], seed), device)
-    pool = []
-    for s in range(args.decode_pool):
-        t = synth.decode_token(NS, H, dk, dv, s, seed, DEC["gate_mean"], DEC["gate_std"])
-        pool.append(tuple(to_dev(t[n], device) for n in ("q", "k", "v", "log_alpha")))
+    n = args.decode_steps
+    # one fresh token per (sequence, head) for every step, drawn on the device before the timed
+    # region from a seeded generator with the workload's distributions: q, k, v ~ N(0, 1) in bf16,
+    # log alpha = logsigmoid(N(4, 1.5)) in fp32 (10.5 MB per step)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    tq = torch.randn((n, NS, H, dk), generator=g, device=device).to(torch.bfloat16)
+    tk = torch.randn((n, NS, H, dk), generator=g, device=device).to(torch.bfloat16)
+    tv = torch.randn((n, NS, H, dv), generator=g, device=device).to(torch.bfloat16)
+    tla = torch.nn.functional.logsigmoid(
+        torch.randn((n, NS, H, dk), generator=g, device=device) * DEC["gate_std"] + DEC["gate_mean"])
     out = torch.empty((NS, H, dv), dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
 
     def step(i):
-        q, k, v, la = pool[i % len(pool)]
-        r = gla.gla_decode_step(q, k, v, la, st, out, NS, H, dk, dv, stream=stream)
+        r = gla.gla_decode_step(tq[i], tk[i], tv[i], tla[i], st, out, NS, H, dk, dv, stream=stream)
         if r != 0:
             raise RuntimeError(gla.gla_status_string(r))
 
     for i in range(8):
         step(i)
     torch.cuda.synchronize(device)
-    n = args.decode_steps
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for i in range(n):
@@ -468,6 +551,8 @@ def bench_decode(args, device, rank):
     torch.cuda.synchronize(device)
     gla.check(gla.gla_device_error(stream))
     ms = ev0.elapsed_time(ev1) / n
+    del tq, tk, tv, tla
+    torch.cuda.empty_cache()
     return dict(ms_per_step=ms, steps=n, NS=NS, H=H, dk=dk, dv=dv)
 
 
@@ -586,6 +671,7 @@ def run_gla(args):
     peaks = load_peaks()
 
     w, BH, pre = bench_prefill(args, device, rank, world)
+    cfgs = bench_configs(args, device, rank) if args.config_calls > 0 else {}
     dec = bench_decode(args, device, rank) if args.decode_steps > 0 else None
     mdec = bench_decode_multi(args, device, rank) if args.multi_calls > 0 else None
     dlt = bench_delta(args, device, rank) if args.delta_calls > 0 else None
@@ -616,6 +702,21 @@ def run_gla(args):
         "gpu_launches": args.steps,
         "clocks": pre["clocks"],
     }
+    if cfgs:
+        line["configs"] = {}
+    for key, r in cfgs.items():
+        cw = r["w"]
+        cb = prefill_bytes(cw, final_state=r["final"])
+        cf = prefill_flops(cw)
+        sec = r["ms"] / 1e3
+        gbs = cb / sec / 1e9
+        line["configs"][key] = {
+            "workload": cw.name, "ms_per_launch": r["ms"], "us_per_launch": r["ms"] * 1e3, "calls": r["calls"],
+            "tokens_per_s": cw.B * cw.L / sec, "tflops": cf / sec / 1e12, "tensor_frac": cf / sec / 1e12 /
+            peaks["bf16_tflops"], "dtype": cw.dtype, "l2": "flushed (256 MB write) before every timed launch",
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "alg_bytes_per_launch": cb,
+                         "kernel": "gla_prefill_simt_kernel" if cw.dtype == "f32" else "gla_prefill_tc_kernel"}}
     if dec is not None:
         dbytes = decode_bytes(dec["NS"], dec["H"], dec["dk"], dec["dv"])
         gbs = dbytes / (dec["ms_per_step"] / 1e3) / 1e9
@@ -626,7 +727,7 @@ def run_gla(args):
                                        "traffic": recorded_traffic("gla_decode_kernel"),
                                        "kernel": "gla_decode_kernel", "alg_bytes_per_launch": dbytes},
                           "tokens_per_s": dec["NS"] * dec["H"] / (dec["ms_per_step"] / 1e3) / dec["H"],
-                          "token_pool": f"{args.decode_pool} distinct token sets reused cyclically"}
+                          "tokens": "a fresh token per (sequence, head) every step, all steps consecutive"}
     if "scalar" in pre:
         sw = pre["scalar"]["w"]
         sbytes = prefill_bytes(sw)
@@ -678,13 +779,17 @@ def run_gla(args):
         e = pre["e2e"]
         line["e2e"] = {"value": tokens * world / (e["ms_per_step"] / 1e3), "unit": "tokens/s",
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
-                       "ms_per_step": e["ms_per_step"], "api": "gla_fwd_host", "head_groups": e["groups"],
+                       "ms_per_step": e["ms_per_step"], "steps": e["steps"], "api": "gla_fwd_host",
+                       "head_groups": e["groups"],
                        "link": {"h2d_gbs": e["h2d_gbs"], "d2h_gbs": e["d2h_gbs"],
                                 "h2d_floor_ms": e["h2d"] / e["h2d_gbs"] / 1e6}}
     if rank == 0 and world == 1 and args.cpu_baseline:
         tps, cores, desc, dt = oracle_sample(args.ref_seconds)
+        tps1, desc1, dt1 = oracle_single_thread()
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                "sample": desc, "seconds": dt}
+                                "sample": desc, "seconds": dt,
+                                "single_thread": {"value": tps1, "unit": "tokens/s", "cores": 1,
+                                                  "extrapolated": True, "sample": desc1, "seconds": dt1}}
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -700,8 +805,10 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gla", choices=["gla", "reference"])
-    ap.add_argument("--decode-steps", type=int, default=256)
-    ap.add_argument("--decode-pool", type=int, default=8)
+    ap.add_argument("--decode-steps", type=int, default=1024,
+                    help="consecutive decode steps timed, each on fresh tokens (0: skip)")
+    ap.add_argument("--config-calls", type=int, default=20,
+                    help="timed launches of each of the fp32, elu+1 and B8 H16 prefill workloads (0: skip)")
     ap.add_argument("--delta-calls", type=int, default=3,
                     help="timed launches of the delta-rule workload (0: skip)")
     ap.add_argument("--bwd-calls", type=int, default=3,

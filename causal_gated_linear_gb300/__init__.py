@@ -20,6 +20,7 @@ The functions mirror the C entry points:
     gla_bwd(q, k, v, dout, dq, dk, dv, B, H, L, dk_dim, dv_dim, log_alpha=None, init_state=None,
             dfinal=None, dlog_alpha=None, dinit=None, in_dtype=BF16, flags=0, stream=None) -> int
     gla_device_error(stream=None) -> int
+    gla_test_set_waits(limit_ns=0, stall=False) -> int   (test only)
     gla_status_string(status) -> str
     gla_version() -> str
 
@@ -39,7 +40,7 @@ BF16, F32 = 0, 1
 FLAG_FEATURE_ELU1, FLAG_NORMALIZE, FLAG_FORCE_SIMT, FLAG_FORCE_CHUNK, FLAG_SCALAR_GATE = 1, 2, 4, 8, 16
 
 EXPORTED = ["gla_fwd", "gla_fwd_ex", "gla_fwd_host", "gla_decode_step", "gla_delta_fwd", "gla_bwd", "gla_device_error",
-            "gla_device_error_detail", "gla_status_string", "gla_version"]
+            "gla_device_error_detail", "gla_test_set_waits", "gla_status_string", "gla_version"]
 
 
 class GlaError(RuntimeError):
@@ -89,6 +90,8 @@ def load(path: str | None = None):
     lib.gla_device_error.restype = i
     lib.gla_device_error_detail.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
     lib.gla_device_error_detail.restype = i
+    lib.gla_test_set_waits.argtypes = [ctypes.c_ulonglong, i]
+    lib.gla_test_set_waits.restype = i
     lib.gla_status_string.argtypes = [i]
     lib.gla_status_string.restype = ctypes.c_char_p
     lib.gla_version.argtypes = []
@@ -185,6 +188,12 @@ def gla_device_error_detail(stream=None):
     buf = (ctypes.c_uint * 4)()
     st = load().gla_device_error_detail(_stream(stream), buf)
     return st, list(buf)
+
+
+def gla_test_set_waits(limit_ns: int = 0, stall: bool = False) -> int:
+    """Test only: limit of the prefill kernel's pipeline waits for later calls (0: the 2 s default),
+    and whether its gate role first waits on a barrier that nothing completes."""
+    return load().gla_test_set_waits(int(limit_ns), 1 if stall else 0)
 
 
 def gla_status_string(status: int) -> str:

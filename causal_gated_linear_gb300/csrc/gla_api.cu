@@ -7,6 +7,7 @@
 #include <cstring>
 
 #include "gla_internal.h"
+#include "gla_ptx.cuh"
 
 namespace gla {
 
@@ -37,6 +38,18 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 bool sync_check_enabled() {
     const char* e = std::getenv("GLA_SYNC_CHECK");
+    return e && e[0] == '1';
+}
+
+// Test hooks (see gla_test_set_waits in gla.h): the limit of the prefill
+// kernel's pipeline waits, whether its gate role first waits on a barrier that
+// nothing completes, and a launch failure injected after validation when
+// GLA_TEST_FAIL_LAUNCH=1 is set in the environment.
+unsigned long long g_wait_ns = kWaitLimitNs;
+int g_stall = 0;
+
+bool launch_failure_injected() {
+    const char* e = std::getenv("GLA_TEST_FAIL_LAUNCH");
     return e && e[0] == '1';
 }
 
@@ -128,6 +141,8 @@ int gla_fwd_ex(const gla_fwd_args* a, void* stream) {
     pa.out_dtype = a->out_dtype;
     pa.flags = a->flags;
     pa.pf_dist = 0;
+    pa.wait_ns = g_wait_ns;
+    pa.test_stall = g_stall;
     const size_t BH = (size_t)a->B * a->H;
     if (a->L == 0) {
         // no tokens: the final state is the initial one
@@ -141,6 +156,7 @@ int gla_fwd_ex(const gla_fwd_args* a, void* stream) {
                           : cudaMemsetAsync(a->final_z, 0, nz, s);
         return finish(e, s);
     }
+    if (launch_failure_injected()) return GLA_ERR_CUDA;
     pa.err_word = err_word_ptr();
     if (!pa.err_word) return GLA_ERR_CUDA;
     cudaError_t e;
@@ -304,6 +320,7 @@ int gla_decode_step(const void* q, const void* k, const void* v, const float* lo
     a.dk = dk;
     a.dv = dv;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (launch_failure_injected()) return GLA_ERR_CUDA;
     return finish(launch_decode(a, s), s);
 }
 
@@ -350,6 +367,7 @@ int gla_delta_fwd(const void* q, const void* k, const void* v, const float* beta
     a.dk = dk;
     a.dv = dv;
     a.out_dtype = out_dtype;
+    if (launch_failure_injected()) return GLA_ERR_CUDA;
     return finish(launch_delta(a, s), s);
 }
 
@@ -407,6 +425,7 @@ int gla_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
     a.dv = dv;
     a.in_dtype = in_dtype;
     a.flags = flags;
+    if (launch_failure_injected()) return GLA_ERR_CUDA;
     // a per-token gate's gradient is accumulated across the row blocks of a head
     if (scalar && dlog_alpha && cudaMemsetAsync(dlog_alpha, 0, nla * 4, s) != cudaSuccess) return GLA_ERR_CUDA;
     return finish(launch_bwd(a, s), s);
@@ -433,6 +452,12 @@ const char* gla_status_string(int status) {
     }
 }
 
-const char* gla_version(void) { return "gla-gb300 0.1.0 (sm_103a)"; }
+int gla_test_set_waits(unsigned long long limit_ns, int stall) {
+    g_wait_ns = limit_ns ? limit_ns : kWaitLimitNs;
+    g_stall = stall ? 1 : 0;
+    return GLA_OK;
+}
+
+const char* gla_version(void) { return "gla-gb300 0.2.0 (sm_103a)"; }
 
 }  // extern "C"

@@ -24,6 +24,8 @@ struct PrefillArgs {
     unsigned flags;
     unsigned* err_word;  // device address of the error word
     int pf_dist;         // short-sequence kernel: CTAs ahead whose inputs it prefetches into L2
+    unsigned long long wait_ns;  // tensor-core kernel: limit of its pipeline waits
+    int test_stall;              // tensor-core kernel: gate role first waits on a barrier nothing completes
 };
 
 struct DecodeArgs {

@@ -12,7 +12,9 @@ namespace gla {
 // Device error word bits (see gla_device_error in gla.h).
 constexpr unsigned kErrTimeout = 1u;
 
-// A pipeline wait gives up after this many nanoseconds of global time.
+// A pipeline wait gives up after this many nanoseconds of global time (the
+// default; a launch may pass a shorter limit for its pipeline waits, but the
+// teardown waits that drain copies and products in flight always use this one).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -96,16 +98,16 @@ __device__ __forceinline__ void record_timeout_code(unsigned* err_word, uint32_t
 
 // Wait until the phase with the given parity has completed.  Returns false
 // (and raises the CTA's abort flag and the device error word) if it does not
-// complete within kWaitLimitNs, or if another role already aborted.
+// complete within `limit_ns`, or if another role already aborted.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned* err_word) {
+                                          unsigned* err_word, unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
+            if (globaltimer() - t0 > limit_ns) {
                 *abort_flag = 1;
                 if (err_word) record_timeout(err_word, bar, parity);
                 return false;
@@ -136,8 +138,8 @@ __device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t count, bool pr
 
 // Warp-uniform bounded wait: every lane gets the same answer.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                               unsigned* err_word) {
-    const bool ok = mbar_wait(bar, parity, abort_flag, err_word);
+                                               unsigned* err_word, unsigned long long limit_ns = kWaitLimitNs) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, err_word, limit_ns);
     return __all_sync(0xffffffffu, ok);
 }
 

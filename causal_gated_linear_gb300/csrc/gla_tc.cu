@@ -124,6 +124,7 @@ enum {
     B_O_FULL = B_SB_EMPTY + 2,   // 2
     B_O_EMPTY = B_O_FULL + 2,  // 2
     B_DRAIN = B_O_EMPTY + 2,
+    B_STALL,  // completed by nothing: the test-only stall waits on it
     B_COUNT
 };
 
@@ -176,6 +177,8 @@ struct TcParams {
     float* final_state;
     float* final_z;
     unsigned* err;
+    unsigned long long wait_ns;  // limit of the pipeline waits (the drain waits keep kWaitLimitNs)
+    int test_stall;              // gate role first waits on B_STALL (error-path tests)
     int L, dv, nchunks, ntile;
     unsigned flags;
     int out_f32;
@@ -402,14 +405,14 @@ __device__ __noinline__ void strong_scores(uint32_t taddr, int t, int nval, uint
 
 // Wait (bounded) until the gate has published the strong-channel masks of chunk c.
 __device__ __forceinline__ bool ring_wait(const volatile uint32_t* slot, uint32_t c, volatile int* abort_flag,
-                                          unsigned* err_word) {
+                                          unsigned* err_word, unsigned long long limit_ns) {
     if (slot[0] == c) return true;
     const unsigned long long t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (slot[0] == c) return true;
         if ((it & 255u) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
+            if (globaltimer() - t0 > limit_ns) {
                 *abort_flag = 1;
                 if (err_word) record_timeout_code(err_word, 0x10000000u | ((c & 0xffffu) << 1));
                 return false;
@@ -501,6 +504,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
         mbar_init(bar(B_O_EMPTY), 4);
         mbar_init(bar(B_O_EMPTY + 1), 4);
         mbar_init(bar(B_DRAIN), 2);
+        mbar_init(bar(B_STALL), 1);
         *abort_flag = 0;
         *oi_issued = 0;
         *strong_flag = 0;
@@ -540,11 +544,14 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
         const int quad = gt % QUADS, seg = gt / QUADS;
         const int ch = 4 * quad;
         const int atom = ch >> 6, col = ch & 63;
+        // error-path tests: a wait that nothing completes runs out and stops every role
+        bool ok0 = true;
+        if (p.test_stall) ok0 = mbar_wait(bar(B_STALL), 0, abort_flag, p.err, p.wait_ns);
         for (int c = 0; c < N; c++) {
             const int s = c % NS, l = c % NL;
-            bool ok = true;
-            if (GATE) ok = mbar_wait(bar(B_LA_FULL + l), (c / NL) & 1, abort_flag, p.err);
-            if (ok) ok = mbar_wait(bar(B_QK_FULL + s), (c / NS) & 1, abort_flag, p.err);
+            bool ok = ok0;
+            if (GATE && ok) ok = mbar_wait(bar(B_LA_FULL + l), (c / NL) & 1, abort_flag, p.err, p.wait_ns);
+            if (ok) ok = mbar_wait(bar(B_QK_FULL + s), (c / NS) & 1, abort_flag, p.err, p.wait_ns);
             if (threadIdx.x == 0) GLA_TRACE_POINT(0, c);
             // Phase 1: per-segment cumulative sums of log alpha, exchanged across the
             // gate warps to give each thread the prefix before its segment (off) and
@@ -693,12 +700,12 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
             for (int c = 0; c < N; c++) {
                 const int s = c % NS;
                 const int sb = c & 1;
-                ok = mbar_wait_warp(bar(B_DS_FULL), c & 1, abort_flag, p.err);
+                ok = mbar_wait_warp(bar(B_DS_FULL), c & 1, abort_flag, p.err, p.wait_ns);
                 if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(16, c);
-                if (ok && GATE) ok = mbar_wait_warp(bar(B_QK_GATED + s), (c / NS) & 1, abort_flag, p.err);
+                if (ok && GATE) ok = mbar_wait_warp(bar(B_QK_GATED + s), (c / NS) & 1, abort_flag, p.err, p.wait_ns);
                 if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(17, c);
                 // this chunk's bf16 copy of S' is free once O_i(c-2) has completed
-                if (ok) ok = mbar_wait_warp(bar(B_SB_EMPTY + sb), ((c >> 1) & 1) ^ 1, abort_flag, p.err);
+                if (ok) ok = mbar_wait_warp(bar(B_SB_EMPTY + sb), ((c >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                 if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(18, c);
                 if (!ok) break;
                 tc_fence_after();
@@ -795,10 +802,10 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
             bool ok = true;
             for (int c = 0; c < N; c++) {
                 const int s = c % NS;
-                ok = mbar_wait_warp(bar(B_DS_FULL), c & 1, abort_flag, p.err);
-                if (ok && GATE) ok = mbar_wait_warp(bar(B_QK_GATED + s), (c / NS) & 1, abort_flag, p.err);
+                ok = mbar_wait_warp(bar(B_DS_FULL), c & 1, abort_flag, p.err, p.wait_ns);
+                if (ok && GATE) ok = mbar_wait_warp(bar(B_QK_GATED + s), (c / NS) & 1, abort_flag, p.err, p.wait_ns);
                 // the single bf16 copy of S' is free once O_i(c-1) has completed
-                if (ok) ok = mbar_wait_warp(bar(B_SB_EMPTY), (c & 1) ^ 1, abort_flag, p.err);
+                if (ok) ok = mbar_wait_warp(bar(B_SB_EMPTY), (c & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t tSB = tmem + lane_field + TM_SB;
@@ -873,7 +880,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
         const bool leader = warp == W_OUT0 && lane == 0;
         uint8_t* ost = sm + Ly::off_ost;
         for (int c = 0; c < N; c++) {
-            bool ok = mbar_wait_warp(bar(B_O_FULL + (c & 1)), (c >> 1) & 1, abort_flag, p.err);
+            bool ok = mbar_wait_warp(bar(B_O_FULL + (c & 1)), (c >> 1) & 1, abort_flag, p.err, p.wait_ns);
             // staging may be rewritten once the previous bulk store has read it
             if (leader && !p.out_f32) bulk_wait_group_read0();
             ok = bar_red_and(2, 128, ok);
@@ -963,15 +970,15 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
         for (int c = 0; c < N; c++) {
             const int pb = c % Ly::NP;
             uint8_t* P = sm + Ly::off_p + pb * Ly::PB;
-            if (!mbar_wait_warp(bar(B_A_FULL), c & 1, abort_flag, p.err)) break;
-            if (!mbar_wait_warp(bar(B_P_EMPTY + pb), ((c / Ly::NP) & 1) ^ 1, abort_flag, p.err)) break;
+            if (!mbar_wait_warp(bar(B_A_FULL), c & 1, abort_flag, p.err, p.wait_ns)) break;
+            if (!mbar_wait_warp(bar(B_P_EMPTY + pb), ((c / Ly::NP) & 1) ^ 1, abort_flag, p.err, p.wait_ns)) break;
             tc_fence_after();
             if (t == 0) GLA_TRACE_POINT(10, c);
             // strong channels of this chunk (published by the gate before the chunk's A product)
             uint32_t smask[4] = {0u, 0u, 0u, 0u};
             if constexpr (SAFE && GATE) {
                 const volatile uint32_t* slot = ring + (c % kRing) * 5;
-                if (!__all_sync(0xffffffffu, ring_wait(slot, static_cast<uint32_t>(c), abort_flag, p.err))) break;
+                if (!__all_sync(0xffffffffu, ring_wait(slot, static_cast<uint32_t>(c), abort_flag, p.err, p.wait_ns))) break;
                 __threadfence_block();
 #pragma unroll
                 for (int e = 0; e < 4; e++) smask[e] = slot[1 + e];
@@ -1095,7 +1102,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     const unsigned long long now = globaltimer();
                     if (idle == 256) {
                         t_last = now;
-                    } else if (now - t_last > kWaitLimitNs) {
+                    } else if (now - t_last > p.wait_ns) {
                         *abort_flag = 1;
                         record_timeout_code(p.err, 0x20000000u | ((pl_n & 0xff) << 16) | ((pq_n & 0xff) << 8) |
                                                        (pv_n & 0xff));
@@ -1209,7 +1216,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     if (*abort_flag) break;
                     const unsigned long long now = globaltimer();
                     if (idle == 256) t_last = now;
-                    else if (now - t_last > kWaitLimitNs) {
+                    else if (now - t_last > p.wait_ns) {
                         *abort_flag = 1;
                         // scheduler progress at the time: next dS, A, O_i, O_a chunk (8 bits each)
                         record_timeout_code(p.err, 0x40000000u | ((nd & 0xff) << 22) | ((na & 0xff) << 14) |
@@ -1307,6 +1314,8 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
     p.final_state = a.final_state;
     p.final_z = a.final_z;
     p.err = a.err_word;
+    p.wait_ns = a.wait_ns;
+    p.test_stall = a.test_stall;
     p.L = a.L;
     p.dv = a.dv;
     p.nchunks = (a.L + C - 1) / C;

@@ -229,6 +229,11 @@ int gla_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
 /*
  * gla_device_error -- synchronise `stream`, read and clear the device error
  * word that bounded waits set.  Returns GLA_OK, GLA_ERR_TIMEOUT or GLA_ERR_CUDA.
+ * The record is one per device and process, shared by every call on every
+ * stream: a wait that ran out in a call on one stream is reported to (and
+ * cleared by) whichever caller reads the record next, on any stream.  Callers
+ * that run concurrent calls on several streams should read it only after
+ * synchronising all of them.
  */
 int gla_device_error(void* stream);
 
@@ -242,6 +247,23 @@ int gla_device_error(void* stream);
  * [3] CTA index.  For diagnosing a GLA_ERR_TIMEOUT; gla_device_error clears it.
  */
 int gla_device_error_detail(void* stream, unsigned* detail4);
+
+/*
+ * gla_test_set_waits -- TEST ONLY.  For the calls that follow: `limit_ns` is
+ * the limit, in nanoseconds, of the tensor-core prefill kernel's pipeline
+ * waits (0 restores the default of 2 s; the waits that drain copies and
+ * products still in flight before a CTA exits always keep the default), and
+ * with `stall` nonzero the kernel's gate role first waits on a barrier that
+ * nothing completes, so that wait runs out after `limit_ns`, every role of the
+ * CTA stops, and the call reports GLA_ERR_TIMEOUT through gla_device_error
+ * (outputs undefined).  Used to check the error path and that the device stays
+ * usable afterwards.  Process-wide; not thread-safe.  Returns GLA_OK.
+ *
+ * Also for tests: with GLA_TEST_FAIL_LAUNCH=1 in the environment, every entry
+ * point that launches a kernel returns GLA_ERR_CUDA after its argument
+ * validation and before any launch (an injected launch failure).
+ */
+int gla_test_set_waits(unsigned long long limit_ns, int stall);
 
 /* Human-readable name of a gla_status value (static string). */
 const char* gla_status_string(int status);

@@ -66,3 +66,12 @@ def test_clock_samples_outside_the_timed_region_are_dropped(tmp_path, monkeypatc
     assert s["samples"] == 2 and s["sm_mhz"] == 2062.5 and s["reasons"] == ["sw_power_cap"]
     c.mark(t0 + 5.0, t0 + 6.0)
     assert c.summary()["samples"] == 0
+
+
+def test_prefill_bytes_of_the_other_workloads():
+    # fp32 B1 H1 L256 d32: q, k, v, log alpha, out in fp32 (5 x 128 B per token) + the final state
+    assert bench.prefill_bytes(synth.FP32_SMALL) == 256 * 640 + 32 * 32 * 4 == 167936
+    # elu+1 normalised, B4 H8 L2048 d64, no gate, no state written: q, k, v, out in bf16
+    assert bench.prefill_bytes(synth.ELU_NORM, final_state=False) == 32 * 2048 * (3 * 128 + 128) == 33554432
+    # gated B8 H16 L4096 d128, zero initial state, final state written
+    assert bench.prefill_bytes(synth.PREFILL) == 128 * (4096 * (3 * 256 + 512 + 256) + 128 * 128 * 4) == 813694976

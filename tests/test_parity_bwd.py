@@ -154,3 +154,20 @@ def test_bwd_full_sampled_and_homogeneity():
     ref = oracle.gla_bwd(f(xs["q"]), f(xs["k"]), f(xs["v"]), f(xs["dout"]), f(xs["log_alpha"]))
     got = [None if a is None else a.reshape((BH,) + a.shape[2:])[heads] for a in (dq, dk, dv, dla)]
     _check(got + [None], list(ref[:4]) + [None], True)
+
+
+@pytest.mark.parametrize("scalar", [False, True])
+def test_bwd_deterministic_bitwise(scalar):
+    """Two runs on the same inputs give bit-identical gradients.  With one gate per channel every
+    output is a fixed-order fp32 computation; with one gate per token the token gradient is summed
+    across the row blocks of a head by fp32 atomics (include/gla.h), so that one output is only
+    held to the fp32 bar between runs and every other output must still be bit-identical."""
+    w = synth.with_shape(_w(1, 3, 333, 128, 128, seed=41), scalar_gate=scalar)
+    x = synth.make_bwd(w, dfinal_std=0.5)
+    a = run_bwd(w, x)
+    b = run_bwd(w, x)
+    for name, ga, gb in zip(("dq", "dk", "dv", "dlog_alpha", "dinit"), a, b):
+        if scalar and name == "dlog_alpha":
+            assert rel_l2(ga, gb) <= F32_REL, name
+        else:
+            assert np.array_equal(ga, gb), name
