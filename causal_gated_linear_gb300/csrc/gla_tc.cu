@@ -93,9 +93,12 @@ constexpr uint32_t TM_S = 0;     // S^T fp32, dk columns (128-column tile)
 constexpr uint32_t TM_DS = 128;  // dS^T fp32, dk columns
 constexpr uint32_t TM_SB = 256;  // bf16 copy of S'^T, dk/2 columns (128-column tile)
 // With the 64-column tile (M = 64) S^T is held in the state warps'
-// registers instead, and columns 0..127 hold two bf16 copies of S'^T (one
-// per chunk parity), so the state update of chunk c+1 need not wait for
-// O_i(c) to finish reading its copy.
+// registers instead, and the map is: dS^T buffers for even and odd chunks at
+// 0..127 and 128..255, O^T 2 x 64 at 256..383, A at 448..511.  The bf16 copy
+// of S'^T for O_i(c) is written into chunk c's own dS buffer once the state
+// warps have read dS(c) from it (each half of the key channels into its own
+// half of the buffer), and the buffer is released when O_i(c) completes: the
+// state update never waits on a product, only dS(c+2) waits on O_i(c).
 constexpr uint32_t TM_O = 320;   // 2 x O^T fp32, 64 columns each
 constexpr uint32_t TM_A = 448;   // A fp32, 64 columns
 constexpr uint32_t TM_COLS = 512;
@@ -117,9 +120,9 @@ enum {
     B_A_EMPTY,
     B_P_FULL,    // 2
     B_P_EMPTY = B_P_FULL + 2,  // 2
-    B_DS_FULL = B_P_EMPTY + 2,
-    B_DS_EMPTY,
-    B_S_READY,   // 2
+    B_DS_FULL = B_P_EMPTY + 2,    // 2 (one per dS buffer; the 128-column tile uses one)
+    B_DS_EMPTY = B_DS_FULL + 2,   // 2
+    B_S_READY = B_DS_EMPTY + 2,   // 2
     B_SB_EMPTY = B_S_READY + 2,  // 2
     B_O_FULL = B_SB_EMPTY + 2,   // 2
     B_O_EMPTY = B_O_FULL + 2,  // 2
@@ -461,6 +464,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
     // A(c) comes from the TMA producer thread (128-column tile) or, with the
     // 64-column tile, from the MMA thread together with the other three products
     constexpr bool kTwoIssuers = DVT == 128;
+    constexpr uint32_t kTmO = DVT == 64 ? 256u : TM_O;  // the two O^T buffers
     const int tile = blockIdx.x % p.ntile;
     const int bh = blockIdx.x / p.ntile;
     const int j0 = tile * DVT;
@@ -495,8 +499,11 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
             mbar_init(bar(B_P_EMPTY + i), 1);
             mbar_init(bar(B_SB_EMPTY + i), 1);
         }
-        mbar_init(bar(B_DS_FULL), 1);
-        mbar_init(bar(B_DS_EMPTY), 8);
+        for (int i = 0; i < 2; i++) {
+            mbar_init(bar(B_DS_FULL + i), 1);
+            // 64-column tile: released by the commit after O_i; 128-column tile: by the state warps
+            mbar_init(bar(B_DS_EMPTY + i), DVT == 64 ? 1 : 8);
+        }
         mbar_init(bar(B_S_READY), 8);
         mbar_init(bar(B_S_READY + 1), 8);
         mbar_init(bar(B_O_FULL), 1);
@@ -682,7 +689,6 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
             const int jl = lane_to_col<DVT>(warp & 3, lane & 15);
             const int j = j0 + jl;
             const bool jv = jl < jvalid;
-            const uint32_t tD = tmem + lane_field + TM_DS;
             float S[NG * 16];
             {
                 const float* s0 = (p.init_state && jv) ? p.init_state + (long)bh * DK * dv + j : nullptr;
@@ -691,26 +697,21 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
 #pragma unroll
                     for (int i = 0; i < 16; i++)
                         S[g * 16 + i] = s0 ? s0[(long)(cbase + g * 32 + hi * 16 + i) * dv] : 0.f;
-                // first phase of the dS buffer's release (the protocol shared with the
-                // 128-column tile, whose state initialisation writes TMEM)
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_DS_EMPTY));
             }
             bool ok = true;
             for (int c = 0; c < N; c++) {
                 const int s = c % NS;
-                const int sb = c & 1;
-                ok = mbar_wait_warp(bar(B_DS_FULL), c & 1, abort_flag, p.err, p.wait_ns);
+                ok = mbar_wait_warp(bar(B_DS_FULL + (c & 1)), (c >> 1) & 1, abort_flag, p.err, p.wait_ns);
                 if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(16, c);
                 if (ok && GATE) ok = mbar_wait_warp(bar(B_QK_GATED + s), (c / NS) & 1, abort_flag, p.err, p.wait_ns);
                 if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(17, c);
-                // this chunk's bf16 copy of S' is free once O_i(c-2) has completed
-                if (ok) ok = mbar_wait_warp(bar(B_SB_EMPTY + sb), ((c >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
-                if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(18, c);
                 if (!ok) break;
                 tc_fence_after();
                 if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(4, c);
-                const uint32_t tSB = tmem + lane_field + (uint32_t)sb * 64u;
+                // dS(c) and, once read, this chunk's bf16 copy of S' for O_i: this half's key
+                // channels [cbase, cbase + COLS) occupy columns [cbase, cbase + COLS) of the buffer,
+                // and their copy goes to [cbase, cbase + COLS / 2)
+                const uint32_t tB = tmem + lane_field + (uint32_t)(c & 1) * 128u;
                 // a chunk with a strong channel: that channel's copy feeding O_i is S itself
                 // (its q carries e^{b_t}), every other channel's is e^{b_C} S as usual
                 const uint32_t* slot = ring + (c % kRing) * 5;
@@ -718,35 +719,45 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                 auto update = [&](auto strong_tag) {
                     constexpr bool ST = decltype(strong_tag)::value;
 #pragma unroll
-                    for (int g = 0; g < NG * 2; g++) {
-                        // 8 key channels per half-warp: c0 + [0, 8) for threads 0-15, c0 + 16 + [0, 8)
-                        // for threads 16-31 (S index g/2 * 16 + (g&1) * 8 + i)
-                        const int c0 = cbase + (g >> 1) * 32 + (g & 1) * 8;
-                        uint32_t d[8];
-                        tmem_ld16x2_x8<16>(tD + c0, d);
-                        tmem_wait_ld();
-                        const float* gm = gamma + s * DK + c0 + hi * 16;
-                        uint32_t pk[4];
+                    for (int gp = 0; gp < NG * 2; gp += 2) {
+                        // two groups of 8 key channels per half-warp (c0 + [0, 8) for threads 0-15,
+                        // c0 + 16 + [0, 8) for threads 16-31; S index g/2 * 16 + (g&1) * 8 + i), both
+                        // read before either copy is written: the copy of group gp lands on columns
+                        // that group gp + 1 reads
+                        uint32_t d[2][8];
 #pragma unroll
-                        for (int i = 0; i < 8; i += 4) {
-                            float4 gv = make_float4(1.f, 1.f, 1.f, 1.f);
-                            if (GATE) gv = *reinterpret_cast<const float4*>(gm + i);
-                            float* sv = S + g * 8 + i;
-                            const float a0 = sv[0] * gv.x, a1 = sv[1] * gv.y, a2 = sv[2] * gv.z, a3 = sv[3] * gv.w;
-                            if (ST) {
-                                pk[i / 2] = pack_bf16x2(gv.x < kStrongGamma ? sv[0] : a0, gv.y < kStrongGamma ? sv[1] : a1);
-                                pk[i / 2 + 1] =
-                                    pack_bf16x2(gv.z < kStrongGamma ? sv[2] : a2, gv.w < kStrongGamma ? sv[3] : a3);
-                            } else {
-                                pk[i / 2] = pack_bf16x2(a0, a1);
-                                pk[i / 2 + 1] = pack_bf16x2(a2, a3);
+                        for (int u = 0; u < 2; u++)
+                            tmem_ld16x2_x8<16>(tB + cbase + ((gp + u) >> 1) * 32 + ((gp + u) & 1) * 8, d[u]);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int u = 0; u < 2; u++) {
+                            const int g = gp + u;
+                            const int c0 = cbase + (g >> 1) * 32 + (g & 1) * 8;
+                            const float* gm = gamma + s * DK + c0 + hi * 16;
+                            uint32_t pk[4];
+#pragma unroll
+                            for (int i = 0; i < 8; i += 4) {
+                                float4 gv = make_float4(1.f, 1.f, 1.f, 1.f);
+                                if (GATE) gv = *reinterpret_cast<const float4*>(gm + i);
+                                float* sv = S + g * 8 + i;
+                                const float a0 = sv[0] * gv.x, a1 = sv[1] * gv.y, a2 = sv[2] * gv.z,
+                                            a3 = sv[3] * gv.w;
+                                if (ST) {
+                                    pk[i / 2] = pack_bf16x2(gv.x < kStrongGamma ? sv[0] : a0,
+                                                            gv.y < kStrongGamma ? sv[1] : a1);
+                                    pk[i / 2 + 1] = pack_bf16x2(gv.z < kStrongGamma ? sv[2] : a2,
+                                                                gv.w < kStrongGamma ? sv[3] : a3);
+                                } else {
+                                    pk[i / 2] = pack_bf16x2(a0, a1);
+                                    pk[i / 2 + 1] = pack_bf16x2(a2, a3);
+                                }
+                                sv[0] = a0 + __uint_as_float(d[u][i]);
+                                sv[1] = a1 + __uint_as_float(d[u][i + 1]);
+                                sv[2] = a2 + __uint_as_float(d[u][i + 2]);
+                                sv[3] = a3 + __uint_as_float(d[u][i + 3]);
                             }
-                            sv[0] = a0 + __uint_as_float(d[i]);
-                            sv[1] = a1 + __uint_as_float(d[i + 1]);
-                            sv[2] = a2 + __uint_as_float(d[i + 2]);
-                            sv[3] = a3 + __uint_as_float(d[i + 3]);
+                            tmem_st16x2_x4<8>(tB + cbase + (c0 - cbase) / 2, pk);
                         }
-                        tmem_st16x2_x4<8>(tSB + c0 / 2, pk);
                     }
                 };
                 if (sgc)
@@ -756,10 +767,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bar(B_DS_EMPTY));
-                    mbar_arrive(bar(B_S_READY + (c & 1)));
-                }
+                if (lane == 0) mbar_arrive(bar(B_S_READY + (c & 1)));
                 if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(5, c);
             }
             // a marked slice leaves its final state to the exact pass (init_state may alias it)
@@ -894,7 +902,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                 const int jr = lane_to_col<DVT>(warp & 3, lane & 15);
                 const int t0 = (lane >> 4) * 32;
                 uint32_t r[32];
-                tmem_ld16x2_x32<32>(tmem + lane_field + TM_O + (c & 1) * 64, r);
+                tmem_ld16x2_x32<32>(tmem + lane_field + kTmO + (c & 1) * 64, r);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
@@ -915,7 +923,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
 #pragma unroll 1
             for (int h = 0; h < 2; h++) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_field + TM_O + (c & 1) * 64 + h * 32, r);
+                tmem_ld32(tmem + lane_field + kTmO + (c & 1) * 64 + h * 32, r);
                 tmem_wait_ld();
                 if (h == 1) {
                     tc_fence_before();
@@ -1141,7 +1149,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     const uint64_t pd = kK | ((sbase + Ly::off_p + (no % Ly::NP) * Ly::PB) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < C / 16; kk++)
-                        mma_ss(tmem + TM_O + (no & 1) * 64, vd + kk * (2048 >> 4), pd + kk * (32 >> 4), idOa, 1);
+                        mma_ss(tmem + kTmO + (no & 1) * 64, vd + kk * (2048 >> 4), pd + kk * (32 >> 4), idOa, 1);
                     mma_commit(bar(B_O_FULL + (no & 1)));
                     mma_commit(bar(B_P_EMPTY + no % Ly::NP));
                     mma_commit(bar(B_V_EMPTY + no % NV));
@@ -1155,13 +1163,17 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                         tc_fence_after();
                         // O^T = S'^T Qh^T  (A operand: bf16 copy of the decayed state in TMEM)
                         const uint64_t qd = kK | (qs_of(ni) >> 4);
-                        const uint32_t tsb = tmem + (DVT == 64 ? (uint32_t)(ni & 1) * 64u : TM_SB);
+                        // 64-column tile: the copy sits in chunk ni's dS buffer, key channels
+                        // [0, DK/2) at columns [0, DK/4) and [DK/2, DK) at [DK/2, 3 DK/4)
+                        const uint32_t tsb = tmem + (DVT == 64 ? (uint32_t)(ni & 1) * 128u : TM_SB);
 #pragma unroll
                         for (int kk = 0; kk < DK / 16; kk++) {
                             const uint32_t off = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-                            mma_ts(tmem + TM_O + (ni & 1) * 64, tsb + kk * 8, qd + off, idOi, kk > 0);
+                            const uint32_t acol = DVT == 64 ? kk * 8 + (kk * 16 >= DK / 2 ? DK / 4 : 0) : kk * 8;
+                            mma_ts(tmem + kTmO + (ni & 1) * 64, tsb + acol, qd + off, idOi, kk > 0);
                         }
-                        mma_commit(bar(B_SB_EMPTY + (DVT == 64 ? (ni & 1) : 0)));
+                        // the copy's buffer takes dS(ni + 2) once O_i(ni) has read it
+                        mma_commit(bar(DVT == 64 ? B_DS_EMPTY + (ni & 1) : B_SB_EMPTY));
                         ni++;
                         *oi_issued = ni;
                         i_s = i_o = false;
@@ -1169,7 +1181,9 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     }
                 }
                 if (nd < N) {
-                    if (!d_e) d_e = mbar_test(bar(B_DS_EMPTY), nd & 1);
+                    if (!d_e)
+                        d_e = DVT == 64 ? mbar_test(bar(B_DS_EMPTY + (nd & 1)), ((nd >> 1) & 1) ^ 1)
+                                        : mbar_test(bar(B_DS_EMPTY), nd & 1);
                     if (d_e && !d_g) d_g = mbar_test(bar(B_QK_GATED + nd % NS), (nd / NS) & 1);
                     if (d_g && !d_v) d_v = mbar_test(bar(B_V_FULL + nd % NV), (nd / NV) & 1);
                     if (d_v) {
@@ -1178,8 +1192,9 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                         const uint64_t vd = kMN | (vs_of(nd) >> 4), kd = kMN | ((qs_of(nd) + Ly::QB) >> 4);
 #pragma unroll
                         for (int kk = 0; kk < C / 16; kk++)
-                            mma_ss(tmem + TM_DS, vd + kk * (2048 >> 4), kd + kk * (2048 >> 4), idS, kk > 0);
-                        mma_commit(bar(B_DS_FULL));
+                            mma_ss(tmem + (DVT == 64 ? (uint32_t)(nd & 1) * 128u : TM_DS), vd + kk * (2048 >> 4),
+                                   kd + kk * (2048 >> 4), idS, kk > 0);
+                        mma_commit(bar(B_DS_FULL + (DVT == 64 ? (nd & 1) : 0)));
                         nd++;
                         d_e = d_g = d_v = false;
                         prog = true;
