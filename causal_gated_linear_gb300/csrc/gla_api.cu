@@ -376,7 +376,7 @@ int gla_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
             float* dinit, int B, int H, int L, int dk, int dv, int in_dtype, unsigned flags, void* stream) {
     if (B < 1 || H < 1 || L < 0 || dk < 1 || dv < 1) return GLA_ERR_INVALID;
     if (in_dtype != GLA_DTYPE_BF16 && in_dtype != GLA_DTYPE_F32) return GLA_ERR_INVALID;
-    if (flags & ~(unsigned)GLA_FLAG_SCALAR_GATE) return GLA_ERR_INVALID;
+    if (flags & ~(unsigned)(GLA_FLAG_SCALAR_GATE | GLA_FLAG_FORCE_SIMT)) return GLA_ERR_INVALID;
     const bool scalar = flags & GLA_FLAG_SCALAR_GATE;
     if (L > 0 && (!q || !k || !v || !dout || !dq || !dk_out || !dv_out)) return GLA_ERR_INVALID;
     if (dlog_alpha && !log_alpha) return GLA_ERR_INVALID;
@@ -425,8 +425,16 @@ int gla_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
     a.dv = dv;
     a.in_dtype = in_dtype;
     a.flags = flags;
+    a.err_word = nullptr;
+    a.wait_ns = g_wait_ns;
+    a.only_marked = 0;
     if (launch_failure_injected()) return GLA_ERR_CUDA;
     // a per-token gate's gradient is accumulated across the row blocks of a head
+    if (bwd_tc_supported(a)) {
+        a.err_word = err_word_ptr();
+        if (!a.err_word) return GLA_ERR_CUDA;
+        return finish(launch_bwd_tc(a, s), s);
+    }
     if (scalar && dlog_alpha && cudaMemsetAsync(dlog_alpha, 0, nla * 4, s) != cudaSuccess) return GLA_ERR_CUDA;
     return finish(launch_bwd(a, s), s);
 }

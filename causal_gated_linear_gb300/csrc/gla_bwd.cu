@@ -604,6 +604,14 @@ __global__ void __launch_bounds__(kThreads, 2) gla_bwd_kernel(const BwdArgs a) {
     const long BH = (long)a.B * a.H;
     const int rb = (a.dk + kBlock - 1) / kBlock, cb = (a.dv + kBlock - 1) / kBlock;
     const long b = blockIdx.x;
+    if (a.only_marked) {
+        // after the chunk-form backward: only the blocks of the heads it marked
+        const uint32_t* mk = b < BH * rb
+                                 ? reinterpret_cast<const uint32_t*>(a.dk_out) + (b / rb) * a.L * a.dk + (b % rb) * kBlock
+                                 : reinterpret_cast<const uint32_t*>(a.dv_out) + ((b - BH * rb) / cb) * a.L * a.dv +
+                                       ((b - BH * rb) % cb) * kBlock;
+        if (*mk != kBwdMark) return;
+    }
     if (b < BH * rb)
         rows_body<CPL, GATE, T>(a, sm, b / rb, (int)(b % rb));
     else

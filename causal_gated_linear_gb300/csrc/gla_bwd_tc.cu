@@ -1,0 +1,696 @@
+// gla_bwd_tc.cu -- backward pass of the gated recurrence in chunk form on the
+// tensor cores (tcgen05 + TMEM + TMA), sm_103a.
+//
+// Method ("Gated Linear Attention", GLA Recurrent Form and Chunk-Wise
+// Block-Parallel): the forward computes, per chunk of C = 64 tokens with b_t the
+// in-chunk inclusive cumsum of log alpha and b_C its last value,
+//   o_t = (q_t e^{b_t})^T S_{c-1} + sum_{i<=t} [sum_d q_td k_id e^{b_td - b_id}] v_i
+//   S_c = Diag(e^{b_C}) S_{c-1} + sum_i (k_i e^{b_C - b_i}) v_i^T.
+// With Qh_t = q_t e^{b_t - b_C}, Kh_i = k_i e^{b_C - b_i}, S' = Diag(e^{b_C}) S_{c-1},
+// D = dO V^T and D_m / P_m = D / (Qh Kh^T) masked to i <= t, and G_c = dL/dS_c,
+// differentiating those two lines gives, per chunk,
+//   dq_t = e^{b_t - b_C} (S' do_t + (D_m Kh)_t)
+//   dk_i = e^{b_C - b_i} (G_c v_i + (D_m^T Qh)_i)
+//   dv_i = G_c^T Kh_i + (P_m^T dO)_i
+//   G_{c-1} = Diag(e^{b_C}) (G_c + Qh^T dO)
+// and the gate enters only through its cumulative sums, so
+//   dlog_alpha_t = sum_{s >= t} (q_s dq_s - k_s dk_s)  (+ rowsum(dS_{L-1} S_{L-1}))
+// -- the same identity the recurrent backward uses.
+//
+// Two kernels, one CTA of 128 threads per (batch, head), thread d <-> key
+// channel d <-> tensor-memory lane d (d_k = d_v = 128):
+//   dq pass: chunks in order, S fp32 in TMEM; products D = dO V^T, dS = Kh^T V,
+//            dQ^T = S'(TMEM) dO^T + Kh^T D_m^T; dq written with its factor.
+//            At the end rowsum(dS_{L-1} S_{L-1}) is left in the last token's row
+//            of dlog_alpha for the second pass.
+//   dk/dv pass: chunks in reverse, G fp32 in TMEM; products P = Qh Kh^T,
+//            D = dO V^T, dG = Qh^T dO, dK^T = G V^T + Qh^T D_m, dV^T = G^T Kh^T +
+//            dO^T P_m; dk, dv, the gate gradient (suffix sums over the tokens,
+//            reading q, k and the dq of the first pass) and dS_init.
+// Every phase runs on all threads in turn (gate factors, products issued by one
+// thread, epilogues), with bounded waits; the next chunk's tiles are loaded as
+// soon as the last product that reads the current ones has completed, so the
+// copy overlaps the epilogues.  The state copies that enter the products (S' in
+// the dq pass, G in the dk/dv pass) are split into bf16 high and low parts
+// (x = hi + lo to about 2^-17), two products each: for slowly decaying gates the
+// state carries most of a gradient, and one bf16 copy would set its error.  A chunk over which
+// some channel decays by more than e^-64 is outside the factorisation's range;
+// the dk/dv pass then marks the head (a NaN pattern in its dk and dv rows) and
+// the recurrent kernel recomputes exactly the marked heads afterwards.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "gla_internal.h"
+#include "gla_ptx.cuh"
+
+namespace gla {
+namespace {
+
+constexpr int C = 64;         // chunk length
+constexpr int D = 128;        // d_k = d_v
+constexpr int kThr = 128;     // one thread per channel / TMEM lane
+constexpr int TB = C * D * 2;  // bf16 tile [64 tokens][128 channels]: two 8 KB swizzle atoms
+constexpr int LAB = C * D * 4;  // fp32 log alpha tile
+constexpr int PB = C * C * 2;  // bf16 [64][64] (one atom)
+constexpr int GSB = D * D * 2;  // bf16 [128][128] state gradient copy: two 16 KB atoms
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kStrongLog = -64.f;
+
+struct BwdTcParams {
+    CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_la;
+    const uint16_t* q;  // raw bf16 inputs (gate-gradient epilogue)
+    const uint16_t* k;
+    const float* init_state;
+    const float* dfinal;
+    float* dq;
+    float* dk;
+    float* dv;
+    float* dla;
+    float* dinit;
+    unsigned* err;
+    unsigned long long wait_ns;
+    int L, nchunks, gate;
+};
+
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+
+__device__ __forceinline__ uint16_t f2bf(float x) {
+    __nv_bfloat16 h = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// Element (row, col) of a bf16 tile of rows of 128 channels stored as two 128-byte
+// swizzled atoms of 64 columns, `atom` bytes apart.
+__device__ __forceinline__ uint32_t tile_off(int row, int col, int atom) {
+    return (col >> 6) * atom + sw128_offset(row, col & 63);
+}
+
+// Shared-memory descriptors (128-byte swizzle).  K-major: K steps of 16 elements
+// (32 bytes) inside a 64-element atom row, `atom` bytes between the two atoms of
+// a 128-wide K.  MN-major: K steps of 16 rows (2048 bytes), `lbo` bytes between
+// the 64-element M/N blocks.
+__device__ __forceinline__ uint64_t desc_k(uint32_t tile, int kk, int atom) {
+    return sdesc_const(16, 1024) | ((tile + (kk >> 2) * atom + (kk & 3) * 32) >> 4);
+}
+__device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int kk, int lbo) {
+    return sdesc_const(lbo, 1024) | ((tile + kk * 2048) >> 4);
+}
+
+// Bounded wait of every thread on an mbarrier phase; false (and the error record)
+// when it runs out.
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         const BwdTcParams& p) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, p.err, p.wait_ns);
+    return __syncthreads_and(ok) != 0;
+}
+
+// Loads of one chunk's bf16 tiles (two boxes of 64 channels each), and of its log alpha.
+__device__ __forceinline__ void load_tiles(uint32_t bar, const CUtensorMap* const* maps, const uint32_t* dst, int n,
+                                           int c, int bh) {
+    mbar_arrive_expect_tx(bar, n * TB);
+    for (int m = 0; m < n; m++) {
+        tma_load_3d(dst[m], maps[m], bar, 0, c * C, bh);
+        tma_load_3d(dst[m] + 8192, maps[m], bar, 64, c * C, bh);
+    }
+}
+__device__ __forceinline__ void load_la(const BwdTcParams& p, uint32_t bar, uint32_t dst, int c, int bh) {
+    mbar_arrive_expect_tx(bar, LAB);
+    tma_load_3d(dst, &p.tm_la, bar, 0, c * C, bh);
+}
+
+// bf16 high and low parts of a pair: hi = bf16(x), lo = bf16(x - hi)
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16x2(x0, x1);
+    const float2 h = unpack_bf16x2(hi);
+    lo = pack_bf16x2(x0 - h.x, x1 - h.y);
+}
+
+// In-chunk sum of log alpha of channel d (rows past the sequence end arrive as zeros).
+__device__ __forceinline__ float chunk_total(const float* la, int d) {
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll 8
+    for (int t = 0; t < C; t += 2) {
+        s0 += la[t * D + d];
+        s1 += la[(t + 1) * D + d];
+    }
+    return s0 + s1;
+}
+
+// D_m (and P_m) = lower triangle (i <= t) of a 64x64 fp32 accumulator in TMEM lanes
+// 0..63 -> bf16 [t][i] tile.  Threads 0..63 (warps 0, 1); row t = lane t.
+__device__ __forceinline__ void mask_rows(uint32_t taddr, uint8_t* dst, int t) {
+#pragma unroll 1
+    for (int h = 0; h < 2; h++) {
+        uint32_t r[32];
+        tmem_ld32(taddr + h * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k8 = 0; k8 < 4; k8++) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                const int i = h * 32 + k8 * 8 + e;
+                x[e] = (i <= t) ? __uint_as_float(r[k8 * 8 + e]) : 0.f;
+            }
+            uint4 w;
+            w.x = pack_bf16x2(x[0], x[1]);
+            w.y = pack_bf16x2(x[2], x[3]);
+            w.z = pack_bf16x2(x[4], x[5]);
+            w.w = pack_bf16x2(x[6], x[7]);
+            *reinterpret_cast<uint4*>(dst + sw128_offset(t, h * 32 + k8 * 8)) = w;
+        }
+    }
+}
+
+// Drain before a CTA that gave up leaves: the loads in flight and the issued products.
+__device__ __forceinline__ void drain(uint32_t bar_t, uint32_t par_t, bool pend_t, uint32_t bar_l, uint32_t par_l,
+                                      bool pend_l, uint32_t bar_drain) {
+    volatile int no_abort = 0;
+    if (threadIdx.x == 0) {
+        if (pend_t) mbar_wait(bar_t, par_t, &no_abort, nullptr);
+        if (pend_l) mbar_wait(bar_l, par_l, &no_abort, nullptr);
+        mma_commit(bar_drain);
+        mbar_wait(bar_drain, 0, &no_abort, nullptr);
+    }
+    __syncthreads();
+}
+
+// ================================================================ dq pass
+// smem: k | v | dO | log alpha | D_m | barriers
+constexpr int A_K = 0, A_V = TB, A_DO = 2 * TB, A_LA = 3 * TB, A_DM = 3 * TB + LAB, A_BAR = A_DM + PB;
+constexpr int A_SMEM = A_BAR + 64 + 1024;
+// TMEM: S 0..127, dS 128..255, bf16 S' high 256..319, D 320..383, dQ^T 384..447, S' low 448..511
+constexpr uint32_t TA_S = 0, TA_DS = 128, TA_SB = 256, TA_D = 320, TA_Q = 384, TA_SL = 448;
+
+__global__ void __launch_bounds__(kThr, 1) gla_bwd_dq_kernel(const __grid_constant__ BwdTcParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(sm);
+    const int d = threadIdx.x, warp = d >> 5;
+    const int bh = blockIdx.x;
+    const int L = p.L, N = p.nchunks;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + A_BAR);
+    const uint32_t bar_t = smem_u32(&bars[0]), bar_l = smem_u32(&bars[1]), bar_mma = smem_u32(&bars[2]),
+                   bar_drain = smem_u32(&bars[3]);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + A_BAR + 40);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + A_BAR + 44);
+    const CUtensorMap* maps[3] = {&p.tm_k, &p.tm_v, &p.tm_do};
+    const uint32_t dsts[3] = {sb + A_K, sb + A_V, sb + A_DO};
+    if (d == 0) {
+        mbar_init(bar_t, 1);
+        mbar_init(bar_l, 1);
+        mbar_init(bar_mma, 1);
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        if (N > 0) {
+            load_tiles(bar_t, maps, dsts, 3, 0, bh);
+            if (p.gate) load_la(p, bar_l, sb + A_LA, 0, bh);
+        }
+    }
+    if (warp == 0) tmem_alloc(smem_u32(tslot), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t lane = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lanes
+    // S_{-1}: row d of the initial state
+    {
+        const float* s0 = p.init_state ? p.init_state + ((long)bh * D + d) * D : nullptr;
+#pragma unroll 1
+        for (int h = 0; h < 4; h++) {
+            uint32_t r[32];
+#pragma unroll
+            for (int e = 0; e < 32; e++) r[e] = __float_as_uint(s0 ? s0[h * 32 + e] : 0.f);
+            tmem_st32(lane + TA_S + h * 32, r);
+        }
+        tmem_wait_st();
+    }
+    const float* la = reinterpret_cast<const float*>(sm + A_LA);
+    bool ok = true, pend_t = N > 0, pend_l = N > 0 && p.gate;
+    int c = 0;
+    for (; c < N; c++) {
+        if (!(ok = wait_all(bar_t, c & 1, abort_flag, p))) break;
+        pend_t = false;
+        if (p.gate) {
+            if (!(ok = wait_all(bar_l, c & 1, abort_flag, p))) break;
+            pend_l = false;
+        }
+        const int nval = min(C, L - c * C);
+        // gate: b_C of channel d, Kh = k e^{b_C - b_t} in place
+        float bC = 0.f;
+        if (p.gate) {
+            bC = chunk_total(la, d);
+            float b = 0.f;
+            uint8_t* kt = sm + A_K;
+#pragma unroll 4
+            for (int t = 0; t < C; t++) {
+                b += la[t * D + d];
+                uint16_t* e = reinterpret_cast<uint16_t*>(kt + tile_off(t, d, 8192));
+                *e = f2bf(bf2f(*e) * ex2f((bC - b) * kLog2e));
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (d == 0) {
+            // D = dO V^T (M = 128, rows 64..127 read past the dO tile and are ignored)
+            constexpr uint32_t idD = make_idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + TA_D, desc_k(sb + A_DO, kk, 8192), desc_k(sb + A_V, kk, 8192), idD, kk > 0);
+            // dS = Kh^T V (both MN-major)
+            constexpr uint32_t idS = make_idesc_bf16(128, 128, 1, 1);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; kk++)
+                mma_ss(tmem + TA_DS, desc_mn(sb + A_K, kk, 8192), desc_mn(sb + A_V, kk, 8192), idS, kk > 0);
+            mma_commit(bar_mma);
+        }
+        if (!(ok = wait_all(bar_mma, 0, abort_flag, p))) break;
+        tc_fence_after();
+        // state: S' = e^{b_C} S (bf16 high and low copies for the dQ product), S = S' + dS
+        {
+            const float g = p.gate ? ex2f(bC * kLog2e) : 1.f;
+#pragma unroll 1
+            for (int h = 0; h < 4; h++) {
+                uint32_t rs[32], rd[32], pk[16], pl[16];
+                tmem_ld32(lane + TA_S + h * 32, rs);
+                tmem_ld32(lane + TA_DS + h * 32, rd);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const float a0 = __uint_as_float(rs[e]) * g, a1 = __uint_as_float(rs[e + 1]) * g;
+                    split_pair(a0, a1, pk[e / 2], pl[e / 2]);
+                    rs[e] = __float_as_uint(a0 + __uint_as_float(rd[e]));
+                    rs[e + 1] = __float_as_uint(a1 + __uint_as_float(rd[e + 1]));
+                }
+                tmem_st32(lane + TA_S + h * 32, rs);
+                tmem_st16(lane + TA_SB + h * 16, pk);
+                tmem_st16(lane + TA_SL + h * 16, pl);
+            }
+        }
+        if (d < C) mask_rows(lane + TA_D, sm + A_DM, d);
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (d == 0) {
+            // dQ^T = (S'_hi + S'_lo) dO^T (A operands from TMEM) + Kh^T D_m^T
+            constexpr uint32_t idQ = make_idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ts(tmem + TA_Q, tmem + TA_SB + kk * 8, desc_k(sb + A_DO, kk, 8192), idQ, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ts(tmem + TA_Q, tmem + TA_SL + kk * 8, desc_k(sb + A_DO, kk, 8192), idQ, 1);
+            constexpr uint32_t idQ2 = make_idesc_bf16(128, 64, 1, 0);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; kk++)
+                mma_ss(tmem + TA_Q, desc_mn(sb + A_K, kk, 8192), desc_k(sb + A_DM, kk, 8192), idQ2, 1);
+            mma_commit(bar_mma);
+        }
+        if (!(ok = wait_all(bar_mma, 1, abort_flag, p))) break;
+        tc_fence_after();
+        // every product that reads this chunk's tiles has completed: load the next chunk's
+        if (d == 0 && c + 1 < N) {
+            load_tiles(bar_t, maps, dsts, 3, c + 1, bh);
+            pend_t = true;
+        }
+        // dq_t = e^{b_t - b_C} dQ^T[d][t]
+        {
+            float* dqp = p.dq + ((long)bh * L + (long)c * C) * D + d;
+            float b = 0.f;
+#pragma unroll 1
+            for (int h = 0; h < 2; h++) {
+                uint32_t r[32];
+                tmem_ld32(lane + TA_Q + h * 32, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; e++) {
+                    const int t = h * 32 + e;
+                    float f = 1.f;
+                    if (p.gate) {
+                        b += la[t * D + d];
+                        f = ex2f((b - bC) * kLog2e);
+                    }
+                    if (t < nval) dqp[(long)t * D] = __uint_as_float(r[e]) * f;
+                }
+            }
+        }
+        // log alpha is read until here
+        __syncthreads();
+        if (d == 0 && c + 1 < N && p.gate) {
+            load_la(p, bar_l, sb + A_LA, c + 1, bh);
+            pend_l = true;
+        }
+        pend_t = __syncthreads_or(pend_t);
+        pend_l = __syncthreads_or(pend_l);
+    }
+    if (!ok) {
+        drain(bar_t, c & 1, pend_t, bar_l, c & 1, pend_l, bar_drain);
+    } else if (p.dla && p.dfinal) {
+        // the final-state part of the gate gradient, rowsum(dS_{L-1} * S_{L-1}), for the second pass
+        const float* df = p.dfinal + ((long)bh * D + d) * D;
+        float s = 0.f;
+#pragma unroll 1
+        for (int h = 0; h < 4; h++) {
+            uint32_t r[32];
+            tmem_ld32(lane + TA_S + h * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; e++) s = fmaf(df[h * 32 + e], __uint_as_float(r[e]), s);
+        }
+        p.dla[((long)bh * L + L - 1) * D + d] = s;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ================================================================ dk / dv pass
+// smem: q | k | v | dO | log alpha | G high (bf16) | G low | P_m | D_m | barriers
+constexpr int B_Q = 0, B_K = TB, B_V = 2 * TB, B_DO = 3 * TB, B_LA = 4 * TB, B_GS = 4 * TB + LAB,
+              B_GL = B_GS + GSB, B_PM = B_GL + GSB, B_DM = B_PM + PB, B_BAR = B_DM + PB;
+constexpr int B_SMEM = B_BAR + 64 + 1024;
+// TMEM: G 0..127, dG 128..255, P 256..319, D 320..383, dK^T 384..447, dV^T 448..511
+constexpr uint32_t TB_G = 0, TB_DG = 128, TB_P = 256, TB_D = 320, TB_K = 384, TB_V = 448;
+
+__global__ void __launch_bounds__(kThr, 1) gla_bwd_dkdv_kernel(const __grid_constant__ BwdTcParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(sm);
+    const int d = threadIdx.x, warp = d >> 5;
+    const int bh = blockIdx.x;
+    const int L = p.L, N = p.nchunks;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + B_BAR);
+    const uint32_t bar_t = smem_u32(&bars[0]), bar_l = smem_u32(&bars[1]), bar_mma = smem_u32(&bars[2]),
+                   bar_drain = smem_u32(&bars[3]);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + B_BAR + 40);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + B_BAR + 44);
+    const CUtensorMap* maps[4] = {&p.tm_q, &p.tm_k, &p.tm_v, &p.tm_do};
+    const uint32_t dsts[4] = {sb + B_Q, sb + B_K, sb + B_V, sb + B_DO};
+    if (d == 0) {
+        mbar_init(bar_t, 1);
+        mbar_init(bar_l, 1);
+        mbar_init(bar_mma, 1);
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        if (N > 0) {
+            load_tiles(bar_t, maps, dsts, 4, N - 1, bh);
+            if (p.gate) load_la(p, bar_l, sb + B_LA, N - 1, bh);
+        }
+    }
+    if (warp == 0) tmem_alloc(smem_u32(tslot), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t lane = tmem + ((uint32_t)(warp * 32) << 16);
+    // G_{N-1} = dL/dS_{L-1}: row d of dfinal
+    {
+        const float* g0 = p.dfinal ? p.dfinal + ((long)bh * D + d) * D : nullptr;
+#pragma unroll 1
+        for (int h = 0; h < 4; h++) {
+            uint32_t r[32];
+#pragma unroll
+            for (int e = 0; e < 32; e++) r[e] = __float_as_uint(g0 ? g0[h * 32 + e] : 0.f);
+            tmem_st32(lane + TB_G + h * 32, r);
+        }
+        tmem_wait_st();
+    }
+    // running suffix of the gate gradient for channel d (starts from the final-state part the
+    // dq pass left in the last token's row)
+    float acc = 0.f;
+    if (p.dla && p.dfinal) acc = p.dla[((long)bh * L + L - 1) * D + d];
+    const float* la = reinterpret_cast<const float*>(sm + B_LA);
+    bool ok = true, pend_t = N > 0, pend_l = N > 0 && p.gate, strong = false;
+    int it = 0;
+    for (int c = N - 1; c >= 0; c--, it++) {
+        if (!(ok = wait_all(bar_t, it & 1, abort_flag, p))) break;
+        pend_t = false;
+        if (p.gate) {
+            if (!(ok = wait_all(bar_l, it & 1, abort_flag, p))) break;
+            pend_l = false;
+        }
+        const int nval = min(C, L - c * C);
+        // gate: Qh = q e^{b_t - b_C}, Kh = k e^{b_C - b_t} in place
+        float bC = 0.f;
+        if (p.gate) {
+            bC = chunk_total(la, d);
+            strong |= bC < kStrongLog;
+            float b = 0.f;
+            uint8_t* qt = sm + B_Q;
+            uint8_t* kt = sm + B_K;
+#pragma unroll 4
+            for (int t = 0; t < C; t++) {
+                b += la[t * D + d];
+                const uint32_t o = tile_off(t, d, 8192);
+                uint16_t* eq = reinterpret_cast<uint16_t*>(qt + o);
+                uint16_t* ek = reinterpret_cast<uint16_t*>(kt + o);
+                *eq = f2bf(bf2f(*eq) * ex2f((b - bC) * kLog2e));
+                *ek = f2bf(bf2f(*ek) * ex2f((bC - b) * kLog2e));
+            }
+        }
+        // bf16 high and low copies of G_c into shared memory, row d ([d][j], two atoms of 64 columns)
+#pragma unroll 1
+        for (int h = 0; h < 4; h++) {
+            uint32_t r[32];
+            tmem_ld32(lane + TB_G + h * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e8 = 0; e8 < 4; e8++) {
+                uint4 wh, wl;
+                const float* x = reinterpret_cast<const float*>(r + e8 * 8);
+                split_pair(x[0], x[1], wh.x, wl.x);
+                split_pair(x[2], x[3], wh.y, wl.y);
+                split_pair(x[4], x[5], wh.z, wl.z);
+                split_pair(x[6], x[7], wh.w, wl.w);
+                const uint32_t o = tile_off(d, h * 32 + e8 * 8, 16384);
+                *reinterpret_cast<uint4*>(sm + B_GS + o) = wh;
+                *reinterpret_cast<uint4*>(sm + B_GL + o) = wl;
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (d == 0) {
+            constexpr uint32_t id64 = make_idesc_bf16(128, 64, 0, 0);
+            // P = Qh Kh^T and D = dO V^T (M = 128: rows 64..127 read past the tile and are ignored)
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + TB_P, desc_k(sb + B_Q, kk, 8192), desc_k(sb + B_K, kk, 8192), id64, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + TB_D, desc_k(sb + B_DO, kk, 8192), desc_k(sb + B_V, kk, 8192), id64, kk > 0);
+            // dG = Qh^T dO
+            constexpr uint32_t id128 = make_idesc_bf16(128, 128, 1, 1);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; kk++)
+                mma_ss(tmem + TB_DG, desc_mn(sb + B_Q, kk, 8192), desc_mn(sb + B_DO, kk, 8192), id128, kk > 0);
+            mma_commit(bar_mma);
+        }
+        if (!(ok = wait_all(bar_mma, 0, abort_flag, p))) break;
+        tc_fence_after();
+        if (d < C) {
+            mask_rows(lane + TB_P, sm + B_PM, d);
+            mask_rows(lane + TB_D, sm + B_DM, d);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (d == 0) {
+            // dK^T = G V^T + Qh^T D_m
+            constexpr uint32_t idK1 = make_idesc_bf16(128, 64, 0, 0), idK2 = make_idesc_bf16(128, 64, 1, 1);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + TB_K, desc_k(sb + B_GS, kk, 16384), desc_k(sb + B_V, kk, 8192), idK1, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + TB_K, desc_k(sb + B_GL, kk, 16384), desc_k(sb + B_V, kk, 8192), idK1, 1);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; kk++)
+                mma_ss(tmem + TB_K, desc_mn(sb + B_Q, kk, 8192), desc_mn(sb + B_DM, kk, 8192), idK2, 1);
+            // dV^T = G^T Kh^T + dO^T P_m
+            constexpr uint32_t idV1 = make_idesc_bf16(128, 64, 1, 0), idV2 = make_idesc_bf16(128, 64, 1, 1);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + TB_V, desc_mn(sb + B_GS, kk, 16384), desc_k(sb + B_K, kk, 8192), idV1, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + TB_V, desc_mn(sb + B_GL, kk, 16384), desc_k(sb + B_K, kk, 8192), idV1, 1);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; kk++)
+                mma_ss(tmem + TB_V, desc_mn(sb + B_DO, kk, 8192), desc_mn(sb + B_PM, kk, 8192), idV2, 1);
+            mma_commit(bar_mma);
+        }
+        if (!(ok = wait_all(bar_mma, 1, abort_flag, p))) break;
+        tc_fence_after();
+        // every product that reads this chunk's tiles has completed: load the next chunk's
+        if (d == 0 && c > 0) {
+            load_tiles(bar_t, maps, dsts, 4, c - 1, bh);
+            pend_t = true;
+        }
+        // epilogue, tokens from last to first: dk_i = e^{b_C - b_i} dK^T[d][i], the gate
+        // gradient's suffix sum, dv_i = dV^T[j = d][i]
+        {
+            const long row0 = (long)bh * L + (long)c * C;
+            float* dkp = p.dk + row0 * D + d;
+            float* dvp = p.dv + row0 * D + d;
+            const float* dqp = p.dq + row0 * D + d;
+            const uint16_t* qp = p.q + row0 * D + d;
+            const uint16_t* kp = p.k + row0 * D + d;
+            float* dlp = p.dla ? p.dla + row0 * D + d : nullptr;
+            float r_suf = 0.f;  // b_C - b_i: sum of log alpha over (i, C)
+#pragma unroll 1
+            for (int h = 1; h >= 0; h--) {
+                uint32_t rk[32], rv[32];
+                tmem_ld32(lane + TB_K + h * 32, rk);
+                tmem_ld32(lane + TB_V + h * 32, rv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 31; e >= 0; e--) {
+                    const int i = h * 32 + e;
+                    if (i < nval) {
+                        const float f = p.gate ? ex2f(r_suf * kLog2e) : 1.f;
+                        const float dki = __uint_as_float(rk[e]) * f;
+                        dkp[(long)i * D] = dki;
+                        dvp[(long)i * D] = __uint_as_float(rv[e]);
+                        if (dlp) {
+                            acc += bf2f(qp[(long)i * D]) * dqp[(long)i * D] - bf2f(kp[(long)i * D]) * dki;
+                            dlp[(long)i * D] = acc;
+                        }
+                    }
+                    if (p.gate) r_suf += la[i * D + d];
+                }
+            }
+        }
+        // G_{c-1} = e^{b_C} (G_c + dG)
+        {
+            const float g = p.gate ? ex2f(bC * kLog2e) : 1.f;
+#pragma unroll 1
+            for (int h = 0; h < 4; h++) {
+                uint32_t rg[32], rd[32];
+                tmem_ld32(lane + TB_G + h * 32, rg);
+                tmem_ld32(lane + TB_DG + h * 32, rd);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; e++)
+                    rg[e] = __float_as_uint(g * (__uint_as_float(rg[e]) + __uint_as_float(rd[e])));
+                tmem_st32(lane + TB_G + h * 32, rg);
+            }
+            tmem_wait_st();
+        }
+        // log alpha is read until here
+        tc_fence_before();
+        __syncthreads();
+        if (d == 0 && c > 0 && p.gate) {
+            load_la(p, bar_l, sb + B_LA, c - 1, bh);
+            pend_l = true;
+        }
+        pend_t = __syncthreads_or(pend_t);
+        pend_l = __syncthreads_or(pend_l);
+    }
+    if (!ok) drain(bar_t, it & 1, pend_t, bar_l, it & 1, pend_l, bar_drain);
+    const bool mark = __syncthreads_or(strong) != 0;
+    if (ok && !mark && p.dinit) {
+        float* di = p.dinit + ((long)bh * D + d) * D;
+#pragma unroll 1
+        for (int h = 0; h < 4; h++) {
+            uint32_t r[32];
+            tmem_ld32(lane + TB_G + h * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; e++) di[h * 32 + e] = __uint_as_float(r[e]);
+        }
+    }
+    if (ok && mark && d < D / 32) {
+        // the exact recurrent backward recomputes this head: one mark per row and column block
+        reinterpret_cast<uint32_t*>(p.dk)[(long)bh * L * D + d * 32] = kBwdMark;
+        reinterpret_cast<uint32_t*>(p.dv)[(long)bh * L * D + d * 32] = kBwdMark;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+CUresult encode(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* ptr, int d0, int d1, int d2,
+                int box0, int box1, CUtensorMapSwizzle sw) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return CUDA_ERROR_NOT_FOUND;
+    cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+    cuuint64_t strides[2] = {(cuuint64_t)d0 * esize, (cuuint64_t)d0 * d1 * esize};
+    cuuint32_t box[3] = {(cuuint32_t)box0, (cuuint32_t)box1, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace
+
+bool bwd_tc_supported(const BwdArgs& a) {
+    return a.in_dtype == GLA_DTYPE_BF16 && a.dk == D && a.dv == D && !(a.flags & GLA_FLAG_SCALAR_GATE) &&
+           !(a.flags & GLA_FLAG_FORCE_SIMT) && a.L >= 1 && (long)a.B * a.H <= 0x7fffffffL;
+}
+
+cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
+    BwdTcParams p;
+    memset(&p, 0, sizeof(p));
+    const int BH = a.B * a.H;
+    const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    if (encode(&p.tm_q, bf, 2, a.q, D, a.L, BH, 64, C, sw) != CUDA_SUCCESS ||
+        encode(&p.tm_k, bf, 2, a.k, D, a.L, BH, 64, C, sw) != CUDA_SUCCESS ||
+        encode(&p.tm_v, bf, 2, a.v, D, a.L, BH, 64, C, sw) != CUDA_SUCCESS ||
+        encode(&p.tm_do, bf, 2, a.dout, D, a.L, BH, 64, C, sw) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    if (a.log_alpha && encode(&p.tm_la, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.log_alpha, D, a.L, BH, D, C,
+                              CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    p.q = static_cast<const uint16_t*>(a.q);
+    p.k = static_cast<const uint16_t*>(a.k);
+    p.init_state = a.init_state;
+    p.dfinal = a.dfinal;
+    p.dq = a.dq;
+    p.dk = a.dk_out;
+    p.dv = a.dv_out;
+    p.dla = a.dlog_alpha;
+    p.dinit = a.dinit;
+    p.err = a.err_word;
+    p.wait_ns = a.wait_ns;
+    p.L = a.L;
+    p.nchunks = (a.L + C - 1) / C;
+    p.gate = a.log_alpha != nullptr;
+    cudaError_t e = cudaFuncSetAttribute(gla_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, A_SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gla_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, B_SMEM);
+    if (e != cudaSuccess) return e;
+    gla_bwd_dq_kernel<<<BH, kThr, A_SMEM, s>>>(p);
+    gla_bwd_dkdv_kernel<<<BH, kThr, B_SMEM, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // heads with a chunk outside the factorisation's range: the exact recurrent kernel
+    BwdArgs r = a;
+    r.only_marked = 1;
+    return launch_bwd(r, s);
+}
+
+}  // namespace gla

@@ -86,13 +86,27 @@ struct BwdArgs {
     int B, H, L, dk, dv;
     int in_dtype;
     unsigned flags;  // GLA_FLAG_SCALAR_GATE: log_alpha and dlog_alpha are [B][H][L]
+    unsigned* err_word;          // device address of the error word (chunk-form kernels)
+    unsigned long long wait_ns;  // limit of the chunk-form kernels' waits
+    int only_marked;             // recurrent kernel: only the CTAs whose block carries kBwdMark
 };
+
+// Written by the chunk-form backward into the first dk / dv element of every
+// 32-column block of a head it leaves to the recurrent kernel (a NaN pattern
+// that arithmetic does not produce).
+constexpr uint32_t kBwdMark = 0xFFC00001u;
 
 // Gradients of the recurrence (row CTAs: dq, dk, dlog_alpha, dS_init;
 // column CTAs: dv), one launch.
 bool bwd_supported(int dk, int dv);
 int bwd_blocks(int d);  // CTAs per head along one dimension (row CTAs for dk, column CTAs for dv)
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s);
+
+// Gradients in chunk form on the tensor cores (bf16, d_k = d_v = 128, one gate
+// per channel or none): a dq pass, a dk/dv pass, then the recurrent kernel on
+// the heads the chunk form marked.
+bool bwd_tc_supported(const BwdArgs& a);
+cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s);
 
 // Memory-bound decode step.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);

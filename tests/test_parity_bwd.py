@@ -1,4 +1,5 @@
-"""GPU parity of the backward pass (gla_bwd) against the fp64 oracle.
+"""GPU parity of the recurrent backward kernel (gla_bwd with GLA_FLAG_FORCE_SIMT,
+and every call the chunk-form kernels do not take) against the fp64 oracle.
 
 The kernel runs the recurrence token by token in fp32 on the same rounded
 inputs the oracle receives.  dq, dk, dv and dinit are held to the fp32 bar
@@ -28,7 +29,7 @@ def _w(B, H, L, dk, dv, gate=True, init=True, dtype="bf16", seed=0):
                             init_std=0.1 if init else 0.0, seed=synth.BWD.seed + seed)
 
 
-def run_bwd(w, x, want_dla=True, want_dinit=True):
+def run_bwd(w, x, want_dla=True, want_dinit=True, force_simt=True):
     import torch
     B, H, L, dk, dv = w.B, w.H, w.L, w.dk, w.dv
     q, k, v, do = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"]), to_dev(x["dout"])
@@ -41,7 +42,8 @@ def run_bwd(w, x, want_dla=True, want_dinit=True):
         dla = nan(B, H, L)
     gla.check(gla.gla_bwd(q, k, v, do, dq, dk_, dv_, B, H, L, dk, dv, log_alpha=la, init_state=s0, dfinal=df,
                           dlog_alpha=dla, dinit=di, in_dtype=gla.F32 if w.dtype == "f32" else gla.BF16,
-                          flags=gla.FLAG_SCALAR_GATE if w.scalar_gate else 0))
+                          flags=(gla.FLAG_SCALAR_GATE if w.scalar_gate else 0) |
+                          (gla.FLAG_FORCE_SIMT if force_simt else 0)))
     torch.cuda.synchronize()
     gla.check(gla.gla_device_error())
     c = lambda t: None if t is None else t.cpu().numpy().astype(np.float64)
@@ -130,6 +132,8 @@ def test_bwd_rejects_bad_calls():
                        in_dtype=F) == gla.GLA_ERR_MISALIGNED
     assert gla.gla_bwd(q, k, v, do, dq, dk, dv, 1, 1, 8, 64, 64, in_dtype=F,
                        flags=gla.FLAG_NORMALIZE) == gla.GLA_ERR_INVALID
+    assert gla.gla_bwd(q, k, v, do, dq, dk, dv, 1, 1, 8, 64, 64, in_dtype=F,
+                       flags=gla.FLAG_FORCE_SIMT) == gla.GLA_OK
 
 
 def test_bwd_full_sampled_and_homogeneity():
