@@ -17,8 +17,9 @@
 //   dlog_alpha_t = sum_{s >= t} (q_s dq_s - k_s dk_s)  (+ rowsum(dS_{L-1} S_{L-1}))
 // -- the same identity the recurrent backward uses.
 //
-// Two kernels, one CTA of 128 threads per (batch, head), thread d <-> key
-// channel d <-> tensor-memory lane d (d_k = d_v = 128):
+// Two kernels, one CTA of 256 threads per (batch, head): thread (d, hf) owns key
+// channel d (tensor-memory lane d) and half hf of the chunk's tokens and of the
+// state's columns (d_k = d_v = 128):
 //   dq pass: chunks in order, S fp32 in TMEM; products D = dO V^T, dS = Kh^T V,
 //            dQ^T = S'(TMEM) dO^T + Kh^T D_m^T; dq written with its factor.
 //            At the end rowsum(dS_{L-1} S_{L-1}) is left in the last token's row
@@ -29,8 +30,9 @@
 //            reading q, k and the dq of the first pass) and dS_init.
 // Every phase runs on all threads in turn (gate factors, products issued by one
 // thread, epilogues), with bounded waits; the next chunk's tiles are loaded as
-// soon as the last product that reads the current ones has completed, so the
-// copy overlaps the epilogues.  The state copies that enter the products (S' in
+// soon as the last product that reads the current ones has completed, and its
+// log alpha (two buffers) as soon as the current one has landed, so the copies
+// overlap the work.  The state copies that enter the products (S' in
 // the dq pass, G in the dk/dv pass) are split into bf16 high and low parts
 // (x = hi + lo to about 2^-17), two products each: for slowly decaying gates the
 // state carries most of a gradient, and one bf16 copy would set its error.  A chunk over which
@@ -50,7 +52,6 @@ namespace {
 
 constexpr int C = 64;         // chunk length
 constexpr int D = 128;        // d_k = d_v
-constexpr int kThr = 128;     // one thread per channel / TMEM lane
 constexpr int TB = C * D * 2;  // bf16 tile [64 tokens][128 channels]: two 8 KB swizzle atoms
 constexpr int LAB = C * D * 4;  // fp32 log alpha tile
 constexpr int PB = C * C * 2;  // bf16 [64][64] (one atom)
@@ -133,87 +134,104 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
     lo = pack_bf16x2(x0 - h.x, x1 - h.y);
 }
 
-// In-chunk sum of log alpha of channel d (rows past the sequence end arrive as zeros).
-__device__ __forceinline__ float chunk_total(const float* la, int d) {
+// Sum of log alpha of channel d over the 32 tokens of half `hf` of the chunk (rows
+// past the sequence end arrive as zeros).
+__device__ __forceinline__ float half_total(const float* la, int d, int hf) {
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll 8
-    for (int t = 0; t < C; t += 2) {
+    for (int t = 32 * hf; t < 32 * hf + 32; t += 2) {
         s0 += la[t * D + d];
         s1 += la[(t + 1) * D + d];
     }
     return s0 + s1;
 }
 
-// D_m (and P_m) = lower triangle (i <= t) of a 64x64 fp32 accumulator in TMEM lanes
-// 0..63 -> bf16 [t][i] tile.  Threads 0..63 (warps 0, 1); row t = lane t.
-__device__ __forceinline__ void mask_rows(uint32_t taddr, uint8_t* dst, int t) {
-#pragma unroll 1
-    for (int h = 0; h < 2; h++) {
-        uint32_t r[32];
-        tmem_ld32(taddr + h * 32, r);
-        tmem_wait_ld();
+// Columns [32 hf, 32 hf + 32) of rows 0..63 of a 64x64 fp32 accumulator in TMEM
+// (row t = lane t), masked to i <= t, as bf16 into a [t][i] tile.  Warps whose
+// lanes are 0..63.
+__device__ __forceinline__ void mask_half(uint32_t taddr, uint8_t* dst, int t, int hf) {
+    uint32_t r[32];
+    tmem_ld32(taddr + hf * 32, r);
+    tmem_wait_ld();
 #pragma unroll
-        for (int k8 = 0; k8 < 4; k8++) {
-            float x[8];
+    for (int k8 = 0; k8 < 4; k8++) {
+        float x[8];
 #pragma unroll
-            for (int e = 0; e < 8; e++) {
-                const int i = h * 32 + k8 * 8 + e;
-                x[e] = (i <= t) ? __uint_as_float(r[k8 * 8 + e]) : 0.f;
-            }
-            uint4 w;
-            w.x = pack_bf16x2(x[0], x[1]);
-            w.y = pack_bf16x2(x[2], x[3]);
-            w.z = pack_bf16x2(x[4], x[5]);
-            w.w = pack_bf16x2(x[6], x[7]);
-            *reinterpret_cast<uint4*>(dst + sw128_offset(t, h * 32 + k8 * 8)) = w;
+        for (int e = 0; e < 8; e++) {
+            const int i = hf * 32 + k8 * 8 + e;
+            x[e] = (i <= t) ? __uint_as_float(r[k8 * 8 + e]) : 0.f;
         }
+        uint4 w;
+        w.x = pack_bf16x2(x[0], x[1]);
+        w.y = pack_bf16x2(x[2], x[3]);
+        w.z = pack_bf16x2(x[4], x[5]);
+        w.w = pack_bf16x2(x[6], x[7]);
+        *reinterpret_cast<uint4*>(dst + sw128_offset(t, hf * 32 + k8 * 8)) = w;
     }
 }
 
-// Drain before a CTA that gave up leaves: the loads in flight and the issued products.
-__device__ __forceinline__ void drain(uint32_t bar_t, uint32_t par_t, bool pend_t, uint32_t bar_l, uint32_t par_l,
-                                      bool pend_l, uint32_t bar_drain) {
+// Loads issued by thread 0 and not yet waited for, so that a CTA that gives up
+// waits for them before it leaves: tiles (one barrier) and log alpha (two).
+struct Pending {
+    int tiles_issued = 0, tiles_done = 0;
+    int la_issued[2] = {0, 0}, la_done[2] = {0, 0};
+};
+
+__device__ __forceinline__ void drain(const Pending& pn, uint32_t bar_t, const uint32_t* bar_l, uint32_t bar_drain) {
     volatile int no_abort = 0;
     if (threadIdx.x == 0) {
-        if (pend_t) mbar_wait(bar_t, par_t, &no_abort, nullptr);
-        if (pend_l) mbar_wait(bar_l, par_l, &no_abort, nullptr);
+        for (int n = pn.tiles_done; n < pn.tiles_issued; n++) mbar_wait(bar_t, n & 1, &no_abort, nullptr);
+        for (int b = 0; b < 2; b++)
+            for (int n = pn.la_done[b]; n < pn.la_issued[b]; n++) mbar_wait(bar_l[b], n & 1, &no_abort, nullptr);
         mma_commit(bar_drain);
         mbar_wait(bar_drain, 0, &no_abort, nullptr);
     }
     __syncthreads();
 }
 
+// Thread layout of both passes: 256 threads, thread (d, hf) = key channel d (TMEM lane d)
+// and half hf of the chunk's tokens / of the state's 128 columns.
+constexpr int kThr2 = 2 * D;
+
 // ================================================================ dq pass
-// smem: k | v | dO | log alpha | D_m | barriers
-constexpr int A_K = 0, A_V = TB, A_DO = 2 * TB, A_LA = 3 * TB, A_DM = 3 * TB + LAB, A_BAR = A_DM + PB;
+// smem: k | v | dO | log alpha x 2 | D_m | exchange | barriers
+constexpr int A_K = 0, A_V = TB, A_DO = 2 * TB, A_LA = 3 * TB, A_DM = 3 * TB + 2 * LAB, A_X = A_DM + PB,
+              A_BAR = A_X + 2048;
 constexpr int A_SMEM = A_BAR + 64 + 1024;
 // TMEM: S 0..127, dS 128..255, bf16 S' high 256..319, D 320..383, dQ^T 384..447, S' low 448..511
 constexpr uint32_t TA_S = 0, TA_DS = 128, TA_SB = 256, TA_D = 320, TA_Q = 384, TA_SL = 448;
 
-__global__ void __launch_bounds__(kThr, 1) gla_bwd_dq_kernel(const __grid_constant__ BwdTcParams p) {
+__global__ void __launch_bounds__(kThr2, 1) gla_bwd_dq_kernel(const __grid_constant__ BwdTcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
-    const int d = threadIdx.x, warp = d >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, d = tid & (D - 1), hf = tid >> 7;
     const int bh = blockIdx.x;
     const int L = p.L, N = p.nchunks;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + A_BAR);
-    const uint32_t bar_t = smem_u32(&bars[0]), bar_l = smem_u32(&bars[1]), bar_mma = smem_u32(&bars[2]),
-                   bar_drain = smem_u32(&bars[3]);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + A_BAR + 40);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + A_BAR + 44);
+    const uint32_t bar_t = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[1]), bar_drain = smem_u32(&bars[2]);
+    const uint32_t bar_l[2] = {smem_u32(&bars[3]), smem_u32(&bars[4])};
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + A_BAR + 48);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + A_BAR + 52);
+    float* xch = reinterpret_cast<float*>(sm + A_X);  // [2][D]: per-half sums of log alpha
     const CUtensorMap* maps[3] = {&p.tm_k, &p.tm_v, &p.tm_do};
     const uint32_t dsts[3] = {sb + A_K, sb + A_V, sb + A_DO};
-    if (d == 0) {
+    Pending pn;
+    if (tid == 0) {
         mbar_init(bar_t, 1);
-        mbar_init(bar_l, 1);
         mbar_init(bar_mma, 1);
         mbar_init(bar_drain, 1);
+        mbar_init(bar_l[0], 1);
+        mbar_init(bar_l[1], 1);
         *abort_flag = 0;
         mbar_fence_init();
         if (N > 0) {
             load_tiles(bar_t, maps, dsts, 3, 0, bh);
-            if (p.gate) load_la(p, bar_l, sb + A_LA, 0, bh);
+            pn.tiles_issued++;
+            if (p.gate) {
+                load_la(p, bar_l[0], sb + A_LA, 0, bh);
+                pn.la_issued[0]++;
+            }
         }
     }
     if (warp == 0) tmem_alloc(smem_u32(tslot), 512);
@@ -221,12 +239,12 @@ __global__ void __launch_bounds__(kThr, 1) gla_bwd_dq_kernel(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t lane = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lanes
-    // S_{-1}: row d of the initial state
+    const uint32_t lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // lanes of this warp's quarter
+    // S_{-1}: columns [64 hf, 64 hf + 64) of row d of the initial state
     {
         const float* s0 = p.init_state ? p.init_state + ((long)bh * D + d) * D : nullptr;
 #pragma unroll 1
-        for (int h = 0; h < 4; h++) {
+        for (int h = 2 * hf; h < 2 * hf + 2; h++) {
             uint32_t r[32];
 #pragma unroll
             for (int e = 0; e < 32; e++) r[e] = __float_as_uint(s0 ? s0[h * 32 + e] : 0.f);
@@ -234,25 +252,35 @@ __global__ void __launch_bounds__(kThr, 1) gla_bwd_dq_kernel(const __grid_consta
         }
         tmem_wait_st();
     }
-    const float* la = reinterpret_cast<const float*>(sm + A_LA);
-    bool ok = true, pend_t = N > 0, pend_l = N > 0 && p.gate;
+    bool ok = true;
     int c = 0;
     for (; c < N; c++) {
+        const float* la = reinterpret_cast<const float*>(sm + A_LA + (c & 1) * LAB);
         if (!(ok = wait_all(bar_t, c & 1, abort_flag, p))) break;
-        pend_t = false;
+        if (tid == 0) pn.tiles_done++;
         if (p.gate) {
-            if (!(ok = wait_all(bar_l, c & 1, abort_flag, p))) break;
-            pend_l = false;
+            if (!(ok = wait_all(bar_l[c & 1], (c >> 1) & 1, abort_flag, p))) break;
+            if (tid == 0) {
+                pn.la_done[c & 1]++;
+                // the other buffer was last read in the previous chunk
+                if (c + 1 < N) {
+                    load_la(p, bar_l[(c + 1) & 1], sb + A_LA + ((c + 1) & 1) * LAB, c + 1, bh);
+                    pn.la_issued[(c + 1) & 1]++;
+                }
+            }
         }
         const int nval = min(C, L - c * C);
-        // gate: b_C of channel d, Kh = k e^{b_C - b_t} in place
-        float bC = 0.f;
+        // gate: b_C of channel d, Kh = k e^{b_C - b_t} in place for this half's tokens
+        float bC = 0.f, pre = 0.f;
         if (p.gate) {
-            bC = chunk_total(la, d);
-            float b = 0.f;
+            xch[hf * D + d] = half_total(la, d, hf);
+            __syncthreads();
+            bC = xch[d] + xch[D + d];
+            pre = hf ? xch[d] : 0.f;
+            float b = pre;
             uint8_t* kt = sm + A_K;
 #pragma unroll 4
-            for (int t = 0; t < C; t++) {
+            for (int t = 32 * hf; t < 32 * hf + 32; t++) {
                 b += la[t * D + d];
                 uint16_t* e = reinterpret_cast<uint16_t*>(kt + tile_off(t, d, 8192));
                 *e = f2bf(bf2f(*e) * ex2f((bC - b) * kLog2e));
@@ -262,7 +290,7 @@ __global__ void __launch_bounds__(kThr, 1) gla_bwd_dq_kernel(const __grid_consta
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (d == 0) {
+        if (tid == 0) {
             // D = dO V^T (M = 128, rows 64..127 read past the dO tile and are ignored)
             constexpr uint32_t idD = make_idesc_bf16(128, 64, 0, 0);
 #pragma unroll
@@ -277,11 +305,12 @@ __global__ void __launch_bounds__(kThr, 1) gla_bwd_dq_kernel(const __grid_consta
         }
         if (!(ok = wait_all(bar_mma, 0, abort_flag, p))) break;
         tc_fence_after();
-        // state: S' = e^{b_C} S (bf16 high and low copies for the dQ product), S = S' + dS
+        // state, columns [64 hf, 64 hf + 64): S' = e^{b_C} S (bf16 high and low copies for the
+        // dQ product), S = S' + dS
         {
             const float g = p.gate ? ex2f(bC * kLog2e) : 1.f;
 #pragma unroll 1
-            for (int h = 0; h < 4; h++) {
+            for (int h = 2 * hf; h < 2 * hf + 2; h++) {
                 uint32_t rs[32], rd[32], pk[16], pl[16];
                 tmem_ld32(lane + TA_S + h * 32, rs);
                 tmem_ld32(lane + TA_DS + h * 32, rd);
@@ -298,13 +327,13 @@ __global__ void __launch_bounds__(kThr, 1) gla_bwd_dq_kernel(const __grid_consta
                 tmem_st16(lane + TA_SL + h * 16, pl);
             }
         }
-        if (d < C) mask_rows(lane + TA_D, sm + A_DM, d);
+        if (d < C) mask_half(lane + TA_D, sm + A_DM, d, hf);
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (d == 0) {
+        if (tid == 0) {
             // dQ^T = (S'_hi + S'_lo) dO^T (A operands from TMEM) + Kh^T D_m^T
             constexpr uint32_t idQ = make_idesc_bf16(128, 64, 0, 0);
 #pragma unroll
@@ -322,55 +351,48 @@ __global__ void __launch_bounds__(kThr, 1) gla_bwd_dq_kernel(const __grid_consta
         if (!(ok = wait_all(bar_mma, 1, abort_flag, p))) break;
         tc_fence_after();
         // every product that reads this chunk's tiles has completed: load the next chunk's
-        if (d == 0 && c + 1 < N) {
+        if (tid == 0 && c + 1 < N) {
             load_tiles(bar_t, maps, dsts, 3, c + 1, bh);
-            pend_t = true;
+            pn.tiles_issued++;
         }
-        // dq_t = e^{b_t - b_C} dQ^T[d][t]
+        // dq_t = e^{b_t - b_C} dQ^T[d][t] for this half's tokens
         {
             float* dqp = p.dq + ((long)bh * L + (long)c * C) * D + d;
-            float b = 0.f;
-#pragma unroll 1
-            for (int h = 0; h < 2; h++) {
-                uint32_t r[32];
-                tmem_ld32(lane + TA_Q + h * 32, r);
-                tmem_wait_ld();
+            float b = pre;
+            uint32_t r[32];
+            tmem_ld32(lane + TA_Q + hf * 32, r);
+            tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; e++) {
-                    const int t = h * 32 + e;
-                    float f = 1.f;
-                    if (p.gate) {
-                        b += la[t * D + d];
-                        f = ex2f((b - bC) * kLog2e);
-                    }
-                    if (t < nval) dqp[(long)t * D] = __uint_as_float(r[e]) * f;
+            for (int e = 0; e < 32; e++) {
+                const int t = hf * 32 + e;
+                float f = 1.f;
+                if (p.gate) {
+                    b += la[t * D + d];
+                    f = ex2f((b - bC) * kLog2e);
                 }
+                if (t < nval) dqp[(long)t * D] = __uint_as_float(r[e]) * f;
             }
         }
-        // log alpha is read until here
+        tc_fence_before();
         __syncthreads();
-        if (d == 0 && c + 1 < N && p.gate) {
-            load_la(p, bar_l, sb + A_LA, c + 1, bh);
-            pend_l = true;
-        }
-        pend_t = __syncthreads_or(pend_t);
-        pend_l = __syncthreads_or(pend_l);
     }
     if (!ok) {
-        drain(bar_t, c & 1, pend_t, bar_l, c & 1, pend_l, bar_drain);
+        drain(pn, bar_t, bar_l, bar_drain);
     } else if (p.dla && p.dfinal) {
         // the final-state part of the gate gradient, rowsum(dS_{L-1} * S_{L-1}), for the second pass
         const float* df = p.dfinal + ((long)bh * D + d) * D;
         float s = 0.f;
 #pragma unroll 1
-        for (int h = 0; h < 4; h++) {
+        for (int h = 2 * hf; h < 2 * hf + 2; h++) {
             uint32_t r[32];
             tmem_ld32(lane + TA_S + h * 32, r);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; e++) s = fmaf(df[h * 32 + e], __uint_as_float(r[e]), s);
         }
-        p.dla[((long)bh * L + L - 1) * D + d] = s;
+        xch[hf * D + d] = s;
+        __syncthreads();
+        if (hf == 0) p.dla[((long)bh * L + L - 1) * D + d] = xch[d] + xch[D + d];
     }
     tc_fence_before();
     __syncthreads();
@@ -381,37 +403,44 @@ __global__ void __launch_bounds__(kThr, 1) gla_bwd_dq_kernel(const __grid_consta
 }
 
 // ================================================================ dk / dv pass
-// smem: q | k | v | dO | log alpha | G high (bf16) | G low | P_m | D_m | barriers
-constexpr int B_Q = 0, B_K = TB, B_V = 2 * TB, B_DO = 3 * TB, B_LA = 4 * TB, B_GS = 4 * TB + LAB,
-              B_GL = B_GS + GSB, B_PM = B_GL + GSB, B_DM = B_PM + PB, B_BAR = B_DM + PB;
+// smem: q | k | v | dO | log alpha x 2 | G high (bf16) | G low | P_m | D_m | exchange | barriers
+constexpr int B_Q = 0, B_K = TB, B_V = 2 * TB, B_DO = 3 * TB, B_LA = 4 * TB, B_GS = 4 * TB + 2 * LAB,
+              B_GL = B_GS + GSB, B_PM = B_GL + GSB, B_DM = B_PM + PB, B_X = B_DM + PB, B_BAR = B_X + 2048;
 constexpr int B_SMEM = B_BAR + 64 + 1024;
 // TMEM: G 0..127, dG 128..255, P 256..319, D 320..383, dK^T 384..447, dV^T 448..511
 constexpr uint32_t TB_G = 0, TB_DG = 128, TB_P = 256, TB_D = 320, TB_K = 384, TB_V = 448;
 
-__global__ void __launch_bounds__(kThr, 1) gla_bwd_dkdv_kernel(const __grid_constant__ BwdTcParams p) {
+__global__ void __launch_bounds__(kThr2, 1) gla_bwd_dkdv_kernel(const __grid_constant__ BwdTcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
-    const int d = threadIdx.x, warp = d >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, d = tid & (D - 1), hf = tid >> 7;
     const int bh = blockIdx.x;
     const int L = p.L, N = p.nchunks;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + B_BAR);
-    const uint32_t bar_t = smem_u32(&bars[0]), bar_l = smem_u32(&bars[1]), bar_mma = smem_u32(&bars[2]),
-                   bar_drain = smem_u32(&bars[3]);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + B_BAR + 40);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + B_BAR + 44);
+    const uint32_t bar_t = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[1]), bar_drain = smem_u32(&bars[2]);
+    const uint32_t bar_l[2] = {smem_u32(&bars[3]), smem_u32(&bars[4])};
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + B_BAR + 48);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + B_BAR + 52);
+    float* xch = reinterpret_cast<float*>(sm + B_X);  // [2][D]: per-half sums
     const CUtensorMap* maps[4] = {&p.tm_q, &p.tm_k, &p.tm_v, &p.tm_do};
     const uint32_t dsts[4] = {sb + B_Q, sb + B_K, sb + B_V, sb + B_DO};
-    if (d == 0) {
+    Pending pn;
+    if (tid == 0) {
         mbar_init(bar_t, 1);
-        mbar_init(bar_l, 1);
         mbar_init(bar_mma, 1);
         mbar_init(bar_drain, 1);
+        mbar_init(bar_l[0], 1);
+        mbar_init(bar_l[1], 1);
         *abort_flag = 0;
         mbar_fence_init();
         if (N > 0) {
             load_tiles(bar_t, maps, dsts, 4, N - 1, bh);
-            if (p.gate) load_la(p, bar_l, sb + B_LA, N - 1, bh);
+            pn.tiles_issued++;
+            if (p.gate) {
+                load_la(p, bar_l[0], sb + B_LA, N - 1, bh);
+                pn.la_issued[0]++;
+            }
         }
     }
     if (warp == 0) tmem_alloc(smem_u32(tslot), 512);
@@ -419,12 +448,12 @@ __global__ void __launch_bounds__(kThr, 1) gla_bwd_dkdv_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t lane = tmem + ((uint32_t)(warp * 32) << 16);
-    // G_{N-1} = dL/dS_{L-1}: row d of dfinal
+    const uint32_t lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    // G_{N-1} = dL/dS_{L-1}: columns [64 hf, 64 hf + 64) of row d of dfinal
     {
         const float* g0 = p.dfinal ? p.dfinal + ((long)bh * D + d) * D : nullptr;
 #pragma unroll 1
-        for (int h = 0; h < 4; h++) {
+        for (int h = 2 * hf; h < 2 * hf + 2; h++) {
             uint32_t r[32];
 #pragma unroll
             for (int e = 0; e < 32; e++) r[e] = __float_as_uint(g0 ? g0[h * 32 + e] : 0.f);
@@ -432,31 +461,41 @@ __global__ void __launch_bounds__(kThr, 1) gla_bwd_dkdv_kernel(const __grid_cons
         }
         tmem_wait_st();
     }
-    // running suffix of the gate gradient for channel d (starts from the final-state part the
-    // dq pass left in the last token's row)
+    // running suffix of the gate gradient of channel d over the chunks done so far (starts from
+    // the final-state part the dq pass left in the last token's row)
     float acc = 0.f;
     if (p.dla && p.dfinal) acc = p.dla[((long)bh * L + L - 1) * D + d];
-    const float* la = reinterpret_cast<const float*>(sm + B_LA);
-    bool ok = true, pend_t = N > 0, pend_l = N > 0 && p.gate, strong = false;
+    bool ok = true, strong = false;
     int it = 0;
     for (int c = N - 1; c >= 0; c--, it++) {
+        const float* la = reinterpret_cast<const float*>(sm + B_LA + (it & 1) * LAB);
         if (!(ok = wait_all(bar_t, it & 1, abort_flag, p))) break;
-        pend_t = false;
+        if (tid == 0) pn.tiles_done++;
         if (p.gate) {
-            if (!(ok = wait_all(bar_l, it & 1, abort_flag, p))) break;
-            pend_l = false;
+            if (!(ok = wait_all(bar_l[it & 1], (it >> 1) & 1, abort_flag, p))) break;
+            if (tid == 0) {
+                pn.la_done[it & 1]++;
+                if (c > 0) {
+                    load_la(p, bar_l[(it + 1) & 1], sb + B_LA + ((it + 1) & 1) * LAB, c - 1, bh);
+                    pn.la_issued[(it + 1) & 1]++;
+                }
+            }
         }
         const int nval = min(C, L - c * C);
-        // gate: Qh = q e^{b_t - b_C}, Kh = k e^{b_C - b_t} in place
-        float bC = 0.f;
+        // gate: Qh = q e^{b_t - b_C}, Kh = k e^{b_C - b_t} in place for this half's tokens
+        float bC = 0.f, pre = 0.f, part1 = 0.f;
         if (p.gate) {
-            bC = chunk_total(la, d);
+            xch[hf * D + d] = half_total(la, d, hf);
+            __syncthreads();
+            bC = xch[d] + xch[D + d];
+            pre = hf ? xch[d] : 0.f;
+            part1 = xch[D + d];  // tokens 32..63
             strong |= bC < kStrongLog;
-            float b = 0.f;
+            float b = pre;
             uint8_t* qt = sm + B_Q;
             uint8_t* kt = sm + B_K;
 #pragma unroll 4
-            for (int t = 0; t < C; t++) {
+            for (int t = 32 * hf; t < 32 * hf + 32; t++) {
                 b += la[t * D + d];
                 const uint32_t o = tile_off(t, d, 8192);
                 uint16_t* eq = reinterpret_cast<uint16_t*>(qt + o);
@@ -465,9 +504,9 @@ __global__ void __launch_bounds__(kThr, 1) gla_bwd_dkdv_kernel(const __grid_cons
                 *ek = f2bf(bf2f(*ek) * ex2f((bC - b) * kLog2e));
             }
         }
-        // bf16 high and low copies of G_c into shared memory, row d ([d][j], two atoms of 64 columns)
+        // bf16 high and low copies of G_c into shared memory: columns [64 hf, 64 hf + 64) of row d
 #pragma unroll 1
-        for (int h = 0; h < 4; h++) {
+        for (int h = 2 * hf; h < 2 * hf + 2; h++) {
             uint32_t r[32];
             tmem_ld32(lane + TB_G + h * 32, r);
             tmem_wait_ld();
@@ -488,7 +527,7 @@ __global__ void __launch_bounds__(kThr, 1) gla_bwd_dkdv_kernel(const __grid_cons
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (d == 0) {
+        if (tid == 0) {
             constexpr uint32_t id64 = make_idesc_bf16(128, 64, 0, 0);
             // P = Qh Kh^T and D = dO V^T (M = 128: rows 64..127 read past the tile and are ignored)
 #pragma unroll
@@ -507,15 +546,15 @@ __global__ void __launch_bounds__(kThr, 1) gla_bwd_dkdv_kernel(const __grid_cons
         if (!(ok = wait_all(bar_mma, 0, abort_flag, p))) break;
         tc_fence_after();
         if (d < C) {
-            mask_rows(lane + TB_P, sm + B_PM, d);
-            mask_rows(lane + TB_D, sm + B_DM, d);
+            mask_half(lane + TB_P, sm + B_PM, d, hf);
+            mask_half(lane + TB_D, sm + B_DM, d, hf);
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (d == 0) {
-            // dK^T = G V^T + Qh^T D_m
+        if (tid == 0) {
+            // dK^T = (G_hi + G_lo) V^T + Qh^T D_m
             constexpr uint32_t idK1 = make_idesc_bf16(128, 64, 0, 0), idK2 = make_idesc_bf16(128, 64, 1, 1);
 #pragma unroll
             for (int kk = 0; kk < D / 16; kk++)
@@ -526,7 +565,7 @@ __global__ void __launch_bounds__(kThr, 1) gla_bwd_dkdv_kernel(const __grid_cons
 #pragma unroll
             for (int kk = 0; kk < C / 16; kk++)
                 mma_ss(tmem + TB_K, desc_mn(sb + B_Q, kk, 8192), desc_mn(sb + B_DM, kk, 8192), idK2, 1);
-            // dV^T = G^T Kh^T + dO^T P_m
+            // dV^T = (G_hi + G_lo)^T Kh^T + dO^T P_m
             constexpr uint32_t idV1 = make_idesc_bf16(128, 64, 1, 0), idV2 = make_idesc_bf16(128, 64, 1, 1);
 #pragma unroll
             for (int kk = 0; kk < D / 16; kk++)
@@ -542,12 +581,12 @@ __global__ void __launch_bounds__(kThr, 1) gla_bwd_dkdv_kernel(const __grid_cons
         if (!(ok = wait_all(bar_mma, 1, abort_flag, p))) break;
         tc_fence_after();
         // every product that reads this chunk's tiles has completed: load the next chunk's
-        if (d == 0 && c > 0) {
+        if (tid == 0 && c > 0) {
             load_tiles(bar_t, maps, dsts, 4, c - 1, bh);
-            pend_t = true;
+            pn.tiles_issued++;
         }
-        // epilogue, tokens from last to first: dk_i = e^{b_C - b_i} dK^T[d][i], the gate
-        // gradient's suffix sum, dv_i = dV^T[j = d][i]
+        // epilogue for this half's tokens, last to first: dk_i = e^{b_C - b_i} dK^T[d][i],
+        // dv_i = dV^T[j = d][i], and the gate gradient's suffix sums
         {
             const long row0 = (long)bh * L + (long)c * C;
             float* dkp = p.dk + row0 * D + d;
@@ -555,36 +594,49 @@ __global__ void __launch_bounds__(kThr, 1) gla_bwd_dkdv_kernel(const __grid_cons
             const float* dqp = p.dq + row0 * D + d;
             const uint16_t* qp = p.q + row0 * D + d;
             const uint16_t* kp = p.k + row0 * D + d;
-            float* dlp = p.dla ? p.dla + row0 * D + d : nullptr;
-            float r_suf = 0.f;  // b_C - b_i: sum of log alpha over (i, C)
-#pragma unroll 1
-            for (int h = 1; h >= 0; h--) {
-                uint32_t rk[32], rv[32];
-                tmem_ld32(lane + TB_K + h * 32, rk);
-                tmem_ld32(lane + TB_V + h * 32, rv);
-                tmem_wait_ld();
+            float r_suf = hf ? 0.f : part1;  // b_C - b_i: sum of log alpha over (i, C)
+            float gl[32];                    // suffix of q dq - k dk inside this half
+            float loc = 0.f;
+            uint32_t rk[32], rv[32];
+            tmem_ld32(lane + TB_K + hf * 32, rk);
+            tmem_ld32(lane + TB_V + hf * 32, rv);
+            tmem_wait_ld();
 #pragma unroll
-                for (int e = 31; e >= 0; e--) {
-                    const int i = h * 32 + e;
-                    if (i < nval) {
-                        const float f = p.gate ? ex2f(r_suf * kLog2e) : 1.f;
-                        const float dki = __uint_as_float(rk[e]) * f;
-                        dkp[(long)i * D] = dki;
-                        dvp[(long)i * D] = __uint_as_float(rv[e]);
-                        if (dlp) {
-                            acc += bf2f(qp[(long)i * D]) * dqp[(long)i * D] - bf2f(kp[(long)i * D]) * dki;
-                            dlp[(long)i * D] = acc;
-                        }
+            for (int e = 31; e >= 0; e--) {
+                const int i = hf * 32 + e;
+                gl[e] = 0.f;
+                if (i < nval) {
+                    const float f = p.gate ? ex2f(r_suf * kLog2e) : 1.f;
+                    const float dki = __uint_as_float(rk[e]) * f;
+                    dkp[(long)i * D] = dki;
+                    dvp[(long)i * D] = __uint_as_float(rv[e]);
+                    if (p.dla) {
+                        loc += bf2f(qp[(long)i * D]) * dqp[(long)i * D] - bf2f(kp[(long)i * D]) * dki;
+                        gl[e] = loc;
                     }
-                    if (p.gate) r_suf += la[i * D + d];
                 }
+                if (p.gate) r_suf += la[i * D + d];
+            }
+            if (p.dla) {
+                // tokens of the second half come after the first half's in the suffix sums
+                __syncthreads();  // xch was last read by the gate of this chunk
+                xch[hf * D + d] = loc;
+                __syncthreads();
+                const float off = acc + (hf ? 0.f : xch[D + d]);
+                float* dlp = p.dla + row0 * D + d;
+#pragma unroll
+                for (int e = 0; e < 32; e++) {
+                    const int i = hf * 32 + e;
+                    if (i < nval) dlp[(long)i * D] = off + gl[e];
+                }
+                acc += xch[d] + xch[D + d];
             }
         }
-        // G_{c-1} = e^{b_C} (G_c + dG)
+        // G_{c-1} = e^{b_C} (G_c + dG), columns [64 hf, 64 hf + 64)
         {
             const float g = p.gate ? ex2f(bC * kLog2e) : 1.f;
 #pragma unroll 1
-            for (int h = 0; h < 4; h++) {
+            for (int h = 2 * hf; h < 2 * hf + 2; h++) {
                 uint32_t rg[32], rd[32];
                 tmem_ld32(lane + TB_G + h * 32, rg);
                 tmem_ld32(lane + TB_DG + h * 32, rd);
@@ -596,22 +648,15 @@ __global__ void __launch_bounds__(kThr, 1) gla_bwd_dkdv_kernel(const __grid_cons
             }
             tmem_wait_st();
         }
-        // log alpha is read until here
         tc_fence_before();
         __syncthreads();
-        if (d == 0 && c > 0 && p.gate) {
-            load_la(p, bar_l, sb + B_LA, c - 1, bh);
-            pend_l = true;
-        }
-        pend_t = __syncthreads_or(pend_t);
-        pend_l = __syncthreads_or(pend_l);
     }
-    if (!ok) drain(bar_t, it & 1, pend_t, bar_l, it & 1, pend_l, bar_drain);
+    if (!ok) drain(pn, bar_t, bar_l, bar_drain);
     const bool mark = __syncthreads_or(strong) != 0;
     if (ok && !mark && p.dinit) {
         float* di = p.dinit + ((long)bh * D + d) * D;
 #pragma unroll 1
-        for (int h = 0; h < 4; h++) {
+        for (int h = 2 * hf; h < 2 * hf + 2; h++) {
             uint32_t r[32];
             tmem_ld32(lane + TB_G + h * 32, r);
             tmem_wait_ld();
@@ -619,10 +664,10 @@ __global__ void __launch_bounds__(kThr, 1) gla_bwd_dkdv_kernel(const __grid_cons
             for (int e = 0; e < 32; e++) di[h * 32 + e] = __uint_as_float(r[e]);
         }
     }
-    if (ok && mark && d < D / 32) {
+    if (ok && mark && tid < D / 32) {
         // the exact recurrent backward recomputes this head: one mark per row and column block
-        reinterpret_cast<uint32_t*>(p.dk)[(long)bh * L * D + d * 32] = kBwdMark;
-        reinterpret_cast<uint32_t*>(p.dv)[(long)bh * L * D + d * 32] = kBwdMark;
+        reinterpret_cast<uint32_t*>(p.dk)[(long)bh * L * D + tid * 32] = kBwdMark;
+        reinterpret_cast<uint32_t*>(p.dv)[(long)bh * L * D + tid * 32] = kBwdMark;
     }
     tc_fence_before();
     __syncthreads();
@@ -683,8 +728,8 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s) {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gla_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, B_SMEM);
     if (e != cudaSuccess) return e;
-    gla_bwd_dq_kernel<<<BH, kThr, A_SMEM, s>>>(p);
-    gla_bwd_dkdv_kernel<<<BH, kThr, B_SMEM, s>>>(p);
+    gla_bwd_dq_kernel<<<BH, kThr2, A_SMEM, s>>>(p);
+    gla_bwd_dkdv_kernel<<<BH, kThr2, B_SMEM, s>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // heads with a chunk outside the factorisation's range: the exact recurrent kernel
