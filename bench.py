@@ -81,6 +81,28 @@ def bwd_flops(w) -> float:
     return float(w.B * w.H * w.L * (15 if w.gate else 12) * w.dk * w.dv)
 
 
+def bwd_bytes(w, dla=True) -> float:
+    """Backward, algorithmic bytes: q, k, v, dout (bf16) and log alpha read once; dq, dk, dv (and
+    dlog_alpha) written once in fp32."""
+    BH, L = w.B * w.H, w.L
+    per_tok = 2 * (2 * w.dk + 2 * w.dv) + (4 * w.dk if w.gate else 0) + 4 * (2 * w.dk + w.dv) + \
+        (4 * w.dk if (dla and w.gate) else 0)
+    return float(BH * L * per_tok)
+
+
+def bwd_chunk_flops(w) -> float:
+    """Backward in chunk form, tensor-core flops per chunk and head (the chunk algorithm's own
+    products, with the state copies counted once): dq pass D = dO V^T (2 C^2 dv), dS = Kh^T V
+    (2 C dk dv), dQ = S' dO^T + Kh^T D_m^T (2 C dk dv + 2 C^2 dk); dk/dv pass P = Qh Kh^T (2 C^2 dk),
+    D (2 C^2 dv), dG = Qh^T dO (2 C dk dv), dK = G V^T + Qh^T D_m (2 C dk dv + 2 C^2 dk),
+    dV = G^T Kh^T + dO^T P_m (2 C dk dv + 2 C^2 dv)."""
+    Cc, dk, dv = C, w.dk, w.dv
+    per_chunk = (2 * Cc * Cc * dv + 2 * Cc * dk * dv + 2 * Cc * dk * dv + 2 * Cc * Cc * dk) + \
+        (2 * Cc * Cc * dk + 2 * Cc * Cc * dv + 2 * Cc * dk * dv + 2 * Cc * dk * dv + 2 * Cc * Cc * dk +
+         2 * Cc * dk * dv + 2 * Cc * Cc * dv)
+    return float(w.B * w.H * math.ceil(w.L / Cc) * per_chunk)
+
+
 def fp32_alu_peak_tflops(peaks) -> float:
     """FP32 FMA peak from unit counts: SMs x 128 FP32 lanes x 2 flops x max SM clock."""
     import torch
@@ -106,6 +128,7 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {
+    "gla_bwd_dkdv_kernel": ("gla_bwd_tc.cu", "gla_ptx.cuh"),
     "gla_prefill_tc_kernel": ("gla_tc.cu", "gla_ptx.cuh"),
     "gla_decode_kernel": ("gla_decode.cu",),
     "gla_prefill_short_kernel": ("gla_short.cu",),
@@ -624,7 +647,8 @@ def bench_delta(args, device, rank):
 
 def bench_bwd(args, device, rank):
     """The backward pass (gla_bwd) on its workload: B8 H16 L4096 dk = dv = 128, bf16, gated;
-    all of dq, dk, dv and dlog_alpha."""
+    all of dq, dk, dv and dlog_alpha (the chunk form on the tensor cores; the recurrent fp32
+    kernel timed beside it)."""
     import torch
 
     import causal_gated_linear_gb300 as gla
@@ -637,25 +661,31 @@ def bench_bwd(args, device, rank):
         f32(w.B, w.H, w.L, w.dk)
     stream = torch.cuda.current_stream(device)
 
-    def call():
+    def call(flags=0):
         r = gla.gla_bwd(q, k, v, do, dq, dk, dv, w.B, w.H, w.L, w.dk, w.dv, log_alpha=la, dlog_alpha=dla,
-                        stream=stream)
+                        flags=flags, stream=stream)
         if r != 0:
             raise RuntimeError(gla.gla_status_string(r))
 
-    for _ in range(2):
-        call()
-    torch.cuda.synchronize(device)
-    evs = []
-    for _ in range(args.bwd_calls):
-        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        call()
-        e.record(stream)
-        evs.append((a, e))
-    torch.cuda.synchronize(device)
-    gla.check(gla.gla_device_error(stream))
-    return dict(w=w, ms=statistics.mean(a.elapsed_time(e) for a, e in evs), calls=args.bwd_calls)
+    def timed(flags, n):
+        for _ in range(2):
+            call(flags)
+        torch.cuda.synchronize(device)
+        evs = []
+        for _ in range(n):
+            a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call(flags)
+            e.record(stream)
+            evs.append((a, e))
+        torch.cuda.synchronize(device)
+        gla.check(gla.gla_device_error(stream))
+        return statistics.mean(a.elapsed_time(e) for a, e in evs)
+
+    res = dict(w=w, ms=timed(0, args.bwd_calls), calls=args.bwd_calls)
+    # the recurrent fp32 kernel on the same workload, for comparison
+    res["recurrent_ms"] = timed(gla.FLAG_FORCE_SIMT, 2)
+    return res
 
 
 def run_gla(args):
@@ -753,16 +783,29 @@ def run_gla(args):
                          "peak_source": "FP32 FMA: SMs x 128 lanes x 2 flops x max SM clock"}}
     if bwd is not None:
         bw = bwd["w"]
-        bfl = bwd_flops(bw)
-        btf = bfl / (bwd["ms"] / 1e3) / 1e12
-        apk = fp32_alu_peak_tflops(peaks)
+        bb = bwd_bytes(bw)
+        sec = bwd["ms"] / 1e3
+        gbs = bb / sec / 1e9
+        bfl = bwd_chunk_flops(bw)
         line["backward"] = {
             "workload": bw.name, "ms_per_launch": bwd["ms"], "calls": bwd["calls"],
-            "tokens_per_s": bw.B * bw.L / (bwd["ms"] / 1e3),
-            "roofline": {"bound": "alu", "achieved": btf, "peak": apk, "unit": "TFLOP/s", "frac": btf / apk,
-                         "traffic": recorded_traffic("gla_bwd_kernel"), "kernel": "gla_bwd_kernel",
-                         "alg_flops_per_launch": bfl,
-                         "peak_source": "FP32 FMA: SMs x 128 lanes x 2 flops x max SM clock"}}
+            "tokens_per_s": bw.B * bw.L / sec, "tflops": bfl / sec / 1e12,
+            "tensor_frac": bfl / sec / 1e12 / peaks["bf16_tflops"],
+            "path": "chunk form on the tensor cores (dq pass + dk/dv pass)",
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"],
+                         "traffic": recorded_traffic("gla_bwd_dkdv_kernel"),
+                         "kernel": "gla_bwd_dq_kernel + gla_bwd_dkdv_kernel", "alg_bytes_per_launch": bb,
+                         "alg_flops_per_launch": bfl}}
+        if "recurrent_ms" in bwd:
+            rf = bwd_flops(bw)
+            apk = fp32_alu_peak_tflops(peaks)
+            rtf = rf / (bwd["recurrent_ms"] / 1e3) / 1e12
+            line["backward"]["recurrent"] = {
+                "ms_per_launch": bwd["recurrent_ms"], "kernel": "gla_bwd_kernel (GLA_FLAG_FORCE_SIMT)",
+                "roofline": {"bound": "alu", "achieved": rtf, "peak": apk, "unit": "TFLOP/s", "frac": rtf / apk,
+                             "alg_flops_per_launch": rf,
+                             "peak_source": "FP32 FMA: SMs x 128 lanes x 2 flops x max SM clock"}}
     if mdec is not None:
         mw = mdec["w"]
         mbytes = decode_multi_bytes(mw)

@@ -75,3 +75,13 @@ def test_prefill_bytes_of_the_other_workloads():
     assert bench.prefill_bytes(synth.ELU_NORM, final_state=False) == 32 * 2048 * (3 * 128 + 128) == 33554432
     # gated B8 H16 L4096 d128, zero initial state, final state written
     assert bench.prefill_bytes(synth.PREFILL) == 128 * (4096 * (3 * 256 + 512 + 256) + 128 * 128 * 4) == 813694976
+
+
+def test_backward_bytes_and_chunk_flops():
+    # 128 heads x 4096 tokens x (q, k, v, dout bf16 4 x 256 + log alpha 512 + dq, dk, dv 3 x 512
+    # + dlog_alpha 512)
+    assert bench.bwd_bytes(synth.BWD) == 128 * 4096 * (1024 + 512 + 1536 + 512)
+    # per chunk: six products over a C x C operand (D twice, P, and the masked parts of dQ, dK, dV:
+    # 2 C^2 d each) and five over the state (dS, dQ, dG, dK, dV: 2 C d^2 each)
+    per_chunk = 6 * 2 * 64 * 64 * 128 + 5 * 2 * 64 * 128 * 128
+    assert bench.bwd_chunk_flops(synth.BWD) == 128 * 64 * per_chunk
