@@ -39,7 +39,8 @@ GLA_OK, GLA_ERR_INVALID, GLA_ERR_UNSUPPORTED, GLA_ERR_MISALIGNED, GLA_ERR_CUDA, 
 BF16, F32 = 0, 1
 FLAG_FEATURE_ELU1, FLAG_NORMALIZE, FLAG_FORCE_SIMT, FLAG_FORCE_CHUNK, FLAG_SCALAR_GATE = 1, 2, 4, 8, 16
 
-EXPORTED = ["gla_fwd", "gla_fwd_ex", "gla_fwd_host", "gla_decode_step", "gla_delta_fwd", "gla_bwd", "gla_device_error",
+EXPORTED = ["gla_fwd", "gla_fwd_ex", "gla_fwd_host", "gla_decode_step", "gla_delta_fwd", "gla_delta_fwd_ex", "gla_bwd",
+            "gla_device_error",
             "gla_device_error_detail", "gla_test_set_waits", "gla_status_string", "gla_version"]
 
 
@@ -84,6 +85,8 @@ def load(path: str | None = None):
     lib.gla_decode_step.restype = i
     lib.gla_delta_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
     lib.gla_delta_fwd.restype = i
+    lib.gla_delta_fwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, ctypes.c_uint, vp]
+    lib.gla_delta_fwd_ex.restype = i
     lib.gla_bwd.argtypes = [vp] * 12 + [i] * 6 + [ctypes.c_uint, vp]
     lib.gla_bwd.restype = i
     lib.gla_device_error.argtypes = [vp]
@@ -167,7 +170,12 @@ def gla_decode_step(q, k, v, log_alpha, state, out, B, H, dk, dv, stream=None) -
 
 
 def gla_delta_fwd(q, k, v, beta, out, B, H, L, dk, dv, log_alpha=None, init_state=None, final_state=None,
-                  out_dtype=BF16, stream=None) -> int:
+                  out_dtype=BF16, flags=0, stream=None) -> int:
+    """The delta rule; `flags` (GLA_FLAG_FORCE_SIMT) goes through gla_delta_fwd_ex."""
+    if flags:
+        return load().gla_delta_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(log_alpha), _ptr(init_state),
+                                       _ptr(out), _ptr(final_state), B, H, L, dk, dv, out_dtype, flags,
+                                       _stream(stream))
     return load().gla_delta_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(log_alpha), _ptr(init_state),
                                 _ptr(out), _ptr(final_state), B, H, L, dk, dv, out_dtype, _stream(stream))
 

@@ -17,7 +17,7 @@ LIB = os.path.join(BUILD, "libgla.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["gla_api.cu", "gla_simt.cu", "gla_decode.cu", "gla_tc.cu", "gla_short.cu", "gla_delta.cu", "gla_bwd.cu",
-           "gla_bwd_tc.cu"]
+           "gla_bwd_tc.cu", "gla_delta_tc.cu"]
 HEADERS = ["gla_internal.h", "gla_ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -324,11 +324,12 @@ int gla_decode_step(const void* q, const void* k, const void* v, const float* lo
     return finish(launch_decode(a, s), s);
 }
 
-int gla_delta_fwd(const void* q, const void* k, const void* v, const float* beta, const float* log_alpha,
-                  const float* init_state, void* out, float* final_state, int B, int H, int L, int dk, int dv,
-                  int out_dtype, void* stream) {
+int gla_delta_fwd_ex(const void* q, const void* k, const void* v, const float* beta, const float* log_alpha,
+                     const float* init_state, void* out, float* final_state, int B, int H, int L, int dk, int dv,
+                     int out_dtype, unsigned flags, void* stream) {
     if (B < 1 || H < 1 || L < 0 || dk < 1 || dv < 1) return GLA_ERR_INVALID;
     if (out_dtype != GLA_DTYPE_BF16 && out_dtype != GLA_DTYPE_F32) return GLA_ERR_INVALID;
+    if (flags & ~(unsigned)GLA_FLAG_FORCE_SIMT) return GLA_ERR_INVALID;
     if (L > 0 && (!q || !k || !v || !beta || !out)) return GLA_ERR_INVALID;
     if (!delta_supported(dk, dv)) return GLA_ERR_UNSUPPORTED;
     if ((size_t)B * H > 0x7fffffffu || (dv + 63) / 64 > 65535) return GLA_ERR_UNSUPPORTED;
@@ -367,8 +368,24 @@ int gla_delta_fwd(const void* q, const void* k, const void* v, const float* beta
     a.dk = dk;
     a.dv = dv;
     a.out_dtype = out_dtype;
+    a.flags = flags;
+    a.err_word = nullptr;
+    a.wait_ns = g_wait_ns;
+    a.only_marked = 0;
     if (launch_failure_injected()) return GLA_ERR_CUDA;
+    if (delta_tc_supported(a)) {
+        a.err_word = err_word_ptr();
+        if (!a.err_word) return GLA_ERR_CUDA;
+        return finish(launch_delta_tc(a, s), s);
+    }
     return finish(launch_delta(a, s), s);
+}
+
+int gla_delta_fwd(const void* q, const void* k, const void* v, const float* beta, const float* log_alpha,
+                  const float* init_state, void* out, float* final_state, int B, int H, int L, int dk, int dv,
+                  int out_dtype, void* stream) {
+    return gla_delta_fwd_ex(q, k, v, beta, log_alpha, init_state, out, final_state, B, H, L, dk, dv, out_dtype, 0u,
+                            stream);
 }
 
 int gla_bwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* init_state,

@@ -132,6 +132,14 @@ __global__ void __launch_bounds__(kThreads, 2) gla_delta_kernel(const DeltaArgs 
     const long bh = blockIdx.x;
     const int col0 = blockIdx.y * kCols;
     const int ncols = min(kCols, dv - col0);
+    if (a.only_marked) {
+        // after the chunk-form kernel: only the column blocks of the heads it marked
+        const long m = bh * L * dv + col0;
+        const bool marked = a.out_dtype == GLA_DTYPE_F32
+                                ? reinterpret_cast<const uint32_t*>(a.out)[m] == kDeltaMarkF32
+                                : reinterpret_cast<const uint16_t*>(a.out)[m] == kDeltaMarkBf16;
+        if (!marked) return;
+    }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rg = lane >> 1, cp = lane & 1;
     const int c = warp * 4 + cp * 2;        // this lane's first column within the CTA's block

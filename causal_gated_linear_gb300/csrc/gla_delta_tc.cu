@@ -1,0 +1,612 @@
+// gla_delta_tc.cu -- the delta rule in chunk form on the tensor cores
+// (tcgen05 + TMEM + TMA), sm_103a.
+//
+// "linear-attention" blog, Delta attention and its Prefill section: the writes
+// of a sequence solve one lower-triangular system.  Per token (gated form: the
+// state decays first, "Gated Linear Attention", GLA Recurrent Form)
+//   S <- Diag(alpha_t) S;  u_t = beta_t (v_t - S^T k_t);  S <- S + k_t u_t^T;  o_t = S^T q_t.
+// Over a chunk of C = 64 tokens starting from S_0, with b_t the in-chunk
+// inclusive cumsum of log alpha and b_C its last value, put
+//   Kr_t = k_t e^{b_t - b_C},  Kh_i = k_i e^{b_C - b_i},  Qh_t = q_t e^{b_t - b_C},
+//   S' = Diag(e^{b_C}) S_0,   A = Kr Kh^T  (A_ti = sum_d k_td k_id e^{b_td - b_id}).
+// Unrolling the recurrence, the chunk's writes U solve the unit lower-triangular
+// system (I + Diag(beta) tril_strict(A)) U = Diag(beta) (V - Kr S'), so with
+// T = (I + Diag(beta) tril_strict(A))^{-1} and M = T Diag(beta):
+//   U = M V - (M Kr) S'
+//   O = Qh S' + tril(Qh Kh^T) U            (inclusive diagonal)
+//   S_C = S' + Kh^T U.
+// Every product is a tcgen05 MMA on 128-byte-swizzled bf16 tiles; T is the
+// inverse of a 64 x 64 unit lower-triangular matrix, computed in fp32 by blocked
+// forward substitution (16 x 16 diagonal blocks, then the off-diagonal blocks
+// level by level).  The state copy S' and the writes U enter their products as
+// bf16 high and low parts (x = hi + lo to ~2^-17).
+//
+// One CTA of 256 threads per (batch, head), d_k = d_v = 128: thread (d, hf) owns
+// key channel d (TMEM lane d) and half hf of the chunk's tokens / of the state's
+// columns.  Phases run on all threads in turn with bounded waits.  A chunk over
+// which some channel decays by more than e^-64 is outside the factorisation's
+// range: the head is marked (a NaN pattern in the first output element of each
+// 64-column block) and the token-by-token kernel recomputes exactly the marked
+// heads afterwards.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "gla_internal.h"
+#include "gla_ptx.cuh"
+
+namespace gla {
+namespace {
+
+constexpr int C = 64, D = 128;
+constexpr int kThr = 256;
+constexpr int TB = C * D * 2;    // bf16 [64][128]: two 8 KB atoms
+constexpr int LAB = C * D * 4;   // fp32 log alpha tile
+constexpr int PB = C * C * 2;    // bf16 [64][64]: one atom
+constexpr int SB2 = D * D * 2;   // bf16 [128][128]: two 16 KB atoms
+constexpr int FB = C * C * 4;    // fp32 [64][64]
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kStrongLog = -64.f;
+
+struct DeltaTcParams {
+    CUtensorMap tm_q, tm_k, tm_v, tm_la;
+    const float* beta;
+    const float* init_state;
+    void* out;
+    float* final_state;
+    unsigned* err;
+    unsigned long long wait_ns;
+    int L, nchunks, gate, out_f32;
+};
+
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+__device__ __forceinline__ uint16_t f2bf(float x) {
+    __nv_bfloat16 h = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t*>(&h);
+}
+__device__ __forceinline__ uint32_t tile_off(int row, int col, int atom) {
+    return (col >> 6) * atom + sw128_offset(row, col & 63);
+}
+__device__ __forceinline__ uint64_t desc_k(uint32_t tile, int kk, int atom) {
+    return sdesc_const(16, 1024) | ((tile + (kk >> 2) * atom + (kk & 3) * 32) >> 4);
+}
+__device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int kk, int lbo) {
+    return sdesc_const(lbo, 1024) | ((tile + kk * 2048) >> 4);
+}
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16x2(x0, x1);
+    const float2 h = unpack_bf16x2(hi);
+    lo = pack_bf16x2(x0 - h.x, x1 - h.y);
+}
+
+// smem: q->Qh | k->Kh | Kr (later U high) | v (later U low) | log alpha | S' high | S' low |
+//       M | P_m | N, then -(M Kr) | T | beta | exchange | barriers
+constexpr int S_Q = 0, S_K = TB, S_KR = 2 * TB, S_V = 3 * TB, S_LA = 4 * TB, S_SH = 4 * TB + LAB,
+              S_SL = S_SH + SB2, S_M = S_SL + SB2, S_PM = S_M + PB, S_N = S_PM + PB, S_T = S_N + FB,
+              S_BETA = S_T + FB, S_X = S_BETA + C * 4, S_BAR = S_X + 2 * D * 4;
+constexpr int S_SMEM = S_BAR + 64 + 1024;
+static_assert(S_SMEM <= 227 * 1024, "shared memory budget");
+// TMEM: S 0..127, dS 128..255, U 256..383; 384..511 holds A and P (64 each), then M Kr, then O^T
+constexpr uint32_t T_S = 0, T_DS = 128, T_U = 256, T_A = 384, T_P = 448, T_W = 384, T_O = 384;
+
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         const DeltaTcParams& p) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, p.err, p.wait_ns);
+    return __syncthreads_and(ok) != 0;
+}
+
+__device__ __forceinline__ void load_tiles(const DeltaTcParams& p, uint32_t bar, uint32_t sb, int c, int bh) {
+    mbar_arrive_expect_tx(bar, 3 * TB);
+    const CUtensorMap* maps[3] = {&p.tm_q, &p.tm_k, &p.tm_v};
+    const uint32_t dst[3] = {sb + S_Q, sb + S_K, sb + S_V};
+    for (int m = 0; m < 3; m++) {
+        tma_load_3d(dst[m], maps[m], bar, 0, c * C, bh);
+        tma_load_3d(dst[m] + 8192, maps[m], bar, 64, c * C, bh);
+    }
+}
+
+// T = (I + N)^{-1} for N strictly lower triangular (fp32 [64][64] in shared
+// memory): 16 x 16 diagonal blocks by forward substitution (one thread per
+// column), then the off-diagonal blocks level by level,
+//   T_IJ = -T_II sum_{J <= K < I} N_IK T_KJ   (I > J).
+// Every thread of the CTA takes part (the barriers are CTA-wide).
+__device__ __forceinline__ void unit_lower_inverse(const float* N, float* T, int tid) {
+    // zero the upper part (including the diagonal blocks' upper triangles)
+    for (int e = tid; e < C * C; e += kThr) T[e] = 0.f;
+    __syncthreads();
+    if (tid < C) {
+        const int blk = tid >> 4, j = tid & 15, o = blk * 16;
+        float col[16];
+#pragma unroll
+        for (int t = 0; t < 16; t++) {
+            float x = (t == j) ? 1.f : 0.f;
+            if (t > j) {
+#pragma unroll
+                for (int i = 0; i < 16; i++)
+                    if (i >= j && i < t) x -= N[(o + t) * C + o + i] * col[i];
+            }
+            col[t] = x;
+        }
+#pragma unroll
+        for (int t = 0; t < 16; t++) T[(o + t) * C + o + j] = col[t];
+    }
+    __syncthreads();
+    for (int lvl = 1; lvl < 4; lvl++) {
+        // Y_IJ = sum_{J <= K < I} N_IK T_KJ for the 4 - lvl blocks (I, J = I - lvl): one entry per
+        // thread and block
+        float y[3];
+        const int a = tid >> 4, b = tid & 15;
+#pragma unroll
+        for (int n = 0; n < 3; n++) {
+            y[n] = 0.f;
+            if (n < 4 - lvl) {
+                const int I = n + lvl, J = n;
+                for (int Kb = J; Kb < I; Kb++)
+#pragma unroll
+                    for (int cc = 0; cc < 16; cc++)
+                        y[n] += N[(I * 16 + a) * C + Kb * 16 + cc] * T[(Kb * 16 + cc) * C + J * 16 + b];
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int n = 0; n < 3; n++)
+            if (n < 4 - lvl) T[((n + lvl) * 16 + a) * C + n * 16 + b] = y[n];  // Y, temporarily
+        __syncthreads();
+        float z[3];
+#pragma unroll
+        for (int n = 0; n < 3; n++) {
+            z[n] = 0.f;
+            if (n < 4 - lvl) {
+                const int I = n + lvl, J = n;
+#pragma unroll
+                for (int cc = 0; cc < 16; cc++)
+                    z[n] -= T[(I * 16 + a) * C + I * 16 + cc] * T[(I * 16 + cc) * C + J * 16 + b];
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int n = 0; n < 3; n++)
+            if (n < 4 - lvl) T[((n + lvl) * 16 + a) * C + n * 16 + b] = z[n];
+        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_constant__ DeltaTcParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, d = tid & (D - 1), hf = tid >> 7;
+    const int bh = blockIdx.x;
+    const int L = p.L, N = p.nchunks;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S_BAR);
+    const uint32_t bar_t = smem_u32(&bars[0]), bar_l = smem_u32(&bars[1]), bar_mma = smem_u32(&bars[2]),
+                   bar_drain = smem_u32(&bars[3]);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S_BAR + 40);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S_BAR + 44);
+    float* xch = reinterpret_cast<float*>(sm + S_X);
+    float* betas = reinterpret_cast<float*>(sm + S_BETA);
+    float* Nf = reinterpret_cast<float*>(sm + S_N);
+    float* Tf = reinterpret_cast<float*>(sm + S_T);
+    int tiles_issued = 0, tiles_done = 0, la_issued = 0, la_done = 0;
+    if (tid == 0) {
+        mbar_init(bar_t, 1);
+        mbar_init(bar_l, 1);
+        mbar_init(bar_mma, 1);
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        load_tiles(p, bar_t, sb, 0, bh);
+        tiles_issued++;
+        if (p.gate) {
+            mbar_arrive_expect_tx(bar_l, LAB);
+            tma_load_3d(sb + S_LA, &p.tm_la, bar_l, 0, 0, bh);
+            la_issued++;
+        }
+    }
+    if (warp == 0) tmem_alloc(smem_u32(tslot), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    {
+        const float* s0 = p.init_state ? p.init_state + ((long)bh * D + d) * D : nullptr;
+#pragma unroll 1
+        for (int h = 2 * hf; h < 2 * hf + 2; h++) {
+            uint32_t r[32];
+#pragma unroll
+            for (int e = 0; e < 32; e++) r[e] = __float_as_uint(s0 ? s0[h * 32 + e] : 0.f);
+            tmem_st32(lane + T_S + h * 32, r);
+        }
+        tmem_wait_st();
+    }
+    const float* la = reinterpret_cast<const float*>(sm + S_LA);
+    bool ok = true, strong = false;
+    int mph = 0;  // phases of bar_mma completed
+    for (int c = 0; c < N; c++) {
+        if (!(ok = wait_all(bar_t, c & 1, abort_flag, p))) break;
+        if (tid == 0) tiles_done++;
+        if (p.gate) {
+            if (!(ok = wait_all(bar_l, c & 1, abort_flag, p))) break;
+            if (tid == 0) la_done++;
+        }
+        const int nval = min(C, L - c * C);
+        if (tid < C) betas[tid] = tid < nval ? p.beta[(long)bh * L + (long)c * C + tid] : 0.f;
+        // gate and factors for this half's tokens: Kr = k e^{b_t - b_C} (new tile), Kh = k e^{b_C - b_t}
+        // and Qh = q e^{b_t - b_C} in place
+        float bC = 0.f;
+        {
+            float pre = 0.f;
+            if (p.gate) {
+                float s0 = 0.f;
+#pragma unroll 8
+                for (int t = 32 * hf; t < 32 * hf + 32; t++) s0 += la[t * D + d];
+                xch[hf * D + d] = s0;
+                __syncthreads();
+                bC = xch[d] + xch[D + d];
+                pre = hf ? xch[d] : 0.f;
+                strong |= bC < kStrongLog;
+            }
+            float b = pre;
+#pragma unroll 4
+            for (int t = 32 * hf; t < 32 * hf + 32; t++) {
+                const uint32_t o = tile_off(t, d, 8192);
+                uint16_t* eq = reinterpret_cast<uint16_t*>(sm + S_Q + o);
+                uint16_t* ek = reinterpret_cast<uint16_t*>(sm + S_K + o);
+                uint16_t* er = reinterpret_cast<uint16_t*>(sm + S_KR + o);
+                const float kv = bf2f(*ek);
+                if (p.gate) {
+                    b += la[t * D + d];
+                    const float fu = ex2f((b - bC) * kLog2e), fd = ex2f((bC - b) * kLog2e);
+                    *eq = f2bf(bf2f(*eq) * fu);
+                    *er = f2bf(kv * fu);
+                    *ek = f2bf(kv * fd);
+                } else {
+                    *er = *ek;
+                }
+            }
+        }
+        __syncthreads();
+        // log alpha is read until here: the next chunk's may load
+        if (tid == 0 && p.gate && c + 1 < N) {
+            mbar_arrive_expect_tx(bar_l, LAB);
+            tma_load_3d(sb + S_LA, &p.tm_la, bar_l, 0, (c + 1) * C, bh);
+            la_issued++;
+        }
+        // S' = e^{b_C} S: bf16 high and low copies in shared memory ([d][j], MN-major operand)
+        {
+            const float g = p.gate ? ex2f(bC * kLog2e) : 1.f;
+#pragma unroll 1
+            for (int h = 2 * hf; h < 2 * hf + 2; h++) {
+                uint32_t r[32];
+                tmem_ld32(lane + T_S + h * 32, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e8 = 0; e8 < 4; e8++) {
+                    uint4 wh, wl;
+                    const float* x = reinterpret_cast<const float*>(r + e8 * 8);
+                    split_pair(x[0] * g, x[1] * g, wh.x, wl.x);
+                    split_pair(x[2] * g, x[3] * g, wh.y, wl.y);
+                    split_pair(x[4] * g, x[5] * g, wh.z, wl.z);
+                    split_pair(x[6] * g, x[7] * g, wh.w, wl.w);
+                    const uint32_t o = tile_off(d, h * 32 + e8 * 8, 16384);
+                    *reinterpret_cast<uint4*>(sm + S_SH + o) = wh;
+                    *reinterpret_cast<uint4*>(sm + S_SL + o) = wl;
+                    // keep the fp32 S' for the state update
+                    r[e8 * 8 + 0] = __float_as_uint(x[0] * g);
+                    r[e8 * 8 + 1] = __float_as_uint(x[1] * g);
+                    r[e8 * 8 + 2] = __float_as_uint(x[2] * g);
+                    r[e8 * 8 + 3] = __float_as_uint(x[3] * g);
+                    r[e8 * 8 + 4] = __float_as_uint(x[4] * g);
+                    r[e8 * 8 + 5] = __float_as_uint(x[5] * g);
+                    r[e8 * 8 + 6] = __float_as_uint(x[6] * g);
+                    r[e8 * 8 + 7] = __float_as_uint(x[7] * g);
+                }
+                tmem_st32(lane + T_S + h * 32, r);
+            }
+            tmem_wait_st();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            // A = Kr Kh^T and P = Qh Kh^T (M = 128: rows 64..127 read past the tile and are ignored)
+            constexpr uint32_t id64 = make_idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + T_A, desc_k(sb + S_KR, kk, 8192), desc_k(sb + S_K, kk, 8192), id64, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + T_P, desc_k(sb + S_Q, kk, 8192), desc_k(sb + S_K, kk, 8192), id64, kk > 0);
+            mma_commit(bar_mma);
+        }
+        if (!(ok = wait_all(bar_mma, mph++ & 1, abort_flag, p))) break;
+        tc_fence_after();
+        // N = Diag(beta) tril_strict(A) in fp32; P_m = tril(P) in bf16 (rows t = lanes 0..63)
+        if (d < C) {
+            const int t = d;
+            uint32_t ra[32], rp[32];
+            tmem_ld32(lane + T_A + hf * 32, ra);
+            tmem_ld32(lane + T_P + hf * 32, rp);
+            tmem_wait_ld();
+            const float bt = betas[t];
+#pragma unroll
+            for (int k8 = 0; k8 < 4; k8++) {
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    const int i = hf * 32 + k8 * 8 + e;
+                    x[e] = (i <= t) ? __uint_as_float(rp[k8 * 8 + e]) : 0.f;
+                    Nf[t * C + i] = (i < t) ? bt * __uint_as_float(ra[k8 * 8 + e]) : 0.f;
+                }
+                uint4 w;
+                w.x = pack_bf16x2(x[0], x[1]);
+                w.y = pack_bf16x2(x[2], x[3]);
+                w.z = pack_bf16x2(x[4], x[5]);
+                w.w = pack_bf16x2(x[6], x[7]);
+                *reinterpret_cast<uint4*>(sm + S_PM + sw128_offset(t, hf * 32 + k8 * 8)) = w;
+            }
+        }
+        __syncthreads();
+        unit_lower_inverse(Nf, Tf, tid);
+        // M = T Diag(beta) in bf16 ([t][i], K-major operand); thread (t, half of the columns)
+        if (tid < 2 * C) {
+            const int t = tid & (C - 1), h2 = tid >> 6;
+#pragma unroll
+            for (int k8 = 0; k8 < 4; k8++) {
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    const int i = h2 * 32 + k8 * 8 + e;
+                    x[e] = Tf[t * C + i] * betas[i];
+                }
+                uint4 w;
+                w.x = pack_bf16x2(x[0], x[1]);
+                w.y = pack_bf16x2(x[2], x[3]);
+                w.z = pack_bf16x2(x[4], x[5]);
+                w.w = pack_bf16x2(x[6], x[7]);
+                *reinterpret_cast<uint4*>(sm + S_M + sw128_offset(t, h2 * 32 + k8 * 8)) = w;
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            // U = M V and W = M Kr (A = M K-major, B = V / Kr MN-major), N = 128
+            constexpr uint32_t id128 = make_idesc_bf16(128, 128, 0, 1);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; kk++)
+                mma_ss(tmem + T_U, desc_k(sb + S_M, kk, 8192), desc_mn(sb + S_V, kk, 8192), id128, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; kk++)
+                mma_ss(tmem + T_W, desc_k(sb + S_M, kk, 8192), desc_mn(sb + S_KR, kk, 8192), id128, kk > 0);
+            mma_commit(bar_mma);
+        }
+        if (!(ok = wait_all(bar_mma, mph++ & 1, abort_flag, p))) break;
+        tc_fence_after();
+        // -W in bf16 ([t][d], K-major operand) over N's buffer (rows t = lanes 0..63)
+        if (d < C) {
+            const int t = d;
+#pragma unroll 1
+            for (int h = 2 * hf; h < 2 * hf + 2; h++) {
+                uint32_t r[32];
+                tmem_ld32(lane + T_W + h * 32, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k8 = 0; k8 < 4; k8++) {
+                    uint4 w;
+                    const float* x = reinterpret_cast<const float*>(r + k8 * 8);
+                    w.x = pack_bf16x2(-x[0], -x[1]);
+                    w.y = pack_bf16x2(-x[2], -x[3]);
+                    w.z = pack_bf16x2(-x[4], -x[5]);
+                    w.w = pack_bf16x2(-x[6], -x[7]);
+                    *reinterpret_cast<uint4*>(sm + S_N + tile_off(t, h * 32 + k8 * 8, 8192)) = w;
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            // U += (-W) (S'_hi + S'_lo): A = -W [t][d] K-major, B = S' [d][j] MN-major
+            constexpr uint32_t id128 = make_idesc_bf16(128, 128, 0, 1);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + T_U, desc_k(sb + S_N, kk, 8192), desc_mn(sb + S_SH, kk, 16384), id128, 1);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + T_U, desc_k(sb + S_N, kk, 8192), desc_mn(sb + S_SL, kk, 16384), id128, 1);
+            mma_commit(bar_mma);
+        }
+        if (!(ok = wait_all(bar_mma, mph++ & 1, abort_flag, p))) break;
+        tc_fence_after();
+        // U in bf16 high and low parts over Kr and V ([i][j], MN-major operands; rows i = lanes 0..63)
+        if (d < C) {
+            const int i = d;
+#pragma unroll 1
+            for (int h = 2 * hf; h < 2 * hf + 2; h++) {
+                uint32_t r[32];
+                tmem_ld32(lane + T_U + h * 32, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k8 = 0; k8 < 4; k8++) {
+                    uint4 wh, wl;
+                    const float* x = reinterpret_cast<const float*>(r + k8 * 8);
+                    split_pair(x[0], x[1], wh.x, wl.x);
+                    split_pair(x[2], x[3], wh.y, wl.y);
+                    split_pair(x[4], x[5], wh.z, wl.z);
+                    split_pair(x[6], x[7], wh.w, wl.w);
+                    const uint32_t o = tile_off(i, h * 32 + k8 * 8, 8192);
+                    *reinterpret_cast<uint4*>(sm + S_KR + o) = wh;
+                    *reinterpret_cast<uint4*>(sm + S_V + o) = wl;
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            // O^T = S'^T Qh^T + U^T P_m^T  (M = j: A = S' / U MN-major, B = Qh / P_m K-major)
+            constexpr uint32_t idO = make_idesc_bf16(128, 64, 1, 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + T_O, desc_mn(sb + S_SH, kk, 16384), desc_k(sb + S_Q, kk, 8192), idO, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + T_O, desc_mn(sb + S_SL, kk, 16384), desc_k(sb + S_Q, kk, 8192), idO, 1);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; kk++)
+                mma_ss(tmem + T_O, desc_mn(sb + S_KR, kk, 8192), desc_k(sb + S_PM, kk, 8192), idO, 1);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; kk++)
+                mma_ss(tmem + T_O, desc_mn(sb + S_V, kk, 8192), desc_k(sb + S_PM, kk, 8192), idO, 1);
+            // dS = Kh^T U (A = Kh MN-major, B = U MN-major)
+            constexpr uint32_t idS = make_idesc_bf16(128, 128, 1, 1);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; kk++)
+                mma_ss(tmem + T_DS, desc_mn(sb + S_K, kk, 8192), desc_mn(sb + S_KR, kk, 8192), idS, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; kk++)
+                mma_ss(tmem + T_DS, desc_mn(sb + S_K, kk, 8192), desc_mn(sb + S_V, kk, 8192), idS, 1);
+            mma_commit(bar_mma);
+        }
+        if (!(ok = wait_all(bar_mma, mph++ & 1, abort_flag, p))) break;
+        tc_fence_after();
+        // every product that reads this chunk's tiles has completed: load the next chunk's
+        if (tid == 0 && c + 1 < N) {
+            load_tiles(p, bar_t, sb, c + 1, bh);
+            tiles_issued++;
+        }
+        // output: thread (j = d, half hf of the tokens) writes o[t][j]; state S = S' + dS
+        {
+            uint32_t r[32];
+            tmem_ld32(lane + T_O + hf * 32, r);
+            tmem_wait_ld();
+            const long row0 = (long)bh * L + (long)c * C + hf * 32;
+#pragma unroll
+            for (int e = 0; e < 32; e++) {
+                if (hf * 32 + e < nval) {
+                    const long idx = (row0 + e) * D + d;
+                    if (p.out_f32)
+                        static_cast<float*>(p.out)[idx] = __uint_as_float(r[e]);
+                    else
+                        static_cast<uint16_t*>(p.out)[idx] = f2bf(__uint_as_float(r[e]));
+                }
+            }
+#pragma unroll 1
+            for (int h = 2 * hf; h < 2 * hf + 2; h++) {
+                uint32_t rs[32], rd[32];
+                tmem_ld32(lane + T_S + h * 32, rs);
+                tmem_ld32(lane + T_DS + h * 32, rd);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; e++) rs[e] = __float_as_uint(__uint_as_float(rs[e]) + __uint_as_float(rd[e]));
+                tmem_st32(lane + T_S + h * 32, rs);
+            }
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
+    if (!ok) {
+        volatile int no_abort = 0;
+        if (tid == 0) {
+            for (int n = tiles_done; n < tiles_issued; n++) mbar_wait(bar_t, n & 1, &no_abort, nullptr);
+            for (int n = la_done; n < la_issued; n++) mbar_wait(bar_l, n & 1, &no_abort, nullptr);
+            mma_commit(bar_drain);
+            mbar_wait(bar_drain, 0, &no_abort, nullptr);
+        }
+        __syncthreads();
+    }
+    const bool mark = __syncthreads_or(strong) != 0;
+    if (ok && !mark && p.final_state) {
+        float* fs = p.final_state + ((long)bh * D + d) * D;
+#pragma unroll 1
+        for (int h = 2 * hf; h < 2 * hf + 2; h++) {
+            uint32_t r[32];
+            tmem_ld32(lane + T_S + h * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; e++) fs[h * 32 + e] = __uint_as_float(r[e]);
+        }
+    }
+    if (ok && mark && tid < D / 64) {
+        // the token-by-token kernel recomputes this head: one mark per 64-column block
+        const long idx = (long)bh * L * D + tid * 64;
+        if (p.out_f32)
+            static_cast<uint32_t*>(p.out)[idx] = kDeltaMarkF32;
+        else
+            static_cast<uint16_t*>(p.out)[idx] = kDeltaMarkBf16;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+CUresult encode(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* ptr, int d0, int d1, int d2,
+                int box0, int box1, CUtensorMapSwizzle sw) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return CUDA_ERROR_NOT_FOUND;
+    cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+    cuuint64_t strides[2] = {(cuuint64_t)d0 * esize, (cuuint64_t)d0 * d1 * esize};
+    cuuint32_t box[3] = {(cuuint32_t)box0, (cuuint32_t)box1, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace
+
+bool delta_tc_supported(const DeltaArgs& a) {
+    return a.dk == D && a.dv == D && a.L >= 1 && !(a.flags & GLA_FLAG_FORCE_SIMT) &&
+           (long)a.B * a.H <= 0x7fffffffL;
+}
+
+cudaError_t launch_delta_tc(const DeltaArgs& a, cudaStream_t s) {
+    DeltaTcParams p;
+    memset(&p, 0, sizeof(p));
+    const int BH = a.B * a.H;
+    const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    if (encode(&p.tm_q, bf, 2, a.q, D, a.L, BH, 64, C, sw) != CUDA_SUCCESS ||
+        encode(&p.tm_k, bf, 2, a.k, D, a.L, BH, 64, C, sw) != CUDA_SUCCESS ||
+        encode(&p.tm_v, bf, 2, a.v, D, a.L, BH, 64, C, sw) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    if (a.log_alpha && encode(&p.tm_la, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.log_alpha, D, a.L, BH, D, C,
+                              CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    p.beta = a.beta;
+    p.init_state = a.init_state;
+    p.out = a.out;
+    p.final_state = a.final_state;
+    p.err = a.err_word;
+    p.wait_ns = a.wait_ns;
+    p.L = a.L;
+    p.nchunks = (a.L + C - 1) / C;
+    p.gate = a.log_alpha != nullptr;
+    p.out_f32 = a.out_dtype == GLA_DTYPE_F32;
+    cudaError_t e = cudaFuncSetAttribute(gla_delta_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S_SMEM);
+    if (e != cudaSuccess) return e;
+    gla_delta_tc_kernel<<<BH, kThr, S_SMEM, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // heads with a chunk outside the factorisation's range: the token-by-token kernel
+    DeltaArgs r = a;
+    r.only_marked = 1;
+    return launch_delta(r, s);
+}
+
+}  // namespace gla

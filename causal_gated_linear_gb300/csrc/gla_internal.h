@@ -64,11 +64,26 @@ struct DeltaArgs {
     float* final_state;
     int B, H, L, dk, dv;
     int out_dtype;
+    unsigned flags;              // GLA_FLAG_FORCE_SIMT: the token-by-token kernel
+    unsigned* err_word;          // device address of the error word (chunk-form kernel)
+    unsigned long long wait_ns;  // limit of the chunk-form kernel's waits
+    int only_marked;             // token-by-token kernel: only the CTAs whose block carries the mark
 };
+
+// Written by the chunk-form delta rule into the first output element of every
+// 64-column block of a head it leaves to the token-by-token kernel (NaN
+// patterns that arithmetic does not produce).
+constexpr uint16_t kDeltaMarkBf16 = 0xFFC1u;
+constexpr uint32_t kDeltaMarkF32 = 0xFFC00001u;
 
 // Delta rule, token by token (one warp per 16 value columns of a head).
 bool delta_supported(int dk, int dv);
 cudaError_t launch_delta(const DeltaArgs& a, cudaStream_t s);
+
+// Delta rule in chunk form on the tensor cores (d_k = d_v = 128), then the
+// token-by-token kernel on the heads it marked.
+bool delta_tc_supported(const DeltaArgs& a);
+cudaError_t launch_delta_tc(const DeltaArgs& a, cudaStream_t s);
 
 struct BwdArgs {
     const void* q;

@@ -182,13 +182,33 @@ int gla_decode_step(const void* q, const void* k, const void* v, const float* lo
  *   init_state  fp32 [B][H][dk][dv], or NULL for S_{-1} = 0
  *   out         [B][H][L][dv], bf16 or fp32 (out_dtype = GLA_DTYPE_BF16 / _F32)
  *   final_state fp32 [B][H][dk][dv], or NULL; may alias init_state
- * The recurrence runs token by token in fp32.  Supported: dk in {32, 64, 128},
- * dv a multiple of 16.  Pointers 16-byte aligned; out must not alias an input.
+ * With d_k = d_v = 128 it runs in chunk form on the tensor cores (see
+ * gla_delta_fwd_ex); otherwise the recurrence runs token by token in fp32.
+ * Supported: dk in {32, 64, 128}, dv a multiple of 16.  Pointers 16-byte
+ * aligned; out must not alias an input.
  * Validation failures return before any launch.
  */
 int gla_delta_fwd(const void* q, const void* k, const void* v, const float* beta, const float* log_alpha,
                   const float* init_state, void* out, float* final_state, int B, int H, int L, int dk, int dv,
                   int out_dtype, void* stream);
+
+/*
+ * gla_delta_fwd_ex -- gla_delta_fwd with flags (0 or GLA_FLAG_FORCE_SIMT).
+ *
+ * With d_k = d_v = 128 the delta rule runs in chunk form on the tensor cores
+ * ("linear-attention" blog, Delta attention / Prefill: the writes of a chunk
+ * solve one unit lower-triangular system): per chunk of 64 tokens, with
+ * A = (k e^{b_t-b_C}) (k e^{b_C-b_i})^T, T = (I + Diag(beta) tril_strict(A))^{-1}
+ * and M = T Diag(beta), the writes are U = M V - (M Kr) S' and
+ * o = Qh S' + tril(Qh Kh^T) U, S_C = S' + Kh^T U (bf16 tensor-core products,
+ * fp32 accumulation and state; T in fp32).  Heads with a chunk over which a
+ * channel decays by more than e^-64 are recomputed by the token-by-token
+ * kernel, which also serves every other shape and GLA_FLAG_FORCE_SIMT.
+ * Same arguments, validation and error behaviour as gla_delta_fwd.
+ */
+int gla_delta_fwd_ex(const void* q, const void* k, const void* v, const float* beta, const float* log_alpha,
+                     const float* init_state, void* out, float* final_state, int B, int H, int L, int dk, int dv,
+                     int out_dtype, unsigned flags, void* stream);
 
 /*
  * gla_bwd -- gradients of the recurrence ("Gated Linear Attention", GLA

@@ -1,4 +1,6 @@
-"""GPU parity of the delta rule (gla_delta_fwd) against the fp64 oracle.
+"""GPU parity of the token-by-token delta-rule kernel (gla_delta_fwd_ex with
+GLA_FLAG_FORCE_SIMT, and every shape the chunk form does not take) against the
+fp64 oracle.
 
 The kernel runs the recurrence token by token in fp32 on the same rounded
 inputs the oracle receives, so fp32 output is held to relative L2 1e-5 on
@@ -24,7 +26,7 @@ def _w(B, H, L, dk, dv, gate=True, init=True, seed=0):
                             init_std=0.1 if init else 0.0, seed=synth.DELTA.seed + seed)
 
 
-def run_delta(w, x, out_f32=False, in_place=False):
+def run_delta(w, x, out_f32=False, in_place=False, force_simt=True):
     import torch
     q, k, v, b = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"]), to_dev(x["beta"])
     la, s0 = to_dev(x["log_alpha"]), to_dev(x["init_state"])
@@ -35,7 +37,8 @@ def run_delta(w, x, out_f32=False, in_place=False):
     else:
         fs = torch.full((w.B, w.H, w.dk, w.dv), float("nan"), dtype=torch.float32, device="cuda:0")
     gla.check(gla.gla_delta_fwd(q, k, v, b, out, w.B, w.H, w.L, w.dk, w.dv, log_alpha=la, init_state=s0,
-                                final_state=fs, out_dtype=gla.F32 if out_f32 else gla.BF16))
+                                final_state=fs, out_dtype=gla.F32 if out_f32 else gla.BF16,
+                                flags=gla.FLAG_FORCE_SIMT if force_simt else 0))
     torch.cuda.synchronize()
     gla.check(gla.gla_device_error())
     return out.float().cpu().numpy().astype(np.float64), fs.cpu().numpy().astype(np.float64)
