@@ -9,7 +9,7 @@ JSON object: the other prefill workloads ("configs": fp32 B1 H1 L256 d32,
 elu+1 normalised B4 H8 L2048 d64, gated B8 H16 L4096 d128); the decode step
 (256 sequences x H32, d128, fp32 state, 1024 consecutive steps on fresh
 tokens) as state HBM GB/s; the 8-token hand-off on that state; the
-long-context prefill with one gate per token; the delta rule and the backward
+long-context prefill with one gate per token; the delta rule (chunk form) and the backward
 pass; and the end-to-end step through gla_fwd_host with host buffers.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gla|reference]
@@ -81,6 +81,22 @@ def bwd_flops(w) -> float:
     return float(w.B * w.H * w.L * (15 if w.gate else 12) * w.dk * w.dv)
 
 
+def delta_bytes(w) -> float:
+    """Delta rule, algorithmic bytes: q, k, v (bf16), beta, log alpha read once; out (bf16) written
+    once; initial (if any) and final fp32 state."""
+    BH, L = w.B * w.H, w.L
+    per_tok = 2 * (2 * w.dk + w.dv) + 4 + (4 * w.dk if w.gate else 0) + 2 * w.dv
+    states = ((1 if w.init_std > 0 else 0) + 1) * w.dk * w.dv * 4
+    return float(BH * (L * per_tok + states))
+
+
+def delta_chunk_flops(w) -> float:
+    """Delta rule in chunk form, tensor-core flops per chunk and head: A = Kr Kh^T, P = Qh Kh^T,
+    M V, M Kr and P U (2 C^2 d each), W S', Qh S' and Kh^T U (2 C dk dv each)."""
+    per_chunk = 5 * 2 * C * C * w.dk + 3 * 2 * C * w.dk * w.dv
+    return float(w.B * w.H * math.ceil(w.L / C) * per_chunk)
+
+
 def bwd_bytes(w, dla=True) -> float:
     """Backward, algorithmic bytes: q, k, v, dout (bf16) and log alpha read once; dq, dk, dv (and
     dlog_alpha) written once in fp32."""
@@ -128,6 +144,7 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {
+    "gla_delta_tc_kernel": ("gla_delta_tc.cu", "gla_ptx.cuh"),
     "gla_bwd_dkdv_kernel": ("gla_bwd_tc.cu", "gla_ptx.cuh"),
     "gla_prefill_tc_kernel": ("gla_tc.cu", "gla_ptx.cuh"),
     "gla_decode_kernel": ("gla_decode.cu",),
@@ -624,25 +641,31 @@ def bench_delta(args, device, rank):
     fs = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
 
-    def call():
+    def call(flags=0):
         r = gla.gla_delta_fwd(q, k, v, b, out, w.B, w.H, w.L, w.dk, w.dv, log_alpha=la, final_state=fs,
-                              stream=stream)
+                              flags=flags, stream=stream)
         if r != 0:
             raise RuntimeError(gla.gla_status_string(r))
 
-    for _ in range(2):
-        call()
-    torch.cuda.synchronize(device)
-    evs = []
-    for _ in range(args.delta_calls):
-        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        call()
-        e.record(stream)
-        evs.append((a, e))
-    torch.cuda.synchronize(device)
-    gla.check(gla.gla_device_error(stream))
-    return dict(w=w, ms=statistics.mean(a.elapsed_time(e) for a, e in evs), calls=args.delta_calls)
+    def timed(flags, n):
+        for _ in range(2):
+            call(flags)
+        torch.cuda.synchronize(device)
+        evs = []
+        for _ in range(n):
+            a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call(flags)
+            e.record(stream)
+            evs.append((a, e))
+        torch.cuda.synchronize(device)
+        gla.check(gla.gla_device_error(stream))
+        return statistics.mean(a.elapsed_time(e) for a, e in evs)
+
+    res = dict(w=w, ms=timed(0, args.delta_calls), calls=args.delta_calls)
+    # the token-by-token fp32 kernel on the same workload, for comparison
+    res["token_ms"] = timed(gla.FLAG_FORCE_SIMT, 2)
+    return res
 
 
 def bench_bwd(args, device, rank):
@@ -771,16 +794,27 @@ def run_gla(args):
                          "kernel": "gla_prefill_tc_kernel (per-token gate)", "alg_bytes_per_launch": sbytes}}
     if dlt is not None:
         dw = dlt["w"]
-        dfl = delta_flops(dw)
-        dtf = dfl / (dlt["ms"] / 1e3) / 1e12
-        apk = fp32_alu_peak_tflops(peaks)
+        sec = dlt["ms"] / 1e3
+        db = delta_bytes(dw)
+        dgbs = db / sec / 1e9
+        cfl = delta_chunk_flops(dw)
         line["delta"] = {
             "workload": dw.name, "ms_per_launch": dlt["ms"], "calls": dlt["calls"],
-            "tokens_per_s": dw.B * dw.L / (dlt["ms"] / 1e3),
-            "roofline": {"bound": "alu", "achieved": dtf, "peak": apk, "unit": "TFLOP/s", "frac": dtf / apk,
-                         "traffic": recorded_traffic("gla_delta_kernel"), "kernel": "gla_delta_kernel",
-                         "alg_flops_per_launch": dfl,
-                         "peak_source": "FP32 FMA: SMs x 128 lanes x 2 flops x max SM clock"}}
+            "tokens_per_s": dw.B * dw.L / sec, "tflops": cfl / sec / 1e12,
+            "tensor_frac": cfl / sec / 1e12 / peaks["bf16_tflops"],
+            "path": "chunk form on the tensor cores (per-chunk triangular solve)",
+            "roofline": {"bound": "hbm", "achieved": dgbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": dgbs / peaks["hbm_gbs"], "traffic": recorded_traffic("gla_delta_tc_kernel"),
+                         "kernel": "gla_delta_tc_kernel", "alg_bytes_per_launch": db, "alg_flops_per_launch": cfl}}
+        if "token_ms" in dlt:
+            dfl = delta_flops(dw)
+            apk = fp32_alu_peak_tflops(peaks)
+            dtf = dfl / (dlt["token_ms"] / 1e3) / 1e12
+            line["delta"]["token_by_token"] = {
+                "ms_per_launch": dlt["token_ms"], "kernel": "gla_delta_kernel (GLA_FLAG_FORCE_SIMT)",
+                "roofline": {"bound": "alu", "achieved": dtf, "peak": apk, "unit": "TFLOP/s", "frac": dtf / apk,
+                             "alg_flops_per_launch": dfl,
+                             "peak_source": "FP32 FMA: SMs x 128 lanes x 2 flops x max SM clock"}}
     if bwd is not None:
         bw = bwd["w"]
         bb = bwd_bytes(bw)
