@@ -634,6 +634,8 @@ def bench_delta(args, device, rank):
 
     import causal_gated_linear_gb300 as gla
     w = synth.with_shape(synth.DELTA, seed=synth.DELTA.seed + 1000 * rank)
+    if args.aux_L:  # reduced sequence length (profiling a small case); the line names it
+        w = synth.with_shape(w, L=args.aux_L, name=f"{w.name}_L{args.aux_L}")
     x = synth.make_delta(w)
     q, k, v, b = (to_dev(x[n], device) for n in ("q", "k", "v", "beta"))
     la = to_dev(x["log_alpha"], device)
@@ -676,6 +678,8 @@ def bench_bwd(args, device, rank):
 
     import causal_gated_linear_gb300 as gla
     w = synth.with_shape(synth.BWD, seed=synth.BWD.seed + 1000 * rank)
+    if args.aux_L:  # reduced sequence length (profiling a small case); the line names it
+        w = synth.with_shape(w, L=args.aux_L, name=f"{w.name}_L{args.aux_L}")
     x = synth.make_bwd(w)
     q, k, v, do = (to_dev(x[n], device) for n in ("q", "k", "v", "dout"))
     la = to_dev(x["log_alpha"], device)
@@ -901,6 +905,8 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--L", type=int, default=0,
                     help="override the prefill sequence length (small cases for ncu captures)")
+    ap.add_argument("--aux-L", type=int, default=0,
+                    help="override the delta-rule and backward sequence length (small cases for ncu captures)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # timing rule: at least 3 warm-up steps
     if args.impl == "reference":
