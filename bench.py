@@ -145,7 +145,7 @@ def load_peaks():
 
 KERNEL_SOURCES = {
     "gla_delta_tc_kernel": ("gla_delta_tc.cu", "gla_ptx.cuh"),
-    "gla_bwd_dkdv_kernel": ("gla_bwd_tc.cu", "gla_ptx.cuh"),
+    "gla_bwd_tc": ("gla_bwd_tc.cu", "gla_ptx.cuh"),  # the dq and dk/dv kernels together
     "gla_prefill_tc_kernel": ("gla_tc.cu", "gla_ptx.cuh"),
     "gla_decode_kernel": ("gla_decode.cu",),
     "gla_prefill_short_kernel": ("gla_short.cu",),
@@ -832,7 +832,7 @@ def run_gla(args):
             "path": "chunk form on the tensor cores (dq pass + dk/dv pass)",
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"],
-                         "traffic": recorded_traffic("gla_bwd_dkdv_kernel"),
+                         "traffic": recorded_traffic("gla_bwd_tc"),
                          "kernel": "gla_bwd_dq_kernel + gla_bwd_dkdv_kernel", "alg_bytes_per_launch": bb,
                          "alg_flops_per_launch": bfl}}
         if "recurrent_ms" in bwd:
