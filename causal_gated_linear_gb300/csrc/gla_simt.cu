@@ -10,7 +10,10 @@
 // Every exponent is <= 0 (log alpha <= 0), so no intermediate can overflow
 // whatever the gate values; the intra-block decay is evaluated per (t, i, d)
 // rather than factored, which costs exps but keeps this kernel a robust
-// reference-grade GPU path for any shape.
+// reference-grade GPU path for any shape.  The factors of the inter-block
+// term and of the state update (q_t e^{b_t}, k_i e^{b_last - b_i}) are formed
+// once per block; the per-pair weights use the fast hardware exponential
+// (arguments all <= 0), well inside the fp32 parity bar.
 //
 // Grid: (value-column tiles of kDVT, B*H).  Block: 256 threads.  Each CTA
 // keeps its d_k x kDVT slice of S (plus the normaliser column) in shared
@@ -64,6 +67,9 @@ __global__ void __launch_bounds__(kThreads) gla_prefill_simt_kernel(PrefillArgs 
     float* S = vv + TB * NC;         // [dk][NC]
     float* A = S + dk * NC;          // [TB][TB]
     float* os = A + TB * TB;         // [TB][NC]
+    float* qe = os + TB * NC;        // [TB][dk] q_t e^{b_t}
+    float* kh = qe + TB * dk;        // [TB][dk] k_i e^{b_last - b_i}
+    float* gl = kh + TB * dk;        // [dk] e^{b_last}
 
     const int tid = threadIdx.x;
     const int j0 = blockIdx.x * kDVT;
@@ -128,16 +134,22 @@ __global__ void __launch_bounds__(kThreads) gla_prefill_simt_kernel(PrefillArgs 
                 run += bb[t * dk + d];
                 bb[t * dk + d] = run;
             }
+            gl[d] = expf(run);
         }
         __syncthreads();
-        // intra-block scores with the exact decay weight
+        // factors of the inter-block term and of the state update (exponents <= 0)
+        for (int idx = tid; idx < TB * dk; idx += kThreads) {
+            const int d = idx % dk;
+            qe[idx] = qf[idx] * expf(bb[idx]);
+            kh[idx] = kf[idx] * expf(bb[(TB - 1) * dk + d] - bb[idx]);
+        }
+        // intra-block scores with the exact decay weight of every pair
         for (int idx = tid; idx < TB * TB; idx += kThreads) {
             int t = idx / TB, i = idx % TB;
             float acc = 0.f;
             if (i <= t) {
                 for (int d = 0; d < dk; d++)
-                    acc = fmaf(qf[t * dk + d] * kf[i * dk + d], expf(bb[t * dk + d] - bb[i * dk + d]),
-                               acc);
+                    acc = fmaf(qf[t * dk + d] * kf[i * dk + d], __expf(bb[t * dk + d] - bb[i * dk + d]), acc);
             }
             A[idx] = acc;
         }
@@ -146,7 +158,7 @@ __global__ void __launch_bounds__(kThreads) gla_prefill_simt_kernel(PrefillArgs 
         for (int idx = tid; idx < TB * NC; idx += kThreads) {
             int t = idx / NC, jj = idx % NC;
             float acc = 0.f;
-            for (int d = 0; d < dk; d++) acc = fmaf(qf[t * dk + d] * expf(bb[t * dk + d]), S[d * NC + jj], acc);
+            for (int d = 0; d < dk; d++) acc = fmaf(qe[t * dk + d], S[d * NC + jj], acc);
             for (int i = 0; i <= t; i++) acc = fmaf(A[t * TB + i], vv[i * NC + jj], acc);
             os[idx] = acc;
         }
@@ -162,9 +174,8 @@ __global__ void __launch_bounds__(kThreads) gla_prefill_simt_kernel(PrefillArgs 
         // state update (every column incl. the normaliser)
         for (int idx = tid; idx < dk * NC; idx += kThreads) {
             int d = idx / NC, jj = idx % NC;
-            const float bl = bb[(TB - 1) * dk + d];
-            float acc = expf(bl) * S[idx];
-            for (int i = 0; i < TB; i++) acc = fmaf(kf[i * dk + d] * expf(bl - bb[i * dk + d]), vv[i * NC + jj], acc);
+            float acc = gl[d] * S[idx];
+            for (int i = 0; i < TB; i++) acc = fmaf(kh[i * dk + d], vv[i * NC + jj], acc);
             S[idx] = acc;
         }
         __syncthreads();
@@ -182,7 +193,7 @@ __global__ void __launch_bounds__(kThreads) gla_prefill_simt_kernel(PrefillArgs 
 
 size_t simt_smem_bytes(int dk, int TB) {
     const int NC = kDVT + 1;
-    return sizeof(float) * (size_t)(3 * TB * dk + TB * NC + dk * NC + TB * TB + TB * NC);
+    return sizeof(float) * (size_t)(5 * TB * dk + TB * NC + dk * NC + TB * TB + TB * NC + dk);
 }
 
 template <typename TI, typename TO>
