@@ -6,12 +6,13 @@
 // ("linear-attention" blog, Gated linear attention: a write at i reaches t
 // weighted by the product of alpha over (i, t]) and writing b_t for the
 // inclusive cumsum of log alpha from the chunk start, b_C for its last value:
-//   Qh_t = q_t * e^{b_t - b_C}        (>= 1 factor)
-//   Kh_i = k_i * e^{b_C - b_i}        (<= 1 factor)
-//   S'   = Diag(e^{b_C}) S_prev                      (decay first)
-//   o_t  = Qh_t^T S' + sum_{i<=t} (Qh_t . Kh_i) v_i    (inter + intra)
-//   S    = S' + Kh^T V
+//   Qh_t = q_t * e^{b_t}              (<= 1 factor)
+//   Kh_i = k_i * e^{-b_i}             (>= 1 factor, at most e^{-b_C})
+//   o_t  = Qh_t^T S_prev + sum_{i<=t} (Qh_t . Kh_i) v_i    (inter + intra)
+//   S    = Diag(e^{b_C}) (S_prev + Kh^T V)
 // which is exactly the recurrence, since (Qh_t . Kh_i) carries e^{b_t - b_i}.
+// The output product reads the state from before the chunk, so it can start as
+// soon as the chunk's factors are written; the state update is off its path.
 //
 // One CTA owns one (batch*head, DVT-column slice of d_v) for the whole
 // sequence (DVT = 64 or 128, chosen by the host so that enough CTAs exist to
@@ -20,12 +21,12 @@
 // product has M = DVT:
 //   MMA_A   A[t][i] = Qh Kh^T          M=128 (rows 64..127 unused), N=64, K=dk
 //   MMA_dS  dS^T    = V^T Kh           M=DVT, N=dk, K=64  (V, Kh MN-major; own buffer)
-//   MMA_Oi  O^T     = S'^T_bf16 Qh^T   M=DVT, N=64, K=dk  (A operand from TMEM)
+//   MMA_Oi  O^T     = S^T_bf16 Qh^T    M=DVT, N=64, K=dk  (A operand from TMEM)
 //   MMA_Oa  O^T    += V^T P^T          M=DVT, N=64, K=64  (P = tril(A) in bf16)
-// The state warps apply S' = Diag(e^{b_C}) S, write the bf16 copy of S' into
-// TMEM and S = S' + dS in fp32 (in TMEM for the 128-column tile, in their
-// registers for the 64-column tile); no state ever leaves the chip between
-// chunks.  With M = 64 the accumulator rows live in TMEM lanes
+// The state warps form S = Diag(e^{b_C}) (S + dS) in fp32 (in TMEM for the
+// 128-column tile, in their registers for the 64-column tile) and write its
+// bf16 copy into TMEM for the next chunk's MMA_Oi; no state ever leaves the
+// chip between chunks.  With M = 64 the accumulator rows live in TMEM lanes
 // 16q + r -> lane 32q + r (r < 16) of each 32-lane quarter q.
 //
 // Warp roles (24 warps): 0-7 gate (cumsum with a cross-warp segment
@@ -36,11 +37,11 @@
 // (gla_ptx.cuh).
 //
 // Strong gates: alpha has no lower bound, and once a channel decays by more
-// than e^-64 over a chunk the factor e^{b_t - b_C} could overflow.  The pass
-// every call runs only detects such a chunk; the CTA then skips its final-state
-// write and runs its slice a second time (exact_pass) in which strong channels
-// take q e^{b_t} against the unscaled state and their intra-chunk scores are
-// added on the P warps with exponents <= 0.
+// than e^-64 over a chunk the factor e^{-b_i} could overflow.  The pass every
+// call runs only detects such a chunk; the CTA then skips its final-state write
+// and runs its slice a second time (exact_pass) in which strong channels take
+// k e^{b_C - b_i} (already decayed to the chunk end, <= 1) and their
+// intra-chunk scores are added on the P warps with exponents <= 0.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -79,11 +80,11 @@ constexpr int W_STATE0 = 8, W_OUT0 = 16, W_P0 = 20, W_TMA = 22, W_MMA = 23;
 constexpr int kGateThreads = 256;
 
 // A key channel whose gate decays by more than e^-64 over one chunk is "strong"
-// for that chunk: the factorisation relative to the chunk end (q e^{b_t - b_C},
-// k e^{b_C - b_i}) would overflow, so such channels take factors relative to
-// the chunk start on the q side and their intra-chunk scores are added on the
-// P warps with exponents <= 0 (see gate_factors_strong, strong_scores).  The
-// test is made on e^{b_C} exactly as the gate writes it, so every role agrees.
+// for that chunk: the factor k e^{-b_i} could overflow, so such channels take
+// k e^{b_C - b_i} (the state update then adds their dS after the decay) and
+// their intra-chunk scores are added on the P warps with exponents <= 0 (see
+// gate_factors_strong, strong_scores).  The test is made on e^{b_C} exactly as
+// the gate writes it, so every role agrees.
 constexpr float kStrongGamma = 1.6038109e-28f;  // e^-64
 constexpr float kStrongLog = -64.f;
 constexpr int kRing = 8;  // chunks whose strong-channel masks are kept (ring slots)
@@ -91,14 +92,16 @@ constexpr int kRing = 8;  // chunks whose strong-channel masks are kept (ring sl
 // tensor-memory column map (512 columns allocated)
 constexpr uint32_t TM_S = 0;     // S^T fp32, dk columns (128-column tile)
 constexpr uint32_t TM_DS = 128;  // dS^T fp32, dk columns
-constexpr uint32_t TM_SB = 256;  // bf16 copy of S'^T, dk/2 columns (128-column tile)
+constexpr uint32_t TM_SB = 256;  // bf16 copy of S^T for the next O_i, dk/2 columns (128-column tile)
 // With the 64-column tile (M = 64) S^T is held in the state warps'
-// registers instead, and the map is: dS^T buffers for even and odd chunks at
-// 0..127 and 128..255, O^T 2 x 64 at 256..383, A at 448..511.  The bf16 copy
-// of S'^T for O_i(c) is written into chunk c's own dS buffer once the state
-// warps have read dS(c) from it (each half of the key channels into its own
-// half of the buffer), and the buffer is released when O_i(c) completes: the
-// state update never waits on a product, only dS(c+2) waits on O_i(c).
+// registers instead, and the map is: two dS^T buffers at 0..127 and
+// 128..255 (dS(c) in buffer (c + 1) & 1), O^T 2 x 64 at 256..383, A at
+// 448..511.  The bf16 copy of the state after chunk c, read by O_i(c + 1), is
+// written into dS(c)'s buffer once the state warps have read dS(c) from it
+// (each half of the key channels into its own half of the buffer; the initial
+// state's copy goes to buffer 0 for O_i(0)), and the buffer is released when
+// O_i(c + 1) completes: the state update never waits on a product, only
+// dS(c + 2) waits on O_i(c + 1).
 constexpr uint32_t TM_O = 320;   // 2 x O^T fp32, 64 columns each
 constexpr uint32_t TM_A = 448;   // A fp32, 64 columns
 constexpr uint32_t TM_COLS = 512;
@@ -239,12 +242,12 @@ __device__ __forceinline__ void gate_factors(uint8_t* qt, uint8_t* kt, const flo
                 k23 = make_float2(elu1(k23.x), elu1(k23.y));
             }
             float2 fq01 = make_float2(1.f, 1.f), fq23 = fq01, fk01 = fq01, fk23 = fq01;
-            if (GATE && SCALAR) {  // run = (b_t - b_C) log2 e >= 0, the same for every channel
+            if (GATE && SCALAR) {  // run = b_t log2 e <= 0, the same for every channel
                 run_s = fmaf(lx[u].x, kLog2e, run_s);
                 const float fq = ex2_approx(run_s), fk = ex2_approx(-run_s);
                 fq01 = fq23 = make_float2(fq, fq);
                 fk01 = fk23 = make_float2(fk, fk);
-            } else if (GATE) {  // run = (b_t - b_C) log2 e >= 0
+            } else if (GATE) {  // run = b_t log2 e <= 0
                 run01 = fma2(make_float2(lx[u].x, lx[u].y), l2e, run01);
                 run23 = fma2(make_float2(lx[u].z, lx[u].w), l2e, run23);
                 fq01 = make_float2(ex2_approx(run01.x), ex2_approx(run01.y));
@@ -295,11 +298,11 @@ template <int DK, int TPS, bool ELU, bool SCALAR>
 __device__ __noinline__ void gate_factors_strong(uint8_t* qt, uint8_t* kt, const float* la, int seg, int col,
                                                  int nval, float4 pre, float4 tot, float4 suf, unsigned strong4) {
     constexpr float kLog2e = 1.4426950408889634f;
-    float rq[4] = {(strong4 & 1u) ? pre.x : pre.x - tot.x, (strong4 & 2u) ? pre.y : pre.y - tot.y,
-                   (strong4 & 4u) ? pre.z : pre.z - tot.z, (strong4 & 8u) ? pre.w : pre.w - tot.w};
-    float rk[4] = {suf.x, suf.y, suf.z, suf.w};
+    float rq[4] = {pre.x, pre.y, pre.z, pre.w};
+    float rk[4] = {(strong4 & 1u) ? suf.x : suf.x - tot.x, (strong4 & 2u) ? suf.y : suf.y - tot.y,
+                   (strong4 & 4u) ? suf.z : suf.z - tot.z, (strong4 & 8u) ? suf.w : suf.w - tot.w};
 #pragma unroll 1
-    for (int i = 0; i < TPS; i++) {  // q: forward running sum b_t (- b_C on the other channels)
+    for (int i = 0; i < TPS; i++) {  // q: forward running sum b_t
         const int t = seg * TPS + i;
         const float4 x = load_la4<DK, SCALAR>(la, t);
         rq[0] += x.x;
@@ -322,7 +325,7 @@ __device__ __noinline__ void gate_factors_strong(uint8_t* qt, uint8_t* kt, const
         *reinterpret_cast<uint2*>(qt + o) = w;
     }
 #pragma unroll 1
-    for (int i = TPS - 1; i >= 0; i--) {  // k: suffix sum b_C - b_t, from the chunk end
+    for (int i = TPS - 1; i >= 0; i--) {  // k: suffix sum b_C - b_t (- b_C off the strong channels)
         const int t = seg * TPS + i;
         const uint32_t o = sw128_offset(t, col);
         const uint2 kr = *reinterpret_cast<const uint2*>(kt + o);
@@ -625,10 +628,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     if (fminf(fminf(tot[0], tot[1]), fminf(tot[2], tot[3])) < kStrongLog) *strong_flag = 1;
                 }
 #pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    pre[e] = off[e];
-                    off[e] -= tot[e];  // running value is now b_t - b_C
-                }
+                for (int e = 0; e < 4; e++) pre[e] = off[e];  // the running value is b_t
             } else {
                 if (!bar_red_and(1, kGateThreads, ok)) break;
             }
@@ -698,22 +698,41 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     for (int i = 0; i < 16; i++)
                         S[g * 16 + i] = s0 ? s0[(long)(cbase + g * 32 + hi * 16 + i) * dv] : 0.f;
             }
+            // bf16 copy of the state for O_i: group g (8 key channels c0 + [0, 8) of this
+            // half-warp) goes to column cbase + (c0 - cbase) / 2 of the buffer
+            auto write_copy = [&](uint32_t tbuf) {
+#pragma unroll
+                for (int g = 0; g < NG * 2; g++) {
+                    const int c0 = cbase + (g >> 1) * 32 + (g & 1) * 8;
+                    const float* sv = S + g * 8;
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int i = 0; i < 4; i++) pk[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
+                    tmem_st16x2_x4<8>(tbuf + cbase + (c0 - cbase) / 2, pk);
+                }
+            };
+            // O_i(0) reads the initial state's copy from buffer 0 (dS(c) lands in buffer (c + 1) & 1)
+            write_copy(tmem + lane_field);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_S_READY));
             bool ok = true;
             for (int c = 0; c < N; c++) {
                 const int s = c % NS;
-                ok = mbar_wait_warp(bar(B_DS_FULL + (c & 1)), (c >> 1) & 1, abort_flag, p.err, p.wait_ns);
+                ok = mbar_wait_warp(bar(B_DS_FULL + ((c + 1) & 1)), (c >> 1) & 1, abort_flag, p.err, p.wait_ns);
                 if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(16, c);
                 if (ok && GATE) ok = mbar_wait_warp(bar(B_QK_GATED + s), (c / NS) & 1, abort_flag, p.err, p.wait_ns);
                 if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(17, c);
                 if (!ok) break;
                 tc_fence_after();
                 if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(4, c);
-                // dS(c) and, once read, this chunk's bf16 copy of S' for O_i: this half's key
-                // channels [cbase, cbase + COLS) occupy columns [cbase, cbase + COLS) of the buffer,
-                // and their copy goes to [cbase, cbase + COLS / 2)
-                const uint32_t tB = tmem + lane_field + (uint32_t)(c & 1) * 128u;
-                // a chunk with a strong channel: that channel's copy feeding O_i is S itself
-                // (its q carries e^{b_t}), every other channel's is e^{b_C} S as usual
+                // dS(c) and, once read, the bf16 copy of the updated state for O_i(c + 1): this
+                // half's key channels [cbase, cbase + COLS) occupy columns [cbase, cbase + COLS)
+                // of the buffer, and their copy goes to [cbase, cbase + COLS / 2)
+                const uint32_t tB = tmem + lane_field + (uint32_t)((c + 1) & 1) * 128u;
+                // S <- e^{b_C} (S + dS): dS carries k e^{-b_i}.  A chunk with a strong channel:
+                // that channel's dS carries k e^{b_C - b_i} (already decayed), so S <- e^{b_C} S + dS
                 const uint32_t* slot = ring + (c % kRing) * 5;
                 const bool sgc = SAFE && GATE && ((slot[1] | slot[2] | slot[3] | slot[4]) != 0u);
                 auto update = [&](auto strong_tag) {
@@ -740,21 +759,21 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                                 float4 gv = make_float4(1.f, 1.f, 1.f, 1.f);
                                 if (GATE) gv = *reinterpret_cast<const float4*>(gm + i);
                                 float* sv = S + g * 8 + i;
-                                const float a0 = sv[0] * gv.x, a1 = sv[1] * gv.y, a2 = sv[2] * gv.z,
-                                            a3 = sv[3] * gv.w;
+                                const float d0 = __uint_as_float(d[u][i]), d1 = __uint_as_float(d[u][i + 1]),
+                                            d2 = __uint_as_float(d[u][i + 2]), d3 = __uint_as_float(d[u][i + 3]);
                                 if (ST) {
-                                    pk[i / 2] = pack_bf16x2(gv.x < kStrongGamma ? sv[0] : a0,
-                                                            gv.y < kStrongGamma ? sv[1] : a1);
-                                    pk[i / 2 + 1] = pack_bf16x2(gv.z < kStrongGamma ? sv[2] : a2,
-                                                                gv.w < kStrongGamma ? sv[3] : a3);
+                                    sv[0] = gv.x < kStrongGamma ? fmaf(sv[0], gv.x, d0) : (sv[0] + d0) * gv.x;
+                                    sv[1] = gv.y < kStrongGamma ? fmaf(sv[1], gv.y, d1) : (sv[1] + d1) * gv.y;
+                                    sv[2] = gv.z < kStrongGamma ? fmaf(sv[2], gv.z, d2) : (sv[2] + d2) * gv.z;
+                                    sv[3] = gv.w < kStrongGamma ? fmaf(sv[3], gv.w, d3) : (sv[3] + d3) * gv.w;
                                 } else {
-                                    pk[i / 2] = pack_bf16x2(a0, a1);
-                                    pk[i / 2 + 1] = pack_bf16x2(a2, a3);
+                                    sv[0] = (sv[0] + d0) * gv.x;
+                                    sv[1] = (sv[1] + d1) * gv.y;
+                                    sv[2] = (sv[2] + d2) * gv.z;
+                                    sv[3] = (sv[3] + d3) * gv.w;
                                 }
-                                sv[0] = a0 + __uint_as_float(d[u][i]);
-                                sv[1] = a1 + __uint_as_float(d[u][i + 1]);
-                                sv[2] = a2 + __uint_as_float(d[u][i + 2]);
-                                sv[3] = a3 + __uint_as_float(d[u][i + 3]);
+                                pk[i / 2] = pack_bf16x2(sv[0], sv[1]);
+                                pk[i / 2 + 1] = pack_bf16x2(sv[2], sv[3]);
                             }
                             tmem_st16x2_x4<8>(tB + cbase + (c0 - cbase) / 2, pk);
                         }
@@ -767,7 +786,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_S_READY + (c & 1)));
+                if (lane == 0) mbar_arrive(bar(B_S_READY + ((c + 1) & 1)));
                 if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(5, c);
             }
             // a marked slice leaves its final state to the exact pass (init_state may alias it)
@@ -800,24 +819,35 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                         r[i] = __float_as_uint(x);
                     }
                     tmem_st16(tS + cbase + g * 16, r);
+                    // the initial state's bf16 copy feeds O_i(0)
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int i = 0; i < 16; i += 2)
+                        pk[i / 2] = pack_bf16x2(__uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                    tmem_st8(tmem + lane_field + TM_SB + (cbase + g * 16) / 2, pk);
                 }
                 tmem_wait_st();
-                // first phase of the dS buffer's release
+                // first phase of the dS buffer's release; the copy for O_i(0) is ready
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_DS_EMPTY));
+                if (lane == 0) {
+                    mbar_arrive(bar(B_DS_EMPTY));
+                    mbar_arrive(bar(B_S_READY));
+                }
             }
             bool ok = true;
             for (int c = 0; c < N; c++) {
                 const int s = c % NS;
                 ok = mbar_wait_warp(bar(B_DS_FULL), c & 1, abort_flag, p.err, p.wait_ns);
                 if (ok && GATE) ok = mbar_wait_warp(bar(B_QK_GATED + s), (c / NS) & 1, abort_flag, p.err, p.wait_ns);
-                // the single bf16 copy of S' is free once O_i(c-1) has completed
-                if (ok) ok = mbar_wait_warp(bar(B_SB_EMPTY), (c & 1) ^ 1, abort_flag, p.err, p.wait_ns);
+                // the single bf16 copy (of the state before this chunk) is free once O_i(c) has
+                // completed; it then takes the updated state for O_i(c + 1)
+                if (ok) ok = mbar_wait_warp(bar(B_SB_EMPTY), c & 1, abort_flag, p.err, p.wait_ns);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t tSB = tmem + lane_field + TM_SB;
-                // a chunk with a strong channel: that channel's copy feeding O_i is S itself
+                // S <- e^{b_C} (S + dS) (dS carries k e^{-b_i}); a strong channel's dS carries
+                // k e^{b_C - b_i}: S <- e^{b_C} S + dS
                 const uint32_t* slot = ring + (c % kRing) * 5;
                 const bool sgc = SAFE && GATE && ((slot[1] | slot[2] | slot[3] | slot[4]) != 0u);
 #pragma unroll 1
@@ -832,23 +862,26 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
 #pragma unroll
                         for (int i = 0; i < 16; i += 2) {
                             const float s0v = __uint_as_float(rs[i]), s1v = __uint_as_float(rs[i + 1]);
+                            const float d0 = __uint_as_float(rd[i]), d1 = __uint_as_float(rd[i + 1]);
                             const float g0 = gamma[s * DK + c0 + i], g1 = gamma[s * DK + c0 + i + 1];
-                            const float a0 = s0v * g0, a1 = s1v * g1;
-                            pk[i / 2] = pack_bf16x2(g0 < kStrongGamma ? s0v : a0, g1 < kStrongGamma ? s1v : a1);
-                            rs[i] = __float_as_uint(a0 + __uint_as_float(rd[i]));
-                            rs[i + 1] = __float_as_uint(a1 + __uint_as_float(rd[i + 1]));
+                            const float a0 = g0 < kStrongGamma ? fmaf(s0v, g0, d0) : (s0v + d0) * g0;
+                            const float a1 = g1 < kStrongGamma ? fmaf(s1v, g1, d1) : (s1v + d1) * g1;
+                            pk[i / 2] = pack_bf16x2(a0, a1);
+                            rs[i] = __float_as_uint(a0);
+                            rs[i + 1] = __float_as_uint(a1);
                         }
                     } else {
 #pragma unroll
                         for (int i = 0; i < 16; i += 2) {
-                            float s0v = __uint_as_float(rs[i]), s1v = __uint_as_float(rs[i + 1]);
+                            float a0 = __uint_as_float(rs[i]) + __uint_as_float(rd[i]);
+                            float a1 = __uint_as_float(rs[i + 1]) + __uint_as_float(rd[i + 1]);
                             if (GATE) {
-                                s0v *= gamma[s * DK + c0 + i];
-                                s1v *= gamma[s * DK + c0 + i + 1];
+                                a0 *= gamma[s * DK + c0 + i];
+                                a1 *= gamma[s * DK + c0 + i + 1];
                             }
-                            pk[i / 2] = pack_bf16x2(s0v, s1v);
-                            rs[i] = __float_as_uint(s0v + __uint_as_float(rd[i]));
-                            rs[i + 1] = __float_as_uint(s1v + __uint_as_float(rd[i + 1]));
+                            pk[i / 2] = pack_bf16x2(a0, a1);
+                            rs[i] = __float_as_uint(a0);
+                            rs[i + 1] = __float_as_uint(a1);
                         }
                     }
                     tmem_st16(tS + c0, rs);
@@ -859,7 +892,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(bar(B_DS_EMPTY));
-                    mbar_arrive(bar(B_S_READY + (c & 1)));
+                    mbar_arrive(bar(B_S_READY + ((c + 1) & 1)));
                 }
             }
             if (ok && !(GATE && !SAFE && *strong_flag)) {
@@ -1138,12 +1171,36 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
             int nd = 0, na = 0, ni = 0, no = 0, nq = 0;
             bool d_e = false, d_g = false, d_v = false;  // dS(nd): dS buffer free, gated, V landed
             bool a_e = false, a_g = false;               // A(na): A buffer free, gated
-            bool i_s = false, i_o = false;               // O_i(ni): state written, O buffer free
+            bool i_s = false, i_o = false, i_g = false;  // O_i(ni): previous state's copy, O buffer free, gated
             unsigned long long t_last = globaltimer();
             uint32_t idle = 0;
             while (no < N) {
                 bool prog = false;
-                if (no < ni && mbar_test(bar(B_P_FULL + no % Ly::NP), (no / Ly::NP) & 1)) {
+                // dS(c) = V_c^T Kh_c first: the state chain waits on it.  64-column tile: dS(c)
+                // lands in buffer (c + 1) & 1, whose previous content (the state copy read by
+                // O_i(c - 1), or the initial state's for c = 1) is released by that O_i
+                if (nd < N) {
+                    if (!d_e)
+                        d_e = DVT == 64 ? mbar_test(bar(B_DS_EMPTY + ((nd + 1) & 1)), (((nd + 1) >> 1) & 1) ^ 1)
+                                        : mbar_test(bar(B_DS_EMPTY), nd & 1);
+                    if (d_e && !d_g) d_g = mbar_test(bar(B_QK_GATED + nd % NS), (nd / NS) & 1);
+                    if (d_g && !d_v) d_v = mbar_test(bar(B_V_FULL + nd % NV), (nd / NV) & 1);
+                    if (d_v) {
+                        tc_fence_after();
+                        const uint64_t vd = kMN | (vs_of(nd) >> 4), kd = kMN | ((qs_of(nd) + Ly::QB) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < C / 16; kk++)
+                            mma_ss(tmem + (DVT == 64 ? (uint32_t)((nd + 1) & 1) * 128u : TM_DS),
+                                   vd + kk * (2048 >> 4), kd + kk * (2048 >> 4), idS, kk > 0);
+                        mma_commit(bar(B_DS_FULL + (DVT == 64 ? ((nd + 1) & 1) : 0)));
+                        nd++;
+                        d_e = d_g = d_v = false;
+                        prog = true;
+                    }
+                }
+                // O_a(c) reads V(c): it goes only after dS(c), which this thread issued once
+                // V(c) had landed (O_i(c) no longer implies that)
+                if (no < ni && no < nd && mbar_test(bar(B_P_FULL + no % Ly::NP), (no / Ly::NP) & 1)) {
                     tc_fence_after();
                     const uint64_t vd = kMN | (vs_of(no) >> 4);
                     const uint64_t pd = kK | ((sbase + Ly::off_p + (no % Ly::NP) * Ly::PB) >> 4);
@@ -1156,14 +1213,17 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     no++;
                     prog = true;
                 }
-                if (ni < nd) {
+                if (ni < N) {
+                    // the copy of the state before chunk ni (written after chunk ni - 1)
                     if (!i_s) i_s = mbar_test(bar(B_S_READY + (ni & 1)), (ni >> 1) & 1);
                     if (i_s && !i_o) i_o = mbar_test(bar(B_O_EMPTY + (ni & 1)), ((ni >> 1) & 1) ^ 1);
-                    if (i_s && i_o) {
+                    if (i_o && !i_g) i_g = mbar_test(bar(B_QK_GATED + ni % NS), (ni / NS) & 1);
+                    if (i_g) {
                         tc_fence_after();
-                        // O^T = S'^T Qh^T  (A operand: bf16 copy of the decayed state in TMEM)
+                        // O^T = S^T Qh^T  (A operand: bf16 copy of the state before the chunk, in
+                        // TMEM; Qh = q e^{b_t} carries the decay from the chunk start)
                         const uint64_t qd = kK | (qs_of(ni) >> 4);
-                        // 64-column tile: the copy sits in chunk ni's dS buffer, key channels
+                        // 64-column tile: the copy sits in buffer ni & 1, key channels
                         // [0, DK/2) at columns [0, DK/4) and [DK/2, DK) at [DK/2, 3 DK/4)
                         const uint32_t tsb = tmem + (DVT == 64 ? (uint32_t)(ni & 1) * 128u : TM_SB);
 #pragma unroll
@@ -1172,31 +1232,12 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                             const uint32_t acol = DVT == 64 ? kk * 8 + (kk * 16 >= DK / 2 ? DK / 4 : 0) : kk * 8;
                             mma_ts(tmem + kTmO + (ni & 1) * 64, tsb + acol, qd + off, idOi, kk > 0);
                         }
-                        // the copy's buffer takes dS(ni + 2) once O_i(ni) has read it
+                        // the copy's buffer takes dS(ni + 1) (the next state copy with the
+                        // 128-column tile) once O_i(ni) has read it
                         mma_commit(bar(DVT == 64 ? B_DS_EMPTY + (ni & 1) : B_SB_EMPTY));
                         ni++;
                         *oi_issued = ni;
-                        i_s = i_o = false;
-                        prog = true;
-                    }
-                }
-                if (nd < N) {
-                    if (!d_e)
-                        d_e = DVT == 64 ? mbar_test(bar(B_DS_EMPTY + (nd & 1)), ((nd >> 1) & 1) ^ 1)
-                                        : mbar_test(bar(B_DS_EMPTY), nd & 1);
-                    if (d_e && !d_g) d_g = mbar_test(bar(B_QK_GATED + nd % NS), (nd / NS) & 1);
-                    if (d_g && !d_v) d_v = mbar_test(bar(B_V_FULL + nd % NV), (nd / NV) & 1);
-                    if (d_v) {
-                        tc_fence_after();
-                        // dS(c) = V_c^T Kh_c into its own TMEM buffer
-                        const uint64_t vd = kMN | (vs_of(nd) >> 4), kd = kMN | ((qs_of(nd) + Ly::QB) >> 4);
-#pragma unroll
-                        for (int kk = 0; kk < C / 16; kk++)
-                            mma_ss(tmem + (DVT == 64 ? (uint32_t)(nd & 1) * 128u : TM_DS), vd + kk * (2048 >> 4),
-                                   kd + kk * (2048 >> 4), idS, kk > 0);
-                        mma_commit(bar(B_DS_FULL + (DVT == 64 ? (nd & 1) : 0)));
-                        nd++;
-                        d_e = d_g = d_v = false;
+                        i_s = i_o = i_g = false;
                         prog = true;
                     }
                 }
@@ -1220,8 +1261,8 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     }
                 }
                 // the q/k stage of chunk nq is free once A (from this thread), dS and O_i
-                // of nq have finished
-                while (nq < ni && (kTwoIssuers || nq < na)) {
+                // of nq have finished (O_i(nq) may go before dS(nq))
+                while (nq < ni && nq < nd && (kTwoIssuers || nq < na)) {
                     mma_commit(bar(B_QK_EMPTY + nq % NS));
                     nq++;
                 }
