@@ -131,7 +131,10 @@ enum {
     B_O_EMPTY = B_O_FULL + 2,  // 2
     B_DRAIN = B_O_EMPTY + 2,
     B_STALL,  // completed by nothing: the test-only stall waits on it
-    B_COUNT
+    // 64-column tile only (last, so that the 128-column tile's layout does not hold them):
+    // e^{b_C} (and the strong masks) of chunk c written to slot c % kRing
+    B_G_READY,
+    B_COUNT = B_G_READY + kRing
 };
 
 // SCALAR: one log alpha per token (shared by all channels): its tile is 256
@@ -155,16 +158,20 @@ struct Layout {
     static constexpr int off_la = off_qk + NS * STAGE_QK;
     static constexpr int off_v = off_la + LA_REGION;
     // a second P buffer where it fits: P(c+1) need not wait for O_a(c)
-    static constexpr int NP = NS * STAGE_QK + LA_REGION + NV * VB + 2 * PB + OSB + NS * DK * 4 + 2 * SEG * DK * 4 +
-                                      B_COUNT * 8 + 16 + kRing * 20 + 1008 <= 232448
+    // e^{b_C} slots: a ring of its own with the 64-column tile, one per q/k stage with the
+    // 128-column tile (whose state update finishes before the stage is released)
+    static constexpr int NG = DVT == 64 ? kRing : NS;
+    static constexpr int NBAR = DVT == 64 ? B_COUNT : B_G_READY;
+    static constexpr int NP = NS * STAGE_QK + LA_REGION + NV * VB + 2 * PB + OSB + NG * DK * 4 + 2 * SEG * DK * 4 +
+                                      NBAR * 8 + 16 + kRing * 20 + 1008 <= 232448
                                   ? 2
                                   : 1;
     static constexpr int off_p = off_v + NV * VB;
     static constexpr int off_ost = off_p + NP * PB;
     static constexpr int off_gamma = off_ost + OSB;
-    static constexpr int off_segtot = off_gamma + NS * DK * 4;
+    static constexpr int off_segtot = off_gamma + NG * DK * 4;  // e^{b_C} of chunk c in slot c % NG
     static constexpr int off_bar = off_segtot + 2 * SEG * DK * 4;
-    static constexpr int off_misc = off_bar + B_COUNT * 8;
+    static constexpr int off_misc = off_bar + NBAR * 8;
     // ring of per-chunk strong-channel masks: {sequence, 4 x 32-bit masks} per slot
     static constexpr int off_ring = off_misc + 16;
     static constexpr int total = off_ring + kRing * 20;  // misc: TMEM base address, abort flag, O_i count
@@ -513,6 +520,8 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
         mbar_init(bar(B_O_FULL + 1), 1);
         mbar_init(bar(B_O_EMPTY), 4);
         mbar_init(bar(B_O_EMPTY + 1), 4);
+        if (DVT == 64)
+            for (int i = 0; i < kRing; i++) mbar_init(bar(B_G_READY + i), 8);
         mbar_init(bar(B_DRAIN), 2);
         mbar_init(bar(B_STALL), 1);
         *abort_flag = 0;
@@ -608,7 +617,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     const float4 gm4 = make_float4(__expf(tot[0]), __expf(tot[1]), __expf(tot[2]), __expf(tot[3]));
                     strong4 = (gm4.x < kStrongGamma ? 1u : 0u) | (gm4.y < kStrongGamma ? 2u : 0u) |
                               (gm4.z < kStrongGamma ? 4u : 0u) | (gm4.w < kStrongGamma ? 8u : 0u);
-                    if (seg == 0) *reinterpret_cast<float4*>(gamma + s * DK + ch) = gm4;
+                    if (seg == 0) *reinterpret_cast<float4*>(gamma + (c % Ly::NG) * DK + ch) = gm4;
                     if (warp == 0) {  // every segment-0 thread (one per channel quad) is in warp 0
                         uint32_t m[4];
     #pragma unroll
@@ -623,7 +632,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     }
                 } else {
                     if (seg == 0)
-                        *reinterpret_cast<float4*>(gamma + s * DK + ch) =
+                        *reinterpret_cast<float4*>(gamma + (c % Ly::NG) * DK + ch) =
                             make_float4(__expf(tot[0]), __expf(tot[1]), __expf(tot[2]), __expf(tot[3]));
                     if (fminf(fminf(tot[0], tot[1]), fminf(tot[2], tot[3])) < kStrongLog) *strong_flag = 1;
                 }
@@ -633,6 +642,14 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                 if (!bar_red_and(1, kGateThreads, ok)) break;
             }
             if (threadIdx.x == 0) GLA_TRACE_POINT(2, c);
+            // 64-column tile: e^{b_C} of chunk c is in its slot, the state update may start.
+            // (The slots outlive the q/k stage: the gate is at most NS + 1 chunks ahead of
+            // the last finished state update, since a stage is reloaded only after its O_i,
+            // which read the state after the chunk before.)
+            if (GATE && DVT == 64) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_G_READY + c % kRing));
+            }
             const int nval = min(C, L - c * C);
             // Rows past the sequence end arrive zero-filled (q, k and log alpha), so they
             // add nothing to A, dS or O; only the feature map (phi(0) = 1) needs them masked.
@@ -722,7 +739,8 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                 const int s = c % NS;
                 ok = mbar_wait_warp(bar(B_DS_FULL + ((c + 1) & 1)), (c >> 1) & 1, abort_flag, p.err, p.wait_ns);
                 if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(16, c);
-                if (ok && GATE) ok = mbar_wait_warp(bar(B_QK_GATED + s), (c / NS) & 1, abort_flag, p.err, p.wait_ns);
+                if (ok && GATE)
+                    ok = mbar_wait_warp(bar(B_G_READY + c % kRing), (c / kRing) & 1, abort_flag, p.err, p.wait_ns);
                 if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(17, c);
                 if (!ok) break;
                 tc_fence_after();
@@ -752,7 +770,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                         for (int u = 0; u < 2; u++) {
                             const int g = gp + u;
                             const int c0 = cbase + (g >> 1) * 32 + (g & 1) * 8;
-                            const float* gm = gamma + s * DK + c0 + hi * 16;
+                            const float* gm = gamma + (c % Ly::NG) * DK + c0 + hi * 16;
                             uint32_t pk[4];
 #pragma unroll
                             for (int i = 0; i < 8; i += 4) {
@@ -839,7 +857,8 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
             for (int c = 0; c < N; c++) {
                 const int s = c % NS;
                 ok = mbar_wait_warp(bar(B_DS_FULL), c & 1, abort_flag, p.err, p.wait_ns);
-                if (ok && GATE) ok = mbar_wait_warp(bar(B_QK_GATED + s), (c / NS) & 1, abort_flag, p.err, p.wait_ns);
+                if (ok && GATE)
+                    ok = mbar_wait_warp(bar(B_QK_GATED + s), (c / NS) & 1, abort_flag, p.err, p.wait_ns);
                 // the single bf16 copy (of the state before this chunk) is free once O_i(c) has
                 // completed; it then takes the updated state for O_i(c + 1)
                 if (ok) ok = mbar_wait_warp(bar(B_SB_EMPTY), c & 1, abort_flag, p.err, p.wait_ns);
@@ -863,7 +882,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                         for (int i = 0; i < 16; i += 2) {
                             const float s0v = __uint_as_float(rs[i]), s1v = __uint_as_float(rs[i + 1]);
                             const float d0 = __uint_as_float(rd[i]), d1 = __uint_as_float(rd[i + 1]);
-                            const float g0 = gamma[s * DK + c0 + i], g1 = gamma[s * DK + c0 + i + 1];
+                            const float g0 = gamma[(c % Ly::NG) * DK + c0 + i], g1 = gamma[(c % Ly::NG) * DK + c0 + i + 1];
                             const float a0 = g0 < kStrongGamma ? fmaf(s0v, g0, d0) : (s0v + d0) * g0;
                             const float a1 = g1 < kStrongGamma ? fmaf(s1v, g1, d1) : (s1v + d1) * g1;
                             pk[i / 2] = pack_bf16x2(a0, a1);
@@ -876,8 +895,8 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                             float a0 = __uint_as_float(rs[i]) + __uint_as_float(rd[i]);
                             float a1 = __uint_as_float(rs[i + 1]) + __uint_as_float(rd[i + 1]);
                             if (GATE) {
-                                a0 *= gamma[s * DK + c0 + i];
-                                a1 *= gamma[s * DK + c0 + i + 1];
+                                a0 *= gamma[(c % Ly::NG) * DK + c0 + i];
+                                a1 *= gamma[(c % Ly::NG) * DK + c0 + i + 1];
                             }
                             pk[i / 2] = pack_bf16x2(a0, a1);
                             rs[i] = __float_as_uint(a0);
@@ -1164,11 +1183,17 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
             constexpr uint64_t kMN = sdesc_const(8192, 1024);  // MN-major, 64-column blocks 8 KB apart
             auto qs_of = [&](int c) { return sbase + Ly::off_qk + (c % NS) * Ly::STAGE_QK; };
             auto vs_of = [&](int c) { return sbase + Ly::off_v + (c % NV) * Ly::VB; };
+            // chunk c's Qh/Kh are in its stage
+            auto gated = [&](int c) { return mbar_test(bar(B_QK_GATED + c % NS), (c / NS) & 1); };
             // Issue each chunk's products as soon as their inputs are ready (A only with
             // the 64-column tile).  A phase that has completed stays complete until the
             // product waiting on it is issued, so each barrier is polled only until it
             // first passes.
             int nd = 0, na = 0, ni = 0, no = 0, nq = 0;
+            // 128-column tile: state updates known to be complete (chunks 0 .. ns-1); its
+            // state warps read e^{b_C} from the q/k stage's slot and wait on the stage's gate
+            // barrier, so a stage is released only after the chunk's state update
+            int ns = 0;
             bool d_e = false, d_g = false, d_v = false;  // dS(nd): dS buffer free, gated, V landed
             bool a_e = false, a_g = false;               // A(na): A buffer free, gated
             bool i_s = false, i_o = false, i_g = false;  // O_i(ni): previous state's copy, O buffer free, gated
@@ -1183,7 +1208,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     if (!d_e)
                         d_e = DVT == 64 ? mbar_test(bar(B_DS_EMPTY + ((nd + 1) & 1)), (((nd + 1) >> 1) & 1) ^ 1)
                                         : mbar_test(bar(B_DS_EMPTY), nd & 1);
-                    if (d_e && !d_g) d_g = mbar_test(bar(B_QK_GATED + nd % NS), (nd / NS) & 1);
+                    if (d_e && !d_g) d_g = gated(nd);
                     if (d_g && !d_v) d_v = mbar_test(bar(B_V_FULL + nd % NV), (nd / NV) & 1);
                     if (d_v) {
                         tc_fence_after();
@@ -1217,7 +1242,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     // the copy of the state before chunk ni (written after chunk ni - 1)
                     if (!i_s) i_s = mbar_test(bar(B_S_READY + (ni & 1)), (ni >> 1) & 1);
                     if (i_s && !i_o) i_o = mbar_test(bar(B_O_EMPTY + (ni & 1)), ((ni >> 1) & 1) ^ 1);
-                    if (i_o && !i_g) i_g = mbar_test(bar(B_QK_GATED + ni % NS), (ni / NS) & 1);
+                    if (i_o && !i_g) i_g = gated(ni);
                     if (i_g) {
                         tc_fence_after();
                         // O^T = S^T Qh^T  (A operand: bf16 copy of the state before the chunk, in
@@ -1238,13 +1263,20 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                         ni++;
                         *oi_issued = ni;
                         i_s = i_o = i_g = false;
+                        if (ns < ni - 1) ns = ni - 1;  // O_i(c) read the state after chunk c - 1
                         prog = true;
                     }
+                }
+                // state(ns) complete: its S_READY phase (no later phase of that barrier can have
+                // completed: the state warps' next update there waits on O_i(ns + 1), not issued)
+                if (DVT == 128 && ns < nd && mbar_test(bar(B_S_READY + ((ns + 1) & 1)), ((ns + 1) >> 1) & 1)) {
+                    ns++;
+                    prog = true;
                 }
                 // A(c) enters the tensor pipe only after O_i(c-1), which the state chain waits on
                 if (!kTwoIssuers && na < N && na <= ni) {
                     if (!a_e) a_e = mbar_test(bar(B_A_EMPTY), (na & 1) ^ 1);
-                    if (a_e && !a_g) a_g = mbar_test(bar(B_QK_GATED + na % NS), (na / NS) & 1);
+                    if (a_e && !a_g) a_g = gated(na);
                     if (a_g) {
                         tc_fence_after();
                         // rows 64..127 of the M = 128 tile read past the Q tile and are ignored
@@ -1261,8 +1293,9 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     }
                 }
                 // the q/k stage of chunk nq is free once A (from this thread), dS and O_i
-                // of nq have finished (O_i(nq) may go before dS(nq))
-                while (nq < ni && nq < nd && (kTwoIssuers || nq < na)) {
+                // of nq have finished (O_i(nq) may go before dS(nq)), and with the 128-column
+                // tile the state update of nq
+                while (nq < ni && nq < nd && (kTwoIssuers || nq < na) && (DVT == 64 || nq < ns)) {
                     mma_commit(bar(B_QK_EMPTY + nq % NS));
                     nq++;
                 }
