@@ -60,16 +60,20 @@ __global__ void __launch_bounds__(kThreads) gla_prefill_simt_kernel(PrefillArgs 
     const bool elu = a.flags & GLA_FLAG_FEATURE_ELU1;
     const bool norm = a.flags & GLA_FLAG_NORMALIZE;
     const int NC = kDVT + 1;  // local value columns (+ normaliser)
-    float* qf = sm;                  // [TB][dk]
-    float* kf = qf + TB * dk;        // [TB][dk]
-    float* bb = kf + TB * dk;        // [TB][dk] cumsum of log alpha
-    float* vv = bb + TB * dk;        // [TB][NC]
+    // per-token rows of the [TB][dk] tables are padded to DKP = dk + 1 floats: the pair loop
+    // reads column d of consecutive rows across a warp, which an unpadded stride of dk
+    // (a multiple of 32 words) would put in one shared-memory bank
+    const int DKP = dk + 1;
+    float* qf = sm;                  // [TB][DKP]
+    float* kf = qf + TB * DKP;       // [TB][DKP]
+    float* bb = kf + TB * DKP;       // [TB][DKP] cumsum of log alpha
+    float* vv = bb + TB * DKP;       // [TB][NC]
     float* S = vv + TB * NC;         // [dk][NC]
     float* A = S + dk * NC;          // [TB][TB]
     float* os = A + TB * TB;         // [TB][NC]
-    float* qe = os + TB * NC;        // [TB][dk] q_t e^{b_t}
-    float* kh = qe + TB * dk;        // [TB][dk] k_i e^{b_last - b_i}
-    float* gl = kh + TB * dk;        // [dk] e^{b_last}
+    float* qe = os + TB * NC;        // [TB][DKP] q_t e^{b_t}
+    float* kh = qe + TB * DKP;       // [TB][DKP] k_i e^{b_last - b_i}
+    float* gl = kh + TB * DKP;       // [dk] e^{b_last}
 
     const int tid = threadIdx.x;
     const int j0 = blockIdx.x * kDVT;
@@ -110,9 +114,9 @@ __global__ void __launch_bounds__(kThreads) gla_prefill_simt_kernel(PrefillArgs 
                 }
                 if (la) xl = la[(long)(t0 + t) * la_t + d * la_d];
             }
-            qf[idx] = xq;
-            kf[idx] = xk;
-            bb[idx] = xl;
+            qf[t * DKP + d] = xq;
+            kf[t * DKP + d] = xk;
+            bb[t * DKP + d] = xl;
         }
         for (int idx = tid; idx < TB * NC; idx += kThreads) {
             int t = idx / NC, jj = idx % NC;
@@ -131,17 +135,17 @@ __global__ void __launch_bounds__(kThreads) gla_prefill_simt_kernel(PrefillArgs 
         for (int d = tid; d < dk; d += kThreads) {
             float run = 0.f;
             for (int t = 0; t < TB; t++) {
-                run += bb[t * dk + d];
-                bb[t * dk + d] = run;
+                run += bb[t * DKP + d];
+                bb[t * DKP + d] = run;
             }
             gl[d] = expf(run);
         }
         __syncthreads();
         // factors of the inter-block term and of the state update (exponents <= 0)
         for (int idx = tid; idx < TB * dk; idx += kThreads) {
-            const int d = idx % dk;
-            qe[idx] = qf[idx] * expf(bb[idx]);
-            kh[idx] = kf[idx] * expf(bb[(TB - 1) * dk + d] - bb[idx]);
+            const int t = idx / dk, d = idx % dk, o = t * DKP + d;
+            qe[o] = qf[o] * expf(bb[o]);
+            kh[o] = kf[o] * expf(bb[(TB - 1) * DKP + d] - bb[o]);
         }
         // intra-block scores with the exact decay weight of every pair
         for (int idx = tid; idx < TB * TB; idx += kThreads) {
@@ -149,7 +153,7 @@ __global__ void __launch_bounds__(kThreads) gla_prefill_simt_kernel(PrefillArgs 
             float acc = 0.f;
             if (i <= t) {
                 for (int d = 0; d < dk; d++)
-                    acc = fmaf(qf[t * dk + d] * kf[i * dk + d], __expf(bb[t * dk + d] - bb[i * dk + d]), acc);
+                    acc = fmaf(qf[t * DKP + d] * kf[i * DKP + d], __expf(bb[t * DKP + d] - bb[i * DKP + d]), acc);
             }
             A[idx] = acc;
         }
@@ -158,7 +162,7 @@ __global__ void __launch_bounds__(kThreads) gla_prefill_simt_kernel(PrefillArgs 
         for (int idx = tid; idx < TB * NC; idx += kThreads) {
             int t = idx / NC, jj = idx % NC;
             float acc = 0.f;
-            for (int d = 0; d < dk; d++) acc = fmaf(qe[t * dk + d], S[d * NC + jj], acc);
+            for (int d = 0; d < dk; d++) acc = fmaf(qe[t * DKP + d], S[d * NC + jj], acc);
             for (int i = 0; i <= t; i++) acc = fmaf(A[t * TB + i], vv[i * NC + jj], acc);
             os[idx] = acc;
         }
@@ -175,7 +179,7 @@ __global__ void __launch_bounds__(kThreads) gla_prefill_simt_kernel(PrefillArgs 
         for (int idx = tid; idx < dk * NC; idx += kThreads) {
             int d = idx / NC, jj = idx % NC;
             float acc = gl[d] * S[idx];
-            for (int i = 0; i < TB; i++) acc = fmaf(kh[i * dk + d], vv[i * NC + jj], acc);
+            for (int i = 0; i < TB; i++) acc = fmaf(kh[i * DKP + d], vv[i * NC + jj], acc);
             S[idx] = acc;
         }
         __syncthreads();
@@ -193,7 +197,7 @@ __global__ void __launch_bounds__(kThreads) gla_prefill_simt_kernel(PrefillArgs 
 
 size_t simt_smem_bytes(int dk, int TB) {
     const int NC = kDVT + 1;
-    return sizeof(float) * (size_t)(5 * TB * dk + TB * NC + dk * NC + TB * TB + TB * NC + dk);
+    return sizeof(float) * (size_t)(5 * TB * (dk + 1) + TB * NC + dk * NC + TB * TB + TB * NC + dk);
 }
 
 template <typename TI, typename TO>
