@@ -482,6 +482,17 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dkdv_kernel(const __grid_con
             }
         }
         const int nval = min(C, L - c * C);
+        // the epilogue reads this chunk's rows of q, k and dq from global memory: bring them
+        // into L2 now (contiguous blocks of nval rows), while the products run
+        if (tid == 0 && p.dla) {
+            const long row0 = (long)bh * L + (long)c * C;
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.dq + row0 * D), "r"(nval * D * 4)
+                         : "memory");
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.q + row0 * D), "r"(nval * D * 2)
+                         : "memory");
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.k + row0 * D), "r"(nval * D * 2)
+                         : "memory");
+        }
         // gate: Qh = q e^{b_t - b_C}, Kh = k e^{b_C - b_t} in place for this half's tokens
         float bC = 0.f, pre = 0.f, part1 = 0.f;
         if (p.gate) {
@@ -601,21 +612,38 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dkdv_kernel(const __grid_con
             tmem_ld32(lane + TB_K + hf * 32, rk);
             tmem_ld32(lane + TB_V + hf * 32, rv);
             tmem_wait_ld();
+            // groups of 8 tokens, last to first: a group's q, k and dq are loaded together
+            // (read-only path) before its stores, so the loads do not wait one by one
 #pragma unroll
-            for (int e = 31; e >= 0; e--) {
-                const int i = hf * 32 + e;
-                gl[e] = 0.f;
-                if (i < nval) {
-                    const float f = p.gate ? ex2f(r_suf * kLog2e) : 1.f;
-                    const float dki = __uint_as_float(rk[e]) * f;
-                    dkp[(long)i * D] = dki;
-                    dvp[(long)i * D] = __uint_as_float(rv[e]);
-                    if (p.dla) {
-                        loc += bf2f(qp[(long)i * D]) * dqp[(long)i * D] - bf2f(kp[(long)i * D]) * dki;
-                        gl[e] = loc;
+            for (int g = 3; g >= 0; g--) {
+                float qv[8], kv[8], dqv[8];
+                if (p.dla) {
+#pragma unroll
+                    for (int u = 0; u < 8; u++) {
+                        const int i = hf * 32 + g * 8 + u;
+                        const bool in = i < nval;
+                        qv[u] = in ? bf2f(__ldg(qp + (long)i * D)) : 0.f;
+                        kv[u] = in ? bf2f(__ldg(kp + (long)i * D)) : 0.f;
+                        dqv[u] = in ? __ldg(dqp + (long)i * D) : 0.f;
                     }
                 }
-                if (p.gate) r_suf += la[i * D + d];
+#pragma unroll
+                for (int u = 7; u >= 0; u--) {
+                    const int e = g * 8 + u;
+                    const int i = hf * 32 + e;
+                    gl[e] = 0.f;
+                    if (i < nval) {
+                        const float f = p.gate ? ex2f(r_suf * kLog2e) : 1.f;
+                        const float dki = __uint_as_float(rk[e]) * f;
+                        dkp[(long)i * D] = dki;
+                        dvp[(long)i * D] = __uint_as_float(rv[e]);
+                        if (p.dla) {
+                            loc += qv[u] * dqv[u] - kv[u] * dki;
+                            gl[e] = loc;
+                        }
+                    }
+                    if (p.gate) r_suf += la[i * D + d];
+                }
             }
             if (p.dla) {
                 // tokens of the second half come after the first half's in the suffix sums
