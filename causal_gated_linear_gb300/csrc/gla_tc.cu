@@ -95,13 +95,13 @@ constexpr uint32_t TM_DS = 128;  // dS^T fp32, dk columns
 constexpr uint32_t TM_SB = 256;  // bf16 copy of S^T for the next O_i, dk/2 columns (128-column tile)
 // With the 64-column tile (M = 64) S^T is held in the state warps'
 // registers instead, and the map is: two dS^T buffers at 0..127 and
-// 128..255 (dS(c) in buffer (c + 1) & 1), O^T 2 x 64 at 256..383, A at
-// 448..511.  The bf16 copy of the state after chunk c, read by O_i(c + 1), is
-// written into dS(c)'s buffer once the state warps have read dS(c) from it
-// (each half of the key channels into its own half of the buffer; the initial
-// state's copy goes to buffer 0 for O_i(0)), and the buffer is released when
-// O_i(c + 1) completes: the state update never waits on a product, only
-// dS(c + 2) waits on O_i(c + 1).
+// 128..255 (dS(c) in buffer c & 1, released by the state warps once read),
+// O^T 2 x 64 at 256..383, the bf16 copy of the state at 384..447 (key
+// channels 2x, 2x + 1 in column x), A at 448..511.  The copy of the state
+// after chunk c, read by O_i(c + 1), is written once O_i(c) has read the
+// previous one: only the copy write waits on a product, never the fp32 state
+// update, and a dS buffer waits only on the state warps' read.
+constexpr uint32_t TM_CP64 = 384;  // 64-column tile: bf16 copy of S^T, 64 columns
 constexpr uint32_t TM_O = 320;   // 2 x O^T fp32, 64 columns each
 constexpr uint32_t TM_A = 448;   // A fp32, 64 columns
 constexpr uint32_t TM_COLS = 512;
@@ -511,8 +511,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
         }
         for (int i = 0; i < 2; i++) {
             mbar_init(bar(B_DS_FULL + i), 1);
-            // 64-column tile: released by the commit after O_i; 128-column tile: by the state warps
-            mbar_init(bar(B_DS_EMPTY + i), DVT == 64 ? 1 : 8);
+            mbar_init(bar(B_DS_EMPTY + i), 8);  // released by the state warps once they have read dS
         }
         mbar_init(bar(B_S_READY), 8);
         mbar_init(bar(B_S_READY + 1), 8);
@@ -716,8 +715,9 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                         S[g * 16 + i] = s0 ? s0[(long)(cbase + g * 32 + hi * 16 + i) * dv] : 0.f;
             }
             // bf16 copy of the state for O_i: group g (8 key channels c0 + [0, 8) of this
-            // half-warp) goes to column cbase + (c0 - cbase) / 2 of the buffer
-            auto write_copy = [&](uint32_t tbuf) {
+            // half-warp, and c0 + 16 + [0, 8) for threads 16-31) goes to column c0 / 2
+            const uint32_t tCP = tmem + lane_field + TM_CP64;
+            auto write_copy = [&]() {
 #pragma unroll
                 for (int g = 0; g < NG * 2; g++) {
                     const int c0 = cbase + (g >> 1) * 32 + (g & 1) * 8;
@@ -725,11 +725,10 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     uint32_t pk[4];
 #pragma unroll
                     for (int i = 0; i < 4; i++) pk[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
-                    tmem_st16x2_x4<8>(tbuf + cbase + (c0 - cbase) / 2, pk);
+                    tmem_st16x2_x4<8>(tCP + c0 / 2, pk);
                 }
             };
-            // O_i(0) reads the initial state's copy from buffer 0 (dS(c) lands in buffer (c + 1) & 1)
-            write_copy(tmem + lane_field);
+            write_copy();  // the initial state's, for O_i(0)
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -737,7 +736,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
             bool ok = true;
             for (int c = 0; c < N; c++) {
                 const int s = c % NS;
-                ok = mbar_wait_warp(bar(B_DS_FULL + ((c + 1) & 1)), (c >> 1) & 1, abort_flag, p.err, p.wait_ns);
+                ok = mbar_wait_warp(bar(B_DS_FULL + (c & 1)), (c >> 1) & 1, abort_flag, p.err, p.wait_ns);
                 if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(16, c);
                 if (ok && GATE)
                     ok = mbar_wait_warp(bar(B_G_READY + c % kRing), (c / kRing) & 1, abort_flag, p.err, p.wait_ns);
@@ -745,10 +744,9 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                 if (!ok) break;
                 tc_fence_after();
                 if (warp == W_STATE0 && lane == 0) GLA_TRACE_POINT(4, c);
-                // dS(c) and, once read, the bf16 copy of the updated state for O_i(c + 1): this
-                // half's key channels [cbase, cbase + COLS) occupy columns [cbase, cbase + COLS)
-                // of the buffer, and their copy goes to [cbase, cbase + COLS / 2)
-                const uint32_t tB = tmem + lane_field + (uint32_t)((c + 1) & 1) * 128u;
+                // dS(c): this half's key channels [cbase, cbase + COLS) occupy columns
+                // [cbase, cbase + COLS) of buffer c & 1
+                const uint32_t tB = tmem + lane_field + (uint32_t)(c & 1) * 128u;
                 // S <- e^{b_C} (S + dS): dS carries k e^{-b_i}.  A chunk with a strong channel:
                 // that channel's dS carries k e^{b_C - b_i} (already decayed), so S <- e^{b_C} S + dS
                 const uint32_t* slot = ring + (c % kRing) * 5;
@@ -758,9 +756,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
 #pragma unroll
                     for (int gp = 0; gp < NG * 2; gp += 2) {
                         // two groups of 8 key channels per half-warp (c0 + [0, 8) for threads 0-15,
-                        // c0 + 16 + [0, 8) for threads 16-31; S index g/2 * 16 + (g&1) * 8 + i), both
-                        // read before either copy is written: the copy of group gp lands on columns
-                        // that group gp + 1 reads
+                        // c0 + 16 + [0, 8) for threads 16-31; S index g/2 * 16 + (g&1) * 8 + i)
                         uint32_t d[2][8];
 #pragma unroll
                         for (int u = 0; u < 2; u++)
@@ -771,7 +767,6 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                             const int g = gp + u;
                             const int c0 = cbase + (g >> 1) * 32 + (g & 1) * 8;
                             const float* gm = gamma + (c % Ly::NG) * DK + c0 + hi * 16;
-                            uint32_t pk[4];
 #pragma unroll
                             for (int i = 0; i < 8; i += 4) {
                                 float4 gv = make_float4(1.f, 1.f, 1.f, 1.f);
@@ -790,10 +785,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                                     sv[2] = (sv[2] + d2) * gv.z;
                                     sv[3] = (sv[3] + d3) * gv.w;
                                 }
-                                pk[i / 2] = pack_bf16x2(sv[0], sv[1]);
-                                pk[i / 2 + 1] = pack_bf16x2(sv[2], sv[3]);
                             }
-                            tmem_st16x2_x4<8>(tB + cbase + (c0 - cbase) / 2, pk);
                         }
                     }
                 };
@@ -801,6 +793,17 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     update(std::true_type{});
                 else
                     update(std::false_type{});
+                // dS(c) has been read: its buffer takes dS(c + 2)
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_DS_EMPTY + (c & 1)));
+                // the copy of the state after chunk c, once O_i(c) has read the previous one
+                if (!mbar_wait_warp(bar(B_SB_EMPTY), c & 1, abort_flag, p.err, p.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                write_copy();
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -1202,11 +1205,10 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
             while (no < N) {
                 bool prog = false;
                 // dS(c) = V_c^T Kh_c first: the state chain waits on it.  64-column tile: dS(c)
-                // lands in buffer (c + 1) & 1, whose previous content (the state copy read by
-                // O_i(c - 1), or the initial state's for c = 1) is released by that O_i
+                // lands in buffer c & 1, released by the state warps' read of dS(c - 2)
                 if (nd < N) {
                     if (!d_e)
-                        d_e = DVT == 64 ? mbar_test(bar(B_DS_EMPTY + ((nd + 1) & 1)), (((nd + 1) >> 1) & 1) ^ 1)
+                        d_e = DVT == 64 ? mbar_test(bar(B_DS_EMPTY + (nd & 1)), ((nd >> 1) & 1) ^ 1)
                                         : mbar_test(bar(B_DS_EMPTY), nd & 1);
                     if (d_e && !d_g) d_g = gated(nd);
                     if (d_g && !d_v) d_v = mbar_test(bar(B_V_FULL + nd % NV), (nd / NV) & 1);
@@ -1215,9 +1217,9 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                         const uint64_t vd = kMN | (vs_of(nd) >> 4), kd = kMN | ((qs_of(nd) + Ly::QB) >> 4);
 #pragma unroll
                         for (int kk = 0; kk < C / 16; kk++)
-                            mma_ss(tmem + (DVT == 64 ? (uint32_t)((nd + 1) & 1) * 128u : TM_DS),
-                                   vd + kk * (2048 >> 4), kd + kk * (2048 >> 4), idS, kk > 0);
-                        mma_commit(bar(B_DS_FULL + (DVT == 64 ? ((nd + 1) & 1) : 0)));
+                            mma_ss(tmem + (DVT == 64 ? (uint32_t)(nd & 1) * 128u : TM_DS), vd + kk * (2048 >> 4),
+                                   kd + kk * (2048 >> 4), idS, kk > 0);
+                        mma_commit(bar(B_DS_FULL + (DVT == 64 ? (nd & 1) : 0)));
                         nd++;
                         d_e = d_g = d_v = false;
                         prog = true;
@@ -1248,18 +1250,15 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                         // O^T = S^T Qh^T  (A operand: bf16 copy of the state before the chunk, in
                         // TMEM; Qh = q e^{b_t} carries the decay from the chunk start)
                         const uint64_t qd = kK | (qs_of(ni) >> 4);
-                        // 64-column tile: the copy sits in buffer ni & 1, key channels
-                        // [0, DK/2) at columns [0, DK/4) and [DK/2, DK) at [DK/2, 3 DK/4)
-                        const uint32_t tsb = tmem + (DVT == 64 ? (uint32_t)(ni & 1) * 128u : TM_SB);
+                        // the copy: key channels 2x, 2x + 1 in column x
+                        const uint32_t tsb = tmem + (DVT == 64 ? TM_CP64 : TM_SB);
 #pragma unroll
                         for (int kk = 0; kk < DK / 16; kk++) {
                             const uint32_t off = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-                            const uint32_t acol = DVT == 64 ? kk * 8 + (kk * 16 >= DK / 2 ? DK / 4 : 0) : kk * 8;
-                            mma_ts(tmem + kTmO + (ni & 1) * 64, tsb + acol, qd + off, idOi, kk > 0);
+                            mma_ts(tmem + kTmO + (ni & 1) * 64, tsb + kk * 8, qd + off, idOi, kk > 0);
                         }
-                        // the copy's buffer takes dS(ni + 1) (the next state copy with the
-                        // 128-column tile) once O_i(ni) has read it
-                        mma_commit(bar(DVT == 64 ? B_DS_EMPTY + (ni & 1) : B_SB_EMPTY));
+                        // the copy takes the next state once O_i(ni) has read it
+                        mma_commit(bar(B_SB_EMPTY));
                         ni++;
                         *oi_issued = ni;
                         i_s = i_o = i_g = false;
