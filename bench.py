@@ -447,7 +447,10 @@ def bench_prefill(args, device, rank, world):
         del las
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region:
-    # gla_fwd_host copies each head group in, computes it and copies it out, overlapping the groups
+    # gla_fwd_host copies each head group in, computes it and copies it out, overlapping the groups.
+    # Consecutive steps alternate between two sets of device buffers and streams (as a caller
+    # streaming batches would): a call overwrites its device inputs only after that set's earlier
+    # kernels have read them, so with one set a step's copies could not overlap the previous step.
     if args.e2e:
         hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
         hla, hs0 = la.cpu().pin_memory(), s0.cpu().pin_memory()
@@ -455,18 +458,25 @@ def bench_prefill(args, device, rank, world):
         hfs = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hla, hs0))
         d2h = hout.numel() * hout.element_size() + hfs.numel() * hfs.element_size()
-        dq, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        dla, ds0 = torch.empty_like(la), torch.empty_like(s0)
         host = dict(q=hq, k=hk, v=hv, log_alpha=hla, init_state=hs0, out=hout, final_state=hfs)
-        devb = dict(q=dq, k=dk_, v=dv_, log_alpha=dla, init_state=ds0, out=out, final_state=fs)
-        s_in, s_c, s_out = (torch.cuda.Stream(device) for _ in range(3))
+        sets = []
+        for b in range(2):
+            devb = dict(q=torch.empty_like(q), k=torch.empty_like(k), v=torch.empty_like(v),
+                        log_alpha=torch.empty_like(la), init_state=torch.empty_like(s0),
+                        out=out if b == 0 else torch.empty_like(out), final_state=fs if b == 0 else torch.empty_like(fs))
+            sets.append((devb, tuple(torch.cuda.Stream(device) for _ in range(3))))
+        dv_, s_in = sets[0][0]["v"], sets[0][1][0]
+        step_no = [0]
 
         def e2e_step():
+            devb, (si, sc, so) = sets[step_no[0] & 1]
+            step_no[0] += 1
             st = gla.gla_fwd_host(host, devb, w.B, w.H, w.L, w.dk, w.dv, C, groups=args.e2e_groups,
-                                  copy_in=s_in, compute=s_c, copy_out=s_out)
+                                  copy_in=si, compute=sc, copy_out=so)
             if st != 0:
                 raise RuntimeError(gla.gla_status_string(st))
 
+        e2e_step()
         e2e_step()
         torch.cuda.synchronize(device)
         # the host link's own rate on these buffers: one timed copy of v in, one of out back
@@ -483,17 +493,25 @@ def bench_prefill(args, device, rank, world):
         ne = args.steps
         barrier(world)
         torch.cuda.synchronize(device)
+        # CUDA events: the start on the first step's copy-in stream, the end on a stream that
+        # waits for the last work of both stream sets
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s_in)
         for _ in range(ne):
             e2e_step()
-        e1.record(s_out)
+        join = torch.cuda.Stream(device)
+        for _, streams in sets:
+            for st_ in streams:
+                ev = torch.cuda.Event()
+                ev.record(st_)
+                join.wait_event(ev)
+        e1.record(join)
         torch.cuda.synchronize(device)
-        gla.check(gla.gla_device_error(s_out))
         e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
+        gla.check(gla.gla_device_error())
         res["e2e"] = dict(ms_per_step=e_ms / ne, steps=ne, h2d=h2d, d2h=d2h, groups=args.e2e_groups,
-                          h2d_gbs=h2d_gbs, d2h_gbs=d2h_gbs)
-        del hq, hk, hv, hla, hs0, hout, hfs, dq, dk_, dv_, dla, ds0, host, devb
+                          h2d_gbs=h2d_gbs, d2h_gbs=d2h_gbs, buffer_sets=2)
+        del hq, hk, hv, hla, hs0, hout, hfs, dv_, host, sets
     del q, k, v, la, s0, out, fs
     torch.cuda.empty_cache()
     return w, BH, res
@@ -861,7 +879,7 @@ def run_gla(args):
         line["e2e"] = {"value": tokens * world / (e["ms_per_step"] / 1e3), "unit": "tokens/s",
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
                        "ms_per_step": e["ms_per_step"], "steps": e["steps"], "api": "gla_fwd_host",
-                       "head_groups": e["groups"],
+                       "head_groups": e["groups"], "device_buffer_sets": e["buffer_sets"],
                        "link": {"h2d_gbs": e["h2d_gbs"], "d2h_gbs": e["d2h_gbs"],
                                 "h2d_floor_ms": e["h2d"] / e["h2d_gbs"] / 1e6}}
     if rank == 0 and world == 1 and args.cpu_baseline:
