@@ -212,9 +212,9 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 // Gate factor phase of one gate thread: TPS tokens (its segment) x 4 key
-// channels.  `off` holds (prefix of earlier segments - chunk total) in natural
-// log units; the running value is kept in log2 units so that each factor is a
-// single ex2:  Qh = q * 2^{(b_t - b_C) log2 e},  Kh = k * 2^{-(b_t - b_C) log2 e}.
+// channels.  `off` holds the prefix of the earlier segments (b before the
+// segment) in natural log units; the running value b_t is kept in log2 units so
+// that each factor is a single ex2:  Qh = q * 2^{b_t log2 e},  Kh = k * 2^{-b_t log2 e}.
 // The feature map and the gate are compile-time branches so that the token
 // loop stays one basic block the scheduler can interleave.
 // With SCALAR (one log alpha per token) all four channels share one running
@@ -294,11 +294,11 @@ __device__ __forceinline__ float4 load_la4(const float* la, int t) {
 }
 
 // Gate factors of a thread that owns at least one strong channel in this chunk
-// (its gate decays by more than e^-64 over the chunk, so e^{b_t - b_C} could
-// overflow).  On strong channels q takes the factor e^{b_t} (relative to the
-// chunk start, <= 1); k always takes e^{b_C - b_t} (<= 1), here accumulated as a
-// suffix sum from the chunk end so that it stays exact however large |b_C| is.
-// Channels of the thread that are not strong keep q e^{b_t - b_C}.
+// (its gate decays by more than e^-64 over the chunk, so k e^{-b_t} could
+// overflow).  q takes e^{b_t} on every channel; on strong channels k takes
+// e^{b_C - b_t} (<= 1, already decayed to the chunk end), accumulated as a
+// suffix sum from the chunk end so that it stays exact however large |b_C| is;
+// the thread's other channels keep k e^{-b_t}.
 //   pre: sum of log alpha over the segments before this thread's, suf: over the
 //   segments after it, tot: over the whole chunk (b_C).
 template <int DK, int TPS, bool ELU, bool SCALAR>
@@ -437,7 +437,7 @@ __device__ __forceinline__ bool ring_wait(const volatile uint32_t* slot, uint32_
 // One pass of a CTA over its (batch*head, value slice).
 // SAFE = false: the pass every call makes.  A chunk whose gate decays by more
 // than e^-64 on some channel is not computed exactly by the factorisation
-// relative to the chunk end; such a chunk only raises a flag, the pass then
+// (k e^{-b_t} could overflow); such a chunk only raises a flag, the pass then
 // skips the final-state write and returns true (its outputs are rewritten).
 // SAFE = true: the pass that follows in the same CTA when the first returned
 // true; it recomputes the slice with strong channels handled exactly
