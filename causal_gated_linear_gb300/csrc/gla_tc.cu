@@ -205,6 +205,26 @@ __device__ __forceinline__ int lane_to_col(int warp_quarter, int lane) {
     return lane < 16 ? warp_quarter * 16 + lane : -1;
 }
 
+// Packed fp32 pair add and multiply (one instruction each, IEEE round-to-nearest,
+// bit-identical to the scalar forms).
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -238,41 +258,67 @@ __device__ __forceinline__ void gate_factors(uint8_t* qt, uint8_t* kt, const flo
             kr[u] = *reinterpret_cast<const uint2*>(kt + o);
             if (GATE) lx[u] = SCALAR ? make_float4(la[t], 0.f, 0.f, 0.f) : *reinterpret_cast<const float4*>(la + t * DK);
         }
+        if constexpr (GATE && !ELU) {
+            // products as packed fp32 pairs (each rounded once to bf16, as the scalar form)
 #pragma unroll
-        for (int u = 0; u < G; u++) {
-            float2 q01 = unpack_bf16x2(qr[u].x), q23 = unpack_bf16x2(qr[u].y);
-            float2 k01 = unpack_bf16x2(kr[u].x), k23 = unpack_bf16x2(kr[u].y);
-            if (ELU) {
-                q01 = make_float2(elu1(q01.x), elu1(q01.y));
-                q23 = make_float2(elu1(q23.x), elu1(q23.y));
-                k01 = make_float2(elu1(k01.x), elu1(k01.y));
-                k23 = make_float2(elu1(k23.x), elu1(k23.y));
+            for (int u = 0; u < G; u++) {
+                float2 f_q01, f_q23, f_k01, f_k23;
+                if (SCALAR) {
+                    run_s = fmaf(lx[u].x, kLog2e, run_s);
+                    const float fq = ex2_approx(run_s), fk = ex2_approx(-run_s);
+                    f_q01 = f_q23 = make_float2(fq, fq);
+                    f_k01 = f_k23 = make_float2(fk, fk);
+                } else {
+                    run01 = fma2(make_float2(lx[u].x, lx[u].y), l2e, run01);
+                    run23 = fma2(make_float2(lx[u].z, lx[u].w), l2e, run23);
+                    f_q01 = make_float2(ex2_approx(run01.x), ex2_approx(run01.y));
+                    f_q23 = make_float2(ex2_approx(run23.x), ex2_approx(run23.y));
+                    f_k01 = make_float2(ex2_approx(-run01.x), ex2_approx(-run01.y));
+                    f_k23 = make_float2(ex2_approx(-run23.x), ex2_approx(-run23.y));
+                }
+                const float2 q01 = unpack_bf16x2(qr[u].x), q23 = unpack_bf16x2(qr[u].y);
+                const float2 k01 = unpack_bf16x2(kr[u].x), k23 = unpack_bf16x2(kr[u].y);
+                const float2 a = mul2(q01, f_q01), b = mul2(q23, f_q23), c = mul2(k01, f_k01), d = mul2(k23, f_k23);
+                qr[u] = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(b.x, b.y));
+                kr[u] = make_uint2(pack_bf16x2(c.x, c.y), pack_bf16x2(d.x, d.y));
             }
-            float2 fq01 = make_float2(1.f, 1.f), fq23 = fq01, fk01 = fq01, fk23 = fq01;
-            if (GATE && SCALAR) {  // run = b_t log2 e <= 0, the same for every channel
-                run_s = fmaf(lx[u].x, kLog2e, run_s);
-                const float fq = ex2_approx(run_s), fk = ex2_approx(-run_s);
-                fq01 = fq23 = make_float2(fq, fq);
-                fk01 = fk23 = make_float2(fk, fk);
-            } else if (GATE) {  // run = b_t log2 e <= 0
-                run01 = fma2(make_float2(lx[u].x, lx[u].y), l2e, run01);
-                run23 = fma2(make_float2(lx[u].z, lx[u].w), l2e, run23);
-                fq01 = make_float2(ex2_approx(run01.x), ex2_approx(run01.y));
-                fq23 = make_float2(ex2_approx(run23.x), ex2_approx(run23.y));
-                fk01 = make_float2(ex2_approx(-run01.x), ex2_approx(-run01.y));
-                fk23 = make_float2(ex2_approx(-run23.x), ex2_approx(-run23.y));
+        } else {
+#pragma unroll
+            for (int u = 0; u < G; u++) {
+                float2 q01 = unpack_bf16x2(qr[u].x), q23 = unpack_bf16x2(qr[u].y);
+                float2 k01 = unpack_bf16x2(kr[u].x), k23 = unpack_bf16x2(kr[u].y);
+                if (ELU) {
+                    q01 = make_float2(elu1(q01.x), elu1(q01.y));
+                    q23 = make_float2(elu1(q23.x), elu1(q23.y));
+                    k01 = make_float2(elu1(k01.x), elu1(k01.y));
+                    k23 = make_float2(elu1(k23.x), elu1(k23.y));
+                }
+                float2 fq01 = make_float2(1.f, 1.f), fq23 = fq01, fk01 = fq01, fk23 = fq01;
+                if (GATE && SCALAR) {  // run = b_t log2 e <= 0, the same for every channel
+                    run_s = fmaf(lx[u].x, kLog2e, run_s);
+                    const float fq = ex2_approx(run_s), fk = ex2_approx(-run_s);
+                    fq01 = fq23 = make_float2(fq, fq);
+                    fk01 = fk23 = make_float2(fk, fk);
+                } else if (GATE) {  // run = b_t log2 e <= 0
+                    run01 = fma2(make_float2(lx[u].x, lx[u].y), l2e, run01);
+                    run23 = fma2(make_float2(lx[u].z, lx[u].w), l2e, run23);
+                    fq01 = make_float2(ex2_approx(run01.x), ex2_approx(run01.y));
+                    fq23 = make_float2(ex2_approx(run23.x), ex2_approx(run23.y));
+                    fk01 = make_float2(ex2_approx(-run01.x), ex2_approx(-run01.y));
+                    fk23 = make_float2(ex2_approx(-run23.x), ex2_approx(-run23.y));
+                }
+                if (GATE) {
+                    // the feature map's path keeps scalar products (packed pairs spill here)
+                    q01 = make_float2(q01.x * fq01.x, q01.y * fq01.y);
+                    q23 = make_float2(q23.x * fq23.x, q23.y * fq23.y);
+                    k01 = make_float2(k01.x * fk01.x, k01.y * fk01.y);
+                    k23 = make_float2(k23.x * fk23.x, k23.y * fk23.y);
+                }
+                qr[u] = make_uint2(pack_bf16x2(q01.x, q01.y), pack_bf16x2(q23.x, q23.y));
+                kr[u] = make_uint2(pack_bf16x2(k01.x, k01.y), pack_bf16x2(k23.x, k23.y));
+                // rows past the sequence end arrive zero-filled; only phi(0) = 1 needs masking
+                if (ELU && seg * TPS + i0 + u >= nval) qr[u] = kr[u] = make_uint2(0u, 0u);
             }
-            if (GATE) {
-                // scalar products: packed pairs here need aligned register pairs and spill
-                q01 = make_float2(q01.x * fq01.x, q01.y * fq01.y);
-                q23 = make_float2(q23.x * fq23.x, q23.y * fq23.y);
-                k01 = make_float2(k01.x * fk01.x, k01.y * fk01.y);
-                k23 = make_float2(k23.x * fk23.x, k23.y * fk23.y);
-            }
-            qr[u] = make_uint2(pack_bf16x2(q01.x, q01.y), pack_bf16x2(q23.x, q23.y));
-            kr[u] = make_uint2(pack_bf16x2(k01.x, k01.y), pack_bf16x2(k23.x, k23.y));
-            // rows past the sequence end arrive zero-filled; only phi(0) = 1 needs masking
-            if (ELU && seg * TPS + i0 + u >= nval) qr[u] = kr[u] = make_uint2(0u, 0u);
         }
 #pragma unroll
         for (int u = 0; u < G; u++) {
@@ -582,34 +628,42 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
             if (GATE) {
                 float* st = segtot + (c & 1) * SEG * DK;
                 if (ok) {
-                    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+                    float2 r01 = make_float2(0.f, 0.f), r23 = r01;
 #pragma unroll
                     for (int i = 0; i < TPS; i++) {
                         const float4 x = SCALAR ? make_float4(la[seg * TPS + i], la[seg * TPS + i], la[seg * TPS + i],
                                                               la[seg * TPS + i])
                                                 : *reinterpret_cast<const float4*>(la + (seg * TPS + i) * DK);
-                        r.x += x.x;
-                        r.y += x.y;
-                        r.z += x.z;
-                        r.w += x.w;
+                        r01 = add2(r01, make_float2(x.x, x.y));
+                        r23 = add2(r23, make_float2(x.z, x.w));
                     }
-                    *reinterpret_cast<float4*>(st + seg * DK + ch) = r;
+                    *reinterpret_cast<float4*>(st + seg * DK + ch) = make_float4(r01.x, r01.y, r23.x, r23.y);
                 }
                 // the segment-total exchange doubles as the gate role's agreement to go on
                 if (!bar_red_and(1, kGateThreads, ok)) break;
+                {
+                    // all segment totals in flight at once; the prefix takes those before this
+                    // thread's segment (seg is the warp index: the test is warp-uniform)
+                    float2 o01 = make_float2(0.f, 0.f), o23 = o01, t01 = o01, t23 = o01;
+                    // the chunk total is needed by segment 0 only (e^{b_C}, the strong test),
+                    // except in the exact pass, where every thread tests its own channels
+                    const bool need_tot = SAFE || seg == 0;
 #pragma unroll
-                for (int g = 0; g < SEG; g++) {
-                    const float4 u = *reinterpret_cast<const float4*>(st + g * DK + ch);
-                    if (g < seg) {
-                        off[0] += u.x;
-                        off[1] += u.y;
-                        off[2] += u.z;
-                        off[3] += u.w;
+                    for (int g = 0; g < SEG; g++) {
+                        if (!(g < seg || need_tot)) continue;
+                        const float4 u = *reinterpret_cast<const float4*>(st + g * DK + ch);
+                        if (g < seg) {
+                            o01 = add2(o01, make_float2(u.x, u.y));
+                            o23 = add2(o23, make_float2(u.z, u.w));
+                        } else {
+                            t01 = add2(t01, make_float2(u.x, u.y));
+                            t23 = add2(t23, make_float2(u.z, u.w));
+                        }
                     }
-                    tot[0] += u.x;
-                    tot[1] += u.y;
-                    tot[2] += u.z;
-                    tot[3] += u.w;
+                    t01 = add2(t01, o01);
+                    t23 = add2(t23, o23);
+                    off[0] = o01.x; off[1] = o01.y; off[2] = o23.x; off[3] = o23.y;
+                    tot[0] = t01.x; tot[1] = t01.y; tot[2] = t23.x; tot[3] = t23.y;
                 }
                 if constexpr (SAFE) {
                     // e^{b_C} per channel: the state's decay; below e^-64 the channel is strong
@@ -633,7 +687,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     if (seg == 0)
                         *reinterpret_cast<float4*>(gamma + (c % Ly::NG) * DK + ch) =
                             make_float4(__expf(tot[0]), __expf(tot[1]), __expf(tot[2]), __expf(tot[3]));
-                    if (fminf(fminf(tot[0], tot[1]), fminf(tot[2], tot[3])) < kStrongLog) *strong_flag = 1;
+                    if (seg == 0 && fminf(fminf(tot[0], tot[1]), fminf(tot[2], tot[3])) < kStrongLog) *strong_flag = 1;
                 }
 #pragma unroll
                 for (int e = 0; e < 4; e++) pre[e] = off[e];  // the running value is b_t
@@ -780,10 +834,14 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                                     sv[2] = gv.z < kStrongGamma ? fmaf(sv[2], gv.z, d2) : (sv[2] + d2) * gv.z;
                                     sv[3] = gv.w < kStrongGamma ? fmaf(sv[3], gv.w, d3) : (sv[3] + d3) * gv.w;
                                 } else {
-                                    sv[0] = (sv[0] + d0) * gv.x;
-                                    sv[1] = (sv[1] + d1) * gv.y;
-                                    sv[2] = (sv[2] + d2) * gv.z;
-                                    sv[3] = (sv[3] + d3) * gv.w;
+                                    const float2 a01 = mul2(add2(make_float2(sv[0], sv[1]), make_float2(d0, d1)),
+                                                            make_float2(gv.x, gv.y));
+                                    const float2 a23 = mul2(add2(make_float2(sv[2], sv[3]), make_float2(d2, d3)),
+                                                            make_float2(gv.z, gv.w));
+                                    sv[0] = a01.x;
+                                    sv[1] = a01.y;
+                                    sv[2] = a23.x;
+                                    sv[3] = a23.y;
                                 }
                             }
                         }
@@ -1158,6 +1216,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     pv_n++;
                     prog = true;
                 }
+                if (!prog) __nanosleep(20);
                 if (prog) {
                     idle = 0;
                 } else if ((++idle & 255u) == 0) {
@@ -1298,6 +1357,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     mma_commit(bar(B_QK_EMPTY + nq % NS));
                     nq++;
                 }
+                if (!prog) __nanosleep(20);
                 if (prog) {
                     idle = 0;
                 } else if ((++idle & 255u) == 0) {
