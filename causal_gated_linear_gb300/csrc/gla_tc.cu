@@ -519,7 +519,6 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
     const int lane = threadIdx.x & 31;
     // A(c) comes from the TMA producer thread (128-column tile) or, with the
     // 64-column tile, from the MMA thread together with the other three products
-    constexpr bool kTwoIssuers = DVT == 128;
     constexpr uint32_t kTmO = DVT == 64 ? 256u : TM_O;  // the two O^T buffers
     const int tile = blockIdx.x % p.ntile;
     const int bh = blockIdx.x / p.ntile;
@@ -538,7 +537,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
         for (int i = 0; i < NS; i++) {
             mbar_init(bar(B_QK_FULL + i), 1);
             mbar_init(bar(B_QK_GATED + i), 8);
-            mbar_init(bar(B_QK_EMPTY + i), kTwoIssuers ? 2 : 1);  // released by the issuer(s) of A, dS, O_i
+            mbar_init(bar(B_QK_EMPTY + i), 2);  // released by the issuers of A (TMA thread) and of dS, O_i
         }
         for (int i = 0; i < NL; i++) {
             mbar_init(bar(B_LA_FULL + i), 1);
@@ -1154,11 +1153,11 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
             if (!p.out_f32) tma_prefetch_desc(&p.tm_out);
             // The three rings are refilled independently (a full V ring must not hold
             // back the next chunk's q/k and log alpha loads).
-            // With the 128-column tile this thread also issues A(c) = Qh_c Kh_c^T: its
-            // M = 128 products take twice as long as the 64-column tile's, and one
-            // issuing thread would then hold back the other products.
+            // This thread also issues A(c) = Qh_c Kh_c^T: a tensor-core instruction costs
+            // its issuing thread about as much as any other step of the MMA thread's
+            // chunk, so the products are split between two issuers.
             constexpr uint32_t idA = make_idesc_bf16(128, 64, 0, 0);
-            int na = kTwoIssuers ? 0 : N;
+            int na = 0;
             uint32_t idle = 0;
             unsigned long long t_last = 0;
             const int nl_end = GATE ? N : 0;
@@ -1166,7 +1165,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                 bool prog = false;
                 // A(c) goes into the tensor pipe only after O_i(c-1): the state chain
                 // waits on O_i(c-1), which must not queue behind A(c).
-                if (kTwoIssuers && na < pq_n && na <= *oi_issued && mbar_test(bar(B_QK_GATED + na % NS), (na / NS) & 1) &&
+                if (na < pq_n && na <= *oi_issued && mbar_test(bar(B_QK_GATED + na % NS), (na / NS) & 1) &&
                     mbar_test(bar(B_A_EMPTY), (na & 1) ^ 1)) {
                     tc_fence_after();
                     GLA_TRACE_POINT(19, na);
@@ -1237,7 +1236,6 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
     } else {
         // ============================================================ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idA = make_idesc_bf16(128, 64, 0, 0);
             constexpr uint32_t idS = make_idesc_bf16(DVT, DK, 1, 1);
             constexpr uint32_t idOi = make_idesc_bf16(DVT, 64, 0, 0);
             constexpr uint32_t idOa = make_idesc_bf16(DVT, 64, 1, 0);
@@ -1247,17 +1245,16 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
             auto vs_of = [&](int c) { return sbase + Ly::off_v + (c % NV) * Ly::VB; };
             // chunk c's Qh/Kh are in its stage
             auto gated = [&](int c) { return mbar_test(bar(B_QK_GATED + c % NS), (c / NS) & 1); };
-            // Issue each chunk's products as soon as their inputs are ready (A only with
-            // the 64-column tile).  A phase that has completed stays complete until the
+            // Issue each chunk's dS, O_i and O_a as soon as their inputs are ready (A is
+            // the TMA thread's).  A phase that has completed stays complete until the
             // product waiting on it is issued, so each barrier is polled only until it
             // first passes.
-            int nd = 0, na = 0, ni = 0, no = 0, nq = 0;
+            int nd = 0, ni = 0, no = 0, nq = 0;
             // 128-column tile: state updates known to be complete (chunks 0 .. ns-1); its
             // state warps read e^{b_C} from the q/k stage's slot and wait on the stage's gate
             // barrier, so a stage is released only after the chunk's state update
             int ns = 0;
             bool d_e = false, d_g = false, d_v = false;  // dS(nd): dS buffer free, gated, V landed
-            bool a_e = false, a_g = false;               // A(na): A buffer free, gated
             bool i_s = false, i_o = false, i_g = false;  // O_i(ni): previous state's copy, O buffer free, gated
             unsigned long long t_last = globaltimer();
             uint32_t idle = 0;
@@ -1331,29 +1328,10 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     ns++;
                     prog = true;
                 }
-                // A(c) enters the tensor pipe only after O_i(c-1), which the state chain waits on
-                if (!kTwoIssuers && na < N && na <= ni) {
-                    if (!a_e) a_e = mbar_test(bar(B_A_EMPTY), (na & 1) ^ 1);
-                    if (a_e && !a_g) a_g = gated(na);
-                    if (a_g) {
-                        tc_fence_after();
-                        // rows 64..127 of the M = 128 tile read past the Q tile and are ignored
-                        const uint64_t qd = kK | (qs_of(na) >> 4), kd = kK | ((qs_of(na) + Ly::QB) >> 4);
-#pragma unroll
-                        for (int kk = 0; kk < DK / 16; kk++) {
-                            const uint32_t off = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-                            mma_ss(tmem + TM_A, qd + off, kd + off, idA, kk > 0);
-                        }
-                        mma_commit(bar(B_A_FULL));
-                        na++;
-                        a_e = a_g = false;
-                        prog = true;
-                    }
-                }
-                // the q/k stage of chunk nq is free once A (from this thread), dS and O_i
-                // of nq have finished (O_i(nq) may go before dS(nq)), and with the 128-column
-                // tile the state update of nq
-                while (nq < ni && nq < nd && (kTwoIssuers || nq < na) && (DVT == 64 || nq < ns)) {
+                // this thread's share of the release of chunk nq's q/k stage: its dS and O_i
+                // have finished (O_i(nq) may go before dS(nq)), and with the 128-column tile
+                // the state update of nq (the TMA thread releases its A)
+                while (nq < ni && nq < nd && (DVT == 64 || nq < ns)) {
                     mma_commit(bar(B_QK_EMPTY + nq % NS));
                     nq++;
                 }
@@ -1366,8 +1344,8 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
                     if (idle == 256) t_last = now;
                     else if (now - t_last > p.wait_ns) {
                         *abort_flag = 1;
-                        // scheduler progress at the time: next dS, A, O_i, O_a chunk (8 bits each)
-                        record_timeout_code(p.err, 0x40000000u | ((nd & 0xff) << 22) | ((na & 0xff) << 14) |
+                        // scheduler progress at the time: next dS, stage release, O_i, O_a chunk
+                        record_timeout_code(p.err, 0x40000000u | ((nd & 0xff) << 22) | ((nq & 0xff) << 14) |
                                                        ((ni & 0xff) << 6) | ((no & 0x1f) << 1));
                         break;
                     }
