@@ -32,8 +32,8 @@
 // Warp roles (24 warps): 0-7 gate (cumsum with a cross-warp segment
 // exchange, factors written in place over the TMA-landed q/k tiles), 8-15
 // state, 16-19 output (TMEM -> shared staging -> TMA bulk store), 20-21 P
-// (mask A -> bf16 P), 22 TMA producer (and A issuer with the 128-column
-// tile), 23 MMA issuer and TMEM owner.  Every pipeline wait is bounded
+// (mask A -> bf16 P), 22 TMA producer and issuer of MMA_A, 23 issuer of the
+// other products and TMEM owner.  Every pipeline wait is bounded
 // (gla_ptx.cuh).
 //
 // Strong gates: alpha has no lower bound, and once a channel decays by more
@@ -517,8 +517,7 @@ __device__ __forceinline__ bool prefill_pass(const TcParams& p, uint8_t* smem_ra
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // A(c) comes from the TMA producer thread (128-column tile) or, with the
-    // 64-column tile, from the MMA thread together with the other three products
+    // A(c) comes from the TMA producer thread, the other three products from the MMA thread
     constexpr uint32_t kTmO = DVT == 64 ? 256u : TM_O;  // the two O^T buffers
     const int tile = blockIdx.x % p.ntile;
     const int bh = blockIdx.x / p.ntile;
