@@ -467,14 +467,24 @@ def bench_prefill(args, device, rank, world):
             sets.append((devb, tuple(torch.cuda.Stream(device) for _ in range(3))))
         dv_, s_in = sets[0][0]["v"], sets[0][1][0]
         step_no = [0]
+        last_in = [None]  # end of the previous step's host-to-device copies
 
         def e2e_step():
             devb, (si, sc, so) = sets[step_no[0] & 1]
             step_no[0] += 1
+            # a step's inputs go over the link after the previous step's: each step's copies
+            # finish as early as they can, so its outputs come back while the next step's
+            # inputs are still going in (the two directions overlap; two steps' inputs sharing
+            # the link would only delay both)
+            if last_in[0] is not None:
+                si.wait_event(last_in[0])
             st = gla.gla_fwd_host(host, devb, w.B, w.H, w.L, w.dk, w.dv, C, groups=args.e2e_groups,
                                   copy_in=si, compute=sc, copy_out=so)
             if st != 0:
                 raise RuntimeError(gla.gla_status_string(st))
+            ev = torch.cuda.Event()
+            ev.record(si)
+            last_in[0] = ev
 
         e2e_step()
         e2e_step()
