@@ -45,7 +45,9 @@ constexpr int TB = C * D * 2;    // bf16 [64][128]: two 8 KB atoms
 constexpr int LAB = C * D * 4;   // fp32 log alpha tile
 constexpr int PB = C * C * 2;    // bf16 [64][64]: one atom
 constexpr int SB2 = D * D * 2;   // bf16 [128][128]: two 16 KB atoms
-constexpr int FB = C * C * 4;    // fp32 [64][64]
+constexpr int LDF = C + 4;       // row stride (floats) of the fp32 [64][64] tiles: a row per lane
+                                 // (and 16-byte groups of 8 rows) fall in distinct banks
+constexpr int FB = C * LDF * 4;  // fp32 [64][64], rows LDF floats apart
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kStrongLog = -64.f;
 
@@ -89,7 +91,7 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
 //       M | P_m | N, then -(M Kr) | T | beta | exchange | barriers
 constexpr int S_Q = 0, S_K = TB, S_KR = 2 * TB, S_V = 3 * TB, S_LA = 4 * TB, S_SH = 4 * TB + LAB,
               S_SL = S_SH + SB2, S_M = S_SL + SB2, S_PM = S_M + PB, S_N = S_PM + PB, S_T = S_N + FB,
-              S_BETA = S_T + FB, S_X = S_BETA + C * 4, S_BAR = S_X + 2 * D * 4;
+              S_BETA = S_T + FB, S_X = S_BETA + C * 4, S_BAR = S_X + 5 * D * 4;
 constexpr int S_SMEM = S_BAR + 64 + 1024;
 static_assert(S_SMEM <= 227 * 1024, "shared memory budget");
 // TMEM: S 0..127, dS 128..255, U 256..383; 384..511 holds A and P (64 each), then M Kr, then O^T
@@ -112,67 +114,58 @@ __device__ __forceinline__ void load_tiles(const DeltaTcParams& p, uint32_t bar,
 }
 
 // T = (I + N)^{-1} for N strictly lower triangular (fp32 [64][64] in shared
-// memory): 16 x 16 diagonal blocks by forward substitution (one thread per
-// column), then the off-diagonal blocks level by level,
-//   T_IJ = -T_II sum_{J <= K < I} N_IK T_KJ   (I > J).
-// Every thread of the CTA takes part (the barriers are CTA-wide).
-__device__ __forceinline__ void unit_lower_inverse(const float* N, float* T, int tid) {
-    // zero the upper part (including the diagonal blocks' upper triangles)
-    for (int e = tid; e < C * C; e += kThr) T[e] = 0.f;
-    __syncthreads();
+// memory, rows LDF floats apart): 16 x 16 diagonal blocks by forward
+// substitution (one thread per column), then the off-diagonal blocks level by
+// level,
+//   T_IJ = -T_II sum_{J <= K < I} N_IK T_KJ   (I > J),
+// the sums held in N's unused upper blocks between the level's two barriers.
+// Only T's lower part (to the block diagonal) is written.  Every thread of the
+// CTA takes part (the barriers are CTA-wide).
+__device__ __forceinline__ void unit_lower_inverse(float* N, float* T, int tid) {
+    // diagonal blocks, one thread per column j: x = T[., j] by forward substitution with the
+    // updates applied as each entry becomes final (entries above j stay 0 and add nothing)
     if (tid < C) {
         const int blk = tid >> 4, j = tid & 15, o = blk * 16;
-        float col[16];
+        float x[16];
 #pragma unroll
-        for (int t = 0; t < 16; t++) {
-            float x = (t == j) ? 1.f : 0.f;
-            if (t > j) {
+        for (int t = 0; t < 16; t++) x[t] = (t == j) ? 1.f : 0.f;
 #pragma unroll
-                for (int i = 0; i < 16; i++)
-                    if (i >= j && i < t) x -= N[(o + t) * C + o + i] * col[i];
-            }
-            col[t] = x;
-        }
+        for (int i = 0; i < 15; i++)
 #pragma unroll
-        for (int t = 0; t < 16; t++) T[(o + t) * C + o + j] = col[t];
+            for (int t = i + 1; t < 16; t++) x[t] -= N[(o + t) * LDF + o + i] * x[i];
+#pragma unroll
+        for (int t = 0; t < 16; t++) T[(o + t) * LDF + o + j] = x[t];
     }
     __syncthreads();
     for (int lvl = 1; lvl < 4; lvl++) {
         // Y_IJ = sum_{J <= K < I} N_IK T_KJ for the 4 - lvl blocks (I, J = I - lvl): one entry per
-        // thread and block
-        float y[3];
+        // thread and block, kept in N's unused upper block (J, I)
         const int a = tid >> 4, b = tid & 15;
 #pragma unroll
         for (int n = 0; n < 3; n++) {
-            y[n] = 0.f;
             if (n < 4 - lvl) {
                 const int I = n + lvl, J = n;
+                float y = 0.f;
                 for (int Kb = J; Kb < I; Kb++)
 #pragma unroll
                     for (int cc = 0; cc < 16; cc++)
-                        y[n] += N[(I * 16 + a) * C + Kb * 16 + cc] * T[(Kb * 16 + cc) * C + J * 16 + b];
+                        y += N[(I * 16 + a) * LDF + Kb * 16 + cc] * T[(Kb * 16 + cc) * LDF + J * 16 + b];
+                N[(J * 16 + a) * LDF + I * 16 + b] = y;
             }
         }
         __syncthreads();
-#pragma unroll
-        for (int n = 0; n < 3; n++)
-            if (n < 4 - lvl) T[((n + lvl) * 16 + a) * C + n * 16 + b] = y[n];  // Y, temporarily
-        __syncthreads();
-        float z[3];
+        // T_IJ = -T_II Y_IJ
 #pragma unroll
         for (int n = 0; n < 3; n++) {
-            z[n] = 0.f;
             if (n < 4 - lvl) {
                 const int I = n + lvl, J = n;
+                float z = 0.f;
 #pragma unroll
                 for (int cc = 0; cc < 16; cc++)
-                    z[n] -= T[(I * 16 + a) * C + I * 16 + cc] * T[(I * 16 + cc) * C + J * 16 + b];
+                    z -= T[(I * 16 + a) * LDF + I * 16 + cc] * N[(J * 16 + cc) * LDF + I * 16 + b];
+                T[(I * 16 + a) * LDF + J * 16 + b] = z;
             }
         }
-        __syncthreads();
-#pragma unroll
-        for (int n = 0; n < 3; n++)
-            if (n < 4 - lvl) T[((n + lvl) * 16 + a) * C + n * 16 + b] = z[n];
         __syncthreads();
     }
 }
@@ -229,6 +222,7 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
     const float* la = reinterpret_cast<const float*>(sm + S_LA);
     bool ok = true, strong = false;
     int mph = 0;  // phases of bar_mma completed
+    float beta_next = (tid < C && tid < L) ? p.beta[(long)bh * L + tid] : 0.f;
     for (int c = 0; c < N; c++) {
         if (!(ok = wait_all(bar_t, c & 1, abort_flag, p))) break;
         if (tid == 0) tiles_done++;
@@ -237,42 +231,67 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
             if (tid == 0) la_done++;
         }
         const int nval = min(C, L - c * C);
-        if (tid < C) betas[tid] = tid < nval ? p.beta[(long)bh * L + (long)c * C + tid] : 0.f;
-        // gate and factors for this half's tokens: Kr = k e^{b_t - b_C} (new tile), Kh = k e^{b_C - b_t}
-        // and Qh = q e^{b_t - b_C} in place
-        float bC = 0.f;
+        // beta of this chunk (loaded one chunk ahead), and the next chunk's load in flight
+        if (tid < C) {
+            betas[tid] = beta_next;
+            const int nn = min(C, L - (c + 1) * C);
+            beta_next = (c + 1 < N && tid < nn) ? p.beta[(long)bh * L + (long)(c + 1) * C + tid] : 0.f;
+        }
+        // gate and factors: Kr = k e^{b_t - b_C} (new tile), Kh = k e^{b_C - b_t} and
+        // Qh = q e^{b_t - b_C} in place.  Thread (channel pair gp, token quarter gq) takes
+        // channels 2gp, 2gp + 1 over tokens 16 gq .. 16 gq + 15 (packed pairs); the quarter
+        // sums of log alpha are exchanged for each quarter's prefix and the chunk total b_C.
         {
-            float pre = 0.f;
+            const int gp = tid & 63, gq = tid >> 6, ch = 2 * gp;
+            float2 b2 = make_float2(0.f, 0.f), bc2 = b2;
             if (p.gate) {
-                float s0 = 0.f;
+                float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll 8
-                for (int t = 32 * hf; t < 32 * hf + 32; t++) s0 += la[t * D + d];
-                xch[hf * D + d] = s0;
+                for (int t = 16 * gq; t < 16 * gq + 16; t++) {
+                    const float2 x = *reinterpret_cast<const float2*>(la + t * D + ch);
+                    s2.x += x.x;
+                    s2.y += x.y;
+                }
+                *reinterpret_cast<float2*>(xch + gq * D + ch) = s2;
                 __syncthreads();
-                bC = xch[d] + xch[D + d];
-                pre = hf ? xch[d] : 0.f;
-                strong |= bC < kStrongLog;
+#pragma unroll
+                for (int g = 0; g < 4; g++) {
+                    const float2 u = *reinterpret_cast<const float2*>(xch + g * D + ch);
+                    if (g < gq) {
+                        b2.x += u.x;
+                        b2.y += u.y;
+                    }
+                    bc2.x += u.x;
+                    bc2.y += u.y;
+                }
+                if (gq == 0) *reinterpret_cast<float2*>(xch + 4 * D + ch) = bc2;  // b_C per channel
+                strong |= fminf(bc2.x, bc2.y) < kStrongLog;
             }
-            float b = pre;
 #pragma unroll 4
-            for (int t = 32 * hf; t < 32 * hf + 32; t++) {
-                const uint32_t o = tile_off(t, d, 8192);
-                uint16_t* eq = reinterpret_cast<uint16_t*>(sm + S_Q + o);
-                uint16_t* ek = reinterpret_cast<uint16_t*>(sm + S_K + o);
-                uint16_t* er = reinterpret_cast<uint16_t*>(sm + S_KR + o);
-                const float kv = bf2f(*ek);
+            for (int t = 16 * gq; t < 16 * gq + 16; t++) {
+                const uint32_t o = tile_off(t, ch, 8192);
+                uint32_t* eq = reinterpret_cast<uint32_t*>(sm + S_Q + o);
+                uint32_t* ek = reinterpret_cast<uint32_t*>(sm + S_K + o);
+                uint32_t* er = reinterpret_cast<uint32_t*>(sm + S_KR + o);
+                const uint32_t kv = *ek;
                 if (p.gate) {
-                    b += la[t * D + d];
-                    const float fu = ex2f((b - bC) * kLog2e), fd = ex2f((bC - b) * kLog2e);
-                    *eq = f2bf(bf2f(*eq) * fu);
-                    *er = f2bf(kv * fu);
-                    *ek = f2bf(kv * fd);
+                    const float2 x = *reinterpret_cast<const float2*>(la + t * D + ch);
+                    b2.x += x.x;
+                    b2.y += x.y;
+                    const float u0 = (b2.x - bc2.x) * kLog2e, u1 = (b2.y - bc2.y) * kLog2e;
+                    const float fu0 = ex2f(u0), fu1 = ex2f(u1), fd0 = ex2f(-u0), fd1 = ex2f(-u1);
+                    const float2 qf = unpack_bf16x2(*eq), kf = unpack_bf16x2(kv);
+                    *eq = pack_bf16x2(qf.x * fu0, qf.y * fu1);
+                    *er = pack_bf16x2(kf.x * fu0, kf.y * fu1);
+                    *ek = pack_bf16x2(kf.x * fd0, kf.y * fd1);
                 } else {
-                    *er = *ek;
+                    *er = kv;
                 }
             }
         }
         __syncthreads();
+        // b_C of this thread's key channel d, for the decay of the state below
+        const float bC = p.gate ? xch[4 * D + d] : 0.f;
         // log alpha is read until here: the next chunk's may load
         if (tid == 0 && p.gate && c + 1 < N) {
             mbar_arrive_expect_tx(bar_l, LAB);
@@ -344,7 +363,7 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
                 for (int e = 0; e < 8; e++) {
                     const int i = hf * 32 + k8 * 8 + e;
                     x[e] = (i <= t) ? __uint_as_float(rp[k8 * 8 + e]) : 0.f;
-                    Nf[t * C + i] = (i < t) ? bt * __uint_as_float(ra[k8 * 8 + e]) : 0.f;
+                    Nf[t * LDF + i] = (i < t) ? bt * __uint_as_float(ra[k8 * 8 + e]) : 0.f;
                 }
                 uint4 w;
                 w.x = pack_bf16x2(x[0], x[1]);
@@ -365,7 +384,8 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
 #pragma unroll
                 for (int e = 0; e < 8; e++) {
                     const int i = h2 * 32 + k8 * 8 + e;
-                    x[e] = Tf[t * C + i] * betas[i];
+                    // T is unit lower triangular; its blocks above the block diagonal are not stored
+                    x[e] = i <= t ? Tf[t * LDF + i] * betas[i] : 0.f;
                 }
                 uint4 w;
                 w.x = pack_bf16x2(x[0], x[1]);
