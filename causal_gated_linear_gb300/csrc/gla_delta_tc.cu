@@ -137,34 +137,32 @@ __device__ __forceinline__ void unit_lower_inverse(float* N, float* T, int tid) 
         for (int t = 0; t < 16; t++) T[(o + t) * LDF + o + j] = x[t];
     }
     __syncthreads();
+#pragma unroll
     for (int lvl = 1; lvl < 4; lvl++) {
         // Y_IJ = sum_{J <= K < I} N_IK T_KJ for the 4 - lvl blocks (I, J = I - lvl): one entry per
-        // thread and block, kept in N's unused upper block (J, I)
+        // thread and block (four partial sums), kept in N's unused upper block (J, I)
         const int a = tid >> 4, b = tid & 15;
 #pragma unroll
-        for (int n = 0; n < 3; n++) {
-            if (n < 4 - lvl) {
-                const int I = n + lvl, J = n;
-                float y = 0.f;
-                for (int Kb = J; Kb < I; Kb++)
+        for (int n = 0; n < 4 - lvl; n++) {
+            const int I = n + lvl, J = n;
+            float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int cc = 0; cc < 16; cc++)
-                        y += N[(I * 16 + a) * LDF + Kb * 16 + cc] * T[(Kb * 16 + cc) * LDF + J * 16 + b];
-                N[(J * 16 + a) * LDF + I * 16 + b] = y;
-            }
+            for (int Kb = J; Kb < I; Kb++)
+#pragma unroll
+                for (int cc = 0; cc < 16; cc++)
+                    y[cc & 3] += N[(I * 16 + a) * LDF + Kb * 16 + cc] * T[(Kb * 16 + cc) * LDF + J * 16 + b];
+            N[(J * 16 + a) * LDF + I * 16 + b] = (y[0] + y[1]) + (y[2] + y[3]);
         }
         __syncthreads();
         // T_IJ = -T_II Y_IJ
 #pragma unroll
-        for (int n = 0; n < 3; n++) {
-            if (n < 4 - lvl) {
-                const int I = n + lvl, J = n;
-                float z = 0.f;
+        for (int n = 0; n < 4 - lvl; n++) {
+            const int I = n + lvl, J = n;
+            float z[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int cc = 0; cc < 16; cc++)
-                    z -= T[(I * 16 + a) * LDF + I * 16 + cc] * N[(J * 16 + cc) * LDF + I * 16 + b];
-                T[(I * 16 + a) * LDF + J * 16 + b] = z;
-            }
+            for (int cc = 0; cc < 16; cc++)
+                z[cc & 3] += T[(I * 16 + a) * LDF + I * 16 + cc] * N[(J * 16 + cc) * LDF + I * 16 + b];
+            T[(I * 16 + a) * LDF + J * 16 + b] = -((z[0] + z[1]) + (z[2] + z[3]));
         }
         __syncthreads();
     }
