@@ -287,14 +287,29 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
                 }
             }
         }
+        fence_proxy_async_smem();  // the factors, read by the products below
+        tc_fence_before();
         __syncthreads();
+        tc_fence_after();
         // b_C of this thread's key channel d, for the decay of the state below
         const float bC = p.gate ? xch[4 * D + d] : 0.f;
-        // log alpha is read until here: the next chunk's may load
-        if (tid == 0 && p.gate && c + 1 < N) {
-            mbar_arrive_expect_tx(bar_l, LAB);
-            tma_load_3d(sb + S_LA, &p.tm_la, bar_l, 0, (c + 1) * C, bh);
-            la_issued++;
+        if (tid == 0) {
+            // log alpha is read until here: the next chunk's may load
+            if (p.gate && c + 1 < N) {
+                mbar_arrive_expect_tx(bar_l, LAB);
+                tma_load_3d(sb + S_LA, &p.tm_la, bar_l, 0, (c + 1) * C, bh);
+                la_issued++;
+            }
+            // A = Kr Kh^T and P = Qh Kh^T (M = 128: rows 64..127 read past the tile and are
+            // ignored); they run while the state is decayed and split below
+            constexpr uint32_t id64 = make_idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + T_A, desc_k(sb + S_KR, kk, 8192), desc_k(sb + S_K, kk, 8192), id64, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + T_P, desc_k(sb + S_Q, kk, 8192), desc_k(sb + S_K, kk, 8192), id64, kk > 0);
+            mma_commit(bar_mma);
         }
         // S' = e^{b_C} S: bf16 high and low copies in shared memory ([d][j], MN-major operand)
         {
@@ -329,21 +344,8 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
             }
             tmem_wait_st();
         }
-        fence_proxy_async_smem();
+        fence_proxy_async_smem();  // S' high and low copies, read by the products after this barrier
         tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid == 0) {
-            // A = Kr Kh^T and P = Qh Kh^T (M = 128: rows 64..127 read past the tile and are ignored)
-            constexpr uint32_t id64 = make_idesc_bf16(128, 64, 0, 0);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; kk++)
-                mma_ss(tmem + T_A, desc_k(sb + S_KR, kk, 8192), desc_k(sb + S_K, kk, 8192), id64, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; kk++)
-                mma_ss(tmem + T_P, desc_k(sb + S_Q, kk, 8192), desc_k(sb + S_K, kk, 8192), id64, kk > 0);
-            mma_commit(bar_mma);
-        }
         if (!(ok = wait_all(bar_mma, mph++ & 1, abort_flag, p))) break;
         tc_fence_after();
         // N = Diag(beta) tril_strict(A) in fp32; P_m = tril(P) in bf16 (rows t = lanes 0..63)
