@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dq_kernel(const __grid_const
 // ================================================================ dk / dv pass
 // smem: q | k | v | dO | log alpha x 2 | G high (bf16) | G low | P_m | D_m | exchange | barriers
 constexpr int B_Q = 0, B_K = TB, B_V = 2 * TB, B_DO = 3 * TB, B_LA = 4 * TB, B_GS = 4 * TB + 2 * LAB,
-              B_GL = B_GS + GSB, B_PM = B_GL + GSB, B_DM = B_PM + PB, B_X = B_DM + PB, B_BAR = B_X + 2048;
+              B_GL = B_GS + GSB, B_PM = B_GL + GSB, B_DM = B_PM + PB, B_X = B_DM + PB, B_BAR = B_X + 6 * D * 4;
 constexpr int B_SMEM = B_BAR + 64 + 1024;
 // TMEM: G 0..127, dG 128..255, P 256..319, D 320..383, dK^T 384..447, dV^T 448..511
 constexpr uint32_t TB_G = 0, TB_DG = 128, TB_P = 256, TB_D = 320, TB_K = 384, TB_V = 448;
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dkdv_kernel(const __grid_con
     const uint32_t bar_l[2] = {smem_u32(&bars[3]), smem_u32(&bars[4])};
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + B_BAR + 48);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + B_BAR + 52);
-    float* xch = reinterpret_cast<float*>(sm + B_X);  // [2][D]: per-half sums
+    float* xch = reinterpret_cast<float*>(sm + B_X);  // [6][D]: gate quarter sums, b_C, second-half sum
     const CUtensorMap* maps[4] = {&p.tm_q, &p.tm_k, &p.tm_v, &p.tm_do};
     const uint32_t dsts[4] = {sb + B_Q, sb + B_K, sb + B_V, sb + B_DO};
     Pending pn;
@@ -493,27 +493,75 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dkdv_kernel(const __grid_con
             asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.k + row0 * D), "r"(nval * D * 2)
                          : "memory");
         }
-        // gate: Qh = q e^{b_t - b_C}, Kh = k e^{b_C - b_t} in place for this half's tokens
-        float bC = 0.f, pre = 0.f, part1 = 0.f;
+        // gate: Qh = q e^{b_t - b_C}, Kh = k e^{b_C - b_t} in place.  Thread (channel pair gp,
+        // token quarter gq) takes channels 2gp, 2gp + 1 over tokens 16 gq .. 16 gq + 15 (packed
+        // pairs); the quarter sums of log alpha give each quarter's prefix, b_C and the sum over
+        // the second half (tokens 32..63) that the epilogue starts from.
         if (p.gate) {
-            xch[hf * D + d] = half_total(la, d, hf);
+            const int gp = tid & 63, gq = tid >> 6, ch = 2 * gp;
+            float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll 8
+            for (int t = 16 * gq; t < 16 * gq + 16; t++) {
+                const float2 x = *reinterpret_cast<const float2*>(la + t * D + ch);
+                s2.x += x.x;
+                s2.y += x.y;
+            }
+            *reinterpret_cast<float2*>(xch + gq * D + ch) = s2;
             __syncthreads();
-            bC = xch[d] + xch[D + d];
-            pre = hf ? xch[d] : 0.f;
-            part1 = xch[D + d];  // tokens 32..63
-            strong |= bC < kStrongLog;
-            float b = pre;
+            float2 b2 = make_float2(0.f, 0.f), bc2 = b2;
+            float2 q[4];
+#pragma unroll
+            for (int g = 0; g < 4; g++) {
+                q[g] = *reinterpret_cast<const float2*>(xch + g * D + ch);
+                if (g < gq) {
+                    b2.x += q[g].x;
+                    b2.y += q[g].y;
+                }
+                bc2.x += q[g].x;
+                bc2.y += q[g].y;
+            }
+            if (gq == 0) {
+                *reinterpret_cast<float2*>(xch + 4 * D + ch) = bc2;
+                *reinterpret_cast<float2*>(xch + 5 * D + ch) = make_float2(q[2].x + q[3].x, q[2].y + q[3].y);
+            }
+            strong |= fminf(bc2.x, bc2.y) < kStrongLog;
             uint8_t* qt = sm + B_Q;
             uint8_t* kt = sm + B_K;
 #pragma unroll 4
-            for (int t = 32 * hf; t < 32 * hf + 32; t++) {
-                b += la[t * D + d];
-                const uint32_t o = tile_off(t, d, 8192);
-                uint16_t* eq = reinterpret_cast<uint16_t*>(qt + o);
-                uint16_t* ek = reinterpret_cast<uint16_t*>(kt + o);
-                *eq = f2bf(bf2f(*eq) * ex2f((b - bC) * kLog2e));
-                *ek = f2bf(bf2f(*ek) * ex2f((bC - b) * kLog2e));
+            for (int t = 16 * gq; t < 16 * gq + 16; t++) {
+                const float2 x = *reinterpret_cast<const float2*>(la + t * D + ch);
+                b2.x += x.x;
+                b2.y += x.y;
+                const uint32_t o = tile_off(t, ch, 8192);
+                uint32_t* eq = reinterpret_cast<uint32_t*>(qt + o);
+                uint32_t* ek = reinterpret_cast<uint32_t*>(kt + o);
+                const float u0 = (b2.x - bc2.x) * kLog2e, u1 = (b2.y - bc2.y) * kLog2e;
+                const float2 qf = unpack_bf16x2(*eq), kf = unpack_bf16x2(*ek);
+                *eq = pack_bf16x2(qf.x * ex2f(u0), qf.y * ex2f(u1));
+                *ek = pack_bf16x2(kf.x * ex2f(-u0), kf.y * ex2f(-u1));
             }
+        }
+        fence_proxy_async_smem();  // the factors, read by the products below
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // b_C of key channel d (the state decay) and its sum of log alpha over tokens 32..63
+        const float bC = p.gate ? xch[4 * D + d] : 0.f, part1 = p.gate ? xch[5 * D + d] : 0.f;
+        if (tid == 0) {
+            constexpr uint32_t id64 = make_idesc_bf16(128, 64, 0, 0);
+            // P = Qh Kh^T and D = dO V^T (M = 128: rows 64..127 read past the tile and are ignored)
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + TB_P, desc_k(sb + B_Q, kk, 8192), desc_k(sb + B_K, kk, 8192), id64, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + TB_D, desc_k(sb + B_DO, kk, 8192), desc_k(sb + B_V, kk, 8192), id64, kk > 0);
+            // dG = Qh^T dO
+            constexpr uint32_t id128 = make_idesc_bf16(128, 128, 1, 1);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; kk++)
+                mma_ss(tmem + TB_DG, desc_mn(sb + B_Q, kk, 8192), desc_mn(sb + B_DO, kk, 8192), id128, kk > 0);
+            mma_commit(bar_mma);
         }
         // bf16 high and low copies of G_c into shared memory: columns [64 hf, 64 hf + 64) of row d
 #pragma unroll 1
@@ -534,26 +582,8 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dkdv_kernel(const __grid_con
                 *reinterpret_cast<uint4*>(sm + B_GL + o) = wl;
             }
         }
-        fence_proxy_async_smem();
+        fence_proxy_async_smem();  // G's high and low copies, read by the second product group
         tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid == 0) {
-            constexpr uint32_t id64 = make_idesc_bf16(128, 64, 0, 0);
-            // P = Qh Kh^T and D = dO V^T (M = 128: rows 64..127 read past the tile and are ignored)
-#pragma unroll
-            for (int kk = 0; kk < D / 16; kk++)
-                mma_ss(tmem + TB_P, desc_k(sb + B_Q, kk, 8192), desc_k(sb + B_K, kk, 8192), id64, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; kk++)
-                mma_ss(tmem + TB_D, desc_k(sb + B_DO, kk, 8192), desc_k(sb + B_V, kk, 8192), id64, kk > 0);
-            // dG = Qh^T dO
-            constexpr uint32_t id128 = make_idesc_bf16(128, 128, 1, 1);
-#pragma unroll
-            for (int kk = 0; kk < C / 16; kk++)
-                mma_ss(tmem + TB_DG, desc_mn(sb + B_Q, kk, 8192), desc_mn(sb + B_DO, kk, 8192), id128, kk > 0);
-            mma_commit(bar_mma);
-        }
         if (!(ok = wait_all(bar_mma, 0, abort_flag, p))) break;
         tc_fence_after();
         if (d < C) {
