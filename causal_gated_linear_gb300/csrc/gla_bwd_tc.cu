@@ -134,18 +134,6 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
     lo = pack_bf16x2(x0 - h.x, x1 - h.y);
 }
 
-// Sum of log alpha of channel d over the 32 tokens of half `hf` of the chunk (rows
-// past the sequence end arrive as zeros).
-__device__ __forceinline__ float half_total(const float* la, int d, int hf) {
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll 8
-    for (int t = 32 * hf; t < 32 * hf + 32; t += 2) {
-        s0 += la[t * D + d];
-        s1 += la[(t + 1) * D + d];
-    }
-    return s0 + s1;
-}
-
 // Columns [32 hf, 32 hf + 32) of rows 0..63 of a 64x64 fp32 accumulator in TMEM
 // (row t = lane t), masked to i <= t, as bf16 into a [t][i] tile.  Warps whose
 // lanes are 0..63.
@@ -196,7 +184,7 @@ constexpr int kThr2 = 2 * D;
 // ================================================================ dq pass
 // smem: k | v | dO | log alpha x 2 | D_m | exchange | barriers
 constexpr int A_K = 0, A_V = TB, A_DO = 2 * TB, A_LA = 3 * TB, A_DM = 3 * TB + 2 * LAB, A_X = A_DM + PB,
-              A_BAR = A_X + 2048;
+              A_BAR = A_X + 6 * D * 4;
 constexpr int A_SMEM = A_BAR + 64 + 1024;
 // TMEM: S 0..127, dS 128..255, bf16 S' high 256..319, D 320..383, dQ^T 384..447, S' low 448..511
 constexpr uint32_t TA_S = 0, TA_DS = 128, TA_SB = 256, TA_D = 320, TA_Q = 384, TA_SL = 448;
@@ -213,7 +201,7 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dq_kernel(const __grid_const
     const uint32_t bar_l[2] = {smem_u32(&bars[3]), smem_u32(&bars[4])};
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + A_BAR + 48);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + A_BAR + 52);
-    float* xch = reinterpret_cast<float*>(sm + A_X);  // [2][D]: per-half sums of log alpha
+    float* xch = reinterpret_cast<float*>(sm + A_X);  // [6][D]: quarter sums of log alpha, b_C, first-half sum
     const CUtensorMap* maps[3] = {&p.tm_k, &p.tm_v, &p.tm_do};
     const uint32_t dsts[3] = {sb + A_K, sb + A_V, sb + A_DO};
     Pending pn;
@@ -270,32 +258,63 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dq_kernel(const __grid_const
             }
         }
         const int nval = min(C, L - c * C);
-        // gate: b_C of channel d, Kh = k e^{b_C - b_t} in place for this half's tokens
-        float bC = 0.f, pre = 0.f;
+        if (tid == 0) {
+            // D = dO V^T (M = 128, rows 64..127 read past the dO tile and are ignored): it needs
+            // no gate factor, so it runs while the gate works
+            tc_fence_after();
+            constexpr uint32_t idD = make_idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + TA_D, desc_k(sb + A_DO, kk, 8192), desc_k(sb + A_V, kk, 8192), idD, kk > 0);
+        }
+        // gate: Kh = k e^{b_C - b_t} in place.  Thread (channel pair gp, token quarter gq) takes
+        // channels 2gp, 2gp + 1 over tokens 16 gq .. 16 gq + 15 (packed pairs); the quarter sums
+        // give each quarter's prefix, b_C and the first half's sum (the epilogue's start)
         if (p.gate) {
-            xch[hf * D + d] = half_total(la, d, hf);
+            const int gp = tid & 63, gq = tid >> 6, ch = 2 * gp;
+            float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll 8
+            for (int t = 16 * gq; t < 16 * gq + 16; t++) {
+                const float2 x = *reinterpret_cast<const float2*>(la + t * D + ch);
+                s2.x += x.x;
+                s2.y += x.y;
+            }
+            *reinterpret_cast<float2*>(xch + gq * D + ch) = s2;
             __syncthreads();
-            bC = xch[d] + xch[D + d];
-            pre = hf ? xch[d] : 0.f;
-            float b = pre;
+            float2 b2 = make_float2(0.f, 0.f), bc2 = b2;
+            float2 q[4];
+#pragma unroll
+            for (int g = 0; g < 4; g++) {
+                q[g] = *reinterpret_cast<const float2*>(xch + g * D + ch);
+                if (g < gq) {
+                    b2.x += q[g].x;
+                    b2.y += q[g].y;
+                }
+                bc2.x += q[g].x;
+                bc2.y += q[g].y;
+            }
+            if (gq == 0) {
+                *reinterpret_cast<float2*>(xch + 4 * D + ch) = bc2;
+                *reinterpret_cast<float2*>(xch + 5 * D + ch) = make_float2(q[0].x + q[1].x, q[0].y + q[1].y);
+            }
             uint8_t* kt = sm + A_K;
 #pragma unroll 4
-            for (int t = 32 * hf; t < 32 * hf + 32; t++) {
-                b += la[t * D + d];
-                uint16_t* e = reinterpret_cast<uint16_t*>(kt + tile_off(t, d, 8192));
-                *e = f2bf(bf2f(*e) * ex2f((bC - b) * kLog2e));
+            for (int t = 16 * gq; t < 16 * gq + 16; t++) {
+                const float2 x = *reinterpret_cast<const float2*>(la + t * D + ch);
+                b2.x += x.x;
+                b2.y += x.y;
+                uint32_t* e = reinterpret_cast<uint32_t*>(kt + tile_off(t, ch, 8192));
+                const float2 kf = unpack_bf16x2(*e);
+                *e = pack_bf16x2(kf.x * ex2f((bc2.x - b2.x) * kLog2e), kf.y * ex2f((bc2.y - b2.y) * kLog2e));
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+        // b_C of key channel d and the log-gate sum before this thread's half of the tokens
+        const float bC = p.gate ? xch[4 * D + d] : 0.f, pre = (p.gate && hf) ? xch[5 * D + d] : 0.f;
         if (tid == 0) {
-            // D = dO V^T (M = 128, rows 64..127 read past the dO tile and are ignored)
-            constexpr uint32_t idD = make_idesc_bf16(128, 64, 0, 0);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; kk++)
-                mma_ss(tmem + TA_D, desc_k(sb + A_DO, kk, 8192), desc_k(sb + A_V, kk, 8192), idD, kk > 0);
             // dS = Kh^T V (both MN-major)
             constexpr uint32_t idS = make_idesc_bf16(128, 128, 1, 1);
 #pragma unroll
