@@ -158,19 +158,31 @@ __device__ __forceinline__ void mask_half(uint32_t taddr, uint8_t* dst, int t, i
     }
 }
 
+// Bulk copy of `bytes` contiguous bytes, global -> shared, completing on an mbarrier
+// (both addresses 16-byte aligned, `bytes` a multiple of 16: the entry point checks the
+// buffers' alignment and every row block here is a multiple of 256 bytes).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // Loads issued by thread 0 and not yet waited for, so that a CTA that gives up
 // waits for them before it leaves: tiles (one barrier) and log alpha (two).
 struct Pending {
     int tiles_issued = 0, tiles_done = 0;
     int la_issued[2] = {0, 0}, la_done[2] = {0, 0};
+    int epi_issued = 0, epi_done = 0;  // the dk/dv pass's epilogue rows (bar_e)
 };
 
-__device__ __forceinline__ void drain(const Pending& pn, uint32_t bar_t, const uint32_t* bar_l, uint32_t bar_drain) {
+__device__ __forceinline__ void drain(const Pending& pn, uint32_t bar_t, const uint32_t* bar_l, uint32_t bar_drain,
+                                      uint32_t bar_e = 0) {
     volatile int no_abort = 0;
     if (threadIdx.x == 0) {
         for (int n = pn.tiles_done; n < pn.tiles_issued; n++) mbar_wait(bar_t, n & 1, &no_abort, nullptr);
         for (int b = 0; b < 2; b++)
             for (int n = pn.la_done[b]; n < pn.la_issued[b]; n++) mbar_wait(bar_l[b], n & 1, &no_abort, nullptr);
+        for (int n = pn.epi_done; n < pn.epi_issued; n++) mbar_wait(bar_e, n & 1, &no_abort, nullptr);
         mma_commit(bar_drain);
         mbar_wait(bar_drain, 0, &no_abort, nullptr);
     }
@@ -439,6 +451,7 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dkdv_kernel(const __grid_con
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + B_BAR);
     const uint32_t bar_t = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[1]), bar_drain = smem_u32(&bars[2]);
     const uint32_t bar_l[2] = {smem_u32(&bars[3]), smem_u32(&bars[4])};
+    const uint32_t bar_e = smem_u32(&bars[5]);  // the epilogue's rows of q, k and dq
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + B_BAR + 48);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + B_BAR + 52);
     float* xch = reinterpret_cast<float*>(sm + B_X);  // [6][D]: gate quarter sums, b_C, second-half sum
@@ -451,6 +464,7 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dkdv_kernel(const __grid_con
         mbar_init(bar_drain, 1);
         mbar_init(bar_l[0], 1);
         mbar_init(bar_l[1], 1);
+        mbar_init(bar_e, 1);
         *abort_flag = 0;
         mbar_fence_init();
         if (N > 0) {
@@ -501,8 +515,8 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dkdv_kernel(const __grid_con
             }
         }
         const int nval = min(C, L - c * C);
-        // the epilogue reads this chunk's rows of q, k and dq from global memory: bring them
-        // into L2 now (contiguous blocks of nval rows), while the products run
+        // the epilogue reads this chunk's rows of q, k and dq: bring them into L2 now, while
+        // the products run (they are copied to shared memory once the products are done)
         if (tid == 0 && p.dla) {
             const long row0 = (long)bh * L + (long)c * C;
             asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.dq + row0 * D), "r"(nval * D * 4)
@@ -649,11 +663,21 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dkdv_kernel(const __grid_con
         // dv_i = dV^T[j = d][i], and the gate gradient's suffix sums
         {
             const long row0 = (long)bh * L + (long)c * C;
+            // the gate gradient needs this chunk's rows of q, k and dq: one bulk copy each into
+            // the space of G's bf16 copies (free until the next chunk's split), while the dk and
+            // dv stores go out
+            uint16_t* qs = reinterpret_cast<uint16_t*>(sm + B_GS);
+            uint16_t* ks = qs + C * D;
+            float* dqs = reinterpret_cast<float*>(sm + B_GL);
+            if (tid == 0 && p.dla) {
+                mbar_arrive_expect_tx(bar_e, nval * D * 8);
+                bulk_load(sb + B_GS, p.q + row0 * D, nval * D * 2, bar_e);
+                bulk_load(sb + B_GS + C * D * 2, p.k + row0 * D, nval * D * 2, bar_e);
+                bulk_load(sb + B_GL, p.dq + row0 * D, nval * D * 4, bar_e);
+                pn.epi_issued++;
+            }
             float* dkp = p.dk + row0 * D + d;
             float* dvp = p.dv + row0 * D + d;
-            const float* dqp = p.dq + row0 * D + d;
-            const uint16_t* qp = p.q + row0 * D + d;
-            const uint16_t* kp = p.k + row0 * D + d;
             float r_suf = hf ? 0.f : part1;  // b_C - b_i: sum of log alpha over (i, C)
             float gl[32];                    // suffix of q dq - k dk inside this half
             float loc = 0.f;
@@ -661,37 +685,29 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dkdv_kernel(const __grid_con
             tmem_ld32(lane + TB_K + hf * 32, rk);
             tmem_ld32(lane + TB_V + hf * 32, rv);
             tmem_wait_ld();
-            // groups of 8 tokens, last to first: a group's q, k and dq are loaded together
-            // (read-only path) before its stores, so the loads do not wait one by one
 #pragma unroll
-            for (int g = 3; g >= 0; g--) {
-                float qv[8], kv[8], dqv[8];
-                if (p.dla) {
-#pragma unroll
-                    for (int u = 0; u < 8; u++) {
-                        const int i = hf * 32 + g * 8 + u;
-                        const bool in = i < nval;
-                        qv[u] = in ? bf2f(__ldg(qp + (long)i * D)) : 0.f;
-                        kv[u] = in ? bf2f(__ldg(kp + (long)i * D)) : 0.f;
-                        dqv[u] = in ? __ldg(dqp + (long)i * D) : 0.f;
-                    }
+            for (int e = 31; e >= 0; e--) {
+                const int i = hf * 32 + e;
+                const float f = p.gate ? ex2f(r_suf * kLog2e) : 1.f;
+                const float dki = __uint_as_float(rk[e]) * f;
+                rk[e] = __float_as_uint(dki);
+                if (i < nval) {
+                    dkp[(long)i * D] = dki;
+                    dvp[(long)i * D] = __uint_as_float(rv[e]);
                 }
+                if (p.gate) r_suf += la[i * D + d];
+            }
+            if (p.dla) {
+                if (!(ok = wait_all(bar_e, it & 1, abort_flag, p))) break;
+                if (tid == 0) pn.epi_done++;
 #pragma unroll
-                for (int u = 7; u >= 0; u--) {
-                    const int e = g * 8 + u;
+                for (int e = 31; e >= 0; e--) {
                     const int i = hf * 32 + e;
                     gl[e] = 0.f;
                     if (i < nval) {
-                        const float f = p.gate ? ex2f(r_suf * kLog2e) : 1.f;
-                        const float dki = __uint_as_float(rk[e]) * f;
-                        dkp[(long)i * D] = dki;
-                        dvp[(long)i * D] = __uint_as_float(rv[e]);
-                        if (p.dla) {
-                            loc += qv[u] * dqv[u] - kv[u] * dki;
-                            gl[e] = loc;
-                        }
+                        loc += bf2f(qs[i * D + d]) * dqs[i * D + d] - bf2f(ks[i * D + d]) * __uint_as_float(rk[e]);
+                        gl[e] = loc;
                     }
-                    if (p.gate) r_suf += la[i * D + d];
                 }
             }
             if (p.dla) {
@@ -728,7 +744,7 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dkdv_kernel(const __grid_con
         tc_fence_before();
         __syncthreads();
     }
-    if (!ok) drain(pn, bar_t, bar_l, bar_drain);
+    if (!ok) drain(pn, bar_t, bar_l, bar_drain, bar_e);
     const bool mark = __syncthreads_or(strong) != 0;
     if (ok && !mark && p.dinit) {
         float* di = p.dinit + ((long)bh * D + d) * D;
