@@ -92,8 +92,8 @@ def delta_bytes(w) -> float:
 
 def delta_chunk_flops(w) -> float:
     """Delta rule in chunk form, tensor-core flops per chunk and head: A = Kr Kh^T, P = Qh Kh^T,
-    M V, M Kr and P U (2 C^2 d each), W S', Qh S' and Kh^T U (2 C dk dv each)."""
-    per_chunk = 5 * 2 * C * C * w.dk + 3 * 2 * C * w.dk * w.dv
+    M V' and P U (2 C^2 d each), Kr S', Qh S' and Kh^T U (2 C dk dv each)."""
+    per_chunk = 4 * 2 * C * C * w.dk + 3 * 2 * C * w.dk * w.dv
     return float(w.B * w.H * math.ceil(w.L / C) * per_chunk)
 
 

@@ -12,14 +12,16 @@
 // Unrolling the recurrence, the chunk's writes U solve the unit lower-triangular
 // system (I + Diag(beta) tril_strict(A)) U = Diag(beta) (V - Kr S'), so with
 // T = (I + Diag(beta) tril_strict(A))^{-1} and M = T Diag(beta):
-//   U = M V - (M Kr) S'
+//   U = M V',  V' = V - Kr S'
 //   O = Qh S' + tril(Qh Kh^T) U            (inclusive diagonal)
 //   S_C = S' + Kh^T U.
 // Every product is a tcgen05 MMA on 128-byte-swizzled bf16 tiles; T is the
 // inverse of a 64 x 64 unit lower-triangular matrix, computed in fp32 by blocked
 // forward substitution (16 x 16 diagonal blocks, then the off-diagonal blocks
 // level by level).  The state copy S' and the writes U enter their products as
-// bf16 high and low parts (x = hi + lo to ~2^-17).
+// bf16 high and low parts (x = hi + lo to ~2^-17); V' is formed in fp32 and
+// rounded once to bf16.  Kr S' needs only the gate and the state, so it runs
+// while the triangular inverse is computed.
 //
 // One CTA of 256 threads per (batch, head), d_k = d_v = 128: thread (d, hf) owns
 // key channel d (TMEM lane d) and half hf of the chunk's tokens / of the state's
@@ -67,7 +69,6 @@ __device__ __forceinline__ float ex2f(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 __device__ __forceinline__ uint16_t f2bf(float x) {
     __nv_bfloat16 h = __float2bfloat16_rn(x);
     return *reinterpret_cast<uint16_t*>(&h);
@@ -94,8 +95,8 @@ constexpr int S_Q = 0, S_K = TB, S_KR = 2 * TB, S_V = 3 * TB, S_LA = 4 * TB, S_S
               S_BETA = S_T + FB, S_X = S_BETA + C * 4, S_BAR = S_X + 5 * D * 4;
 constexpr int S_SMEM = S_BAR + 64 + 1024;
 static_assert(S_SMEM <= 227 * 1024, "shared memory budget");
-// TMEM: S 0..127, dS 128..255, U 256..383; 384..511 holds A and P (64 each), then M Kr, then O^T
-constexpr uint32_t T_S = 0, T_DS = 128, T_U = 256, T_A = 384, T_P = 448, T_W = 384, T_O = 384;
+// TMEM: S 0..127, dS 128..255, Kr S' then U 256..383; 384..511 holds A and P (64 each), then O^T
+constexpr uint32_t T_S = 0, T_DS = 128, T_U = 256, T_A = 384, T_P = 448, T_O = 384;
 
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          const DeltaTcParams& p) {
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
     const int L = p.L, N = p.nchunks;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S_BAR);
     const uint32_t bar_t = smem_u32(&bars[0]), bar_l = smem_u32(&bars[1]), bar_mma = smem_u32(&bars[2]),
-                   bar_drain = smem_u32(&bars[3]);
+                   bar_drain = smem_u32(&bars[3]), bar_x = smem_u32(&bars[4]);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S_BAR + 40);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S_BAR + 44);
     float* xch = reinterpret_cast<float*>(sm + S_X);
@@ -190,6 +191,7 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
         mbar_init(bar_l, 1);
         mbar_init(bar_mma, 1);
         mbar_init(bar_drain, 1);
+        mbar_init(bar_x, 1);
         *abort_flag = 0;
         mbar_fence_init();
         load_tiles(p, bar_t, sb, 0, bh);
@@ -311,14 +313,23 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
                 mma_ss(tmem + T_P, desc_k(sb + S_Q, kk, 8192), desc_k(sb + S_K, kk, 8192), id64, kk > 0);
             mma_commit(bar_mma);
         }
-        // S' = e^{b_C} S: bf16 high and low copies in shared memory ([d][j], MN-major operand)
+        // S' = e^{b_C} S, where S = S' + dS of the previous chunk (its state update is done here):
+        // fp32 in TMEM, bf16 high and low copies in shared memory ([d][j], MN-major operand)
         {
             const float g = p.gate ? ex2f(bC * kLog2e) : 1.f;
 #pragma unroll 1
             for (int h = 2 * hf; h < 2 * hf + 2; h++) {
                 uint32_t r[32];
                 tmem_ld32(lane + T_S + h * 32, r);
-                tmem_wait_ld();
+                if (c > 0) {
+                    uint32_t rd[32];
+                    tmem_ld32(lane + T_DS + h * 32, rd);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; e++) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(rd[e]));
+                } else {
+                    tmem_wait_ld();
+                }
 #pragma unroll
                 for (int e8 = 0; e8 < 4; e8++) {
                     uint4 wh, wl;
@@ -348,6 +359,18 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
         tc_fence_before();
         if (!(ok = wait_all(bar_mma, mph++ & 1, abort_flag, p))) break;
         tc_fence_after();
+        if (tid == 0) {
+            // X = Kr S' (A = Kr K-major, B = S' high and low MN-major, N = 128; M = 128: rows
+            // 64..127 read past the tile and are ignored); it runs during the inverse below
+            constexpr uint32_t id128 = make_idesc_bf16(128, 128, 0, 1);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + T_U, desc_k(sb + S_KR, kk, 8192), desc_mn(sb + S_SH, kk, 16384), id128, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + T_U, desc_k(sb + S_KR, kk, 8192), desc_mn(sb + S_SL, kk, 16384), id128, 1);
+            mma_commit(bar_x);
+        }
         // N = Diag(beta) tril_strict(A) in fp32; P_m = tril(P) in bf16 (rows t = lanes 0..63)
         if (d < C) {
             const int t = d;
@@ -375,9 +398,11 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
         }
         __syncthreads();
         unit_lower_inverse(Nf, Tf, tid);
-        // M = T Diag(beta) in bf16 ([t][i], K-major operand); thread (t, half of the columns)
-        if (tid < 2 * C) {
-            const int t = tid & (C - 1), h2 = tid >> 6;
+        if (!(ok = wait_all(bar_x, c & 1, abort_flag, p))) break;
+        tc_fence_after();
+        if (d >= C) {
+            // M = T Diag(beta) in bf16 ([t][i], K-major operand); thread (t, half of the columns)
+            const int t = d - C, h2 = hf;
 #pragma unroll
             for (int k8 = 0; k8 < 4; k8++) {
                 float x[8];
@@ -394,41 +419,27 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
                 w.w = pack_bf16x2(x[6], x[7]);
                 *reinterpret_cast<uint4*>(sm + S_M + sw128_offset(t, h2 * 32 + k8 * 8)) = w;
             }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid == 0) {
-            // U = M V and W = M Kr (A = M K-major, B = V / Kr MN-major), N = 128
-            constexpr uint32_t id128 = make_idesc_bf16(128, 128, 0, 1);
-#pragma unroll
-            for (int kk = 0; kk < C / 16; kk++)
-                mma_ss(tmem + T_U, desc_k(sb + S_M, kk, 8192), desc_mn(sb + S_V, kk, 8192), id128, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < C / 16; kk++)
-                mma_ss(tmem + T_W, desc_k(sb + S_M, kk, 8192), desc_mn(sb + S_KR, kk, 8192), id128, kk > 0);
-            mma_commit(bar_mma);
-        }
-        if (!(ok = wait_all(bar_mma, mph++ & 1, abort_flag, p))) break;
-        tc_fence_after();
-        // -W in bf16 ([t][d], K-major operand) over N's buffer (rows t = lanes 0..63)
-        if (d < C) {
+        } else {
+            // V' = V - X in bf16, in place over V ([t][j], MN-major operand; rows t = lanes 0..63)
             const int t = d;
 #pragma unroll 1
             for (int h = 2 * hf; h < 2 * hf + 2; h++) {
                 uint32_t r[32];
-                tmem_ld32(lane + T_W + h * 32, r);
+                tmem_ld32(lane + T_U + h * 32, r);
                 tmem_wait_ld();
 #pragma unroll
                 for (int k8 = 0; k8 < 4; k8++) {
-                    uint4 w;
+                    uint4* pv = reinterpret_cast<uint4*>(sm + S_V + tile_off(t, h * 32 + k8 * 8, 8192));
+                    const uint4 vv = *pv;
                     const float* x = reinterpret_cast<const float*>(r + k8 * 8);
-                    w.x = pack_bf16x2(-x[0], -x[1]);
-                    w.y = pack_bf16x2(-x[2], -x[3]);
-                    w.z = pack_bf16x2(-x[4], -x[5]);
-                    w.w = pack_bf16x2(-x[6], -x[7]);
-                    *reinterpret_cast<uint4*>(sm + S_N + tile_off(t, h * 32 + k8 * 8, 8192)) = w;
+                    const float2 v0 = unpack_bf16x2(vv.x), v1 = unpack_bf16x2(vv.y), v2 = unpack_bf16x2(vv.z),
+                                 v3 = unpack_bf16x2(vv.w);
+                    uint4 w;
+                    w.x = pack_bf16x2(v0.x - x[0], v0.y - x[1]);
+                    w.y = pack_bf16x2(v1.x - x[2], v1.y - x[3]);
+                    w.z = pack_bf16x2(v2.x - x[4], v2.y - x[5]);
+                    w.w = pack_bf16x2(v3.x - x[6], v3.y - x[7]);
+                    *pv = w;
                 }
             }
         }
@@ -437,14 +448,11 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
         __syncthreads();
         tc_fence_after();
         if (tid == 0) {
-            // U += (-W) (S'_hi + S'_lo): A = -W [t][d] K-major, B = S' [d][j] MN-major
+            // U = M V' (A = M K-major, B = V' MN-major), N = 128
             constexpr uint32_t id128 = make_idesc_bf16(128, 128, 0, 1);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; kk++)
-                mma_ss(tmem + T_U, desc_k(sb + S_N, kk, 8192), desc_mn(sb + S_SH, kk, 16384), id128, 1);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; kk++)
-                mma_ss(tmem + T_U, desc_k(sb + S_N, kk, 8192), desc_mn(sb + S_SL, kk, 16384), id128, 1);
+            for (int kk = 0; kk < C / 16; kk++)
+                mma_ss(tmem + T_U, desc_k(sb + S_M, kk, 8192), desc_mn(sb + S_V, kk, 8192), id128, kk > 0);
             mma_commit(bar_mma);
         }
         if (!(ok = wait_all(bar_mma, mph++ & 1, abort_flag, p))) break;
@@ -507,7 +515,8 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
             load_tiles(p, bar_t, sb, c + 1, bh);
             tiles_issued++;
         }
-        // output: thread (j = d, half hf of the tokens) writes o[t][j]; state S = S' + dS
+        // output: thread (j = d, half hf of the tokens) writes o[t][j]; the state update
+        // S = S' + dS is done with the next chunk's decay
         {
             uint32_t r[32];
             tmem_ld32(lane + T_O + hf * 32, r);
@@ -523,17 +532,6 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
                         static_cast<uint16_t*>(p.out)[idx] = f2bf(__uint_as_float(r[e]));
                 }
             }
-#pragma unroll 1
-            for (int h = 2 * hf; h < 2 * hf + 2; h++) {
-                uint32_t rs[32], rd[32];
-                tmem_ld32(lane + T_S + h * 32, rs);
-                tmem_ld32(lane + T_DS + h * 32, rd);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; e++) rs[e] = __float_as_uint(__uint_as_float(rs[e]) + __uint_as_float(rd[e]));
-                tmem_st32(lane + T_S + h * 32, rs);
-            }
-            tmem_wait_st();
         }
         tc_fence_before();
         __syncthreads();
@@ -550,12 +548,21 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
     }
     const bool mark = __syncthreads_or(strong) != 0;
     if (ok && !mark && p.final_state) {
+        // S = S' + dS of the last chunk (the initial state when there is none)
         float* fs = p.final_state + ((long)bh * D + d) * D;
 #pragma unroll 1
         for (int h = 2 * hf; h < 2 * hf + 2; h++) {
             uint32_t r[32];
             tmem_ld32(lane + T_S + h * 32, r);
-            tmem_wait_ld();
+            if (N > 0) {
+                uint32_t rd[32];
+                tmem_ld32(lane + T_DS + h * 32, rd);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; e++) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(rd[e]));
+            } else {
+                tmem_wait_ld();
+            }
 #pragma unroll
             for (int e = 0; e < 32; e++) fs[h * 32 + e] = __uint_as_float(r[e]);
         }

@@ -199,7 +199,7 @@ int gla_delta_fwd(const void* q, const void* k, const void* v, const float* beta
  * ("linear-attention" blog, Delta attention / Prefill: the writes of a chunk
  * solve one unit lower-triangular system): per chunk of 64 tokens, with
  * A = (k e^{b_t-b_C}) (k e^{b_C-b_i})^T, T = (I + Diag(beta) tril_strict(A))^{-1}
- * and M = T Diag(beta), the writes are U = M V - (M Kr) S' and
+ * and M = T Diag(beta), the writes are U = M (V - Kr S') and
  * o = Qh S' + tril(Qh Kh^T) U, S_C = S' + Kh^T U (bf16 tensor-core products,
  * fp32 accumulation and state; T in fp32).  Heads with a chunk over which a
  * channel decays by more than e^-64 are recomputed by the token-by-token

@@ -90,4 +90,4 @@ def test_backward_bytes_and_chunk_flops():
 def test_delta_bytes_and_chunk_flops():
     # 128 heads x (4096 tokens x (q, k, v 768 + beta 4 + log alpha 512 + out 256) + final state 64 KB)
     assert bench.delta_bytes(synth.DELTA) == 128 * (4096 * 1540 + 128 * 128 * 4)
-    assert bench.delta_chunk_flops(synth.DELTA) == 128 * 64 * (5 * 2 * 64 * 64 * 128 + 3 * 2 * 64 * 128 * 128)
+    assert bench.delta_chunk_flops(synth.DELTA) == 128 * 64 * (4 * 2 * 64 * 64 * 128 + 3 * 2 * 64 * 128 * 128)
