@@ -54,7 +54,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kStrongLog = -64.f;
 
 struct DeltaTcParams {
-    CUtensorMap tm_q, tm_k, tm_v, tm_la;
+    CUtensorMap tm_q, tm_k, tm_v, tm_la, tm_out;
     const float* beta;
     const float* init_state;
     void* out;
@@ -62,6 +62,7 @@ struct DeltaTcParams {
     unsigned* err;
     unsigned long long wait_ns;
     int L, nchunks, gate, out_f32;
+    int out_tma;  // bf16 output staged in shared memory and written by bulk-tensor stores
 };
 
 __device__ __forceinline__ float ex2f(float x) {
@@ -95,8 +96,9 @@ constexpr int S_Q = 0, S_K = TB, S_KR = 2 * TB, S_V = 3 * TB, S_LA = 4 * TB, S_S
               S_BETA = S_T + FB, S_X = S_BETA + C * 4, S_BAR = S_X + 5 * D * 4;
 constexpr int S_SMEM = S_BAR + 64 + 1024;
 static_assert(S_SMEM <= 227 * 1024, "shared memory budget");
-// TMEM: S 0..127, dS 128..255, Kr S' then U 256..383; 384..511 holds A and P (64 each), then O^T
-constexpr uint32_t T_S = 0, T_DS = 128, T_U = 256, T_A = 384, T_P = 448, T_O = 384;
+// TMEM: S 0..127, O^T 128..191; 256..383 holds in turn Kr S', U and dS (read by the next chunk's
+// state update before its Kr S' is issued); A and P 384..511 (64 each)
+constexpr uint32_t T_S = 0, T_O = 128, T_U = 256, T_DS = 256, T_A = 384, T_P = 448;
 
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          const DeltaTcParams& p) {
@@ -312,6 +314,8 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
             for (int kk = 0; kk < D / 16; kk++)
                 mma_ss(tmem + T_P, desc_k(sb + S_Q, kk, 8192), desc_k(sb + S_K, kk, 8192), id64, kk > 0);
             mma_commit(bar_mma);
+            // the previous chunk's output staging (N's buffer) has been read by its stores
+            if (p.out_tma) bulk_wait_group_read0();
         }
         // S' = e^{b_C} S, where S = S' + dS of the previous chunk (its state update is done here):
         // fp32 in TMEM, bf16 high and low copies in shared memory ([d][j], MN-major operand)
@@ -361,7 +365,9 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
         tc_fence_after();
         if (tid == 0) {
             // X = Kr S' (A = Kr K-major, B = S' high and low MN-major, N = 128; M = 128: rows
-            // 64..127 read past the tile and are ignored); it runs during the inverse below
+            // 64..127 read past the tile and are ignored), then the state's share of the output,
+            // O^T = S'^T Qh^T (M = j: A = S' MN-major, B = Qh K-major); both run during the
+            // inverse below
             constexpr uint32_t id128 = make_idesc_bf16(128, 128, 0, 1);
 #pragma unroll
             for (int kk = 0; kk < D / 16; kk++)
@@ -370,6 +376,13 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
             for (int kk = 0; kk < D / 16; kk++)
                 mma_ss(tmem + T_U, desc_k(sb + S_KR, kk, 8192), desc_mn(sb + S_SL, kk, 16384), id128, 1);
             mma_commit(bar_x);
+            constexpr uint32_t idO = make_idesc_bf16(128, 64, 1, 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + T_O, desc_mn(sb + S_SH, kk, 16384), desc_k(sb + S_Q, kk, 8192), idO, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++)
+                mma_ss(tmem + T_O, desc_mn(sb + S_SL, kk, 16384), desc_k(sb + S_Q, kk, 8192), idO, 1);
         }
         // N = Diag(beta) tril_strict(A) in fp32; P_m = tril(P) in bf16 (rows t = lanes 0..63)
         if (d < C) {
@@ -484,14 +497,8 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
         __syncthreads();
         tc_fence_after();
         if (tid == 0) {
-            // O^T = S'^T Qh^T + U^T P_m^T  (M = j: A = S' / U MN-major, B = Qh / P_m K-major)
+            // O^T += U^T P_m^T  (M = j: A = U MN-major, B = P_m K-major)
             constexpr uint32_t idO = make_idesc_bf16(128, 64, 1, 0);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; kk++)
-                mma_ss(tmem + T_O, desc_mn(sb + S_SH, kk, 16384), desc_k(sb + S_Q, kk, 8192), idO, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; kk++)
-                mma_ss(tmem + T_O, desc_mn(sb + S_SL, kk, 16384), desc_k(sb + S_Q, kk, 8192), idO, 1);
 #pragma unroll
             for (int kk = 0; kk < C / 16; kk++)
                 mma_ss(tmem + T_O, desc_mn(sb + S_KR, kk, 8192), desc_k(sb + S_PM, kk, 8192), idO, 1);
@@ -515,26 +522,45 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
             load_tiles(p, bar_t, sb, c + 1, bh);
             tiles_issued++;
         }
-        // output: thread (j = d, half hf of the tokens) writes o[t][j]; the state update
+        // output: thread (j = d, half hf of the tokens) has o[t][j]; the state update
         // S = S' + dS is done with the next chunk's decay
         {
             uint32_t r[32];
             tmem_ld32(lane + T_O + hf * 32, r);
             tmem_wait_ld();
-            const long row0 = (long)bh * L + (long)c * C + hf * 32;
+            if (p.out_tma) {
+                // bf16 into N's buffer (free after the inverse) as two row-major [64][64] boxes,
+                // written out below by two bulk-tensor stores (rows past L are clipped)
+                uint16_t* ob = reinterpret_cast<uint16_t*>(sm + S_N + (d >> 6) * 8192) + (hf * 32) * 64 + (d & 63);
 #pragma unroll
-            for (int e = 0; e < 32; e++) {
-                if (hf * 32 + e < nval) {
-                    const long idx = (row0 + e) * D + d;
-                    if (p.out_f32)
-                        static_cast<float*>(p.out)[idx] = __uint_as_float(r[e]);
-                    else
-                        static_cast<uint16_t*>(p.out)[idx] = f2bf(__uint_as_float(r[e]));
+                for (int e = 0; e < 32; e++) ob[e * 64] = f2bf(__uint_as_float(r[e]));
+                fence_proxy_async_smem();
+            } else {
+                const long row0 = (long)bh * L + (long)c * C + hf * 32;
+#pragma unroll
+                for (int e = 0; e < 32; e++) {
+                    if (hf * 32 + e < nval) {
+                        const long idx = (row0 + e) * D + d;
+                        if (p.out_f32)
+                            static_cast<float*>(p.out)[idx] = __uint_as_float(r[e]);
+                        else
+                            static_cast<uint16_t*>(p.out)[idx] = f2bf(__uint_as_float(r[e]));
+                    }
                 }
             }
         }
         tc_fence_before();
         __syncthreads();
+        if (p.out_tma && tid == 0) {
+            tma_store_3d(&p.tm_out, sb + S_N, 0, c * C, bh);
+            tma_store_3d(&p.tm_out, sb + S_N + 8192, 64, c * C, bh);
+            bulk_commit_group();
+        }
+    }
+    if (p.out_tma && tid == 0) {
+        // the stores have finished (shared memory stays valid, and the marks below come after them)
+        bulk_wait_group0();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
     }
     if (!ok) {
         volatile int no_abort = 0;
@@ -625,6 +651,10 @@ cudaError_t launch_delta_tc(const DeltaArgs& a, cudaStream_t s) {
     p.nchunks = (a.L + C - 1) / C;
     p.gate = a.log_alpha != nullptr;
     p.out_f32 = a.out_dtype == GLA_DTYPE_F32;
+    // bf16 output by bulk-tensor stores where the output allows a tensor map (16-byte aligned),
+    // else by plain stores
+    p.out_tma = !p.out_f32 && (reinterpret_cast<uintptr_t>(a.out) & 15) == 0 &&
+                encode(&p.tm_out, bf, 2, a.out, D, a.L, BH, 64, C, CU_TENSOR_MAP_SWIZZLE_NONE) == CUDA_SUCCESS;
     cudaError_t e = cudaFuncSetAttribute(gla_delta_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S_SMEM);
     if (e != cudaSuccess) return e;
     gla_delta_tc_kernel<<<BH, kThr, S_SMEM, s>>>(p);
