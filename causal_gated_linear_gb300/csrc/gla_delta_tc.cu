@@ -23,9 +23,12 @@
 // rounded once to bf16.  Kr S' needs only the gate and the state, so it runs
 // while the triangular inverse is computed.
 //
-// One CTA of 256 threads per (batch, head), d_k = d_v = 128: thread (d, hf) owns
-// key channel d (TMEM lane d) and half hf of the chunk's tokens / of the state's
-// columns.  Phases run on all threads in turn with bounded waits.  A chunk over
+// One CTA per (batch, head), d_k = d_v = 128: 256 worker threads, thread (d, hf)
+// owning key channel d (TMEM lane d) and half hf of the chunk's tokens / of the
+// state's columns, run the phases in turn behind their own barrier, with bounded
+// waits; one more warp's first thread issues each group of tensor-core products
+// once the workers have signalled that its operands are in place, so that issuing
+// never holds up a worker.  A chunk over
 // which some channel decays by more than e^-64 is outside the factorisation's
 // range: the head is marked (a NaN pattern in the first output element of each
 // 64-column block) and the token-by-token kernel recomputes exactly the marked
@@ -42,7 +45,8 @@ namespace gla {
 namespace {
 
 constexpr int C = 64, D = 128;
-constexpr int kThr = 256;
+constexpr int kWork = 256;         // worker threads
+constexpr int kThr = kWork + 32;   // and the MMA-issuing warp
 constexpr int TB = C * D * 2;    // bf16 [64][128]: two 8 KB atoms
 constexpr int LAB = C * D * 4;   // fp32 log alpha tile
 constexpr int PB = C * C * 2;    // bf16 [64][64]: one atom
@@ -94,16 +98,31 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
 constexpr int S_Q = 0, S_K = TB, S_KR = 2 * TB, S_V = 3 * TB, S_LA = 4 * TB, S_SH = 4 * TB + LAB,
               S_SL = S_SH + SB2, S_M = S_SL + SB2, S_PM = S_M + PB, S_N = S_PM + PB, S_T = S_N + FB,
               S_BETA = S_T + FB, S_X = S_BETA + C * 4, S_BAR = S_X + 5 * D * 4;
-constexpr int S_SMEM = S_BAR + 64 + 1024;
+constexpr int S_SMEM = S_BAR + 128 + 1024;
 static_assert(S_SMEM <= 227 * 1024, "shared memory budget");
 // TMEM: S 0..127, O^T 128..191; 256..383 holds in turn Kr S', U and dS (read by the next chunk's
 // state update before its Kr S' is issued); A and P 384..511 (64 each)
 constexpr uint32_t T_S = 0, T_O = 128, T_U = 256, T_DS = 256, T_A = 384, T_P = 448;
 
+// Barrier over the worker threads (named barrier 1; the MMA-issuing warp takes no part), and
+// the same with an AND over a flag.
+__device__ __forceinline__ void wbar() { asm volatile("barrier.cta.sync 1, %0;" ::"n"(kWork) : "memory"); }
+__device__ __forceinline__ bool wbar_and(bool x) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.and.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)x), "n"(kWork)
+        : "memory");
+    return r != 0;
+}
+
+// A bounded wait on an mbarrier phase by every worker; false for all of them if any gave up.
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          const DeltaTcParams& p) {
     const bool ok = mbar_wait(bar, parity, abort_flag, p.err, p.wait_ns);
-    return __syncthreads_and(ok) != 0;
+    return wbar_and(ok);
 }
 
 __device__ __forceinline__ void load_tiles(const DeltaTcParams& p, uint32_t bar, uint32_t sb, int c, int bh) {
@@ -122,8 +141,8 @@ __device__ __forceinline__ void load_tiles(const DeltaTcParams& p, uint32_t bar,
 // level,
 //   T_IJ = -T_II sum_{J <= K < I} N_IK T_KJ   (I > J),
 // the sums held in N's unused upper blocks between the level's two barriers.
-// Only T's lower part (to the block diagonal) is written.  Every thread of the
-// CTA takes part (the barriers are CTA-wide).
+// Only T's lower part (to the block diagonal) is written.  Every worker thread
+// takes part (the barriers span the workers).
 __device__ __forceinline__ void unit_lower_inverse(float* N, float* T, int tid) {
     // diagonal blocks, one thread per column j: x = T[., j] by forward substitution with the
     // updates applied as each entry becomes final (entries above j stay 0 and add nothing)
@@ -139,7 +158,7 @@ __device__ __forceinline__ void unit_lower_inverse(float* N, float* T, int tid) 
 #pragma unroll
         for (int t = 0; t < 16; t++) T[(o + t) * LDF + o + j] = x[t];
     }
-    __syncthreads();
+    wbar();
 #pragma unroll
     for (int lvl = 1; lvl < 4; lvl++) {
         // Y_IJ = sum_{J <= K < I} N_IK T_KJ for the 4 - lvl blocks (I, J = I - lvl): one entry per
@@ -156,7 +175,7 @@ __device__ __forceinline__ void unit_lower_inverse(float* N, float* T, int tid) 
                     y[cc & 3] += N[(I * 16 + a) * LDF + Kb * 16 + cc] * T[(Kb * 16 + cc) * LDF + J * 16 + b];
             N[(J * 16 + a) * LDF + I * 16 + b] = (y[0] + y[1]) + (y[2] + y[3]);
         }
-        __syncthreads();
+        wbar();
         // T_IJ = -T_II Y_IJ
 #pragma unroll
         for (int n = 0; n < 4 - lvl; n++) {
@@ -167,7 +186,7 @@ __device__ __forceinline__ void unit_lower_inverse(float* N, float* T, int tid) 
                 z[cc & 3] += T[(I * 16 + a) * LDF + I * 16 + cc] * N[(J * 16 + cc) * LDF + I * 16 + b];
             T[(I * 16 + a) * LDF + J * 16 + b] = -((z[0] + z[1]) + (z[2] + z[3]));
         }
-        __syncthreads();
+        wbar();
     }
 }
 
@@ -181,8 +200,12 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S_BAR);
     const uint32_t bar_t = smem_u32(&bars[0]), bar_l = smem_u32(&bars[1]), bar_mma = smem_u32(&bars[2]),
                    bar_drain = smem_u32(&bars[3]), bar_x = smem_u32(&bars[4]);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S_BAR + 40);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S_BAR + 44);
+    // the workers' signals to the issuing thread: operands of A and P (h1), of Kr S' and the
+    // state's share of O (h2), of U (h3), and of the rest of O and dS (h4)
+    const uint32_t bar_h1 = smem_u32(&bars[5]), bar_h2 = smem_u32(&bars[6]), bar_h3 = smem_u32(&bars[7]),
+                   bar_h4 = smem_u32(&bars[8]);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S_BAR + 96);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S_BAR + 100);
     float* xch = reinterpret_cast<float*>(sm + S_X);
     float* betas = reinterpret_cast<float*>(sm + S_BETA);
     float* Nf = reinterpret_cast<float*>(sm + S_N);
@@ -194,6 +217,10 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
         mbar_init(bar_mma, 1);
         mbar_init(bar_drain, 1);
         mbar_init(bar_x, 1);
+        mbar_init(bar_h1, 1);
+        mbar_init(bar_h2, 1);
+        mbar_init(bar_h3, 1);
+        mbar_init(bar_h4, 1);
         *abort_flag = 0;
         mbar_fence_init();
         load_tiles(p, bar_t, sb, 0, bh);
@@ -210,7 +237,7 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    {
+    if (tid < kWork) {
         const float* s0 = p.init_state ? p.init_state + ((long)bh * D + d) * D : nullptr;
 #pragma unroll 1
         for (int h = 2 * hf; h < 2 * hf + 2; h++) {
@@ -225,88 +252,297 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
     bool ok = true, strong = false;
     int mph = 0;  // phases of bar_mma completed
     float beta_next = (tid < C && tid < L) ? p.beta[(long)bh * L + tid] : 0.f;
-    for (int c = 0; c < N; c++) {
-        if (!(ok = wait_all(bar_t, c & 1, abort_flag, p))) break;
-        if (tid == 0) tiles_done++;
-        if (p.gate) {
-            if (!(ok = wait_all(bar_l, c & 1, abort_flag, p))) break;
-            if (tid == 0) la_done++;
-        }
-        const int nval = min(C, L - c * C);
-        // beta of this chunk (loaded one chunk ahead), and the next chunk's load in flight
-        if (tid < C) {
-            betas[tid] = beta_next;
-            const int nn = min(C, L - (c + 1) * C);
-            beta_next = (c + 1 < N && tid < nn) ? p.beta[(long)bh * L + (long)(c + 1) * C + tid] : 0.f;
-        }
-        // gate and factors: Kr = k e^{b_t - b_C} (new tile), Kh = k e^{b_C - b_t} and
-        // Qh = q e^{b_t - b_C} in place.  Thread (channel pair gp, token quarter gq) takes
-        // channels 2gp, 2gp + 1 over tokens 16 gq .. 16 gq + 15 (packed pairs); the quarter
-        // sums of log alpha are exchanged for each quarter's prefix and the chunk total b_C.
-        {
-            const int gp = tid & 63, gq = tid >> 6, ch = 2 * gp;
-            float2 b2 = make_float2(0.f, 0.f), bc2 = b2;
+    if (tid < kWork) {
+        // the workers
+        for (int c = 0; c < N; c++) {
+            if (!(ok = wait_all(bar_t, c & 1, abort_flag, p))) break;
+            if (tid == 0) tiles_done++;
             if (p.gate) {
-                float2 s2 = make_float2(0.f, 0.f);
-#pragma unroll 8
-                for (int t = 16 * gq; t < 16 * gq + 16; t++) {
-                    const float2 x = *reinterpret_cast<const float2*>(la + t * D + ch);
-                    s2.x += x.x;
-                    s2.y += x.y;
-                }
-                *reinterpret_cast<float2*>(xch + gq * D + ch) = s2;
-                __syncthreads();
-#pragma unroll
-                for (int g = 0; g < 4; g++) {
-                    const float2 u = *reinterpret_cast<const float2*>(xch + g * D + ch);
-                    if (g < gq) {
-                        b2.x += u.x;
-                        b2.y += u.y;
-                    }
-                    bc2.x += u.x;
-                    bc2.y += u.y;
-                }
-                if (gq == 0) *reinterpret_cast<float2*>(xch + 4 * D + ch) = bc2;  // b_C per channel
-                strong |= fminf(bc2.x, bc2.y) < kStrongLog;
+                if (!(ok = wait_all(bar_l, c & 1, abort_flag, p))) break;
+                if (tid == 0) la_done++;
             }
-#pragma unroll 4
-            for (int t = 16 * gq; t < 16 * gq + 16; t++) {
-                const uint32_t o = tile_off(t, ch, 8192);
-                uint32_t* eq = reinterpret_cast<uint32_t*>(sm + S_Q + o);
-                uint32_t* ek = reinterpret_cast<uint32_t*>(sm + S_K + o);
-                uint32_t* er = reinterpret_cast<uint32_t*>(sm + S_KR + o);
-                const uint32_t kv = *ek;
+            const int nval = min(C, L - c * C);
+            // beta of this chunk (loaded one chunk ahead), and the next chunk's load in flight
+            if (tid < C) {
+                betas[tid] = beta_next;
+                const int nn = min(C, L - (c + 1) * C);
+                beta_next = (c + 1 < N && tid < nn) ? p.beta[(long)bh * L + (long)(c + 1) * C + tid] : 0.f;
+            }
+            // gate and factors: Kr = k e^{b_t - b_C} (new tile), Kh = k e^{b_C - b_t} and
+            // Qh = q e^{b_t - b_C} in place.  Thread (channel pair gp, token quarter gq) takes
+            // channels 2gp, 2gp + 1 over tokens 16 gq .. 16 gq + 15 (packed pairs); the quarter
+            // sums of log alpha are exchanged for each quarter's prefix and the chunk total b_C.
+            {
+                const int gp = tid & 63, gq = tid >> 6, ch = 2 * gp;
+                float2 b2 = make_float2(0.f, 0.f), bc2 = b2;
                 if (p.gate) {
-                    const float2 x = *reinterpret_cast<const float2*>(la + t * D + ch);
-                    b2.x += x.x;
-                    b2.y += x.y;
-                    const float u0 = (b2.x - bc2.x) * kLog2e, u1 = (b2.y - bc2.y) * kLog2e;
-                    const float fu0 = ex2f(u0), fu1 = ex2f(u1), fd0 = ex2f(-u0), fd1 = ex2f(-u1);
-                    const float2 qf = unpack_bf16x2(*eq), kf = unpack_bf16x2(kv);
-                    *eq = pack_bf16x2(qf.x * fu0, qf.y * fu1);
-                    *er = pack_bf16x2(kf.x * fu0, kf.y * fu1);
-                    *ek = pack_bf16x2(kf.x * fd0, kf.y * fd1);
-                } else {
-                    *er = kv;
+                    float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll 8
+                    for (int t = 16 * gq; t < 16 * gq + 16; t++) {
+                        const float2 x = *reinterpret_cast<const float2*>(la + t * D + ch);
+                        s2.x += x.x;
+                        s2.y += x.y;
+                    }
+                    *reinterpret_cast<float2*>(xch + gq * D + ch) = s2;
+                    wbar();
+#pragma unroll
+                    for (int g = 0; g < 4; g++) {
+                        const float2 u = *reinterpret_cast<const float2*>(xch + g * D + ch);
+                        if (g < gq) {
+                            b2.x += u.x;
+                            b2.y += u.y;
+                        }
+                        bc2.x += u.x;
+                        bc2.y += u.y;
+                    }
+                    if (gq == 0) *reinterpret_cast<float2*>(xch + 4 * D + ch) = bc2;  // b_C per channel
+                    strong |= fminf(bc2.x, bc2.y) < kStrongLog;
                 }
+#pragma unroll 4
+                for (int t = 16 * gq; t < 16 * gq + 16; t++) {
+                    const uint32_t o = tile_off(t, ch, 8192);
+                    uint32_t* eq = reinterpret_cast<uint32_t*>(sm + S_Q + o);
+                    uint32_t* ek = reinterpret_cast<uint32_t*>(sm + S_K + o);
+                    uint32_t* er = reinterpret_cast<uint32_t*>(sm + S_KR + o);
+                    const uint32_t kv = *ek;
+                    if (p.gate) {
+                        const float2 x = *reinterpret_cast<const float2*>(la + t * D + ch);
+                        b2.x += x.x;
+                        b2.y += x.y;
+                        const float u0 = (b2.x - bc2.x) * kLog2e, u1 = (b2.y - bc2.y) * kLog2e;
+                        const float fu0 = ex2f(u0), fu1 = ex2f(u1), fd0 = ex2f(-u0), fd1 = ex2f(-u1);
+                        const float2 qf = unpack_bf16x2(*eq), kf = unpack_bf16x2(kv);
+                        *eq = pack_bf16x2(qf.x * fu0, qf.y * fu1);
+                        *er = pack_bf16x2(kf.x * fu0, kf.y * fu1);
+                        *ek = pack_bf16x2(kf.x * fd0, kf.y * fd1);
+                    } else {
+                        *er = kv;
+                    }
+                }
+            }
+            fence_proxy_async_smem();  // the factors, read by the products below
+            tc_fence_before();
+            wbar();
+            tc_fence_after();
+            // b_C of this thread's key channel d, for the decay of the state below
+            const float bC = p.gate ? xch[4 * D + d] : 0.f;
+            if (tid == 0) {
+                // log alpha is read until here: the next chunk's may load
+                if (p.gate && c + 1 < N) {
+                    mbar_arrive_expect_tx(bar_l, LAB);
+                    tma_load_3d(sb + S_LA, &p.tm_la, bar_l, 0, (c + 1) * C, bh);
+                    la_issued++;
+                }
+                mbar_arrive(bar_h1);  // A and P may be issued
+                // the previous chunk's output staging (N's buffer) has been read by its stores
+                if (p.out_tma) bulk_wait_group_read0();
+            }
+            // S' = e^{b_C} S, where S = S' + dS of the previous chunk (its state update is done here):
+            // fp32 in TMEM, bf16 high and low copies in shared memory ([d][j], MN-major operand)
+            {
+                const float g = p.gate ? ex2f(bC * kLog2e) : 1.f;
+#pragma unroll 1
+                for (int h = 2 * hf; h < 2 * hf + 2; h++) {
+                    uint32_t r[32];
+                    tmem_ld32(lane + T_S + h * 32, r);
+                    if (c > 0) {
+                        uint32_t rd[32];
+                        tmem_ld32(lane + T_DS + h * 32, rd);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; e++)
+                            r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(rd[e]));
+                    } else {
+                        tmem_wait_ld();
+                    }
+#pragma unroll
+                    for (int e8 = 0; e8 < 4; e8++) {
+                        uint4 wh, wl;
+                        const float* x = reinterpret_cast<const float*>(r + e8 * 8);
+                        split_pair(x[0] * g, x[1] * g, wh.x, wl.x);
+                        split_pair(x[2] * g, x[3] * g, wh.y, wl.y);
+                        split_pair(x[4] * g, x[5] * g, wh.z, wl.z);
+                        split_pair(x[6] * g, x[7] * g, wh.w, wl.w);
+                        const uint32_t o = tile_off(d, h * 32 + e8 * 8, 16384);
+                        *reinterpret_cast<uint4*>(sm + S_SH + o) = wh;
+                        *reinterpret_cast<uint4*>(sm + S_SL + o) = wl;
+                        // keep the fp32 S' for the state update
+                        r[e8 * 8 + 0] = __float_as_uint(x[0] * g);
+                        r[e8 * 8 + 1] = __float_as_uint(x[1] * g);
+                        r[e8 * 8 + 2] = __float_as_uint(x[2] * g);
+                        r[e8 * 8 + 3] = __float_as_uint(x[3] * g);
+                        r[e8 * 8 + 4] = __float_as_uint(x[4] * g);
+                        r[e8 * 8 + 5] = __float_as_uint(x[5] * g);
+                        r[e8 * 8 + 6] = __float_as_uint(x[6] * g);
+                        r[e8 * 8 + 7] = __float_as_uint(x[7] * g);
+                    }
+                    tmem_st32(lane + T_S + h * 32, r);
+                }
+                tmem_wait_st();
+            }
+            fence_proxy_async_smem();  // S' high and low copies, read by the products after this barrier
+            tc_fence_before();
+            if (!(ok = wait_all(bar_mma, mph++ & 1, abort_flag, p))) break;
+            tc_fence_after();
+            if (tid == 0) mbar_arrive(bar_h2);
+            // N = Diag(beta) tril_strict(A) in fp32; P_m = tril(P) in bf16 (rows t = lanes 0..63)
+            if (d < C) {
+                const int t = d;
+                uint32_t ra[32], rp[32];
+                tmem_ld32(lane + T_A + hf * 32, ra);
+                tmem_ld32(lane + T_P + hf * 32, rp);
+                tmem_wait_ld();
+                const float bt = betas[t];
+#pragma unroll
+                for (int k8 = 0; k8 < 4; k8++) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; e++) {
+                        const int i = hf * 32 + k8 * 8 + e;
+                        x[e] = (i <= t) ? __uint_as_float(rp[k8 * 8 + e]) : 0.f;
+                        Nf[t * LDF + i] = (i < t) ? bt * __uint_as_float(ra[k8 * 8 + e]) : 0.f;
+                    }
+                    uint4 w;
+                    w.x = pack_bf16x2(x[0], x[1]);
+                    w.y = pack_bf16x2(x[2], x[3]);
+                    w.z = pack_bf16x2(x[4], x[5]);
+                    w.w = pack_bf16x2(x[6], x[7]);
+                    *reinterpret_cast<uint4*>(sm + S_PM + sw128_offset(t, hf * 32 + k8 * 8)) = w;
+                }
+            }
+            wbar();
+            unit_lower_inverse(Nf, Tf, tid);
+            if (!(ok = wait_all(bar_x, c & 1, abort_flag, p))) break;
+            tc_fence_after();
+            if (d >= C) {
+                // M = T Diag(beta) in bf16 ([t][i], K-major operand); thread (t, half of the columns)
+                const int t = d - C, h2 = hf;
+#pragma unroll
+                for (int k8 = 0; k8 < 4; k8++) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; e++) {
+                        const int i = h2 * 32 + k8 * 8 + e;
+                        // T is unit lower triangular; its blocks above the block diagonal are not stored
+                        x[e] = i <= t ? Tf[t * LDF + i] * betas[i] : 0.f;
+                    }
+                    uint4 w;
+                    w.x = pack_bf16x2(x[0], x[1]);
+                    w.y = pack_bf16x2(x[2], x[3]);
+                    w.z = pack_bf16x2(x[4], x[5]);
+                    w.w = pack_bf16x2(x[6], x[7]);
+                    *reinterpret_cast<uint4*>(sm + S_M + sw128_offset(t, h2 * 32 + k8 * 8)) = w;
+                }
+            } else {
+                // V' = V - X in bf16, in place over V ([t][j], MN-major operand; rows t = lanes 0..63)
+                const int t = d;
+#pragma unroll 1
+                for (int h = 2 * hf; h < 2 * hf + 2; h++) {
+                    uint32_t r[32];
+                    tmem_ld32(lane + T_U + h * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k8 = 0; k8 < 4; k8++) {
+                        uint4* pv = reinterpret_cast<uint4*>(sm + S_V + tile_off(t, h * 32 + k8 * 8, 8192));
+                        const uint4 vv = *pv;
+                        const float* x = reinterpret_cast<const float*>(r + k8 * 8);
+                        const float2 v0 = unpack_bf16x2(vv.x), v1 = unpack_bf16x2(vv.y), v2 = unpack_bf16x2(vv.z),
+                                     v3 = unpack_bf16x2(vv.w);
+                        uint4 w;
+                        w.x = pack_bf16x2(v0.x - x[0], v0.y - x[1]);
+                        w.y = pack_bf16x2(v1.x - x[2], v1.y - x[3]);
+                        w.z = pack_bf16x2(v2.x - x[4], v2.y - x[5]);
+                        w.w = pack_bf16x2(v3.x - x[6], v3.y - x[7]);
+                        *pv = w;
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            wbar();
+            tc_fence_after();
+            if (tid == 0) mbar_arrive(bar_h3);
+            if (!(ok = wait_all(bar_mma, mph++ & 1, abort_flag, p))) break;
+            tc_fence_after();
+            // U in bf16 high and low parts over Kr and V ([i][j], MN-major operands; rows i = lanes 0..63)
+            if (d < C) {
+                const int i = d;
+#pragma unroll 1
+                for (int h = 2 * hf; h < 2 * hf + 2; h++) {
+                    uint32_t r[32];
+                    tmem_ld32(lane + T_U + h * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k8 = 0; k8 < 4; k8++) {
+                        uint4 wh, wl;
+                        const float* x = reinterpret_cast<const float*>(r + k8 * 8);
+                        split_pair(x[0], x[1], wh.x, wl.x);
+                        split_pair(x[2], x[3], wh.y, wl.y);
+                        split_pair(x[4], x[5], wh.z, wl.z);
+                        split_pair(x[6], x[7], wh.w, wl.w);
+                        const uint32_t o = tile_off(i, h * 32 + k8 * 8, 8192);
+                        *reinterpret_cast<uint4*>(sm + S_KR + o) = wh;
+                        *reinterpret_cast<uint4*>(sm + S_V + o) = wl;
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            wbar();
+            tc_fence_after();
+            if (tid == 0) mbar_arrive(bar_h4);
+            if (!(ok = wait_all(bar_mma, mph++ & 1, abort_flag, p))) break;
+            tc_fence_after();
+            // every product that reads this chunk's tiles has completed: load the next chunk's
+            if (tid == 0 && c + 1 < N) {
+                load_tiles(p, bar_t, sb, c + 1, bh);
+                tiles_issued++;
+            }
+            // output: thread (j = d, half hf of the tokens) has o[t][j]; the state update
+            // S = S' + dS is done with the next chunk's decay
+            {
+                uint32_t r[32];
+                tmem_ld32(lane + T_O + hf * 32, r);
+                tmem_wait_ld();
+                if (p.out_tma) {
+                    // bf16 into N's buffer (free after the inverse) as two row-major [64][64] boxes,
+                    // written out below by two bulk-tensor stores (rows past L are clipped)
+                    uint16_t* ob = reinterpret_cast<uint16_t*>(sm + S_N + (d >> 6) * 8192) + (hf * 32) * 64 + (d & 63);
+#pragma unroll
+                    for (int e = 0; e < 32; e++) ob[e * 64] = f2bf(__uint_as_float(r[e]));
+                    fence_proxy_async_smem();
+                } else {
+                    const long row0 = (long)bh * L + (long)c * C + hf * 32;
+#pragma unroll
+                    for (int e = 0; e < 32; e++) {
+                        if (hf * 32 + e < nval) {
+                            const long idx = (row0 + e) * D + d;
+                            if (p.out_f32)
+                                static_cast<float*>(p.out)[idx] = __uint_as_float(r[e]);
+                            else
+                                static_cast<uint16_t*>(p.out)[idx] = f2bf(__uint_as_float(r[e]));
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            wbar();
+            if (p.out_tma && tid == 0) {
+                tma_store_3d(&p.tm_out, sb + S_N, 0, c * C, bh);
+                tma_store_3d(&p.tm_out, sb + S_N + 8192, 64, c * C, bh);
+                bulk_commit_group();
             }
         }
-        fence_proxy_async_smem();  // the factors, read by the products below
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        // b_C of this thread's key channel d, for the decay of the state below
-        const float bC = p.gate ? xch[4 * D + d] : 0.f;
-        if (tid == 0) {
-            // log alpha is read until here: the next chunk's may load
-            if (p.gate && c + 1 < N) {
-                mbar_arrive_expect_tx(bar_l, LAB);
-                tma_load_3d(sb + S_LA, &p.tm_la, bar_l, 0, (c + 1) * C, bh);
-                la_issued++;
-            }
+    } else if (tid == kWork) {
+        // the MMA-issuing thread: each group of products once the workers' signal says that its
+        // operands are in place (their fences and barrier come before the signal)
+        constexpr uint32_t id64 = make_idesc_bf16(128, 64, 0, 0), id128 = make_idesc_bf16(128, 128, 0, 1),
+                           idO = make_idesc_bf16(128, 64, 1, 0), idS = make_idesc_bf16(128, 128, 1, 1);
+        for (int c = 0; c < N; c++) {
             // A = Kr Kh^T and P = Qh Kh^T (M = 128: rows 64..127 read past the tile and are
-            // ignored); they run while the state is decayed and split below
-            constexpr uint32_t id64 = make_idesc_bf16(128, 64, 0, 0);
+            // ignored); they run while the workers decay and split the state
+            if (!(ok = mbar_wait(bar_h1, c & 1, abort_flag, p.err, p.wait_ns))) break;
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < D / 16; kk++)
                 mma_ss(tmem + T_A, desc_k(sb + S_KR, kk, 8192), desc_k(sb + S_K, kk, 8192), id64, kk > 0);
@@ -314,61 +550,11 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
             for (int kk = 0; kk < D / 16; kk++)
                 mma_ss(tmem + T_P, desc_k(sb + S_Q, kk, 8192), desc_k(sb + S_K, kk, 8192), id64, kk > 0);
             mma_commit(bar_mma);
-            // the previous chunk's output staging (N's buffer) has been read by its stores
-            if (p.out_tma) bulk_wait_group_read0();
-        }
-        // S' = e^{b_C} S, where S = S' + dS of the previous chunk (its state update is done here):
-        // fp32 in TMEM, bf16 high and low copies in shared memory ([d][j], MN-major operand)
-        {
-            const float g = p.gate ? ex2f(bC * kLog2e) : 1.f;
-#pragma unroll 1
-            for (int h = 2 * hf; h < 2 * hf + 2; h++) {
-                uint32_t r[32];
-                tmem_ld32(lane + T_S + h * 32, r);
-                if (c > 0) {
-                    uint32_t rd[32];
-                    tmem_ld32(lane + T_DS + h * 32, rd);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; e++) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(rd[e]));
-                } else {
-                    tmem_wait_ld();
-                }
-#pragma unroll
-                for (int e8 = 0; e8 < 4; e8++) {
-                    uint4 wh, wl;
-                    const float* x = reinterpret_cast<const float*>(r + e8 * 8);
-                    split_pair(x[0] * g, x[1] * g, wh.x, wl.x);
-                    split_pair(x[2] * g, x[3] * g, wh.y, wl.y);
-                    split_pair(x[4] * g, x[5] * g, wh.z, wl.z);
-                    split_pair(x[6] * g, x[7] * g, wh.w, wl.w);
-                    const uint32_t o = tile_off(d, h * 32 + e8 * 8, 16384);
-                    *reinterpret_cast<uint4*>(sm + S_SH + o) = wh;
-                    *reinterpret_cast<uint4*>(sm + S_SL + o) = wl;
-                    // keep the fp32 S' for the state update
-                    r[e8 * 8 + 0] = __float_as_uint(x[0] * g);
-                    r[e8 * 8 + 1] = __float_as_uint(x[1] * g);
-                    r[e8 * 8 + 2] = __float_as_uint(x[2] * g);
-                    r[e8 * 8 + 3] = __float_as_uint(x[3] * g);
-                    r[e8 * 8 + 4] = __float_as_uint(x[4] * g);
-                    r[e8 * 8 + 5] = __float_as_uint(x[5] * g);
-                    r[e8 * 8 + 6] = __float_as_uint(x[6] * g);
-                    r[e8 * 8 + 7] = __float_as_uint(x[7] * g);
-                }
-                tmem_st32(lane + T_S + h * 32, r);
-            }
-            tmem_wait_st();
-        }
-        fence_proxy_async_smem();  // S' high and low copies, read by the products after this barrier
-        tc_fence_before();
-        if (!(ok = wait_all(bar_mma, mph++ & 1, abort_flag, p))) break;
-        tc_fence_after();
-        if (tid == 0) {
-            // X = Kr S' (A = Kr K-major, B = S' high and low MN-major, N = 128; M = 128: rows
-            // 64..127 read past the tile and are ignored), then the state's share of the output,
-            // O^T = S'^T Qh^T (M = j: A = S' MN-major, B = Qh K-major); both run during the
-            // inverse below
-            constexpr uint32_t id128 = make_idesc_bf16(128, 128, 0, 1);
+            // X = Kr S' (A = Kr K-major, B = S' high and low MN-major, N = 128; M = 128 as above),
+            // then the state's share of the output, O^T = S'^T Qh^T (M = j: A = S' MN-major,
+            // B = Qh K-major); both run during the triangular inverse
+            if (!(ok = mbar_wait(bar_h2, c & 1, abort_flag, p.err, p.wait_ns))) break;
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < D / 16; kk++)
                 mma_ss(tmem + T_U, desc_k(sb + S_KR, kk, 8192), desc_mn(sb + S_SH, kk, 16384), id128, kk > 0);
@@ -376,137 +562,29 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
             for (int kk = 0; kk < D / 16; kk++)
                 mma_ss(tmem + T_U, desc_k(sb + S_KR, kk, 8192), desc_mn(sb + S_SL, kk, 16384), id128, 1);
             mma_commit(bar_x);
-            constexpr uint32_t idO = make_idesc_bf16(128, 64, 1, 0);
 #pragma unroll
             for (int kk = 0; kk < D / 16; kk++)
                 mma_ss(tmem + T_O, desc_mn(sb + S_SH, kk, 16384), desc_k(sb + S_Q, kk, 8192), idO, kk > 0);
 #pragma unroll
             for (int kk = 0; kk < D / 16; kk++)
                 mma_ss(tmem + T_O, desc_mn(sb + S_SL, kk, 16384), desc_k(sb + S_Q, kk, 8192), idO, 1);
-        }
-        // N = Diag(beta) tril_strict(A) in fp32; P_m = tril(P) in bf16 (rows t = lanes 0..63)
-        if (d < C) {
-            const int t = d;
-            uint32_t ra[32], rp[32];
-            tmem_ld32(lane + T_A + hf * 32, ra);
-            tmem_ld32(lane + T_P + hf * 32, rp);
-            tmem_wait_ld();
-            const float bt = betas[t];
-#pragma unroll
-            for (int k8 = 0; k8 < 4; k8++) {
-                float x[8];
-#pragma unroll
-                for (int e = 0; e < 8; e++) {
-                    const int i = hf * 32 + k8 * 8 + e;
-                    x[e] = (i <= t) ? __uint_as_float(rp[k8 * 8 + e]) : 0.f;
-                    Nf[t * LDF + i] = (i < t) ? bt * __uint_as_float(ra[k8 * 8 + e]) : 0.f;
-                }
-                uint4 w;
-                w.x = pack_bf16x2(x[0], x[1]);
-                w.y = pack_bf16x2(x[2], x[3]);
-                w.z = pack_bf16x2(x[4], x[5]);
-                w.w = pack_bf16x2(x[6], x[7]);
-                *reinterpret_cast<uint4*>(sm + S_PM + sw128_offset(t, hf * 32 + k8 * 8)) = w;
-            }
-        }
-        __syncthreads();
-        unit_lower_inverse(Nf, Tf, tid);
-        if (!(ok = wait_all(bar_x, c & 1, abort_flag, p))) break;
-        tc_fence_after();
-        if (d >= C) {
-            // M = T Diag(beta) in bf16 ([t][i], K-major operand); thread (t, half of the columns)
-            const int t = d - C, h2 = hf;
-#pragma unroll
-            for (int k8 = 0; k8 < 4; k8++) {
-                float x[8];
-#pragma unroll
-                for (int e = 0; e < 8; e++) {
-                    const int i = h2 * 32 + k8 * 8 + e;
-                    // T is unit lower triangular; its blocks above the block diagonal are not stored
-                    x[e] = i <= t ? Tf[t * LDF + i] * betas[i] : 0.f;
-                }
-                uint4 w;
-                w.x = pack_bf16x2(x[0], x[1]);
-                w.y = pack_bf16x2(x[2], x[3]);
-                w.z = pack_bf16x2(x[4], x[5]);
-                w.w = pack_bf16x2(x[6], x[7]);
-                *reinterpret_cast<uint4*>(sm + S_M + sw128_offset(t, h2 * 32 + k8 * 8)) = w;
-            }
-        } else {
-            // V' = V - X in bf16, in place over V ([t][j], MN-major operand; rows t = lanes 0..63)
-            const int t = d;
-#pragma unroll 1
-            for (int h = 2 * hf; h < 2 * hf + 2; h++) {
-                uint32_t r[32];
-                tmem_ld32(lane + T_U + h * 32, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int k8 = 0; k8 < 4; k8++) {
-                    uint4* pv = reinterpret_cast<uint4*>(sm + S_V + tile_off(t, h * 32 + k8 * 8, 8192));
-                    const uint4 vv = *pv;
-                    const float* x = reinterpret_cast<const float*>(r + k8 * 8);
-                    const float2 v0 = unpack_bf16x2(vv.x), v1 = unpack_bf16x2(vv.y), v2 = unpack_bf16x2(vv.z),
-                                 v3 = unpack_bf16x2(vv.w);
-                    uint4 w;
-                    w.x = pack_bf16x2(v0.x - x[0], v0.y - x[1]);
-                    w.y = pack_bf16x2(v1.x - x[2], v1.y - x[3]);
-                    w.z = pack_bf16x2(v2.x - x[4], v2.y - x[5]);
-                    w.w = pack_bf16x2(v3.x - x[6], v3.y - x[7]);
-                    *pv = w;
-                }
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid == 0) {
             // U = M V' (A = M K-major, B = V' MN-major), N = 128
-            constexpr uint32_t id128 = make_idesc_bf16(128, 128, 0, 1);
+            if (!(ok = mbar_wait(bar_h3, c & 1, abort_flag, p.err, p.wait_ns))) break;
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < C / 16; kk++)
                 mma_ss(tmem + T_U, desc_k(sb + S_M, kk, 8192), desc_mn(sb + S_V, kk, 8192), id128, kk > 0);
             mma_commit(bar_mma);
-        }
-        if (!(ok = wait_all(bar_mma, mph++ & 1, abort_flag, p))) break;
-        tc_fence_after();
-        // U in bf16 high and low parts over Kr and V ([i][j], MN-major operands; rows i = lanes 0..63)
-        if (d < C) {
-            const int i = d;
-#pragma unroll 1
-            for (int h = 2 * hf; h < 2 * hf + 2; h++) {
-                uint32_t r[32];
-                tmem_ld32(lane + T_U + h * 32, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int k8 = 0; k8 < 4; k8++) {
-                    uint4 wh, wl;
-                    const float* x = reinterpret_cast<const float*>(r + k8 * 8);
-                    split_pair(x[0], x[1], wh.x, wl.x);
-                    split_pair(x[2], x[3], wh.y, wl.y);
-                    split_pair(x[4], x[5], wh.z, wl.z);
-                    split_pair(x[6], x[7], wh.w, wl.w);
-                    const uint32_t o = tile_off(i, h * 32 + k8 * 8, 8192);
-                    *reinterpret_cast<uint4*>(sm + S_KR + o) = wh;
-                    *reinterpret_cast<uint4*>(sm + S_V + o) = wl;
-                }
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid == 0) {
-            // O^T += U^T P_m^T  (M = j: A = U MN-major, B = P_m K-major)
-            constexpr uint32_t idO = make_idesc_bf16(128, 64, 1, 0);
+            // O^T += U^T P_m^T (M = j: A = U MN-major, B = P_m K-major), then dS = Kh^T U
+            // (A = Kh MN-major, B = U MN-major)
+            if (!(ok = mbar_wait(bar_h4, c & 1, abort_flag, p.err, p.wait_ns))) break;
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < C / 16; kk++)
                 mma_ss(tmem + T_O, desc_mn(sb + S_KR, kk, 8192), desc_k(sb + S_PM, kk, 8192), idO, 1);
 #pragma unroll
             for (int kk = 0; kk < C / 16; kk++)
                 mma_ss(tmem + T_O, desc_mn(sb + S_V, kk, 8192), desc_k(sb + S_PM, kk, 8192), idO, 1);
-            // dS = Kh^T U (A = Kh MN-major, B = U MN-major)
-            constexpr uint32_t idS = make_idesc_bf16(128, 128, 1, 1);
 #pragma unroll
             for (int kk = 0; kk < C / 16; kk++)
                 mma_ss(tmem + T_DS, desc_mn(sb + S_K, kk, 8192), desc_mn(sb + S_KR, kk, 8192), idS, kk > 0);
@@ -515,65 +593,26 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
                 mma_ss(tmem + T_DS, desc_mn(sb + S_K, kk, 8192), desc_mn(sb + S_V, kk, 8192), idS, 1);
             mma_commit(bar_mma);
         }
-        if (!(ok = wait_all(bar_mma, mph++ & 1, abort_flag, p))) break;
-        tc_fence_after();
-        // every product that reads this chunk's tiles has completed: load the next chunk's
-        if (tid == 0 && c + 1 < N) {
-            load_tiles(p, bar_t, sb, c + 1, bh);
-            tiles_issued++;
-        }
-        // output: thread (j = d, half hf of the tokens) has o[t][j]; the state update
-        // S = S' + dS is done with the next chunk's decay
-        {
-            uint32_t r[32];
-            tmem_ld32(lane + T_O + hf * 32, r);
-            tmem_wait_ld();
-            if (p.out_tma) {
-                // bf16 into N's buffer (free after the inverse) as two row-major [64][64] boxes,
-                // written out below by two bulk-tensor stores (rows past L are clipped)
-                uint16_t* ob = reinterpret_cast<uint16_t*>(sm + S_N + (d >> 6) * 8192) + (hf * 32) * 64 + (d & 63);
-#pragma unroll
-                for (int e = 0; e < 32; e++) ob[e * 64] = f2bf(__uint_as_float(r[e]));
-                fence_proxy_async_smem();
-            } else {
-                const long row0 = (long)bh * L + (long)c * C + hf * 32;
-#pragma unroll
-                for (int e = 0; e < 32; e++) {
-                    if (hf * 32 + e < nval) {
-                        const long idx = (row0 + e) * D + d;
-                        if (p.out_f32)
-                            static_cast<float*>(p.out)[idx] = __uint_as_float(r[e]);
-                        else
-                            static_cast<uint16_t*>(p.out)[idx] = f2bf(__uint_as_float(r[e]));
-                    }
-                }
-            }
-        }
-        tc_fence_before();
-        __syncthreads();
-        if (p.out_tma && tid == 0) {
-            tma_store_3d(&p.tm_out, sb + S_N, 0, c * C, bh);
-            tma_store_3d(&p.tm_out, sb + S_N + 8192, 64, c * C, bh);
-            bulk_commit_group();
-        }
     }
     if (p.out_tma && tid == 0) {
         // the stores have finished (shared memory stays valid, and the marks below come after them)
         bulk_wait_group0();
         asm volatile("fence.proxy.async.global;" ::: "memory");
     }
-    if (!ok) {
+    if (tid == 0 && !ok) {
+        // loads still in flight land before the CTA ends
         volatile int no_abort = 0;
-        if (tid == 0) {
-            for (int n = tiles_done; n < tiles_issued; n++) mbar_wait(bar_t, n & 1, &no_abort, nullptr);
-            for (int n = la_done; n < la_issued; n++) mbar_wait(bar_l, n & 1, &no_abort, nullptr);
-            mma_commit(bar_drain);
-            mbar_wait(bar_drain, 0, &no_abort, nullptr);
-        }
-        __syncthreads();
+        for (int n = tiles_done; n < tiles_issued; n++) mbar_wait(bar_t, n & 1, &no_abort, nullptr);
+        for (int n = la_done; n < la_issued; n++) mbar_wait(bar_l, n & 1, &no_abort, nullptr);
+    }
+    if (tid == kWork) {
+        // every product the issuing thread started has completed before TMEM is released
+        volatile int no_abort = 0;
+        mma_commit(bar_drain);
+        mbar_wait(bar_drain, 0, &no_abort, nullptr);
     }
     const bool mark = __syncthreads_or(strong) != 0;
-    if (ok && !mark && p.final_state) {
+    if (tid < kWork && ok && !mark && p.final_state) {
         // S = S' + dS of the last chunk (the initial state when there is none)
         float* fs = p.final_state + ((long)bh * D + d) * D;
 #pragma unroll 1
