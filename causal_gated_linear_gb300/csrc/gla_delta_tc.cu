@@ -171,8 +171,14 @@ __device__ __forceinline__ void unit_lower_inverse(float* N, float* T, int tid) 
 #pragma unroll
             for (int Kb = J; Kb < I; Kb++)
 #pragma unroll
-                for (int cc = 0; cc < 16; cc++)
-                    y[cc & 3] += N[(I * 16 + a) * LDF + Kb * 16 + cc] * T[(Kb * 16 + cc) * LDF + J * 16 + b];
+                for (int c4 = 0; c4 < 4; c4++) {
+                    const float4 nv = *reinterpret_cast<const float4*>(N + (I * 16 + a) * LDF + Kb * 16 + 4 * c4);
+                    const float* tc = T + (Kb * 16 + 4 * c4) * LDF + J * 16 + b;
+                    y[0] += nv.x * tc[0];
+                    y[1] += nv.y * tc[LDF];
+                    y[2] += nv.z * tc[2 * LDF];
+                    y[3] += nv.w * tc[3 * LDF];
+                }
             N[(J * 16 + a) * LDF + I * 16 + b] = (y[0] + y[1]) + (y[2] + y[3]);
         }
         wbar();
@@ -182,8 +188,14 @@ __device__ __forceinline__ void unit_lower_inverse(float* N, float* T, int tid) 
             const int I = n + lvl, J = n;
             float z[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int cc = 0; cc < 16; cc++)
-                z[cc & 3] += T[(I * 16 + a) * LDF + I * 16 + cc] * N[(J * 16 + cc) * LDF + I * 16 + b];
+            for (int c4 = 0; c4 < 4; c4++) {
+                const float4 tv = *reinterpret_cast<const float4*>(T + (I * 16 + a) * LDF + I * 16 + 4 * c4);
+                const float* nc = N + (J * 16 + 4 * c4) * LDF + I * 16 + b;
+                z[0] += tv.x * nc[0];
+                z[1] += tv.y * nc[LDF];
+                z[2] += tv.z * nc[2 * LDF];
+                z[3] += tv.w * nc[3 * LDF];
+            }
             T[(I * 16 + a) * LDF + J * 16 + b] = -((z[0] + z[1]) + (z[2] + z[3]));
         }
         wbar();
@@ -275,13 +287,14 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
             {
                 const int gp = tid & 63, gq = tid >> 6, ch = 2 * gp;
                 float2 b2 = make_float2(0.f, 0.f), bc2 = b2;
+                float2 lx[16];  // this thread's log alpha pairs, read once for both passes
                 if (p.gate) {
                     float2 s2 = make_float2(0.f, 0.f);
-#pragma unroll 8
-                    for (int t = 16 * gq; t < 16 * gq + 16; t++) {
-                        const float2 x = *reinterpret_cast<const float2*>(la + t * D + ch);
-                        s2.x += x.x;
-                        s2.y += x.y;
+#pragma unroll
+                    for (int u = 0; u < 16; u++) {
+                        lx[u] = *reinterpret_cast<const float2*>(la + (16 * gq + u) * D + ch);
+                        s2.x += lx[u].x;
+                        s2.y += lx[u].y;
                     }
                     *reinterpret_cast<float2*>(xch + gq * D + ch) = s2;
                     wbar();
@@ -298,17 +311,17 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
                     if (gq == 0) *reinterpret_cast<float2*>(xch + 4 * D + ch) = bc2;  // b_C per channel
                     strong |= fminf(bc2.x, bc2.y) < kStrongLog;
                 }
-#pragma unroll 4
-                for (int t = 16 * gq; t < 16 * gq + 16; t++) {
+#pragma unroll
+                for (int u = 0; u < 16; u++) {
+                    const int t = 16 * gq + u;
                     const uint32_t o = tile_off(t, ch, 8192);
                     uint32_t* eq = reinterpret_cast<uint32_t*>(sm + S_Q + o);
                     uint32_t* ek = reinterpret_cast<uint32_t*>(sm + S_K + o);
                     uint32_t* er = reinterpret_cast<uint32_t*>(sm + S_KR + o);
                     const uint32_t kv = *ek;
                     if (p.gate) {
-                        const float2 x = *reinterpret_cast<const float2*>(la + t * D + ch);
-                        b2.x += x.x;
-                        b2.y += x.y;
+                        b2.x += lx[u].x;
+                        b2.y += lx[u].y;
                         const float u0 = (b2.x - bc2.x) * kLog2e, u1 = (b2.y - bc2.y) * kLog2e;
                         const float fu0 = ex2f(u0), fu1 = ex2f(u1), fd0 = ex2f(-u0), fd1 = ex2f(-u1);
                         const float2 qf = unpack_bf16x2(*eq), kf = unpack_bf16x2(kv);
@@ -395,13 +408,16 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
                 const float bt = betas[t];
 #pragma unroll
                 for (int k8 = 0; k8 < 4; k8++) {
-                    float x[8];
+                    float x[8], n[8];
 #pragma unroll
                     for (int e = 0; e < 8; e++) {
                         const int i = hf * 32 + k8 * 8 + e;
                         x[e] = (i <= t) ? __uint_as_float(rp[k8 * 8 + e]) : 0.f;
-                        Nf[t * LDF + i] = (i < t) ? bt * __uint_as_float(ra[k8 * 8 + e]) : 0.f;
+                        n[e] = (i < t) ? bt * __uint_as_float(ra[k8 * 8 + e]) : 0.f;
                     }
+                    float4* nr = reinterpret_cast<float4*>(Nf + t * LDF + hf * 32 + k8 * 8);
+                    nr[0] = make_float4(n[0], n[1], n[2], n[3]);
+                    nr[1] = make_float4(n[4], n[5], n[6], n[7]);
                     uint4 w;
                     w.x = pack_bf16x2(x[0], x[1]);
                     w.y = pack_bf16x2(x[2], x[3]);
