@@ -285,11 +285,12 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dq_kernel(const __grid_const
         if (p.gate) {
             const int gp = tid & 63, gq = tid >> 6, ch = 2 * gp;
             float2 s2 = make_float2(0.f, 0.f);
-#pragma unroll 8
-            for (int t = 16 * gq; t < 16 * gq + 16; t++) {
-                const float2 x = *reinterpret_cast<const float2*>(la + t * D + ch);
-                s2.x += x.x;
-                s2.y += x.y;
+            float2 lx[16];  // this thread's log alpha pairs, read once for both passes
+#pragma unroll
+            for (int u = 0; u < 16; u++) {
+                lx[u] = *reinterpret_cast<const float2*>(la + (16 * gq + u) * D + ch);
+                s2.x += lx[u].x;
+                s2.y += lx[u].y;
             }
             *reinterpret_cast<float2*>(xch + gq * D + ch) = s2;
             __syncthreads();
@@ -310,11 +311,11 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dq_kernel(const __grid_const
                 *reinterpret_cast<float2*>(xch + 5 * D + ch) = make_float2(q[0].x + q[1].x, q[0].y + q[1].y);
             }
             uint8_t* kt = sm + A_K;
-#pragma unroll 4
-            for (int t = 16 * gq; t < 16 * gq + 16; t++) {
-                const float2 x = *reinterpret_cast<const float2*>(la + t * D + ch);
-                b2.x += x.x;
-                b2.y += x.y;
+#pragma unroll
+            for (int u = 0; u < 16; u++) {
+                const int t = 16 * gq + u;
+                b2.x += lx[u].x;
+                b2.y += lx[u].y;
                 uint32_t* e = reinterpret_cast<uint32_t*>(kt + tile_off(t, ch, 8192));
                 const float2 kf = unpack_bf16x2(*e);
                 *e = pack_bf16x2(kf.x * ex2f((bc2.x - b2.x) * kLog2e), kf.y * ex2f((bc2.y - b2.y) * kLog2e));
@@ -533,11 +534,12 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dkdv_kernel(const __grid_con
         if (p.gate) {
             const int gp = tid & 63, gq = tid >> 6, ch = 2 * gp;
             float2 s2 = make_float2(0.f, 0.f);
-#pragma unroll 8
-            for (int t = 16 * gq; t < 16 * gq + 16; t++) {
-                const float2 x = *reinterpret_cast<const float2*>(la + t * D + ch);
-                s2.x += x.x;
-                s2.y += x.y;
+            float2 lx[16];  // this thread's log alpha pairs, read once for both passes
+#pragma unroll
+            for (int u = 0; u < 16; u++) {
+                lx[u] = *reinterpret_cast<const float2*>(la + (16 * gq + u) * D + ch);
+                s2.x += lx[u].x;
+                s2.y += lx[u].y;
             }
             *reinterpret_cast<float2*>(xch + gq * D + ch) = s2;
             __syncthreads();
@@ -560,11 +562,11 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dkdv_kernel(const __grid_con
             strong |= fminf(bc2.x, bc2.y) < kStrongLog;
             uint8_t* qt = sm + B_Q;
             uint8_t* kt = sm + B_K;
-#pragma unroll 4
-            for (int t = 16 * gq; t < 16 * gq + 16; t++) {
-                const float2 x = *reinterpret_cast<const float2*>(la + t * D + ch);
-                b2.x += x.x;
-                b2.y += x.y;
+#pragma unroll
+            for (int u = 0; u < 16; u++) {
+                const int t = 16 * gq + u;
+                b2.x += lx[u].x;
+                b2.y += lx[u].y;
                 const uint32_t o = tile_off(t, ch, 8192);
                 uint32_t* eq = reinterpret_cast<uint32_t*>(qt + o);
                 uint32_t* ek = reinterpret_cast<uint32_t*>(kt + o);
