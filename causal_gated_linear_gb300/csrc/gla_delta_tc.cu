@@ -267,8 +267,8 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
     if (tid < kWork) {
         // the workers
         for (int c = 0; c < N; c++) {
-            if (!(ok = wait_all(bar_t, c & 1, abort_flag, p))) break;
-            if (tid == 0) tiles_done++;
+            // log alpha was loaded during the previous chunk; q, k and v are waited for after the
+            // gate's sums, which need log alpha alone
             if (p.gate) {
                 if (!(ok = wait_all(bar_l, c & 1, abort_flag, p))) break;
                 if (tid == 0) la_done++;
@@ -311,6 +311,8 @@ __global__ void __launch_bounds__(kThr, 1) gla_delta_tc_kernel(const __grid_cons
                     if (gq == 0) *reinterpret_cast<float2*>(xch + 4 * D + ch) = bc2;  // b_C per channel
                     strong |= fminf(bc2.x, bc2.y) < kStrongLog;
                 }
+                if (!(ok = wait_all(bar_t, c & 1, abort_flag, p))) break;
+                if (tid == 0) tiles_done++;
 #pragma unroll
                 for (int u = 0; u < 16; u++) {
                     const int t = 16 * gq + u;
