@@ -256,8 +256,7 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dq_kernel(const __grid_const
     int c = 0;
     for (; c < N; c++) {
         const float* la = reinterpret_cast<const float*>(sm + A_LA + (c & 1) * LAB);
-        if (!(ok = wait_all(bar_t, c & 1, abort_flag, p))) break;
-        if (tid == 0) pn.tiles_done++;
+        // log alpha was loaded a chunk ahead; the tiles are waited for after the gate's sums
         if (p.gate) {
             if (!(ok = wait_all(bar_l[c & 1], (c >> 1) & 1, abort_flag, p))) break;
             if (tid == 0) {
@@ -270,15 +269,20 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dq_kernel(const __grid_const
             }
         }
         const int nval = min(C, L - c * C);
-        if (tid == 0) {
-            // D = dO V^T (M = 128, rows 64..127 read past the dO tile and are ignored): it needs
-            // no gate factor, so it runs while the gate works
-            tc_fence_after();
-            constexpr uint32_t idD = make_idesc_bf16(128, 64, 0, 0);
+        // the tiles, then D = dO V^T (M = 128, rows 64..127 read past the dO tile and are
+        // ignored): it needs no gate factor, so it runs while the gate forms its factors
+        auto tiles_then_d = [&]() -> bool {
+            if (!wait_all(bar_t, c & 1, abort_flag, p)) return false;
+            if (tid == 0) {
+                pn.tiles_done++;
+                tc_fence_after();
+                constexpr uint32_t idD = make_idesc_bf16(128, 64, 0, 0);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; kk++)
-                mma_ss(tmem + TA_D, desc_k(sb + A_DO, kk, 8192), desc_k(sb + A_V, kk, 8192), idD, kk > 0);
-        }
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_ss(tmem + TA_D, desc_k(sb + A_DO, kk, 8192), desc_k(sb + A_V, kk, 8192), idD, kk > 0);
+            }
+            return true;
+        };
         // gate: Kh = k e^{b_C - b_t} in place.  Thread (channel pair gp, token quarter gq) takes
         // channels 2gp, 2gp + 1 over tokens 16 gq .. 16 gq + 15 (packed pairs); the quarter sums
         // give each quarter's prefix, b_C and the first half's sum (the epilogue's start)
@@ -310,6 +314,7 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dq_kernel(const __grid_const
                 *reinterpret_cast<float2*>(xch + 4 * D + ch) = bc2;
                 *reinterpret_cast<float2*>(xch + 5 * D + ch) = make_float2(q[0].x + q[1].x, q[0].y + q[1].y);
             }
+            if (!(ok = tiles_then_d())) break;
             uint8_t* kt = sm + A_K;
 #pragma unroll
             for (int u = 0; u < 16; u++) {
@@ -321,6 +326,7 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dq_kernel(const __grid_const
                 *e = pack_bf16x2(kf.x * ex2f((bc2.x - b2.x) * kLog2e), kf.y * ex2f((bc2.y - b2.y) * kLog2e));
             }
         }
+        if (!p.gate && !(ok = tiles_then_d())) break;
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -503,8 +509,7 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dkdv_kernel(const __grid_con
     int it = 0;
     for (int c = N - 1; c >= 0; c--, it++) {
         const float* la = reinterpret_cast<const float*>(sm + B_LA + (it & 1) * LAB);
-        if (!(ok = wait_all(bar_t, it & 1, abort_flag, p))) break;
-        if (tid == 0) pn.tiles_done++;
+        // log alpha was loaded a chunk ahead; the tiles are waited for after the gate's sums
         if (p.gate) {
             if (!(ok = wait_all(bar_l[it & 1], (it >> 1) & 1, abort_flag, p))) break;
             if (tid == 0) {
@@ -560,6 +565,8 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dkdv_kernel(const __grid_con
                 *reinterpret_cast<float2*>(xch + 5 * D + ch) = make_float2(q[2].x + q[3].x, q[2].y + q[3].y);
             }
             strong |= fminf(bc2.x, bc2.y) < kStrongLog;
+            if (!(ok = wait_all(bar_t, it & 1, abort_flag, p))) break;
+            if (tid == 0) pn.tiles_done++;
             uint8_t* qt = sm + B_Q;
             uint8_t* kt = sm + B_K;
 #pragma unroll
@@ -575,6 +582,10 @@ __global__ void __launch_bounds__(kThr2, 1) gla_bwd_dkdv_kernel(const __grid_con
                 *eq = pack_bf16x2(qf.x * ex2f(u0), qf.y * ex2f(u1));
                 *ek = pack_bf16x2(kf.x * ex2f(-u0), kf.y * ex2f(-u1));
             }
+        }
+        if (!p.gate) {
+            if (!(ok = wait_all(bar_t, it & 1, abort_flag, p))) break;
+            if (tid == 0) pn.tiles_done++;
         }
         fence_proxy_async_smem();  // the factors, read by the products below
         tc_fence_before();
