@@ -28,11 +28,10 @@
 // state's columns, run the phases in turn behind their own barrier, with bounded
 // waits; one more warp's first thread issues each group of tensor-core products
 // once the workers have signalled that its operands are in place, so that issuing
-// never holds up a worker.  A chunk over
-// which some channel decays by more than e^-64 is outside the factorisation's
-// range: the head is marked (a NaN pattern in the first output element of each
-// 64-column block) and the token-by-token kernel recomputes exactly the marked
-// heads afterwards.
+// never holds up a worker.  A chunk over which some channel decays by more than
+// e^-64 is outside the factorisation's range: the head is marked (a NaN pattern
+// in the first output element of each 64-column block) and the token-by-token
+// kernel recomputes exactly the marked heads afterwards.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
